@@ -1,0 +1,506 @@
+// Host side of the C ABI declared in include/kvq.h: the cache handle, the
+// cache state machine, argument checks and kernel launches.
+//
+// State machine (unite.ai page, section "System tax"; KIVI summary page,
+// section "Method"): the most recent tokens stay in an fp16 window of R
+// tokens; an append that finds the window full first quantizes those R tokens
+// as one page (the flush) and then stores the new token.  So for T >= 1
+// cached tokens the window holds n_r in [1, R] tokens and Tq = R*floor((T-1)/R)
+// tokens are quantized.  All counts live on the host: no call reads the GPU.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+struct kvq_cache {
+  kvq_config cfg;
+  int device = 0;
+  int sm_count = 0;
+  kvq::PageLayout lay{};
+  int64_t n_units = 0;        // B * Hkv
+  int64_t n_pages_cap = 0;    // pages per unit
+  int64_t unit_page_stride = 0;
+  uint8_t* pages = nullptr;
+  uint16_t* wk = nullptr;
+  uint16_t* wv = nullptr;
+  float* part_ml = nullptr;
+  float* part_acc = nullptr;
+  int* counters = nullptr;
+  int* err = nullptr;
+  unsigned long long* rope_turns = nullptr;
+  int32_t max_splits = 1;
+  int32_t forced_splits = 0;
+  int64_t T = 0, Tq = 0;
+  int32_t n_r = 0;
+  bool prefilled = false;
+  bool broken = false;
+  int64_t launches = 0;
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvq_status fail_cuda(kvq_cache* c) {
+  c->broken = true;
+  return KVQ_ERR_CUDA;
+}
+
+int64_t quantized_tokens(int64_t T, int R) { return T <= 0 ? 0 : (int64_t)R * ((T - 1) / R); }
+
+void free_all(kvq_cache* c) {
+  cudaFree(c->pages);
+  cudaFree(c->wk);
+  cudaFree(c->wv);
+  cudaFree(c->part_ml);
+  cudaFree(c->part_acc);
+  cudaFree(c->counters);
+  cudaFree(c->err);
+  cudaFree(c->rope_turns);
+  c->pages = nullptr;
+  c->wk = c->wv = nullptr;
+  c->part_ml = c->part_acc = nullptr;
+  c->err = nullptr;
+  c->counters = nullptr;
+  c->rope_turns = nullptr;
+}
+
+kvq_status validate(const kvq_config& k) {
+  if (k.batch < 1 || k.num_kv_heads < 1 || k.num_q_heads < 1 || k.head_dim < 1 || k.max_tokens < 1)
+    return KVQ_ERR_INVALID_ARG;
+  if (k.num_q_heads % k.num_kv_heads) return KVQ_ERR_INVALID_ARG;
+  if (k.k_bits < 2 || k.k_bits > 4 || k.v_bits < 2 || k.v_bits > 4) return KVQ_ERR_INVALID_ARG;
+  if (k.group_size < 1 || k.residual < 1 || k.k_sparse < 0 || (k.rope != 0 && k.rope != 1))
+    return KVQ_ERR_INVALID_ARG;
+  if (k.head_dim % k.group_size || k.residual % k.group_size) return KVQ_ERR_INVALID_ARG;
+  if (!(k.softmax_scale > 0.0f) || !std::isfinite(k.softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  if (k.rope && (!(k.rope_base > 1.0f) || !std::isfinite(k.rope_base))) return KVQ_ERR_INVALID_ARG;
+  if (k.k_sparse > k.head_dim) return KVQ_ERR_INVALID_ARG;
+  // what this build implements
+  if (k.head_dim != kvq::kHeadDim) return KVQ_ERR_UNSUPPORTED;
+  if (k.group_size != 32 && k.group_size != 64) return KVQ_ERR_UNSUPPORTED;
+  if (k.residual % 32 || k.residual > 128) return KVQ_ERR_UNSUPPORTED;
+  if (k.k_sparse > 4) return KVQ_ERR_UNSUPPORTED;
+  if ((int64_t)k.batch * k.num_q_heads > (int64_t)1 << 30) return KVQ_ERR_UNSUPPORTED;
+  if (k.max_tokens >= ((int64_t)1 << 31)) return KVQ_ERR_UNSUPPORTED;
+  const int hg = k.num_q_heads / k.num_kv_heads;
+  if (!kvq::decode_supported(k.k_bits, k.v_bits, hg, k.rope != 0)) return KVQ_ERR_UNSUPPORTED;
+  if (!kvq::quantize_supported(k.k_bits, k.v_bits)) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+int32_t auto_splits(const kvq_cache* c) {
+  const int64_t n_pages = c->Tq / c->cfg.residual;
+  if (n_pages <= 0) return 1;
+  if (c->forced_splits > 0) {
+    int64_t s = c->forced_splits;
+    if (s > c->max_splits) s = c->max_splits;
+    if (s > n_pages) s = n_pages;
+    return (int32_t)(s < 1 ? 1 : s);
+  }
+  // about four resident CTAs per SM, at least two pages per split
+  const int64_t target = (int64_t)c->sm_count * 4;
+  int64_t s = (target + c->n_units - 1) / c->n_units;
+  if (s > n_pages / 2) s = n_pages / 2;
+  if (s < 1) s = 1;
+  if (s > c->max_splits) s = c->max_splits;
+  return (int32_t)s;
+}
+
+// 0.64 fixed-point turns per token of frequency i: theta_i / (2 pi), theta_i = base^(-2i/D).
+unsigned long long rope_turn_fraction(double base, int i, int D) {
+  const double theta = std::pow(base, -2.0 * (double)i / (double)D);
+  long double x = (long double)theta / (2.0L * 3.14159265358979323846264338327950288L);
+  x -= std::floor((double)x);
+  const long double hi = std::floor(x * 4294967296.0L);
+  const long double lo = std::floor((x * 4294967296.0L - hi) * 4294967296.0L);
+  return ((unsigned long long)hi << 32) | (unsigned long long)lo;
+}
+
+}  // namespace
+
+namespace kvq {
+
+PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp) {
+  auto r16 = [](int64_t x) { return (int32_t)((x + 15) / 16 * 16); };
+  PageLayout l{};
+  l.off_kc = 0;
+  l.off_km = l.off_kc + r16((int64_t)R * D * bk / 8);
+  l.off_vc = l.off_km + r16((int64_t)(R / G) * D * 4);
+  l.off_vm = l.off_vc + r16((int64_t)R * D * bv / 8);
+  l.off_si = l.off_vm + r16((int64_t)R * (D / G) * 4);
+  l.off_sv = l.off_si + r16((int64_t)R * nsp);
+  l.bytes = l.off_sv + r16((int64_t)R * nsp * 2);
+  return l;
+}
+
+}  // namespace kvq
+
+extern "C" {
+
+int32_t kvq_version(void) { return (1 << 16) | 0; }
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "configuration not supported by this build";
+    case KVQ_ERR_CAPACITY: return "cache capacity exceeded";
+    case KVQ_ERR_STATE: return "call not allowed in the current cache state";
+    case KVQ_ERR_CUDA: return "CUDA error or device-side timeout";
+    case KVQ_ERR_OOM: return "device allocation failed";
+  }
+  return "unknown status";
+}
+
+kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
+  if (!out) return KVQ_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg) return KVQ_ERR_INVALID_ARG;
+  kvq_status st = validate(*cfg);
+  if (st != KVQ_OK) return st;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return device < 0 ? KVQ_ERR_INVALID_ARG : KVQ_ERR_CUDA;
+  }
+  DeviceGuard g(device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+
+  kvq_cache* c = new kvq_cache();
+  c->cfg = *cfg;
+  c->device = device;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) {
+    delete c;
+    return KVQ_ERR_CUDA;
+  }
+  c->sm_count = prop.multiProcessorCount;
+  const int D = cfg->head_dim, R = cfg->residual, G = cfg->group_size;
+  c->lay = kvq::make_layout(R, D, G, cfg->k_bits, cfg->v_bits, cfg->k_sparse);
+  if (kvq::quantize_smem_bytes(R, D, c->lay) > (size_t)prop.sharedMemPerBlockOptin) {
+    delete c;
+    return KVQ_ERR_UNSUPPORTED;
+  }
+  c->n_units = (int64_t)cfg->batch * cfg->num_kv_heads;
+  c->n_pages_cap = quantized_tokens(cfg->max_tokens, R) / R;
+  c->unit_page_stride = c->n_pages_cap * (int64_t)c->lay.bytes;
+  int64_t ms = c->n_pages_cap < 1 ? 1 : c->n_pages_cap;
+  c->max_splits = (int32_t)(ms > 1024 ? 1024 : ms);
+
+  const int64_t heads = (int64_t)cfg->batch * cfg->num_q_heads;
+  cudaError_t e = cudaSuccess;
+  auto alloc = [&](void** p, size_t bytes) {
+    if (e == cudaSuccess) e = cudaMalloc(p, bytes < 16 ? 16 : bytes);
+  };
+  alloc((void**)&c->pages, (size_t)(c->n_units * c->unit_page_stride));
+  alloc((void**)&c->wk, (size_t)(c->n_units * R * D * 2));
+  alloc((void**)&c->wv, (size_t)(c->n_units * R * D * 2));
+  alloc((void**)&c->part_ml, (size_t)(heads * c->max_splits * 2 * sizeof(float)));
+  alloc((void**)&c->part_acc, (size_t)(heads * c->max_splits * D * sizeof(float)));
+  alloc((void**)&c->counters, (size_t)c->n_units * sizeof(int));
+  alloc((void**)&c->err, sizeof(int));
+  alloc((void**)&c->rope_turns, (size_t)(D / 2) * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(c->err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)c->n_units * sizeof(int));
+  if (e == cudaSuccess) {
+    std::vector<unsigned long long> turns(D / 2);
+    for (int i = 0; i < D / 2; ++i) turns[i] = rope_turn_fraction(cfg->rope ? cfg->rope_base : 10000.0, i, D);
+    e = cudaMemcpy(c->rope_turns, turns.data(), turns.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) {
+    const bool oom = e == cudaErrorMemoryAllocation;
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return oom ? KVQ_ERR_OOM : KVQ_ERR_CUDA;
+  }
+  *out = c;
+  return KVQ_OK;
+}
+
+kvq_status kvq_destroy(kvq_cache* c) {
+  if (!c) return KVQ_OK;
+  {
+    DeviceGuard g(c->device);
+    cudaDeviceSynchronize();
+    free_all(c);
+  }
+  delete c;
+  return KVQ_OK;
+}
+
+kvq_status kvq_get_state(const kvq_cache* c, int64_t* t_total, int64_t* t_quant, int32_t* n_resid) {
+  if (!c) return KVQ_ERR_INVALID_ARG;
+  if (t_total) *t_total = c->T;
+  if (t_quant) *t_quant = c->Tq;
+  if (n_resid) *n_resid = c->n_r;
+  return KVQ_OK;
+}
+
+int64_t kvq_launch_count(const kvq_cache* c) { return c ? c->launches : -1; }
+
+kvq_status kvq_reset(kvq_cache* c) {
+  if (!c) return KVQ_ERR_INVALID_ARG;
+  if (c->broken) return KVQ_ERR_CUDA;
+  c->T = 0;
+  c->Tq = 0;
+  c->n_r = 0;
+  c->prefilled = false;
+  return KVQ_OK;
+}
+
+kvq_status kvq_set_splits(kvq_cache* c, int32_t splits) {
+  if (!c || splits < 0) return KVQ_ERR_INVALID_ARG;
+  c->forced_splits = splits;
+  return KVQ_OK;
+}
+
+kvq_status kvq_get_splits(const kvq_cache* c, int32_t* splits) {
+  if (!c || !splits) return KVQ_ERR_INVALID_ARG;
+  *splits = auto_splits(c);
+  return KVQ_OK;
+}
+
+kvq_status kvq_prefill_quantize(kvq_cache* c, const void* k, const void* v, int64_t n_tokens, void* stream) {
+  if (!c || !k || !v) return KVQ_ERR_INVALID_ARG;
+  if (c->broken) return KVQ_ERR_CUDA;
+  if (!aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens < 1) return KVQ_ERR_INVALID_ARG;
+  if (c->prefilled || c->T != 0) return KVQ_ERR_STATE;
+  if (n_tokens > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail_cuda(c);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int R = c->cfg.residual, D = c->cfg.head_dim;
+  const int64_t Tq = quantized_tokens(n_tokens, R);
+  const int64_t n_pages = Tq / R;
+  // one launch per at most 65535 pages in grid.x
+  for (int64_t p0 = 0; p0 < n_pages; p0 += 65535) {
+    const int64_t np = n_pages - p0 < 65535 ? n_pages - p0 : 65535;
+    kvq::QuantizeParams qp{};
+    qp.k_src = static_cast<const uint16_t*>(k);
+    qp.v_src = static_cast<const uint16_t*>(v);
+    qp.src_unit_stride = n_tokens * D;
+    qp.src_tok0 = p0 * R;
+    qp.pages = c->pages;
+    qp.unit_page_stride = c->unit_page_stride;
+    qp.page0 = p0;
+    qp.n_units = (int32_t)c->n_units;
+    qp.Hkv = c->cfg.num_kv_heads;
+    qp.D = D;
+    qp.G = c->cfg.group_size;
+    qp.R = R;
+    qp.nsp = c->cfg.k_sparse;
+    qp.lay = c->lay;
+    qp.err = c->err;
+    if (kvq::launch_quantize(qp, c->cfg.k_bits, c->cfg.v_bits, (int)np, s) != cudaSuccess) return fail_cuda(c);
+    c->launches++;
+  }
+  kvq::CopyTokensParams cp{};
+  cp.k_src = static_cast<const uint16_t*>(k);
+  cp.v_src = static_cast<const uint16_t*>(v);
+  cp.src_unit_stride = n_tokens * D;
+  cp.src_tok0 = Tq;
+  cp.k_dst = c->wk;
+  cp.v_dst = c->wv;
+  cp.dst_unit_stride = (int64_t)R * D;
+  cp.dst_tok0 = 0;
+  cp.n_tok = (int32_t)(n_tokens - Tq);
+  cp.n_units = (int32_t)c->n_units;
+  cp.D = D;
+  if (kvq::launch_copy_tokens(cp, s) != cudaSuccess) return fail_cuda(c);
+  c->launches++;
+  c->T = n_tokens;
+  c->Tq = Tq;
+  c->n_r = (int32_t)(n_tokens - Tq);
+  c->prefilled = true;
+  return KVQ_OK;
+}
+
+kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, void* stream) {
+  if (!c || !k || !v) return KVQ_ERR_INVALID_ARG;
+  if (c->broken) return KVQ_ERR_CUDA;
+  if (!aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
+  if (c->T + 1 > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail_cuda(c);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int R = c->cfg.residual, D = c->cfg.head_dim;
+  if (c->n_r == R) {
+    // flush: the full window becomes page Tq/R
+    kvq::QuantizeParams qp{};
+    qp.k_src = c->wk;
+    qp.v_src = c->wv;
+    qp.src_unit_stride = (int64_t)R * D;
+    qp.src_tok0 = 0;
+    qp.pages = c->pages;
+    qp.unit_page_stride = c->unit_page_stride;
+    qp.page0 = c->Tq / R;
+    qp.n_units = (int32_t)c->n_units;
+    qp.Hkv = c->cfg.num_kv_heads;
+    qp.D = D;
+    qp.G = c->cfg.group_size;
+    qp.R = R;
+    qp.nsp = c->cfg.k_sparse;
+    qp.lay = c->lay;
+    qp.err = c->err;
+    if (kvq::launch_quantize(qp, c->cfg.k_bits, c->cfg.v_bits, 1, s) != cudaSuccess) return fail_cuda(c);
+    c->launches++;
+    c->Tq += R;
+    c->n_r = 0;
+  }
+  kvq::CopyTokensParams cp{};
+  cp.k_src = static_cast<const uint16_t*>(k);
+  cp.v_src = static_cast<const uint16_t*>(v);
+  cp.src_unit_stride = D;
+  cp.src_tok0 = 0;
+  cp.k_dst = c->wk;
+  cp.v_dst = c->wv;
+  cp.dst_unit_stride = (int64_t)R * D;
+  cp.dst_tok0 = c->n_r;
+  cp.n_tok = 1;
+  cp.n_units = (int32_t)c->n_units;
+  cp.D = D;
+  if (kvq::launch_copy_tokens(cp, s) != cudaSuccess) return fail_cuda(c);
+  c->launches++;
+  c->n_r += 1;
+  c->T += 1;
+  c->prefilled = true;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, void* stream) {
+  if (!c || !q || !out) return KVQ_ERR_INVALID_ARG;
+  if (c->broken) return KVQ_ERR_CUDA;
+  if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
+  if (c->T < 1) return KVQ_ERR_STATE;
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail_cuda(c);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int R = c->cfg.residual;
+  const int32_t splits = auto_splits(c);
+  const int hg = c->cfg.num_q_heads / c->cfg.num_kv_heads;
+  kvq::DecodeParams dp{};
+  dp.q = static_cast<const uint16_t*>(q);
+  dp.pages = c->pages;
+  dp.unit_page_stride = c->unit_page_stride;
+  dp.wk = c->wk;
+  dp.wv = c->wv;
+  dp.win_unit_stride = (int64_t)R * c->cfg.head_dim;
+  dp.n_pages = c->Tq / R;
+  dp.n_r = c->n_r;
+  dp.splits = splits;
+  dp.Hkv = c->cfg.num_kv_heads;
+  dp.Hq = c->cfg.num_q_heads;
+  dp.D = c->cfg.head_dim;
+  dp.G = c->cfg.group_size;
+  dp.R = R;
+  dp.nsp = c->cfg.k_sparse;
+  dp.lay = c->lay;
+  dp.qk_scale_log2 = c->cfg.softmax_scale * 1.4426950408889634f;
+  dp.rope_turns = c->rope_turns;
+  dp.part_ml = c->part_ml;
+  dp.part_acc = c->part_acc;
+  dp.counters = c->counters;
+  dp.out = static_cast<uint16_t*>(out);
+  dp.err = c->err;
+  bool supported = false;
+  if (kvq::launch_decode(dp, c->cfg.k_bits, c->cfg.v_bits, hg, c->cfg.rope != 0, (int)c->n_units, s, &supported) !=
+      cudaSuccess)
+    return supported ? fail_cuda(c) : KVQ_ERR_UNSUPPORTED;
+  c->launches++;
+  return KVQ_OK;
+}
+
+kvq_status kvq_sync_status(kvq_cache* c, void* stream) {
+  if (!c) return KVQ_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail_cuda(c);
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return fail_cuda(c);
+  int err = 0;
+  if (cudaMemcpy(&err, c->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return fail_cuda(c);
+  if (err != 0) return fail_cuda(c);
+  return c->broken ? KVQ_ERR_CUDA : KVQ_OK;
+}
+
+kvq_status kvq_unit_sizes(const kvq_cache* c, kvq_unit_view* v) {
+  if (!c || !v) return KVQ_ERR_INVALID_ARG;
+  const int D = c->cfg.head_dim, G = c->cfg.group_size, nsp = c->cfg.k_sparse;
+  const int64_t Tq = c->Tq;
+  v->kcodes_bytes = Tq * D * c->cfg.k_bits / 8;
+  v->kmeta_bytes = (Tq / G) * D * 2;
+  v->vcodes_bytes = Tq * D * c->cfg.v_bits / 8;
+  v->vmeta_bytes = Tq * (D / G) * 2;
+  v->sp_idx_bytes = Tq * nsp;
+  v->sp_val_bytes = Tq * nsp * 2;
+  v->window_bytes = (int64_t)c->n_r * D * 2;
+  return KVQ_OK;
+}
+
+kvq_status kvq_export_unit(kvq_cache* c, int32_t b, int32_t kvh, kvq_unit_view* dst, void* stream) {
+  if (!c || !dst) return KVQ_ERR_INVALID_ARG;
+  if (b < 0 || b >= c->cfg.batch || kvh < 0 || kvh >= c->cfg.num_kv_heads) return KVQ_ERR_INVALID_ARG;
+  if (c->broken) return KVQ_ERR_CUDA;
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail_cuda(c);
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return fail_cuda(c);
+  const int D = c->cfg.head_dim, G = c->cfg.group_size, R = c->cfg.residual, nsp = c->cfg.k_sparse;
+  const int bk = c->cfg.k_bits, bv = c->cfg.v_bits;
+  const int64_t unit = (int64_t)b * c->cfg.num_kv_heads + kvh;
+  const int64_t n_pages = c->Tq / R;
+  const kvq::PageLayout& L = c->lay;
+  std::vector<uint8_t> pg((size_t)(n_pages * L.bytes));
+  if (n_pages > 0 && cudaMemcpy(pg.data(), c->pages + unit * c->unit_page_stride, pg.size(), cudaMemcpyDeviceToHost) !=
+                         cudaSuccess)
+    return fail_cuda(c);
+  const int64_t kc_row = (int64_t)D * bk / 8, vc_row = (int64_t)D * bv / 8;
+  for (int64_t p = 0; p < n_pages; ++p) {
+    const uint8_t* src = pg.data() + p * L.bytes;
+    if (dst->kcodes) std::memcpy((uint8_t*)dst->kcodes + p * R * kc_row, src + L.off_kc, (size_t)(R * kc_row));
+    if (dst->vcodes) std::memcpy((uint8_t*)dst->vcodes + p * R * vc_row, src + L.off_vc, (size_t)(R * vc_row));
+    const uint32_t* km = reinterpret_cast<const uint32_t*>(src + L.off_km);
+    for (int64_t i = 0; i < (int64_t)(R / G) * D; ++i) {
+      const int64_t o = p * (R / G) * D + i;
+      if (dst->kz) ((uint16_t*)dst->kz)[o] = (uint16_t)(km[i] & 0xFFFFu);
+      if (dst->ks) ((uint16_t*)dst->ks)[o] = (uint16_t)(km[i] >> 16);
+    }
+    const uint32_t* vm = reinterpret_cast<const uint32_t*>(src + L.off_vm);
+    for (int64_t i = 0; i < (int64_t)R * (D / G); ++i) {
+      const int64_t o = p * R * (D / G) + i;
+      if (dst->vz) ((uint16_t*)dst->vz)[o] = (uint16_t)(vm[i] & 0xFFFFu);
+      if (dst->vs) ((uint16_t*)dst->vs)[o] = (uint16_t)(vm[i] >> 16);
+    }
+    if (nsp > 0) {
+      if (dst->sp_idx) std::memcpy((uint8_t*)dst->sp_idx + p * R * nsp, src + L.off_si, (size_t)(R * nsp));
+      if (dst->sp_val) std::memcpy((uint8_t*)dst->sp_val + p * R * nsp * 2, src + L.off_sv, (size_t)(R * nsp * 2));
+    }
+  }
+  const size_t wbytes = (size_t)c->n_r * D * 2;
+  if (wbytes) {
+    if (dst->wk && cudaMemcpy(dst->wk, c->wk + unit * R * D, wbytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return fail_cuda(c);
+    if (dst->wv && cudaMemcpy(dst->wv, c->wv + unit * R * D, wbytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return fail_cuda(c);
+  }
+  return KVQ_OK;
+}
+
+}  // extern "C"

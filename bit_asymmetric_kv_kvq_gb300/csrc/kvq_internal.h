@@ -1,0 +1,93 @@
+// Internal declarations shared by the library's translation units.
+//
+// Device layout of one (batch, kv-head) unit:
+//   pages  : [n_pages_cap][page_bytes]; page p holds the R quantized tokens
+//            [p*R, p*R + R) as five 16-byte aligned sections
+//              kc  key codes    [R][D*BK/32] u32  (token-major channel bitstream)
+//              km  key meta     [R/G][D] u32      (fp16 zero point in the low half, scale in the high half)
+//              vc  value codes  [R][D*BV/32] u32
+//              vm  value meta   [R][D/G] u32      (zero point low, scale high)
+//              si  sparse idx   [R][NSP] u8       (padded to 16 bytes)
+//              sv  sparse vals  [R][NSP] fp16     (padded to 16 bytes)
+//   window : K and V fp16 [R][D] each (the recent, not yet quantized tokens).
+// A page is one flush unit, so a flush writes exactly one page and a decode
+// split streams whole pages with one bulk copy each.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace kvq {
+
+constexpr int kHeadDim = 128;
+
+struct PageLayout {
+  int32_t off_kc, off_km, off_vc, off_vm, off_si, off_sv, bytes;
+};
+
+PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp);
+
+// Device error codes written by kernels into the cache's error word.
+enum DeviceError : int {
+  kDevOk = 0,
+  kDevWaitTimeout = 1,    // an mbarrier wait gave up
+  kDevBadArgument = 2,    // a kernel saw parameters it cannot handle
+};
+
+struct QuantizeParams {
+  const uint16_t* k_src;     // fp16 bits; token t of unit u at k_src + u*src_unit_stride + t*D
+  const uint16_t* v_src;
+  int64_t src_unit_stride;   // elements
+  int64_t src_tok0;          // source token of the first page of this launch
+  uint8_t* pages;            // base of all units' pages
+  int64_t unit_page_stride;  // bytes between units
+  int64_t page0;             // index of the first page written by this launch
+  int32_t n_units, Hkv, D, G, R, nsp;
+  PageLayout lay;
+  int* err;
+};
+
+struct CopyTokensParams {
+  const uint16_t* k_src;
+  const uint16_t* v_src;
+  int64_t src_unit_stride;  // elements
+  int64_t src_tok0;
+  uint16_t* k_dst;          // window base
+  uint16_t* v_dst;
+  int64_t dst_unit_stride;  // elements
+  int64_t dst_tok0;
+  int32_t n_tok, n_units, D;
+};
+
+struct DecodeParams {
+  const uint16_t* q;        // [B][Hq][D] fp16 bits
+  const uint8_t* pages;
+  int64_t unit_page_stride;
+  const uint16_t* wk;       // window [units][R][D]
+  const uint16_t* wv;
+  int64_t win_unit_stride;  // elements
+  int64_t n_pages;          // quantized pages per unit (Tq / R)
+  int32_t n_r;              // window tokens
+  int32_t splits;
+  int32_t Hkv, Hq, D, G, R, nsp;
+  PageLayout lay;
+  float qk_scale_log2;      // softmax_scale * log2(e)
+  const unsigned long long* rope_turns;  // [D/2] theta_i / (2*pi) as 0.64 fixed point (rope only)
+  float* part_ml;           // [B*Hq][splits][2]  (running max in log2 units, sum)
+  float* part_acc;          // [B*Hq][splits][D]
+  int* counters;            // [B*Hkv] finished splits, zero between calls
+  uint16_t* out;            // [B][Hq][D] fp16 bits
+  int* err;
+};
+
+// Launchers (return cudaGetLastError() after the launch).
+cudaError_t launch_quantize(const QuantizeParams& p, int bk, int bv, int n_pages, cudaStream_t s);
+cudaError_t launch_copy_tokens(const CopyTokensParams& p, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool rope, int n_units, cudaStream_t s,
+                          bool* supported);
+bool decode_supported(int bk, int bv, int hg, bool rope);
+bool quantize_supported(int bk, int bv);
+size_t quantize_smem_bytes(int R, int D, const PageLayout& lay);
+
+}  // namespace kvq

@@ -1,0 +1,283 @@
+"""Python binding of the C ABI in include/kvq.h (argument marshalling only).
+
+Every step of the cache and of decode attention runs in the CUDA library
+``_lib/libkvq.so``; this module only passes device pointers, sizes and the
+CUDA stream.  If the library is missing it raises: there is no fallback.
+
+Two layers:
+  * functions named exactly like the C ABI (``kvq_create``, ``kvq_prefill_quantize``,
+    ``kvq_append``, ``kvq_decode_attention``, ``kvq_destroy`` ...), taking raw
+    integers (pointers, stream handles) or torch tensors;
+  * ``KVCache``, a small owner object over one handle that takes torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+from . import _build
+
+LIB_PATH = _build.LIB
+
+KVQ_OK = 0
+KVQ_ERR_INVALID_ARG = -1
+KVQ_ERR_UNSUPPORTED = -2
+KVQ_ERR_CAPACITY = -3
+KVQ_ERR_STATE = -4
+KVQ_ERR_CUDA = -5
+KVQ_ERR_OOM = -6
+
+
+class KVQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class kvq_config(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("max_tokens", ctypes.c_int64), ("k_bits", ctypes.c_int32),
+                ("v_bits", ctypes.c_int32), ("group_size", ctypes.c_int32), ("residual", ctypes.c_int32),
+                ("k_sparse", ctypes.c_int32), ("rope", ctypes.c_int32), ("rope_base", ctypes.c_float),
+                ("softmax_scale", ctypes.c_float)]
+
+
+class kvq_unit_view(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("kcodes", "kz", "ks", "vcodes", "vz", "vs", "sp_idx", "sp_val",
+                                               "wk", "wv")] + \
+               [(n, ctypes.c_int64) for n in ("kcodes_bytes", "kmeta_bytes", "vcodes_bytes", "vmeta_bytes",
+                                              "sp_idx_bytes", "sp_val_bytes", "window_bytes")]
+
+
+_P = ctypes.c_void_p
+_lock = threading.Lock()
+_lib = None
+
+# every symbol include/kvq.h declares, with (restype, argtypes)
+SIGNATURES = {
+    "kvq_create": (ctypes.c_int, [ctypes.POINTER(kvq_config), ctypes.c_int, ctypes.POINTER(_P)]),
+    "kvq_destroy": (ctypes.c_int, [_P]),
+    "kvq_prefill_quantize": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, _P]),
+    "kvq_append": (ctypes.c_int, [_P, _P, _P, _P]),
+    "kvq_decode_attention": (ctypes.c_int, [_P, _P, _P, _P]),
+    "kvq_reset": (ctypes.c_int, [_P]),
+    "kvq_get_state": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                     ctypes.POINTER(ctypes.c_int32)]),
+    "kvq_unit_sizes": (ctypes.c_int, [_P, ctypes.POINTER(kvq_unit_view)]),
+    "kvq_export_unit": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(kvq_unit_view), _P]),
+    "kvq_set_splits": (ctypes.c_int, [_P, ctypes.c_int32]),
+    "kvq_get_splits": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
+    "kvq_sync_status": (ctypes.c_int, [_P, _P]),
+    "kvq_launch_count": (ctypes.c_int64, [_P]),
+    "kvq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "kvq_version": (ctypes.c_int32, []),
+}
+
+
+def lib():
+    """Load libkvq.so (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                                   f"g.build()'` (needs nvcc)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().kvq_status_string(status).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def _check(status: int, what: str):
+    if status != KVQ_OK:
+        raise KVQError(status, what)
+
+
+def _ptr(x):
+    """Device pointer of a torch tensor, or an integer address as given."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream, device=None):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_config(batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits, v_bits, group_size, residual,
+                k_sparse=0, rope=0, rope_base=10000.0, softmax_scale=None) -> kvq_config:
+    if softmax_scale is None:
+        softmax_scale = 1.0 / float(head_dim) ** 0.5
+    return kvq_config(batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits, v_bits, group_size, residual,
+                      k_sparse, rope, rope_base, softmax_scale)
+
+
+# ------------------------------------------------------------------ C-ABI named functions
+
+def kvq_create(cfg: kvq_config, device: int = 0) -> int:
+    h = _P()
+    _check(lib().kvq_create(ctypes.byref(cfg), device, ctypes.byref(h)), "kvq_create")
+    return h.value
+
+
+def kvq_destroy(handle) -> None:
+    _check(lib().kvq_destroy(handle), "kvq_destroy")
+
+
+def kvq_prefill_quantize(handle, k, v, n_tokens: int, stream=None) -> None:
+    _check(lib().kvq_prefill_quantize(handle, _ptr(k), _ptr(v), n_tokens, _stream(stream)), "kvq_prefill_quantize")
+
+
+def kvq_append(handle, k, v, stream=None) -> None:
+    _check(lib().kvq_append(handle, _ptr(k), _ptr(v), _stream(stream)), "kvq_append")
+
+
+def kvq_decode_attention(handle, q, out, stream=None) -> None:
+    _check(lib().kvq_decode_attention(handle, _ptr(q), _ptr(out), _stream(stream)), "kvq_decode_attention")
+
+
+def kvq_reset(handle) -> None:
+    _check(lib().kvq_reset(handle), "kvq_reset")
+
+
+def kvq_get_state(handle):
+    t, tq, nr = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    _check(lib().kvq_get_state(handle, ctypes.byref(t), ctypes.byref(tq), ctypes.byref(nr)), "kvq_get_state")
+    return t.value, tq.value, nr.value
+
+
+def kvq_set_splits(handle, splits: int) -> None:
+    _check(lib().kvq_set_splits(handle, splits), "kvq_set_splits")
+
+
+def kvq_get_splits(handle) -> int:
+    s = ctypes.c_int32()
+    _check(lib().kvq_get_splits(handle, ctypes.byref(s)), "kvq_get_splits")
+    return s.value
+
+
+def kvq_sync_status(handle, stream=None) -> int:
+    return int(lib().kvq_sync_status(handle, _stream(stream)))
+
+
+def kvq_launch_count(handle) -> int:
+    return int(lib().kvq_launch_count(handle))
+
+
+def kvq_export_unit(handle, b: int, kvh: int, cfg: kvq_config, stream=None) -> dict:
+    """Unit (b, kvh) in the canonical host layout (numpy arrays), waiting for `stream`."""
+    sizes = kvq_unit_view()
+    _check(lib().kvq_unit_sizes(handle, ctypes.byref(sizes)), "kvq_unit_sizes")
+    t, tq, nr = kvq_get_state(handle)
+    D, G, nsp = cfg.head_dim, cfg.group_size, cfg.k_sparse
+    out = dict(
+        kcodes=np.zeros((tq, D * cfg.k_bits // 32), np.uint32), kz=np.zeros((tq // G, D), np.uint16),
+        ks=np.zeros((tq // G, D), np.uint16), vcodes=np.zeros((tq, D * cfg.v_bits // 32), np.uint32),
+        vz=np.zeros((tq, D // G), np.uint16), vs=np.zeros((tq, D // G), np.uint16),
+        sp_idx=np.zeros((tq, nsp), np.uint8), sp_val=np.zeros((tq, nsp), np.uint16),
+        wk=np.zeros((nr, D), np.uint16), wv=np.zeros((nr, D), np.uint16))
+    assert out["kcodes"].nbytes == sizes.kcodes_bytes and out["wk"].nbytes == sizes.window_bytes
+    view = kvq_unit_view(*[a.ctypes.data if a.size else None for a in out.values()])
+    _check(lib().kvq_export_unit(handle, b, kvh, ctypes.byref(view), _stream(stream)), "kvq_export_unit")
+    return out
+
+
+# ------------------------------------------------------------------ owner object
+
+class KVCache:
+    """One layer's quantized KV cache on one GPU (torch tensors in, torch tensors out)."""
+
+    def __init__(self, batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits=2, v_bits=2, group_size=32,
+                 residual=128, k_sparse=0, rope=0, rope_base=10000.0, softmax_scale=None, device=0):
+        self.cfg = make_config(batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits, v_bits, group_size,
+                               residual, k_sparse, rope, rope_base, softmax_scale)
+        self.device = device
+        self.handle = kvq_create(self.cfg, device)
+
+    @classmethod
+    def for_workload(cls, w, device=0, max_tokens=None):
+        return cls(w.batch, w.kv_heads, w.q_heads, w.head_dim, max_tokens or w.max_tokens, w.k_bits, w.v_bits,
+                   w.group, w.residual, w.k_sparse, w.rope, w.rope_base, w.softmax_scale, device)
+
+    def _need(self, t, shape, name):
+        import torch
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch tensor")
+        if not t.is_cuda or t.dtype != torch.float16 or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name}: need a contiguous CUDA fp16 tensor of shape {tuple(shape)}, got "
+                             f"{t.device} {t.dtype} {tuple(t.shape)} contiguous={t.is_contiguous()}")
+
+    def prefill_quantize(self, k, v, stream=None):
+        c = self.cfg
+        n = k.shape[2]
+        self._need(k, (c.batch, c.num_kv_heads, n, c.head_dim), "k")
+        self._need(v, (c.batch, c.num_kv_heads, n, c.head_dim), "v")
+        kvq_prefill_quantize(self.handle, k, v, n, _stream(stream, self.device))
+
+    def append(self, k, v, stream=None):
+        c = self.cfg
+        self._need(k, (c.batch, c.num_kv_heads, c.head_dim), "k")
+        self._need(v, (c.batch, c.num_kv_heads, c.head_dim), "v")
+        kvq_append(self.handle, k, v, _stream(stream, self.device))
+
+    def decode_attention(self, q, out=None, stream=None):
+        import torch
+        c = self.cfg
+        self._need(q, (c.batch, c.num_q_heads, c.head_dim), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        self._need(out, (c.batch, c.num_q_heads, c.head_dim), "out")
+        kvq_decode_attention(self.handle, q, out, _stream(stream, self.device))
+        return out
+
+    def reset(self):
+        kvq_reset(self.handle)
+
+    def state(self):
+        return kvq_get_state(self.handle)
+
+    def export_unit(self, b, kvh, stream=None):
+        return kvq_export_unit(self.handle, b, kvh, self.cfg, _stream(stream, self.device))
+
+    def set_splits(self, n):
+        kvq_set_splits(self.handle, n)
+
+    def splits(self):
+        return kvq_get_splits(self.handle)
+
+    def sync_status(self, stream=None):
+        return kvq_sync_status(self.handle, _stream(stream, self.device))
+
+    def launch_count(self):
+        return kvq_launch_count(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            kvq_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,205 @@
+/*
+ * kvq.h - asymmetric low-bit KV cache with quantized decode attention, C ABI.
+ *
+ * The library keeps one layer's KV cache for a batch of sequences on one GPU:
+ *
+ *  - Keys are quantized per channel: each group of G consecutive tokens of a
+ *    channel shares one fp16 zero point and one fp16 scale ("KV cache has a
+ *    geometry problem, not a bit problem", section "Keys"; KIVI summary page,
+ *    section "Method").
+ *  - Values are quantized per token: each group of G consecutive channels of a
+ *    token shares one zero point and scale (same page, section "Values").
+ *  - The quantizer is uniform and asymmetric: zero point = group minimum,
+ *    step = range / (2^B - 1), every element rounds to the nearest step (same
+ *    page, section "Quantization error in practice").  B is 2, 3 or 4 bits and
+ *    may differ between keys and values, e.g. K4V2 ("Quantize What Counts:
+ *    More for Keys, Less for Values").
+ *  - The most recent tokens stay in an fp16 window of R tokens; a full window
+ *    is quantized as one block (unite.ai page, section "System tax"; KIVI
+ *    summary page, section "Method": buffer of 128 recent tokens).
+ *  - Optionally keys are kept pre-RoPE and rotated after dequantization, and
+ *    the largest-magnitude entries of each key vector are kept sparse in fp16
+ *    outside the group ranges (KVQuant review, "Proposed method").
+ *
+ * Decode attention reads the whole cache every generated token, which makes
+ * it bound by memory bandwidth (unite.ai page, section "Why the KV cache is a
+ * problem").  kvq_decode_attention computes softmax(q.K^T * scale).V over all
+ * cached tokens for every query head, reading the packed codes directly.
+ *
+ * Conventions for every call:
+ *  - Return value: KVQ_OK (0) or a negative kvq_status.  No exception or
+ *    longjmp crosses the ABI.  Argument, state and capacity errors are found
+ *    on the host before anything is launched and leave the cache unchanged.
+ *  - Device pointers are plain CUDA device addresses of the cache's device;
+ *    `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *    asynchronous on that stream; the caller's buffers must stay valid until
+ *    the stream has passed the call.  The cache state (token counts) is
+ *    tracked on the host, so no call waits for the GPU except kvq_export_unit
+ *    and kvq_sync_status.
+ *  - Input device buffers must be 16-byte aligned and densely packed.
+ *  - The cache owns all of its device memory; it is allocated once by
+ *    kvq_create and freed by kvq_destroy.  The hot calls allocate nothing.
+ *  - One cache must not be used from two host threads or two streams at
+ *    once.  Different caches are independent.
+ *  - A CUDA error inside a call (launch failure, or a device-side wait that
+ *    ran out) makes the cache return KVQ_ERR_CUDA from then on.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned buffer, bad config value */
+  KVQ_ERR_UNSUPPORTED = -2, /* a valid config outside what this build implements */
+  KVQ_ERR_CAPACITY = -3,    /* more tokens than cfg.max_tokens */
+  KVQ_ERR_STATE = -4,       /* call not allowed in the cache's current state */
+  KVQ_ERR_CUDA = -5,        /* CUDA runtime error or device-side timeout (sticky) */
+  KVQ_ERR_OOM = -6          /* device allocation failed in kvq_create */
+} kvq_status;
+
+typedef struct {
+  int32_t batch;         /* B >= 1 sequences */
+  int32_t num_kv_heads;  /* Hkv >= 1 */
+  int32_t num_q_heads;   /* Hq, a multiple of Hkv; q head h reads kv head h / (Hq/Hkv) */
+  int32_t head_dim;      /* D (this build: 128) */
+  int64_t max_tokens;    /* capacity: tokens per sequence after all appends */
+  int32_t k_bits;        /* bits per key code: 2, 3 or 4 */
+  int32_t v_bits;        /* bits per value code: 2, 3 or 4 */
+  int32_t group_size;    /* G: tokens per key group and channels per value group; 32 or 64, divides D and R */
+  int32_t residual;      /* R: fp16 window length; a multiple of 32 and of G, at most 128 */
+  int32_t k_sparse;      /* fp16 outliers kept per key vector, 0..4 (0 = dense keys) */
+  int32_t rope;          /* 0: keys arrive already rotated; 1: keys arrive pre-RoPE and are rotated
+                            after dequantization (rotate-half pairs (i, i+D/2), theta_i = base^(-2i/D),
+                            position = absolute token index) */
+  float rope_base;       /* RoPE base, e.g. 10000 (used when rope = 1) */
+  float softmax_scale;   /* scale applied to q.k, e.g. 1/sqrt(D) */
+} kvq_config;
+
+typedef struct kvq_cache kvq_cache; /* opaque */
+
+/*
+ * Create an empty cache on CUDA device `device` and allocate all its device
+ * memory: the packed pages for max_tokens tokens, the fp16 window and the
+ * split-attention workspace.  On success *out receives the handle.
+ * Errors: KVQ_ERR_INVALID_ARG (null, out-of-range field), KVQ_ERR_UNSUPPORTED,
+ * KVQ_ERR_OOM, KVQ_ERR_CUDA.  On error *out is set to NULL.
+ */
+kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out);
+
+/* Free the cache and its device memory (synchronizes the device first).
+   NULL is a no-op returning KVQ_OK. */
+kvq_status kvq_destroy(kvq_cache* cache);
+
+/*
+ * Prefill: cache the prompt's keys and values, k and v device fp16
+ * [B][Hkv][n_tokens][D], 1 <= n_tokens <= max_tokens.  The first
+ * Tq = R*floor((n_tokens-1)/R) tokens are quantized into packed pages (keys
+ * per channel over G-token groups, values per token over G-channel groups, the
+ * sparse outliers first when k_sparse > 0); the last n_tokens - Tq tokens
+ * (1..R) are copied into the fp16 window.  Allowed once, on an empty cache
+ * (otherwise KVQ_ERR_STATE).  KIVI summary page, section "Method"; unite.ai
+ * page, sections "Keys", "Values", "System tax".
+ */
+kvq_status kvq_prefill_quantize(kvq_cache* cache, const void* k_f16, const void* v_f16, int64_t n_tokens,
+                                void* cuda_stream);
+
+/*
+ * Append one decode token: k and v device fp16 [B][Hkv][D].  If the window
+ * already holds R tokens it is first quantized as one block (the flush), then
+ * the new token is stored in the window.  An append on an empty cache acts as
+ * a prefill of one token.  KVQ_ERR_CAPACITY when the cache already holds
+ * max_tokens tokens.  unite.ai page, section "System tax".
+ */
+kvq_status kvq_append(kvq_cache* cache, const void* k_f16, const void* v_f16, void* cuda_stream);
+
+/*
+ * Decode attention for one query token per sequence and head: q and out
+ * device fp16 [B][Hq][D].  q arrives already rotated (post-RoPE at its own
+ * position).  out[b][h] = softmax(scale * q[b][h] . K^T) . V over all T
+ * cached tokens of sequence b and kv head h/(Hq/Hkv), where K and V are the
+ * dequantized pages (z + s*code; sparse entries restored; keys rotated when
+ * rope = 1) followed by the fp16 window.  Computed as split-K flash decoding
+ * in fp32 (token ranges in parallel, online softmax, log-sum-exp merge), then
+ * rounded to fp16.  KVQ_ERR_STATE on an empty cache.
+ */
+kvq_status kvq_decode_attention(kvq_cache* cache, const void* q_f16, void* out_f16, void* cuda_stream);
+
+/*
+ * Forget every cached token so the cache can take a new batch of sequences
+ * (the next call may be a prefill).  Host-only: no device work, no memory
+ * is freed or cleared; the pages are simply overwritten by later calls.
+ */
+kvq_status kvq_reset(kvq_cache* cache);
+
+/* ---------------- helpers (not on the hot path) ---------------- */
+
+/* Host-tracked state: tokens cached, tokens quantized (Tq), tokens in the window. */
+kvq_status kvq_get_state(const kvq_cache* cache, int64_t* t_total, int64_t* t_quant, int32_t* n_resid);
+
+/*
+ * Host view of one (batch, kv head) unit in the canonical layout.  Every
+ * pointer is caller-allocated host memory of at least the byte size that
+ * kvq_unit_sizes reports for the current state; a NULL pointer skips that
+ * array.  Layouts (Tq = quantized tokens, n_r = window tokens):
+ *   kcodes uint32 [Tq][D*k_bits/32]  codes of one token's D channels as a
+ *                                     little-endian bitstream: code of channel
+ *                                     c at bits [c*k_bits, c*k_bits + k_bits)
+ *   kz, ks uint16 [Tq/G][D]          key zero point / scale (fp16 bits)
+ *   vcodes uint32 [Tq][D*v_bits/32]  same bitstream layout for values
+ *   vz, vs uint16 [Tq][D/G]          value zero point / scale
+ *   sp_idx uint8  [Tq][k_sparse]     sparse key channels, ascending
+ *   sp_val uint16 [Tq][k_sparse]     sparse key values (exact fp16)
+ *   wk, wv uint16 [n_r][D]           fp16 window (tokens Tq .. Tq+n_r-1)
+ */
+typedef struct {
+  void* kcodes; void* kz; void* ks;
+  void* vcodes; void* vz; void* vs;
+  void* sp_idx; void* sp_val;
+  void* wk; void* wv;
+  int64_t kcodes_bytes, kmeta_bytes, vcodes_bytes, vmeta_bytes, sp_idx_bytes, sp_val_bytes, window_bytes;
+} kvq_unit_view;
+
+/* Fill the *_bytes fields of `sizes` for the current state (pointers untouched). */
+kvq_status kvq_unit_sizes(const kvq_cache* cache, kvq_unit_view* sizes);
+
+/* Copy unit (b, kvh) to the host in the canonical layout; waits for `stream`. */
+kvq_status kvq_export_unit(kvq_cache* cache, int32_t b, int32_t kvh, kvq_unit_view* dst, void* cuda_stream);
+
+/*
+ * Force the number of token splits per (batch, kv head) used by decode
+ * attention (0 = automatic, from the SM count and the cache length).  Values
+ * above the workspace capacity are clamped.  Test and tuning aid.
+ */
+kvq_status kvq_set_splits(kvq_cache* cache, int32_t splits);
+
+/* Splits the next decode will use for the current state. */
+kvq_status kvq_get_splits(const kvq_cache* cache, int32_t* splits);
+
+/*
+ * Wait for `stream`, then report the cache's device-side status: KVQ_OK, or
+ * KVQ_ERR_CUDA if a kernel recorded a failed bounded wait or CUDA reports an
+ * error.  Every device-side wait in the kernels gives up after a time limit
+ * and records an error code instead of hanging.
+ */
+kvq_status kvq_sync_status(kvq_cache* cache, void* cuda_stream);
+
+/* Kernel launches issued by this cache since creation (decode, append, flush...). */
+int64_t kvq_launch_count(const kvq_cache* cache);
+
+/* Static text for a status code. */
+const char* kvq_status_string(kvq_status status);
+
+/* Library version, (major << 16) | minor. */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,93 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+and rejects bad configurations on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import bit_asymmetric_kv_kvq_gb300 as kvq
+    from bit_asymmetric_kv_kvq_gb300 import _build
+    try:
+        _build.build()
+    except RuntimeError as e:  # no nvcc on this machine
+        pytest.skip(str(e))
+    return kvq
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ["kvq_create", "kvq_prefill_quantize", "kvq_append", "kvq_decode_attention", "kvq_destroy"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kvq):
+    L = ctypes.CDLL(kvq.kvq.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+    # and the binding knows the signature of each one
+    assert set(declared_functions()) <= set(kvq.kvq.SIGNATURES)
+
+
+def test_status_strings(kvq):
+    for s in range(-6, 1):
+        assert kvq.status_string(s) and kvq.status_string(s) != "unknown status"
+    assert kvq.status_string(-99) == "unknown status"
+    assert kvq.lib().kvq_version() >> 16 == 1
+
+
+def _status(kvq, **over):
+    cfg = kvq.make_config(2, 4, 8, 128, 4096, 2, 2, 32, 128)
+    for k, v in over.items():
+        setattr(cfg, k, v)
+    h = ctypes.c_void_p(123)
+    st = kvq.lib().kvq_create(ctypes.byref(cfg), 0, ctypes.byref(h))
+    assert h.value is None  # *out is cleared on failure
+    return st
+
+
+@pytest.mark.parametrize("field,value,expect", [
+    ("batch", 0, -1), ("num_kv_heads", 0, -1), ("num_q_heads", 6, -1), ("head_dim", 0, -1), ("max_tokens", 0, -1),
+    ("k_bits", 1, -1), ("k_bits", 5, -1), ("v_bits", 8, -1), ("group_size", 48, -1), ("residual", 100, -1),
+    ("k_sparse", -1, -1), ("rope", 2, -1), ("softmax_scale", 0.0, -1), ("softmax_scale", float("inf"), -1),
+    ("head_dim", 64, -2), ("group_size", 16, -2), ("residual", 256, -2), ("k_sparse", 5, -2),
+    ("num_q_heads", 32, -2),  # 8 query heads per kv head: not in this build
+])
+def test_bad_configs_are_rejected_on_the_host(kvq, field, value, expect):
+    assert _status(kvq, **{field: value}) == expect
+
+
+def test_null_arguments(kvq):
+    L = kvq.lib()
+    assert L.kvq_destroy(None) == 0
+    assert L.kvq_create(None, 0, ctypes.byref(ctypes.c_void_p())) == -1
+    cfg = kvq.make_config(1, 1, 1, 128, 16, 2, 2, 32, 128)
+    assert L.kvq_create(ctypes.byref(cfg), 0, None) == -1
+    assert L.kvq_prefill_quantize(None, None, None, 1, None) == -1
+    assert L.kvq_append(None, None, None, None) == -1
+    assert L.kvq_decode_attention(None, None, None, None) == -1
+    assert L.kvq_get_state(None, None, None, None) == -1
+    assert L.kvq_set_splits(None, 0) == -1
+    assert L.kvq_sync_status(None, None) == -1
+    assert L.kvq_launch_count(None) == -1
+    assert L.kvq_reset(None) == -1
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    import bit_asymmetric_kv_kvq_gb300.kvq as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        b.lib()
