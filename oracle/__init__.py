@@ -137,6 +137,11 @@ def float_to_half_n(x) -> np.ndarray:
 
 
 def f16_bits(a) -> np.ndarray:
+    """fp16 bit patterns of `a`: uint16 arrays are taken as bits already, float16 arrays are viewed,
+    anything else is rounded to fp16 first."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return np.ascontiguousarray(a)
     return np.ascontiguousarray(np.asarray(a, np.float16)).view(np.uint16)
 
 
@@ -195,12 +200,15 @@ def quantize_values(V16, G: int, bits: int):
 
 
 def pack_rows(codes, bits: int) -> np.ndarray:
+    """Pack each row (token) as its own bitstream.  Rows are a whole number of 32-bit words, so the
+    rows laid end to end form one bitstream with the same words."""
     c = _c(codes, np.uint8)
     T, D = c.shape
+    if (D * bits) % 32:
+        raise ValueError("row length times bits is not a multiple of 32")
     out = np.zeros((T, D * bits // 32), np.uint32)
-    for t in range(T):
-        if lib().kvqo_pack(_ptr(c[t]), D, bits, _ptr(out[t])) != 0:
-            raise ValueError("row length times bits is not a multiple of 32")
+    if T and lib().kvqo_pack(_ptr(c), T * D, bits, _ptr(out)) != 0:
+        raise ValueError("packing failed")
     return out
 
 

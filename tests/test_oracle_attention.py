@@ -198,6 +198,44 @@ def test_flush_equivalence(T0):
                 assert np.array_equal(a[key], b[key]), (T, key)
 
 
+@pytest.mark.parametrize("bits,G,nsp", [(2, 32, 0), (4, 32, 0), (3, 64, 2)])
+def test_unit_stores_reconstruct_the_input(bits, G, nsp):
+    """The cache state's stores, dequantized by hand, stay within half a step of the original tokens."""
+    D, R, T = 64, 64, 200
+    w = synth.WORKLOADS[4].scaled(batch=1, kv_heads=1, q_heads=1, head_dim=D, prefill_tokens=T - 5, decode_steps=5,
+                                  group=G, residual=R, k_sparse=nsp, k_bits=bits, v_bits=bits)
+    K = synth.keys(w)[0, 0]
+    V = synth.values(w)[0, 0]
+    u = oracle.OracleUnit.for_workload(w)
+    u.prefill(K[:T - 5], V[:T - 5])
+    for t in range(T - 5, T):
+        u.append(K[t], V[t])
+    st = u.stores()
+    Tq = u.Tq
+    assert Tq == oracle.quantized_tokens(T, R) == 192 and u.n_r == T - Tq
+    L = 2 ** bits - 1
+    kc = np.stack([oracle.unpack(st["kcodes"][t], D, bits) for t in range(Tq)]).astype(np.float64)
+    vc = np.stack([oracle.unpack(st["vcodes"][t], D, bits) for t in range(Tq)]).astype(np.float64)
+    kz = oracle.bits_f64(st["kz"]).repeat(G, axis=0)
+    ks = oracle.bits_f64(st["ks"]).repeat(G, axis=0)
+    khat = kz + ks * kc
+    for t in range(Tq):
+        for j in range(nsp):
+            khat[t, st["sp_idx"][t, j]] = oracle.bits_f64(st["sp_val"][t, j])
+    vz = oracle.bits_f64(st["vz"]).repeat(G, axis=1)
+    vs = oracle.bits_f64(st["vs"]).repeat(G, axis=1)
+    vhat = vz + vs * vc
+    Kd, Vd = K[:Tq].astype(np.float64), V[:Tq].astype(np.float64)
+    # half a step plus the fp16 rounding of the step (per group)
+    assert np.all(np.abs(khat - Kd) <= ks * (0.5 + L * 2.0 ** -11) + 1e-6)
+    assert np.all(np.abs(vhat - Vd) <= vs * (0.5 + L * 2.0 ** -11) + 1e-6)
+    # sparse entries are exact, the window is the input verbatim
+    for t in range(Tq):
+        for j in range(nsp):
+            assert khat[t, st["sp_idx"][t, j]] == Kd[t, st["sp_idx"][t, j]]
+    assert np.array_equal(st["wk"], K[Tq:T].view(np.uint16)) and np.array_equal(st["wv"], V[Tq:T].view(np.uint16))
+
+
 def test_prefill_twice_is_rejected():
     u = _unit()
     u.prefill(np.zeros((3, 16), np.float16), np.zeros((3, 16), np.float16))
