@@ -344,7 +344,7 @@ def run_ours(args, dist):
             step(evs)
             torch.cuda.synchronize(dev)
             durs.extend(a.elapsed_time(b) for a, b in evs)
-    dec_ms = statistics.mean(durs)
+    dec_ms = statistics.mean(durs) if durs else float("nan")
     dec_bytes = statistics.mean(decode_bytes(w, T0 + 1 + i) for i in range(S))
     import json as _json
     peaks = _json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(

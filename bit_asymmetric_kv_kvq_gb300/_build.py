@@ -44,19 +44,23 @@ def stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not stale():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib=None, objdir=None, csrc=None) -> str:
+    """Build libkvq.so (or, with `lib`/`objdir`/`csrc`, a variant built elsewhere with extra nvcc flags)."""
+    src_dir = csrc or CSRC
+    target = lib or LIB
+    odir = objdir or OBJDIR
+    if not force and lib is None and not stale():
         return LIB
     nvcc = nvcc_path()
-    os.makedirs(OBJDIR, exist_ok=True)
-    common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
+    os.makedirs(odir, exist_ok=True)
+    common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", src_dir,
                      *extra_flags]
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(odir, os.path.splitext(src)[0] + ".o")
         objs.append(obj)
-        cmd = [nvcc, *common, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *common, "-c", os.path.join(src_dir, src), "-o", obj]
         if src.endswith(".cu"):
             cmd.insert(1, "-Xptxas=-v") if verbose else None
         procs.append((src, cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
@@ -70,13 +74,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if failed:
         msg = "\n".join(f"--- {s} ---\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = target + f".tmp{os.getpid()}"
     link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, target)
+    return target
 
 
 if __name__ == "__main__":

@@ -33,8 +33,9 @@ struct kvq_cache {
   int* counters = nullptr;
   int* err = nullptr;
   unsigned long long* rope_turns = nullptr;
-  int32_t max_splits = 1;
-  int32_t forced_splits = 0;
+  int32_t max_slots = 1;      // partial slots per query head
+  int32_t forced_splits = 0;  // 0: grid = resident CTAs; n: grid = n CTAs per unit
+  int64_t resident = 1;       // decode CTAs resident on the whole GPU
   int64_t T = 0, Tq = 0;
   int32_t n_r = 0;
   bool prefilled = false;
@@ -106,22 +107,25 @@ kvq_status validate(const kvq_config& k) {
   return KVQ_OK;
 }
 
-int32_t auto_splits(const kvq_cache* c) {
-  const int64_t n_pages = c->Tq / c->cfg.residual;
-  if (n_pages <= 0) return 1;
+constexpr int32_t kMaxForcedSplits = 16;
+
+// Grid of the decode launch: the resident CTA count (or n per unit when forced),
+// never more than the work items.
+int64_t decode_grid(const kvq_cache* c) {
+  const int64_t wpu = c->Tq / c->cfg.residual + (c->n_r > 0 ? 1 : 0);
+  const int64_t total = c->n_units * wpu;
+  int64_t g;
   if (c->forced_splits > 0) {
-    int64_t s = c->forced_splits;
-    if (s > c->max_splits) s = c->max_splits;
-    if (s > n_pages) s = n_pages;
-    return (int32_t)(s < 1 ? 1 : s);
+    g = c->n_units * c->forced_splits;
+  } else if (c->resident >= 2 * c->n_units) {
+    // whole units per CTA group: every unit is cut into the same number of slices,
+    // so a CTA never straddles two units (costs at most a third of the slots)
+    g = c->n_units * (c->resident / c->n_units);
+  } else {
+    g = c->resident;
   }
-  // about four resident CTAs per SM, at least two pages per split
-  const int64_t target = (int64_t)c->sm_count * 4;
-  int64_t s = (target + c->n_units - 1) / c->n_units;
-  if (s > n_pages / 2) s = n_pages / 2;
-  if (s < 1) s = 1;
-  if (s > c->max_splits) s = c->max_splits;
-  return (int32_t)s;
+  if (g > total) g = total;
+  return g < 1 ? 1 : g;
 }
 
 // 0.64 fixed-point turns per token of frequency i: theta_i / (2 pi), theta_i = base^(-2i/D).
@@ -202,8 +206,21 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   c->n_units = (int64_t)cfg->batch * cfg->num_kv_heads;
   c->n_pages_cap = quantized_tokens(cfg->max_tokens, R) / R;
   c->unit_page_stride = c->n_pages_cap * (int64_t)c->lay.bytes;
-  int64_t ms = c->n_pages_cap < 1 ? 1 : c->n_pages_cap;
-  c->max_splits = (int32_t)(ms > 1024 ? 1024 : ms);
+  const int hg = cfg->num_q_heads / cfg->num_kv_heads;
+  const int per_sm = kvq::decode_resident_ctas_per_sm(cfg->k_bits, cfg->v_bits, hg, cfg->rope != 0, c->lay.bytes);
+  if (per_sm < 1) {
+    cudaGetLastError();
+    delete c;
+    return KVQ_ERR_UNSUPPORTED;
+  }
+  c->resident = (int64_t)per_sm * c->sm_count;
+  {
+    // a unit's items meet at most ceil(2*grid/units) + 2 CTA slices (and at most its item count)
+    const int64_t grid_cap = c->resident > c->n_units * kMaxForcedSplits ? c->resident : c->n_units * kMaxForcedSplits;
+    int64_t ms = (2 * grid_cap + c->n_units - 1) / c->n_units + 2;
+    if (ms > c->n_pages_cap + 1) ms = c->n_pages_cap + 1;
+    c->max_slots = (int32_t)(ms < 1 ? 1 : ms);
+  }
 
   const int64_t heads = (int64_t)cfg->batch * cfg->num_q_heads;
   cudaError_t e = cudaSuccess;
@@ -213,8 +230,8 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   alloc((void**)&c->pages, (size_t)(c->n_units * c->unit_page_stride));
   alloc((void**)&c->wk, (size_t)(c->n_units * R * D * 2));
   alloc((void**)&c->wv, (size_t)(c->n_units * R * D * 2));
-  alloc((void**)&c->part_ml, (size_t)(heads * c->max_splits * 2 * sizeof(float)));
-  alloc((void**)&c->part_acc, (size_t)(heads * c->max_splits * D * sizeof(float)));
+  alloc((void**)&c->part_ml, (size_t)(heads * c->max_slots * 2 * sizeof(float)));
+  alloc((void**)&c->part_acc, (size_t)(heads * c->max_slots * D * sizeof(float)));
   alloc((void**)&c->counters, (size_t)c->n_units * sizeof(int));
   alloc((void**)&c->err, sizeof(int));
   alloc((void**)&c->rope_turns, (size_t)(D / 2) * sizeof(unsigned long long));
@@ -269,13 +286,13 @@ kvq_status kvq_reset(kvq_cache* c) {
 
 kvq_status kvq_set_splits(kvq_cache* c, int32_t splits) {
   if (!c || splits < 0) return KVQ_ERR_INVALID_ARG;
-  c->forced_splits = splits;
+  c->forced_splits = splits > kMaxForcedSplits ? kMaxForcedSplits : splits;
   return KVQ_OK;
 }
 
 kvq_status kvq_get_splits(const kvq_cache* c, int32_t* splits) {
   if (!c || !splits) return KVQ_ERR_INVALID_ARG;
-  *splits = auto_splits(c);
+  *splits = (int32_t)((decode_grid(c) + c->n_units - 1) / c->n_units);
   return KVQ_OK;
 }
 
@@ -396,7 +413,7 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, void* st
   if (!g.ok) return fail_cuda(c);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int R = c->cfg.residual;
-  const int32_t splits = auto_splits(c);
+  const int64_t grid = decode_grid(c);
   const int hg = c->cfg.num_q_heads / c->cfg.num_kv_heads;
   kvq::DecodeParams dp{};
   dp.q = static_cast<const uint16_t*>(q);
@@ -405,13 +422,16 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, void* st
   dp.wk = c->wk;
   dp.wv = c->wv;
   dp.win_unit_stride = (int64_t)R * c->cfg.head_dim;
+  dp.n_units = c->n_units;
   dp.n_pages = c->Tq / R;
+  dp.work_per_unit = (int32_t)(dp.n_pages + (c->n_r > 0 ? 1 : 0));
   dp.n_r = c->n_r;
-  dp.splits = splits;
+  dp.max_slots = c->max_slots;
   dp.Hkv = c->cfg.num_kv_heads;
   dp.Hq = c->cfg.num_q_heads;
   dp.D = c->cfg.head_dim;
   dp.G = c->cfg.group_size;
+  dp.log2G = c->cfg.group_size == 64 ? 6 : 5;
   dp.R = R;
   dp.nsp = c->cfg.k_sparse;
   dp.lay = c->lay;
@@ -423,7 +443,7 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, void* st
   dp.out = static_cast<uint16_t*>(out);
   dp.err = c->err;
   bool supported = false;
-  if (kvq::launch_decode(dp, c->cfg.k_bits, c->cfg.v_bits, hg, c->cfg.rope != 0, (int)c->n_units, s, &supported) !=
+  if (kvq::launch_decode(dp, c->cfg.k_bits, c->cfg.v_bits, hg, c->cfg.rope != 0, (int)grid, s, &supported) !=
       cudaSuccess)
     return supported ? fail_cuda(c) : KVQ_ERR_UNSUPPORTED;
   c->launches++;

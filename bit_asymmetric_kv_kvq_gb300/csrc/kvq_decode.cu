@@ -1,12 +1,23 @@
-// Split-K flash-decoding attention over the packed cache, with the merge of
-// the splits fused into the same launch.
+// Decode attention over the packed cache: one persistent, load-balanced launch.
 //
 // Decode reads the whole cache for every generated token ("KV cache has a
 // geometry problem, not a bit problem", section "Why the KV cache is a
-// problem"), so the kernel is built around streaming pages: a producer warp
-// issues one bulk (TMA) copy per page into a ring of shared-memory stages,
-// four consumer warps dequantize in registers and never touch global memory
-// for the cache, and the grid is (token splits) x (batch * kv heads).
+// problem"), so the kernel is built around streaming pages at full bandwidth:
+//
+//  * Work list.  Every (batch, kv head) unit contributes n_pages page items
+//    and, when the fp16 window is not empty, one window item.  The items of
+//    all units are laid end to end and the grid (sized to the resident CTA
+//    count) takes equal contiguous slices of that list, so every SM streams
+//    the same number of pages whatever the batch/head/length mix, and a CTA
+//    crosses from one unit into the next without a new launch.
+//  * Streaming.  A producer warp issues one bulk (TMA) copy per page into a
+//    ring of shared-memory stages guarded by mbarriers; four consumer warps
+//    take one 32-token sub-tile of each page and dequantize in registers.
+//  * Merge.  Each CTA writes one unnormalised partial (m, l, acc[D]) per
+//    query head for every unit it touched; the CTA that completes a unit's
+//    item count (an atomic ticket, no waiting) merges the unit's partials
+//    with log-sum-exp weights and writes the fp16 output.  A unit covered by
+//    one CTA is written directly.
 //
 // Keys are quantized per channel over G-token groups, so inside a group the
 // score is linear in the codes:
@@ -21,11 +32,7 @@
 //
 // Softmax is online in base 2 with a lazy maximum: the running maximum only
 // moves when a score exceeds it by more than 8 (log2 units), which keeps
-// every weight below 2^8 and skips most rescales.  Each CTA writes one
-// unnormalised partial (m, l, acc[D]) per query head; the last CTA of a
-// (batch, kv head) to finish (an atomic ticket, no waiting) merges the splits
-// with a log-sum-exp weighting and writes the fp16 output.  One split writes
-// the output directly.
+// every weight below 2^8 and skips most rescales.
 #include <cuda_fp16.h>
 
 #include "kvq_internal.h"
@@ -36,7 +43,8 @@ namespace kvq {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kDecodeThreads = kConsumerThreads + 32;
 constexpr int kStages = 4;
 constexpr float kLazyRescale = 8.0f;
 
@@ -47,6 +55,29 @@ __device__ __forceinline__ float code_to_float(uint32_t code) {
   return __uint_as_float(0x4B000000u | code) - 8388608.0f;
 }
 
+// Codes of one 32-bit word of a B-bit bitstream as floats without a shift per
+// code: OR-ing the masked code into the mantissa of 2^23 gives 2^23 + 2^(B*p)*code
+// exactly for the first NDIRECT positions p; the rest are read the same way
+// from the word shifted right by NDIRECT*B.  Callers subtract 2^23 (exact) and
+// fold 2^(-B*p) into the other factor.
+template <int BITS>
+struct MaskCodes {
+  static constexpr int PER_WORD = 32 / BITS;
+  static constexpr int NDIRECT = BITS == 2 ? 11 : 5;  // (2^B - 1) * 2^(B*(n-1)) < 2^23
+  static constexpr uint32_t MASK = (1u << BITS) - 1u;
+  __device__ static constexpr int pos(int i) { return i < NDIRECT ? i : i - NDIRECT; }
+  // 2^(-B*p) for the code at index i of a word
+  __device__ static float unscale(int i) { return __uint_as_float((uint32_t)(127 - BITS * pos(i)) << 23); }
+  __device__ __forceinline__ static void to_float(uint32_t w, float (&f)[PER_WORD]) {
+    const uint32_t ws = w >> (NDIRECT * BITS);
+#pragma unroll
+    for (int i = 0; i < PER_WORD; ++i) {
+      const uint32_t src = i < NDIRECT ? w : ws;
+      f[i] = __uint_as_float((src & (MASK << (BITS * pos(i)))) | 0x4B000000u);
+    }
+  }
+};
+
 template <int BK, int BV, int HG, bool ROPE>
 struct Shape {
   static constexpr int D = kHeadDim;
@@ -55,15 +86,23 @@ struct Shape {
   static constexpr int TAU = 32 / KAPPA; // token slots per warp
   static constexpr int TPL = 32 / TAU;   // tokens per lane in a 32-token sub-tile
   static constexpr int HALF = CPL / 2;   // rope: channels per lane in each half of the head
+  // one query head per kv head with 2- or 4-bit codes: mask extraction and packed fp32x2 math
+  static constexpr bool FAST_K = HG == 1 && !ROPE && (BK == 2 || BK == 4);
+  static constexpr bool FAST_V = HG == 1 && (BV == 2 || BV == 4);
+  static constexpr int KBITS_FAST = (BK == 2 || BK == 4) ? BK : 2;
+#ifndef KVQ_MHA_MIN_BLOCKS
+#define KVQ_MHA_MIN_BLOCKS 3
+#endif
+  // resident CTAs per SM the register budget is sized for
+  static constexpr int MIN_BLOCKS = ROPE ? (HG == 1 ? 2 : 1) : (HG == 1 ? KVQ_MHA_MIN_BLOCKS : (HG == 2 ? 3 : 1));
 };
 
-// Extract `n` codes of `bits` bits starting at bit `bit0` of a token record
-// held in shared memory, into codes[0..n).
+// Extract N codes of BITS bits starting at bit `bit0` of a token record held
+// in shared memory, into codes[0..N).
 template <int BITS, int N>
 __device__ __forceinline__ void load_codes(const uint32_t* rec, int bit0, uint32_t (&codes)[N]) {
   constexpr uint32_t MASK = (1u << BITS) - 1u;
-  if constexpr (N * BITS <= 32 + 0) {
-    // fits in one 64-bit window from the first word
+  if constexpr (N * BITS <= 32) {
     const int w = bit0 >> 5, off = bit0 & 31;
     uint64_t win = rec[w];
     if (off + N * BITS > 32) win |= (uint64_t)rec[w + 1] << 32;
@@ -103,33 +142,55 @@ __device__ __forceinline__ void rope_cs(unsigned long long F, uint32_t t, float&
   sincospif(x, &s, &c);
 }
 
+// The CTA whose slice of the work list holds item x (slices [k*total/grid, (k+1)*total/grid)).
+__device__ __forceinline__ int cta_of(int64_t x, int64_t total, int grid) {
+  return (int)(((x + 1) * (int64_t)grid - 1) / total);
+}
+
+// Running softmax state of one lane for the current unit.
+template <int HG, int CPL>
+struct LaneState {
+  float m[HG], l[HG], zsum[HG], acc[HG][CPL];
+  bool folded;
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.0f;
+      zsum[h] = 0.0f;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) acc[h][i] = 0.0f;
+    }
+    folded = false;
+  }
+};
+
 template <int BK, int BV, int HG, bool ROPE>
-__global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_BLOCKS))
+    decode_kernel(const DecodeParams p) {
   using S = Shape<BK, BV, HG, ROPE>;
   constexpr int D = S::D, CPL = S::CPL, KAPPA = S::KAPPA, TAU = S::TAU, TPL = S::TPL;
 
-  const int split = blockIdx.x;
-  const int unit = blockIdx.y;  // b * Hkv + kvh
-  const int b = unit / p.Hkv, kvh = unit - b * p.Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cta = blockIdx.x, grid = gridDim.x;
+  const int64_t wpu = p.work_per_unit;
+  const int64_t total = p.n_units * wpu;
+  const int64_t w_begin = (int64_t)cta * total / grid;
+  const int64_t w_end = (int64_t)(cta + 1) * total / grid;
+  const int page_bytes = p.lay.bytes;
 
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ __align__(16) uint16_t q_stage[2][HG * D];  // fp16 query rows of the next units
+  __shared__ __align__(8) uint64_t q_full[2];
+  __shared__ __align__(8) uint64_t q_empty[2];
   __shared__ float q_s[HG][D];
-  __shared__ float qp_s[kConsumerWarps][HG][D];
+  __shared__ __align__(16) float qp_s[kConsumerWarps][HG][D];
   __shared__ float wacc[kConsumerWarps][HG][D];
   __shared__ float wml[kConsumerWarps][HG][2];
   __shared__ int abort_flag;
   __shared__ int last_cta;
-
-  // page range of this split; the last split also reads the fp16 window
-  const int64_t pg_begin = (int64_t)split * p.n_pages / p.splits;
-  const int64_t pg_end = (int64_t)(split + 1) * p.n_pages / p.splits;
-  const int n_pg = (int)(pg_end - pg_begin);
-  const bool do_window = split == p.splits - 1 && p.n_r > 0;
-  const int page_bytes = p.lay.bytes;
-  const uint8_t* unit_pages = p.pages + (int64_t)unit * p.unit_page_stride;
 
   if (tid == 0) {
     abort_flag = 0;
@@ -137,20 +198,42 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(const Deco
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kConsumerWarps);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
     fence_mbar_init();
-  }
-  for (int i = tid; i < HG * D; i += kDecodeThreads) {
-    const int h = i / D, c = i - h * D;
-    q_s[h][c] = h2f(p.q[((int64_t)b * p.Hq + kvh * HG + h) * D + c]);
   }
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    // ---------------- producer: one bulk copy per page into the stage ring
+    // ---------------- producer: one bulk copy per page item into the stage ring
     if (lane == 0) {
       int issued = 0;
-      for (int i = 0; i < n_pg; ++i) {
-        const int st = i % kStages, k = i / kStages;
+      int q_issued = 0;
+      int64_t unit = w_begin / wpu;
+      int loc = (int)(w_begin - unit * wpu);
+      const uint32_t q_bytes = (uint32_t)(HG * D * 2);
+      for (int64_t x = w_begin; x < w_end; ++x, ++loc) {
+        if (loc == wpu) {
+          loc = 0;
+          ++unit;
+        }
+        if (x == w_begin || loc == 0) {
+          // query rows of this unit (q[b][kvh*HG .. kvh*HG+HG-1][:], contiguous) into a double buffer
+          const int qs = q_issued & 1, qk = q_issued >> 1;
+          if (qk > 0 && !mbar_wait(&q_empty[qs], (qk - 1) & 1)) {
+            report_error(p.err, kDevWaitTimeout);
+            atomicExch(&abort_flag, 1);
+            break;
+          }
+          const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
+          mbar_arrive_expect_tx(&q_full[qs], q_bytes);
+          bulk_g2s(q_stage[qs], p.q + (b * p.Hq + kvh * HG) * D, q_bytes, &q_full[qs]);
+          ++q_issued;
+        }
+        if (loc >= p.n_pages) continue;  // window item: read by the consumers directly
+        const int st = issued % kStages, k = issued / kStages;
         if (k > 0 && !mbar_wait(&empty_bar[st], (k - 1) & 1)) {
           report_error(p.err, kDevWaitTimeout);
           atomicExch(&abort_flag, 1);
@@ -158,13 +241,14 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(const Deco
         }
         if (*(volatile int*)&abort_flag) break;
         mbar_arrive_expect_tx(&full_bar[st], (uint32_t)page_bytes);
-        bulk_g2s(stage_mem + (size_t)st * page_bytes, unit_pages + (pg_begin + i) * (int64_t)page_bytes,
+        bulk_g2s(stage_mem + (size_t)st * page_bytes, p.pages + unit * p.unit_page_stride + (int64_t)loc * page_bytes,
                  (uint32_t)page_bytes, &full_bar[st]);
         ++issued;
       }
-      // never leave with a copy in flight: wait (bounded) for the last copy of every stage
+      // never leave with a copy in flight: wait (bounded) for the last copy of every buffer
       for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
         mbar_wait(&full_bar[i % kStages], (i / kStages) & 1);
+      for (int i = (q_issued > 2 ? q_issued - 2 : 0); i < q_issued; ++i) mbar_wait(&q_full[i & 1], (i >> 1) & 1);
     }
     return;
   }
@@ -172,23 +256,24 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(const Deco
   // ---------------- consumers
   const int kap = lane % KAPPA;  // channel chunk
   const int tau = lane / KAPPA;  // token slot
-  float m_run[HG], l_run[HG], zsum[HG], acc[HG][CPL];
-#pragma unroll
-  for (int h = 0; h < HG; ++h) {
-    m_run[h] = -INFINITY;
-    l_run[h] = 0.0f;
-    zsum[h] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) acc[h][i] = 0.0f;
-  }
   // key channels of this lane: a contiguous chunk, or (rope) half a chunk in each half of the head
   const int kc_lo = ROPE ? kap * S::HALF : kap * CPL;
   const int vc_lo = kap * CPL;
   const int sub_tiles = p.R / 32;
-  const int ng = D / p.G;
+  const int ng = D >> p.log2G;
+  const int gv = vc_lo >> p.log2G;
+  // fast key path: 2^(-B*p) of the channels this lane prepares for the group products
+  float k_unscale[D / 32];
+#pragma unroll
+  for (int j = 0; j < D / 32; ++j)
+    k_unscale[j] = S::FAST_K ? MaskCodes<S::KBITS_FAST>::unscale((lane + 32 * j) % MaskCodes<S::KBITS_FAST>::PER_WORD)
+                             : 1.0f;
 
-  // Online-softmax update of one sub-tile; sc[j][h] are final scores (log2 units) of the
-  // lane's tokens (-inf for masked ones).  Returns the weights in sc.
+  LaneState<HG, CPL> st;
+  st.reset();
+
+  // Online-softmax update of one sub-tile: sc[j][h] are final scores (log2 units) of the
+  // lane's tokens (-inf for masked ones); returns the weights in sc.
   auto softmax_update = [&](float (&sc)[TPL][HG]) {
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
@@ -197,372 +282,491 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(const Deco
       for (int j = 1; j < TPL; ++j) tmax = fmaxf(tmax, sc[j][h]);
 #pragma unroll
       for (int off = KAPPA; off < 32; off <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-      if (tmax > m_run[h] + kLazyRescale || (m_run[h] == -INFINITY && tmax != -INFINITY)) {
-        const float mnew = fmaxf(tmax, m_run[h]);
-        const float f = m_run[h] == -INFINITY ? 0.0f : exp2f(m_run[h] - mnew);
-        l_run[h] *= f;
-        zsum[h] *= f;
+      if (tmax > st.m[h] + kLazyRescale || (st.m[h] == -INFINITY && tmax != -INFINITY)) {
+        const float mnew = fmaxf(tmax, st.m[h]);
+        const float f = st.m[h] == -INFINITY ? 0.0f : exp2f(st.m[h] - mnew);
+        st.l[h] *= f;
+        st.zsum[h] *= f;
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) acc[h][i] *= f;
-        m_run[h] = mnew;
+        for (int i = 0; i < CPL; ++i) st.acc[h][i] *= f;
+        st.m[h] = mnew;
       }
-      const bool live = m_run[h] != -INFINITY;
+      const bool live = st.m[h] != -INFINITY;
 #pragma unroll
-      for (int j = 0; j < TPL; ++j) sc[j][h] = live ? exp2f(sc[j][h] - m_run[h]) : 0.0f;
+      for (int j = 0; j < TPL; ++j) sc[j][h] = live ? exp2f(sc[j][h] - st.m[h]) : 0.0f;
     }
   };
 
-  int pg_i = 0;
-  for (; pg_i < n_pg; ++pg_i) {
-    const int st = pg_i % kStages;
-    if (!mbar_wait(&full_bar[st], (pg_i / kStages) & 1)) {
+  // undo the per-position code scale of the fast value path and add the value
+  // zero-point sums (quantized tokens only); done once per unit, before any fp16 token
+  auto fold = [&]() {
+    if (st.folded) return;
+#pragma unroll
+    for (int h = 0; h < HG; ++h)
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        if constexpr (S::FAST_V) st.acc[h][i] *= MaskCodes<S::FAST_V ? BV : 2>::unscale(i % MaskCodes<S::FAST_V ? BV : 2>::PER_WORD);
+        st.acc[h][i] += st.zsum[h];
+      }
+    st.folded = true;
+  };
+
+  int q_seq = 0;
+  auto load_q = [&]() {
+    const int qs = q_seq & 1;
+    if (!mbar_wait(&q_full[qs], (q_seq >> 1) & 1)) {
       report_error(p.err, kDevWaitTimeout);
       atomicExch(&abort_flag, 1);
-      break;
     }
-    const uint8_t* pgm = stage_mem + (size_t)st * page_bytes;
-    const uint32_t* kc = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_kc);
-    const uint32_t* km = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_km);
-    const uint32_t* vcw = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vc);
-    const uint32_t* vm = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vm);
-    const uint8_t* si = pgm + p.lay.off_si;
-    const uint16_t* sv = reinterpret_cast<const uint16_t*>(pgm + p.lay.off_sv);
-    const int64_t page_tok0 = (pg_begin + pg_i) * (int64_t)p.R;
+    for (int i = tid; i < HG * D; i += kConsumerThreads) {
+      const int h = i / D, c = i - h * D;
+      q_s[h][c] = h2f(q_stage[qs][i]);
+    }
+    named_barrier_sync(1, kConsumerThreads);
+    if (tid == 0) mbar_arrive(&q_empty[qs]);
+    ++q_seq;
+  };
 
-    for (int stt = warp; stt < sub_tiles; stt += kConsumerWarps) {
-      const int g = (stt * 32) / p.G;  // key group of this sub-tile (G >= 32)
-      float sc[TPL][HG];
-
-      if constexpr (!ROPE) {
-        // cooperative q'_c = q_c * s_c and Z = sum_c q_c z_c for the group
-        __syncwarp();  // every lane has finished reading the previous sub-tile's q'
-        float zp[HG];
+  // Partial of this CTA for `unit` (covering `done` of its items); merges when it completes the unit.
+  auto epilogue = [&](int64_t unit, int done) {
+    fold();
 #pragma unroll
-        for (int h = 0; h < HG; ++h) zp[h] = 0.0f;
+    for (int h = 0; h < HG; ++h) {
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
-          const int c = lane + 32 * j;
-          const uint32_t mz = km[g * D + c];
-          const float z = h2f((uint16_t)(mz & 0xFFFFu)), s = h2f((uint16_t)(mz >> 16));
+      for (int off = KAPPA; off < 32; off <<= 1) {
+        st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], off);
 #pragma unroll
-          for (int h = 0; h < HG; ++h) {
-            qp_s[warp][h][c] = q_s[h][c] * s;
-            zp[h] = fmaf(q_s[h][c], z, zp[h]);
-          }
+        for (int i = 0; i < CPL; ++i) st.acc[h][i] += __shfl_xor_sync(0xffffffffu, st.acc[h][i], off);
+      }
+    }
+    if (tau == 0) {
+#pragma unroll
+      for (int h = 0; h < HG; ++h)
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) wacc[warp][h][vc_lo + i] = st.acc[h][i];
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        wml[warp][h][0] = st.m[h];
+        wml[warp][h][1] = st.l[h];
+      }
+    }
+    named_barrier_sync(1, kConsumerThreads);
+    constexpr int PER = HG * D / kConsumerThreads;
+    float pa[PER], pm[PER], pl[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i = tid + k * kConsumerThreads;
+      const int h = i / D, c = i - h * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wml[w][h][0]);
+      float a = 0.0f, L = 0.0f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          if (wml[w][h][0] == -INFINITY) continue;
+          const float f = exp2f(wml[w][h][0] - M);
+          a = fmaf(f, wacc[w][h][c], a);
+          L = fmaf(f, wml[w][h][1], L);
         }
+      }
+      pa[k] = a;
+      pm[k] = M;
+      pl[k] = L;
+    }
+    const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
+    const int64_t bh0 = b * p.Hq + kvh * HG;
+    const int k_first = cta_of(unit * wpu, total, grid);
+    const int k_last = cta_of(unit * wpu + wpu - 1, total, grid);
+    if (k_first == k_last) {
 #pragma unroll
-        for (int h = 0; h < HG; ++h)
+      for (int k = 0; k < PER; ++k) {
+        const int i = tid + k * kConsumerThreads;
+        p.out[bh0 * D + i] = __half_as_ushort(__float2half_rn(pa[k] / pl[k]));
+      }
+    } else {
+      const int slot = cta - k_first;
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) zp[h] += __shfl_xor_sync(0xffffffffu, zp[h], off);
-        __syncwarp();
-        float qp[HG][CPL];
+      for (int k = 0; k < PER; ++k) {
+        const int i = tid + k * kConsumerThreads;
+        const int h = i / D, c = i - h * D;
+        const int64_t so = (bh0 + h) * p.max_slots + slot;
+        p.part_acc[so * D + c] = pa[k];
+        if (c == 0) {
+          p.part_ml[so * 2] = pm[k];
+          p.part_ml[so * 2 + 1] = pl[k];
+        }
+      }
+      __threadfence();
+      named_barrier_sync(1, kConsumerThreads);
+      if (tid == 0) last_cta = atomicAdd(&p.counters[unit], done) + done == wpu;
+      named_barrier_sync(1, kConsumerThreads);
+      if (last_cta) {
+        __threadfence();
+        const int nslots = k_last - k_first + 1;
 #pragma unroll
-        for (int h = 0; h < HG; ++h)
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) qp[h][i] = qp_s[warp][h][kc_lo + i];
-
-#pragma unroll
-        for (int j = 0; j < TPL; ++j) {
-          const int tt = stt * 32 + tau + TAU * j;  // token within the page
-          uint32_t codes[CPL];
-          load_codes<BK, CPL>(kc + tt * (D * BK / 32), kc_lo * BK, codes);
-#pragma unroll
-          for (int h = 0; h < HG; ++h) {
-            float a = 0.0f;
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) a = fmaf(qp[h][i], code_to_float(codes[i]), a);
-            sc[j][h] = a;
+        for (int k = 0; k < PER; ++k) {
+          const int i = tid + k * kConsumerThreads;
+          const int h = i / D, c = i - h * D;
+          const float* ml = p.part_ml + (bh0 + h) * p.max_slots * 2;
+          const float* pacc = p.part_acc + (bh0 + h) * p.max_slots * D + c;
+          float M = -INFINITY;
+#pragma unroll 4
+          for (int sp = 0; sp < nslots; ++sp) M = fmaxf(M, __ldcg(ml + 2 * sp));
+          float a = 0.0f, L = 0.0f;
+#pragma unroll 4
+          for (int sp = 0; sp < nslots; ++sp) {
+            const float m = __ldcg(ml + 2 * sp);
+            if (m == -INFINITY) continue;
+            const float f = exp2f(m - M);
+            L = fmaf(f, __ldcg(ml + 2 * sp + 1), L);
+            a = fmaf(f, __ldcg(pacc + (int64_t)sp * D), a);
           }
-          // sparse entries: the dense code there is 0 (value z); add q_c (x_c - z_c)
-          for (int k = 0; k < p.nsp; ++k) {
-            const int c = si[tt * p.nsp + k];
-            if (c >= kc_lo && c < kc_lo + CPL) {
-              const float z = h2f((uint16_t)(km[g * D + c] & 0xFFFFu));
-              const float x = h2f(sv[tt * p.nsp + k]);
+          p.out[bh0 * D + i] = __half_as_ushort(__float2half_rn(a / L));
+        }
+        if (tid == 0) p.counters[unit] = 0;  // ready for the next call on this stream
+      }
+    }
+    named_barrier_sync(1, kConsumerThreads);  // shared scratch is free again
+  };
+
+  int64_t cur = -1;
+  int done = 0;
+  int pg_seq = 0;
+  int64_t unit = w_begin / wpu;
+  int loc = (int)(w_begin - unit * wpu);
+  for (int64_t x = w_begin; x < w_end; ++x, ++loc) {
+    if (loc == wpu) {
+      loc = 0;
+      ++unit;
+    }
+    if (unit != cur) {
+      if (cur >= 0) epilogue(cur, done);
+      cur = unit;
+      done = 0;
+      st.reset();
+      load_q();
+    }
+    ++done;
+    if (*(volatile int*)&abort_flag) continue;
+
+    if (loc < p.n_pages) {
+      // ---------------- a page of quantized tokens
+      const int stg = pg_seq % kStages;
+      if (!mbar_wait(&full_bar[stg], (pg_seq / kStages) & 1)) {
+        report_error(p.err, kDevWaitTimeout);
+        atomicExch(&abort_flag, 1);
+        continue;
+      }
+      const uint8_t* pgm = stage_mem + (size_t)stg * page_bytes;
+      const uint32_t* kc = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_kc);
+      const uint32_t* km = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_km);
+      const uint32_t* vcw = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vc);
+      const uint32_t* vm = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vm);
+      const uint8_t* si = pgm + p.lay.off_si;
+      const uint16_t* sv = reinterpret_cast<const uint16_t*>(pgm + p.lay.off_sv);
+      const int64_t page_tok0 = loc * (int64_t)p.R;
+
+      for (int stt = warp; stt < sub_tiles; stt += kConsumerWarps) {
+        const int g = (stt * 32) >> p.log2G;  // key group of this sub-tile (G >= 32)
+        float sc[TPL][HG];
+
+        if constexpr (!ROPE) {
+          // cooperative q'_c = q_c * s_c and Z = sum_c q_c z_c for the group
+          __syncwarp();  // every lane has finished reading the previous sub-tile's q'
+          float zp[HG];
 #pragma unroll
-              for (int h = 0; h < HG; ++h) sc[j][h] = fmaf(q_s[h][c], x - z, sc[j][h]);
+          for (int h = 0; h < HG; ++h) zp[h] = 0.0f;
+#pragma unroll
+          for (int j = 0; j < D / 32; ++j) {
+            const int c = lane + 32 * j;
+            const uint32_t mz = km[g * D + c];
+            const float z = h2f((uint16_t)(mz & 0xFFFFu));
+            const float s = h2f((uint16_t)(mz >> 16)) * k_unscale[j];
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+              qp_s[warp][h][c] = q_s[h][c] * s;
+              zp[h] = fmaf(q_s[h][c], z, zp[h]);
             }
           }
-        }
-        // sum the channel chunks of each token, then add the group constant
 #pragma unroll
-        for (int j = 0; j < TPL; ++j)
+          for (int h = 0; h < HG; ++h)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) zp[h] += __shfl_xor_sync(0xffffffffu, zp[h], off);
+          __syncwarp();
+          float qp[HG][CPL];
 #pragma unroll
           for (int h = 0; h < HG; ++h) {
-            float a = sc[j][h];
+            const float4* src = reinterpret_cast<const float4*>(&qp_s[warp][h][kc_lo]);
 #pragma unroll
-            for (int off = 1; off < KAPPA; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-            sc[j][h] = (a + zp[h]) * p.qk_scale_log2;
+            for (int i = 0; i < CPL / 4; ++i) {
+              const float4 v = src[i];
+              qp[h][4 * i] = v.x;
+              qp[h][4 * i + 1] = v.y;
+              qp[h][4 * i + 2] = v.z;
+              qp[h][4 * i + 3] = v.w;
+            }
           }
-      } else {
-        // pre-RoPE keys: dequantize, restore sparse entries, rotate, dot
-        constexpr int HF = S::HALF;
-        float zl[HF], sl[HF], zh[HF], sh[HF];
+
 #pragma unroll
-        for (int i = 0; i < HF; ++i) {
-          const uint32_t a = km[g * D + kc_lo + i], c2 = km[g * D + kc_lo + D / 2 + i];
-          zl[i] = h2f((uint16_t)(a & 0xFFFFu));
-          sl[i] = h2f((uint16_t)(a >> 16));
-          zh[i] = h2f((uint16_t)(c2 & 0xFFFFu));
-          sh[i] = h2f((uint16_t)(c2 >> 16));
+          for (int j = 0; j < TPL; ++j) {
+            const int tt = stt * 32 + tau + TAU * j;  // token within the page
+            if constexpr (S::FAST_K) {
+              using MC = MaskCodes<S::KBITS_FAST>;
+              constexpr int NW = CPL * BK / 32;
+              const uint32_t* rec = kc + tt * (D * BK / 32) + kap * NW;
+              float2 a2 = make_float2(0.0f, 0.0f);
+              const float2 magic = make_float2(-8388608.0f, -8388608.0f);
+#pragma unroll
+              for (int wi = 0; wi < NW; ++wi) {
+                float f[MC::PER_WORD];
+                MC::to_float(rec[wi], f);
+#pragma unroll
+                for (int m = 0; m < MC::PER_WORD / 2; ++m) {
+                  const int i = wi * MC::PER_WORD + 2 * m;
+                  const float2 v = __fadd2_rn(make_float2(f[2 * m], f[2 * m + 1]), magic);
+                  a2 = __ffma2_rn(v, make_float2(qp[0][i], qp[0][i + 1]), a2);
+                }
+              }
+              sc[j][0] = a2.x + a2.y;
+            } else {
+              uint32_t codes[CPL];
+              load_codes<BK, CPL>(kc + tt * (D * BK / 32), kc_lo * BK, codes);
+#pragma unroll
+              for (int h = 0; h < HG; ++h) {
+                float a = 0.0f;
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) a = fmaf(qp[h][i], code_to_float(codes[i]), a);
+                sc[j][h] = a;
+              }
+            }
+            // sparse entries: the dense code there is 0 (value z); add q_c (x_c - z_c)
+            for (int k = 0; k < p.nsp; ++k) {
+              const int c = si[tt * p.nsp + k];
+              if (c >= kc_lo && c < kc_lo + CPL) {
+                const float z = h2f((uint16_t)(km[g * D + c] & 0xFFFFu));
+                const float xv = h2f(sv[tt * p.nsp + k]);
+#pragma unroll
+                for (int h = 0; h < HG; ++h) sc[j][h] = fmaf(q_s[h][c], xv - z, sc[j][h]);
+              }
+            }
+          }
+          // sum the channel chunks of each token, then add the group constant
+#pragma unroll
+          for (int j = 0; j < TPL; ++j)
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+              float a = sc[j][h];
+#pragma unroll
+              for (int off = 1; off < KAPPA; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+              sc[j][h] = (a + zp[h]) * p.qk_scale_log2;
+            }
+        } else {
+          // pre-RoPE keys: dequantize, restore sparse entries, rotate, dot
+          constexpr int HF = S::HALF;
+          float zl[HF], sl[HF], zh[HF], sh[HF];
+#pragma unroll
+          for (int i = 0; i < HF; ++i) {
+            const uint32_t a = km[g * D + kc_lo + i], c2 = km[g * D + kc_lo + D / 2 + i];
+            zl[i] = h2f((uint16_t)(a & 0xFFFFu));
+            sl[i] = h2f((uint16_t)(a >> 16));
+            zh[i] = h2f((uint16_t)(c2 & 0xFFFFu));
+            sh[i] = h2f((uint16_t)(c2 >> 16));
+          }
+#pragma unroll
+          for (int j = 0; j < TPL; ++j) {
+            const int tt = stt * 32 + tau + TAU * j;
+            const uint32_t* rec = kc + tt * (D * BK / 32);
+            uint32_t cl[HF], ch[HF];
+            load_codes<BK, HF>(rec, kc_lo * BK, cl);
+            load_codes<BK, HF>(rec, (kc_lo + D / 2) * BK, ch);
+            float kl[HF], kh[HF];
+#pragma unroll
+            for (int i = 0; i < HF; ++i) {
+              kl[i] = fmaf(sl[i], code_to_float(cl[i]), zl[i]);
+              kh[i] = fmaf(sh[i], code_to_float(ch[i]), zh[i]);
+            }
+            for (int k = 0; k < p.nsp; ++k) {
+              const int c = si[tt * p.nsp + k];
+              const float xv = h2f(sv[tt * p.nsp + k]);
+#pragma unroll
+              for (int i = 0; i < HF; ++i) {
+                if (c == kc_lo + i) kl[i] = xv;
+                if (c == kc_lo + D / 2 + i) kh[i] = xv;
+              }
+            }
+            const uint32_t tpos = (uint32_t)(page_tok0 + tt);
+            float a[HG];
+#pragma unroll
+            for (int h = 0; h < HG; ++h) a[h] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < HF; ++i) {
+              float cs, sn;
+              rope_cs(p.rope_turns[kc_lo + i], tpos, cs, sn);
+              const float rl = kl[i] * cs - kh[i] * sn;
+              const float rh = kh[i] * cs + kl[i] * sn;
+#pragma unroll
+              for (int h = 0; h < HG; ++h)
+                a[h] = fmaf(q_s[h][kc_lo + i], rl, fmaf(q_s[h][kc_lo + D / 2 + i], rh, a[h]));
+            }
+#pragma unroll
+            for (int h = 0; h < HG; ++h) sc[j][h] = a[h];
+          }
+#pragma unroll
+          for (int j = 0; j < TPL; ++j)
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+              float a = sc[j][h];
+#pragma unroll
+              for (int off = 1; off < KAPPA; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+              sc[j][h] = a * p.qk_scale_log2;
+            }
         }
+
+        softmax_update(sc);
+
+        // P.V over the value codes of the lane's channel chunk
 #pragma unroll
         for (int j = 0; j < TPL; ++j) {
           const int tt = stt * 32 + tau + TAU * j;
-          const uint32_t* rec = kc + tt * (D * BK / 32);
-          uint32_t cl[HF], ch[HF];
-          load_codes<BK, HF>(rec, kc_lo * BK, cl);
-          load_codes<BK, HF>(rec, (kc_lo + D / 2) * BK, ch);
-          float kl[HF], kh[HF];
+          const uint32_t mv = vm[tt * ng + gv];
+          const float z = h2f((uint16_t)(mv & 0xFFFFu)), s = h2f((uint16_t)(mv >> 16));
+          if constexpr (S::FAST_V) {
+            using MC = MaskCodes<S::FAST_V ? BV : 2>;
+            constexpr int NW = CPL * BV / 32;
+            const uint32_t* rec = vcw + tt * (D * BV / 32) + kap * NW;
+            const float pw = sc[j][0];
+            st.l[0] += pw;
+            st.zsum[0] = fmaf(pw, z, st.zsum[0]);
+            const float ps = pw * s;
+            const float2 ps2 = make_float2(ps, ps);
+            const float2 magic = make_float2(-8388608.0f, -8388608.0f);
 #pragma unroll
-          for (int i = 0; i < HF; ++i) {
-            kl[i] = fmaf(sl[i], code_to_float(cl[i]), zl[i]);
-            kh[i] = fmaf(sh[i], code_to_float(ch[i]), zh[i]);
-          }
-          for (int k = 0; k < p.nsp; ++k) {
-            const int c = si[tt * p.nsp + k];
-            const float x = h2f(sv[tt * p.nsp + k]);
+            for (int wi = 0; wi < NW; ++wi) {
+              float f[MC::PER_WORD];
+              MC::to_float(rec[wi], f);
 #pragma unroll
-            for (int i = 0; i < HF; ++i) {
-              if (c == kc_lo + i) kl[i] = x;
-              if (c == kc_lo + D / 2 + i) kh[i] = x;
+              for (int m = 0; m < MC::PER_WORD / 2; ++m) {
+                const int i = wi * MC::PER_WORD + 2 * m;
+                const float2 v = __fadd2_rn(make_float2(f[2 * m], f[2 * m + 1]), magic);
+                const float2 r = __ffma2_rn(v, ps2, make_float2(st.acc[0][i], st.acc[0][i + 1]));
+                st.acc[0][i] = r.x;
+                st.acc[0][i + 1] = r.y;
+              }
+            }
+          } else {
+            uint32_t codes[CPL];
+            load_codes<BV, CPL>(vcw + tt * (D * BV / 32), vc_lo * BV, codes);
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+              const float pw = sc[j][h];
+              st.l[h] += pw;
+              st.zsum[h] = fmaf(pw, z, st.zsum[h]);
+              const float ps = pw * s;
+#pragma unroll
+              for (int i = 0; i < CPL; ++i) st.acc[h][i] = fmaf(ps, code_to_float(codes[i]), st.acc[h][i]);
             }
           }
-          const uint32_t tpos = (uint32_t)(page_tok0 + tt);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[stg]);
+      ++pg_seq;
+    } else {
+      // ---------------- the fp16 window: tokens Tq .. Tq + n_r - 1, read directly
+      fold();
+      const int64_t tq = p.n_pages * (int64_t)p.R;
+      const uint16_t* wk = p.wk + unit * p.win_unit_stride;
+      const uint16_t* wv = p.wv + unit * p.win_unit_stride;
+      const int wtiles = (p.n_r + 31) / 32;
+      for (int stt = warp; stt < wtiles; stt += kConsumerWarps) {
+        float sc[TPL][HG];
+#pragma unroll
+        for (int j = 0; j < TPL; ++j) {
+          const int tt = stt * 32 + tau + TAU * j;
+          if (tt >= p.n_r) {
+#pragma unroll
+            for (int h = 0; h < HG; ++h) sc[j][h] = 0.0f;
+            continue;
+          }
+          const uint16_t* kr = wk + (int64_t)tt * D;
           float a[HG];
 #pragma unroll
           for (int h = 0; h < HG; ++h) a[h] = 0.0f;
+          if constexpr (!ROPE) {
 #pragma unroll
-          for (int i = 0; i < HF; ++i) {
-            float cs, sn;
-            rope_cs(p.rope_turns[kc_lo + i], tpos, cs, sn);
-            const float rl = kl[i] * cs - kh[i] * sn;
-            const float rh = kh[i] * cs + kl[i] * sn;
+            for (int i = 0; i < CPL; ++i) {
+              const float xv = h2f(kr[kc_lo + i]);
 #pragma unroll
-            for (int h = 0; h < HG; ++h) a[h] = fmaf(q_s[h][kc_lo + i], rl, fmaf(q_s[h][kc_lo + D / 2 + i], rh, a[h]));
+              for (int h = 0; h < HG; ++h) a[h] = fmaf(q_s[h][kc_lo + i], xv, a[h]);
+            }
+          } else {
+            const uint32_t tpos = (uint32_t)(tq + tt);
+#pragma unroll
+            for (int i = 0; i < S::HALF; ++i) {
+              const float xl = h2f(kr[kc_lo + i]), xh = h2f(kr[kc_lo + D / 2 + i]);
+              float cs, sn;
+              rope_cs(p.rope_turns[kc_lo + i], tpos, cs, sn);
+              const float rl = xl * cs - xh * sn, rh = xh * cs + xl * sn;
+#pragma unroll
+              for (int h = 0; h < HG; ++h)
+                a[h] = fmaf(q_s[h][kc_lo + i], rl, fmaf(q_s[h][kc_lo + D / 2 + i], rh, a[h]));
+            }
           }
 #pragma unroll
           for (int h = 0; h < HG; ++h) sc[j][h] = a[h];
         }
 #pragma unroll
-        for (int j = 0; j < TPL; ++j)
+        for (int j = 0; j < TPL; ++j) {
+          const int tt = stt * 32 + tau + TAU * j;
 #pragma unroll
           for (int h = 0; h < HG; ++h) {
             float a = sc[j][h];
 #pragma unroll
             for (int off = 1; off < KAPPA; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-            sc[j][h] = a * p.qk_scale_log2;
-          }
-      }
-
-      softmax_update(sc);
-
-      // P.V over the value codes of the lane's channel chunk
-      const int gv = vc_lo / p.G;
-#pragma unroll
-      for (int j = 0; j < TPL; ++j) {
-        const int tt = stt * 32 + tau + TAU * j;
-        const uint32_t mv = vm[tt * ng + gv];
-        const float z = h2f((uint16_t)(mv & 0xFFFFu)), s = h2f((uint16_t)(mv >> 16));
-        uint32_t codes[CPL];
-        load_codes<BV, CPL>(vcw + tt * (D * BV / 32), vc_lo * BV, codes);
-#pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          const float pw = sc[j][h];
-          l_run[h] += pw;
-          zsum[h] = fmaf(pw, z, zsum[h]);
-          const float ps = pw * s;
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) acc[h][i] = fmaf(ps, code_to_float(codes[i]), acc[h][i]);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[st]);
-  }
-
-  // fold the value zero-point sums into the accumulators (quantized tokens only)
-#pragma unroll
-  for (int h = 0; h < HG; ++h) {
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) acc[h][i] += zsum[h];
-  }
-
-  // ---------------- fp16 window (last split): tokens Tq .. Tq + n_r - 1
-  if (do_window && !*(volatile int*)&abort_flag) {
-    const int64_t tq = p.n_pages * (int64_t)p.R;
-    const uint16_t* wk = p.wk + (int64_t)unit * p.win_unit_stride;
-    const uint16_t* wv = p.wv + (int64_t)unit * p.win_unit_stride;
-    const int wtiles = (p.n_r + 31) / 32;
-    for (int stt = warp; stt < wtiles; stt += kConsumerWarps) {
-      float sc[TPL][HG];
-#pragma unroll
-      for (int j = 0; j < TPL; ++j) {
-        const int tt = stt * 32 + tau + TAU * j;
-        if (tt >= p.n_r) {
-#pragma unroll
-          for (int h = 0; h < HG; ++h) sc[j][h] = 0.0f;
-          continue;
-        }
-        const uint16_t* kr = wk + (int64_t)tt * D;
-        float a[HG];
-#pragma unroll
-        for (int h = 0; h < HG; ++h) a[h] = 0.0f;
-        if constexpr (!ROPE) {
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) {
-            const float x = h2f(kr[kc_lo + i]);
-#pragma unroll
-            for (int h = 0; h < HG; ++h) a[h] = fmaf(q_s[h][kc_lo + i], x, a[h]);
-          }
-        } else {
-          const uint32_t tpos = (uint32_t)(tq + tt);
-#pragma unroll
-          for (int i = 0; i < S::HALF; ++i) {
-            const float xl = h2f(kr[kc_lo + i]), xh = h2f(kr[kc_lo + D / 2 + i]);
-            float cs, sn;
-            rope_cs(p.rope_turns[kc_lo + i], tpos, cs, sn);
-            const float rl = xl * cs - xh * sn, rh = xh * cs + xl * sn;
-#pragma unroll
-            for (int h = 0; h < HG; ++h) a[h] = fmaf(q_s[h][kc_lo + i], rl, fmaf(q_s[h][kc_lo + D / 2 + i], rh, a[h]));
+            sc[j][h] = tt < p.n_r ? a * p.qk_scale_log2 : -INFINITY;
           }
         }
+        softmax_update(sc);
 #pragma unroll
-        for (int h = 0; h < HG; ++h) sc[j][h] = a[h];
-      }
+        for (int j = 0; j < TPL; ++j) {
+          const int tt = stt * 32 + tau + TAU * j;
+          if (tt >= p.n_r) continue;
+          const uint16_t* vr = wv + (int64_t)tt * D;
 #pragma unroll
-      for (int j = 0; j < TPL; ++j) {
-        const int tt = stt * 32 + tau + TAU * j;
+          for (int h = 0; h < HG; ++h) {
+            const float pw = sc[j][h];
+            st.l[h] += pw;
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          float a = sc[j][h];
-#pragma unroll
-          for (int off = 1; off < KAPPA; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-          sc[j][h] = tt < p.n_r ? a * p.qk_scale_log2 : -INFINITY;
-        }
-      }
-      softmax_update(sc);
-#pragma unroll
-      for (int j = 0; j < TPL; ++j) {
-        const int tt = stt * 32 + tau + TAU * j;
-        if (tt >= p.n_r) continue;
-        const uint16_t* vr = wv + (int64_t)tt * D;
-#pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          const float pw = sc[j][h];
-          l_run[h] += pw;
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) acc[h][i] = fmaf(pw, h2f(vr[vc_lo + i]), acc[h][i]);
+            for (int i = 0; i < CPL; ++i) st.acc[h][i] = fmaf(pw, h2f(vr[vc_lo + i]), st.acc[h][i]);
+          }
         }
       }
     }
   }
-
-  // ---------------- reduce the token slots of the warp, then the warps of the CTA
-#pragma unroll
-  for (int h = 0; h < HG; ++h) {
-#pragma unroll
-    for (int off = KAPPA; off < 32; off <<= 1) {
-      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], off);
-#pragma unroll
-      for (int i = 0; i < CPL; ++i) acc[h][i] += __shfl_xor_sync(0xffffffffu, acc[h][i], off);
-    }
-  }
-  if (tau == 0) {
-#pragma unroll
-    for (int h = 0; h < HG; ++h)
-#pragma unroll
-      for (int i = 0; i < CPL; ++i) wacc[warp][h][vc_lo + i] = acc[h][i];
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int h = 0; h < HG; ++h) {
-      wml[warp][h][0] = m_run[h];
-      wml[warp][h][1] = l_run[h];
-    }
-  }
-  named_barrier_sync(1, kConsumerWarps * 32);
-  // this CTA's partial for (head h, channel c) = (i / D, i % D), i = tid + 128 k
-  constexpr int PER = HG * D / (kConsumerWarps * 32);
-  float pa[PER], pm[PER], pl[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int i = tid + k * kConsumerWarps * 32;
-    const int h = i / D, c = i - h * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wml[w][h][0]);
-    float a = 0.0f, L = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        if (wml[w][h][0] == -INFINITY) continue;
-        const float f = exp2f(wml[w][h][0] - M);
-        a = fmaf(f, wacc[w][h][c], a);
-        L = fmaf(f, wml[w][h][1], L);
-      }
-    }
-    pa[k] = a;
-    pm[k] = M;
-    pl[k] = L;
-  }
-  const int64_t bh0 = (int64_t)b * p.Hq + kvh * HG;
-  if (p.splits == 1) {
-#pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int i = tid + k * kConsumerWarps * 32;
-      p.out[bh0 * D + i] = __half_as_ushort(__float2half_rn(pa[k] / pl[k]));
-    }
-    return;
-  }
-  // publish the partial; the last CTA of the unit to finish merges all splits
-#pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int i = tid + k * kConsumerWarps * 32;
-    const int h = i / D, c = i - h * D;
-    const int64_t slot = (bh0 + h) * p.splits + split;
-    p.part_acc[slot * D + c] = pa[k];
-    if (c == 0) {
-      p.part_ml[slot * 2] = pm[k];
-      p.part_ml[slot * 2 + 1] = pl[k];
-    }
-  }
-  __threadfence();
-  named_barrier_sync(1, kConsumerWarps * 32);
-  if (tid == 0) last_cta = atomicAdd(&p.counters[unit], 1) == p.splits - 1;
-  named_barrier_sync(1, kConsumerWarps * 32);
-  if (!last_cta) return;
-  __threadfence();
-#pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int i = tid + k * kConsumerWarps * 32;
-    const int h = i / D, c = i - h * D;
-    const float* ml = p.part_ml + (bh0 + h) * p.splits * 2;
-    const float* pacc = p.part_acc + (bh0 + h) * p.splits * D + c;
-    float M = -INFINITY;
-    for (int sp = 0; sp < p.splits; ++sp) M = fmaxf(M, __ldcg(ml + 2 * sp));
-    float a = 0.0f, L = 0.0f;
-    for (int sp = 0; sp < p.splits; ++sp) {
-      const float m = __ldcg(ml + 2 * sp);
-      if (m == -INFINITY) continue;
-      const float f = exp2f(m - M);
-      L = fmaf(f, __ldcg(ml + 2 * sp + 1), L);
-      a = fmaf(f, __ldcg(pacc + (int64_t)sp * D), a);
-    }
-    p.out[bh0 * D + i] = __half_as_ushort(__float2half_rn(a / L));
-  }
-  if (tid == 0) p.counters[unit] = 0;  // ready for the next call on this stream
+  if (cur >= 0) epilogue(cur, done);
 }
 
 template <int BK, int BV, int HG, bool ROPE>
-cudaError_t launch_decode_t(const DecodeParams& p, int n_units, cudaStream_t s) {
+cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t s) {
   const size_t smem = (size_t)kStages * p.lay.bytes;
-  auto kern = decode_split_kernel<BK, BV, HG, ROPE>;
+  auto kern = decode_kernel<BK, BV, HG, ROPE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.splits, (unsigned)n_units);
   kern<<<grid, kDecodeThreads, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+template <int BK, int BV, int HG, bool ROPE>
+int resident_t(int page_bytes) {
+  const size_t smem = (size_t)kStages * page_bytes;
+  auto kern = decode_kernel<BK, BV, HG, ROPE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDecodeThreads, smem) != cudaSuccess) return 0;
+  return n;
 }
 
 }  // namespace
@@ -581,11 +785,19 @@ bool decode_supported(int bk, int bv, int hg, bool rope) {
   return false;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool rope, int n_units, cudaStream_t s,
+int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int page_bytes) {
+#define KVQ_RES(BKV, BVV, HGV, RP) \
+  if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return resident_t<BKV, BVV, HGV, RP>(page_bytes);
+  KVQ_DECODE_CASES(KVQ_RES)
+#undef KVQ_RES
+  return 0;
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool rope, int grid, cudaStream_t s,
                           bool* supported) {
   *supported = true;
 #define KVQ_DEC(BKV, BVV, HGV, RP) \
-  if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return launch_decode_t<BKV, BVV, HGV, RP>(p, n_units, s);
+  if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return launch_decode_t<BKV, BVV, HGV, RP>(p, grid, s);
   KVQ_DECODE_CASES(KVQ_DEC)
 #undef KVQ_DEC
   *supported = false;

@@ -67,16 +67,19 @@ struct DecodeParams {
   const uint16_t* wk;       // window [units][R][D]
   const uint16_t* wv;
   int64_t win_unit_stride;  // elements
+  int64_t n_units;          // B * Hkv
   int64_t n_pages;          // quantized pages per unit (Tq / R)
+  int32_t work_per_unit;    // n_pages + (n_r > 0): page items then the window item
   int32_t n_r;              // window tokens
-  int32_t splits;
+  int32_t max_slots;        // partial slots per query head
   int32_t Hkv, Hq, D, G, R, nsp;
+  int32_t log2G;            // G = 1 << log2G
   PageLayout lay;
   float qk_scale_log2;      // softmax_scale * log2(e)
   const unsigned long long* rope_turns;  // [D/2] theta_i / (2*pi) as 0.64 fixed point (rope only)
-  float* part_ml;           // [B*Hq][splits][2]  (running max in log2 units, sum)
-  float* part_acc;          // [B*Hq][splits][D]
-  int* counters;            // [B*Hkv] finished splits, zero between calls
+  float* part_ml;           // [B*Hq][max_slots][2]  (running max in log2 units, sum)
+  float* part_acc;          // [B*Hq][max_slots][D]
+  int* counters;            // [B*Hkv] items finished per unit, zero between calls
   uint16_t* out;            // [B][Hq][D] fp16 bits
   int* err;
 };
@@ -84,8 +87,9 @@ struct DecodeParams {
 // Launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_quantize(const QuantizeParams& p, int bk, int bv, int n_pages, cudaStream_t s);
 cudaError_t launch_copy_tokens(const CopyTokensParams& p, cudaStream_t s);
-cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool rope, int n_units, cudaStream_t s,
+cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool rope, int grid, cudaStream_t s,
                           bool* supported);
+int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int page_bytes);
 bool decode_supported(int bk, int bv, int hg, bool rope);
 bool quantize_supported(int bk, int bv);
 size_t quantize_smem_bytes(int R, int D, const PageLayout& lay);

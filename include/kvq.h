@@ -172,13 +172,16 @@ kvq_status kvq_unit_sizes(const kvq_cache* cache, kvq_unit_view* sizes);
 kvq_status kvq_export_unit(kvq_cache* cache, int32_t b, int32_t kvh, kvq_unit_view* dst, void* cuda_stream);
 
 /*
- * Force the number of token splits per (batch, kv head) used by decode
- * attention (0 = automatic, from the SM count and the cache length).  Values
- * above the workspace capacity are clamped.  Test and tuning aid.
+ * Decode work partition.  Decode attention runs as one persistent launch whose
+ * CTAs take equal contiguous slices of the list of all units' pages (plus one
+ * window item per unit); by default the grid is the number of CTAs the GPU
+ * keeps resident.  kvq_set_splits(n) with n > 0 forces a grid of n CTAs per
+ * (batch, kv head) unit instead (clamped to 16; 0 restores the default) -- a
+ * test and tuning aid that changes where units are cut, not the result
+ * beyond rounding.  kvq_get_splits reports the CTAs per unit (rounded up) of
+ * the next decode.
  */
 kvq_status kvq_set_splits(kvq_cache* cache, int32_t splits);
-
-/* Splits the next decode will use for the current state. */
 kvq_status kvq_get_splits(const kvq_cache* cache, int32_t* splits);
 
 /*
