@@ -142,6 +142,12 @@ unsigned long long rope_turn_fraction(double base, int i, int D) {
 
 namespace kvq {
 
+kvq_status check_config(const kvq_config& cfg) { return validate(cfg); }
+
+void rope_table(double base, int D, unsigned long long* out) {
+  for (int i = 0; i < D / 2; ++i) out[i] = rope_turn_fraction(base, i, D);
+}
+
 PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp) {
   auto r16 = [](int64_t x) { return (int32_t)((x + 15) / 16 * 16); };
   PageLayout l{};

@@ -18,6 +18,8 @@
 
 #include <cuda_runtime.h>
 
+#include "kvq.h"
+
 namespace kvq {
 
 constexpr int kHeadDim = 128;
@@ -27,6 +29,12 @@ struct PageLayout {
 };
 
 PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp);
+
+// Host-side validation of a configuration (the checks kvq_create applies).
+kvq_status check_config(const kvq_config& cfg);
+
+// theta_i / (2 pi) as 0.64 fixed-point turns, theta_i = base^(-2i/D), i < D/2.
+void rope_table(double base, int D, unsigned long long* out);
 
 // Device error codes written by kernels into the cache's error word.
 enum DeviceError : int {

@@ -64,6 +64,8 @@ SIGNATURES = {
     "kvq_append": (ctypes.c_int, [_P, _P, _P, _P]),
     "kvq_decode_attention": (ctypes.c_int, [_P, _P, _P, _P]),
     "kvq_reset": (ctypes.c_int, [_P]),
+    "kvq_decode_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(kvq_config), _P, ctypes.c_int64, _P, _P,
+                                                    ctypes.c_int64, _P, _P, _P]),
     "kvq_get_state": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
                                      ctypes.POINTER(ctypes.c_int32)]),
     "kvq_unit_sizes": (ctypes.c_int, [_P, ctypes.POINTER(kvq_unit_view)]),
@@ -154,6 +156,14 @@ def kvq_append(handle, k, v, stream=None) -> None:
 
 def kvq_decode_attention(handle, q, out, stream=None) -> None:
     _check(lib().kvq_decode_attention(handle, _ptr(q), _ptr(out), _stream(stream)), "kvq_decode_attention")
+
+
+def kvq_decode_attention_noalloc(cfg: kvq_config, pages, pages_per_unit: int, window_k, window_v, n_tokens: int,
+                                 q, out, stream=None) -> None:
+    """Decode attention over caller-owned packed buffers, with no device allocation (see include/kvq.h)."""
+    _check(lib().kvq_decode_attention_noalloc(ctypes.byref(cfg), _ptr(pages), pages_per_unit, _ptr(window_k),
+                                              _ptr(window_v), n_tokens, _ptr(q), _ptr(out), _stream(stream)),
+           "kvq_decode_attention_noalloc")
 
 
 def kvq_reset(handle) -> None:

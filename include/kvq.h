@@ -137,6 +137,48 @@ kvq_status kvq_decode_attention(kvq_cache* cache, const void* q_f16, void* out_f
  */
 kvq_status kvq_reset(kvq_cache* cache);
 
+/*
+ * Decode attention with no device allocation, over packed buffers the caller
+ * owns.  (The method pages have no counterpart for this entry point.)
+ *
+ * For callers that cannot allocate device memory when they run attention --
+ * an engine that carves all GPU memory from its own pool and does not let
+ * libraries allocate, or a latency-critical path that must not enter the
+ * allocator -- and that therefore keep the cache in their own buffers instead
+ * of a kvq_cache.  It computes exactly what kvq_decode_attention computes for
+ * a cache holding n_tokens tokens in the layout below; the split-attention
+ * partials, which kvq_decode_attention keeps in each cache's workspace, live
+ * in one 8 MiB file-scope device array inside the library instead (every GPU
+ * that loads the library holds it until the process exits).
+ *
+ *   cfg            a configuration kvq_create would accept
+ *   pages          device, [B*Hkv][pages_per_unit][page_bytes]; page p of a unit
+ *                  holds tokens [p*R, p*R+R) as consecutive sections, each padded
+ *                  to a multiple of 16 bytes: key codes [R][D*k_bits/32] u32
+ *                  (token-major bitstream as in kvq_unit_view), key zero
+ *                  point/scale [R/G][D] u32 (fp16 zero point in the low half,
+ *                  scale in the high half), value codes [R][D*v_bits/32] u32,
+ *                  value zero point/scale [R][D/G] u32, sparse channels [R][k_sparse]
+ *                  u8, sparse values [R][k_sparse] fp16
+ *   window_k/_v    device fp16 [B*Hkv][R][D]; slots 0..n_r-1 hold the newest tokens
+ *   n_tokens       cached tokens T >= 1: Tq = R*floor((T-1)/R) are in the pages,
+ *                  n_r = T - Tq in the window
+ *   q_f16, out_f16 device fp16 [B][Hq][D]
+ *
+ * Errors: KVQ_ERR_INVALID_ARG (nulls, misalignment, Tq/R > pages_per_unit),
+ * KVQ_ERR_UNSUPPORTED, and KVQ_ERR_CAPACITY when B*Hq*(D+2)*8 bytes (two
+ * partial slices per query head) plus the per-unit counters exceed the 8 MiB
+ * array.  The device is the current one.  The first call on a device looks up
+ * the array's address once (a runtime symbol lookup), so make that first call
+ * before any stream capture.  Every call shares the one array: it clears the
+ * counters it needs at the start of each call, but calls whose work overlaps
+ * on the GPU (different streams, or several host threads) race on it.
+ * Nothing is allocated and no allocator is called.
+ */
+kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const void* pages, int64_t pages_per_unit,
+                                        const void* window_k, const void* window_v, int64_t n_tokens,
+                                        const void* q_f16, void* out_f16, void* cuda_stream);
+
 /* ---------------- helpers (not on the hot path) ---------------- */
 
 /* Host-tracked state: tokens cached, tokens quantized (Tq), tokens in the window. */
