@@ -205,7 +205,7 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   c->sm_count = prop.multiProcessorCount;
   const int D = cfg->head_dim, R = cfg->residual, G = cfg->group_size;
   c->lay = kvq::make_layout(R, D, G, cfg->k_bits, cfg->v_bits, cfg->k_sparse);
-  if (kvq::quantize_smem_bytes(R, D, c->lay) > (size_t)prop.sharedMemPerBlockOptin) {
+  if (kvq::quantize_smem_bytes(R, D, G, c->lay) > (size_t)prop.sharedMemPerBlockOptin) {
     delete c;
     return KVQ_ERR_UNSUPPORTED;
   }

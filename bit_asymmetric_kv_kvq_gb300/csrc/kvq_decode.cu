@@ -280,9 +280,12 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
       float tmax = sc[0][h];
 #pragma unroll
       for (int j = 1; j < TPL; ++j) tmax = fmaxf(tmax, sc[j][h]);
+      // the running maximum only moves when a score passes it by the lazy threshold: a vote
+      // settles the common case without a reduction
+      const bool over = tmax > st.m[h] + kLazyRescale || (st.m[h] == -INFINITY && tmax != -INFINITY);
+      if (__any_sync(0xffffffffu, over)) {
 #pragma unroll
-      for (int off = KAPPA; off < 32; off <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-      if (tmax > st.m[h] + kLazyRescale || (st.m[h] == -INFINITY && tmax != -INFINITY)) {
+        for (int off = KAPPA; off < 32; off <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
         const float mnew = fmaxf(tmax, st.m[h]);
         const float f = st.m[h] == -INFINITY ? 0.0f : exp2f(st.m[h] - mnew);
         st.l[h] *= f;
@@ -491,10 +494,6 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
               zp[h] = fmaf(q_s[h][c], z, zp[h]);
             }
           }
-#pragma unroll
-          for (int h = 0; h < HG; ++h)
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) zp[h] += __shfl_xor_sync(0xffffffffu, zp[h], off);
           __syncwarp();
           float qp[HG][CPL];
 #pragma unroll
@@ -517,7 +516,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
               using MC = MaskCodes<S::KBITS_FAST>;
               constexpr int NW = CPL * BK / 32;
               const uint32_t* rec = kc + tt * (D * BK / 32) + kap * NW;
-              float2 a2 = make_float2(0.0f, 0.0f);
+              // four independent partial sums keep the packed FMA chains short
+              float2 a2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                              make_float2(0.0f, 0.0f)};
               const float2 magic = make_float2(-8388608.0f, -8388608.0f);
 #pragma unroll
               for (int wi = 0; wi < NW; ++wi) {
@@ -527,10 +528,12 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
                 for (int m = 0; m < MC::PER_WORD / 2; ++m) {
                   const int i = wi * MC::PER_WORD + 2 * m;
                   const float2 v = __fadd2_rn(make_float2(f[2 * m], f[2 * m + 1]), magic);
-                  a2 = __ffma2_rn(v, make_float2(qp[0][i], qp[0][i + 1]), a2);
+                  a2[m & 3] = __ffma2_rn(v, make_float2(qp[0][i], qp[0][i + 1]), a2[m & 3]);
                 }
               }
-              sc[j][0] = a2.x + a2.y;
+              const float2 s01 = __fadd2_rn(a2[0], a2[1]), s23 = __fadd2_rn(a2[2], a2[3]);
+              const float2 s03 = __fadd2_rn(s01, s23);
+              sc[j][0] = s03.x + s03.y;
             } else {
               uint32_t codes[CPL];
               load_codes<BK, CPL>(kc + tt * (D * BK / 32), kc_lo * BK, codes);
@@ -553,6 +556,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
               }
             }
           }
+          // the group constant Z (reduced here, off the path of the code products)
+#pragma unroll
+          for (int h = 0; h < HG; ++h)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) zp[h] += __shfl_xor_sync(0xffffffffu, zp[h], off);
           // sum the channel chunks of each token, then add the group constant
 #pragma unroll
           for (int j = 0; j < TPL; ++j)

@@ -100,6 +100,6 @@ cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool ro
 int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int page_bytes);
 bool decode_supported(int bk, int bv, int hg, bool rope);
 bool quantize_supported(int bk, int bv);
-size_t quantize_smem_bytes(int R, int D, const PageLayout& lay);
+size_t quantize_smem_bytes(int R, int D, int G, const PageLayout& lay);
 
 }  // namespace kvq

@@ -17,9 +17,19 @@
 // with z and s the stored fp16 values.  A zero minimum is stored as +0 and a
 // zero range gives s = +0 and codes 0.
 //
+// The quotient (x - z) / s only matters through rint, so it is formed as
+// (x - z) * (1/s) with a per-group reciprocal.  That product is within 2^-18
+// of the correctly rounded quotient (|quotient| <= 16, two roundings of at
+// most 2^-24 relative each); when it lies within 2^-14 of a half-integer --
+// the only place where the two could round differently, ties included -- the
+// code takes the IEEE quotient instead.  So every code equals the one the
+// true division gives, at the cost of one multiply for all but ~1e-4 of the
+// elements.
+//
 // Data movement: the two fp16 input tiles (R x D each) arrive by bulk copy
-// into shared memory, the page is assembled in shared memory and leaves by
-// one bulk copy, so all global traffic is 16-byte granular and contiguous.
+// into shared memory, each thread computes and packs whole 32-bit code words
+// straight from the tile, the page is assembled in shared memory and leaves
+// by one bulk copy, so all global traffic is 16-byte granular and contiguous.
 #include <cuda_fp16.h>
 
 #include "kvq_internal.h"
@@ -32,52 +42,95 @@ namespace {
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 __device__ __forceinline__ uint16_t f2h(float f) { return __half_as_ushort(__float2half_rn(f)); }
 
-struct GroupQuant {
-  uint16_t zb, sb;
-  float zf, sf;
+// Per-group quantizer: fp32 zero point and scale as stored (fp16 widened), the
+// reciprocal of the scale, and the two fp16 bit patterns (zero low, scale high).
+struct __align__(16) GroupQ {
+  float zf, sf, inv;
+  uint32_t bits;
 };
 
 // Zero point and scale of a group from its exact min and max.
-__device__ __forceinline__ GroupQuant group_params(float mn, float mx, int L) {
-  GroupQuant g;
+__device__ __forceinline__ GroupQ group_params(float mn, float mx, int L) {
+  GroupQ g;
   mn = __fadd_rn(mn, 0.0f);  // -0 -> +0
   float range = __fsub_rn(mx, mn);
   if (!(range > 0.0f)) range = 0.0f;
   const float s32 = __fdiv_rn(range, (float)L);
-  g.zb = f2h(mn);
-  g.sb = f2h(s32);
-  g.zf = h2f(g.zb);
-  g.sf = h2f(g.sb);
+  const uint16_t zb = f2h(mn), sb = f2h(s32);
+  g.zf = h2f(zb);
+  g.sf = h2f(sb);
+  g.inv = g.sf > 0.0f ? __frcp_rn(g.sf) : 0.0f;
+  g.bits = (uint32_t)zb | ((uint32_t)sb << 16);
   return g;
 }
 
-__device__ __forceinline__ uint8_t quant_code(float x, float zf, float sf, int L) {
-  if (sf == 0.0f) return 0;
-  const float d = __fsub_rn(x, zf);
-  float q = rintf(__fdiv_rn(d, sf));
+__device__ __forceinline__ uint32_t quant_code(float x, const GroupQ& g, int L) {
+  if (g.sf == 0.0f) return 0;
+  const float d = __fsub_rn(x, g.zf);
+  float r = __fmul_rn(d, g.inv);
+  const float frac = r - floorf(r);
+  if (fabsf(frac - 0.5f) <= 0x1.0p-14f) r = __fdiv_rn(d, g.sf);  // near a rounding tie: exact quotient
+  float q = rintf(r);
   q = fminf(fmaxf(q, 0.0f), (float)L);
-  return (uint8_t)q;
-}
-
-// Pack one bitstream word: bits [32w, 32w+32) of a row of byte codes.
-template <int BITS>
-__device__ __forceinline__ uint32_t pack_word(const uint8_t* row, int w) {
-  const int first = (32 * w) / BITS;
-  const int last = (32 * w + 31) / BITS;
-  uint32_t word = 0;
-  for (int i = first; i <= last; ++i) {
-    const int b = i * BITS - 32 * w;
-    const uint32_t c = row[i];
-    word |= b >= 0 ? (c << b) : (c >> (-b));
-  }
-  return word;
+  return (uint32_t)q;
 }
 
 constexpr int kQuantThreads = 256;
 constexpr int kMaxSparse = 4;
 
+// Shared-memory plan of one CTA (bytes, all 16-byte aligned).
+struct QuantSmem {
+  size_t kt, vt, kq, vq, sidx, pg, total;
+};
+
+__host__ __device__ inline QuantSmem quant_smem(int R, int D, int G, int page_bytes) {
+  QuantSmem m;
+  m.kt = 0;
+  m.vt = m.kt + (size_t)R * D * 2;
+  m.kq = m.vt + (size_t)R * D * 2;
+  m.vq = m.kq + (size_t)(R / G) * D * sizeof(GroupQ);
+  m.sidx = m.vq + (size_t)R * (D / G) * sizeof(GroupQ);
+  m.pg = m.sidx + (((size_t)R * kMaxSparse + 15) / 16) * 16;
+  m.total = m.pg + (size_t)page_bytes;
+  return m;
+}
+
+// Key quantizers are stored interleaved by 32-channel chunk: channel c = 32*ch + i
+// lives at slot i*NCH + ch, so the threads of a warp, which take consecutive
+// chunks, read consecutive slots.
+constexpr int kChunk = 32;
+__device__ __forceinline__ int kq_slot(int c) { return (c % kChunk) * (kHeadDim / kChunk) + c / kChunk; }
+
+// Codes of 32 consecutive channels of one token (x: 32 fp16 values, 16-byte aligned),
+// packed into BITS words of the token's bitstream.  grp(i) is the quantizer of channel
+// i of the chunk; excl has bit i set for an excluded channel (code 0).
+template <int BITS, class Params>
+__device__ __forceinline__ void pack_chunk(const uint16_t* x, const Params& grp, uint32_t excl, uint32_t* out) {
+  constexpr int L = (1 << BITS) - 1;
+  uint32_t w[BITS];
+#pragma unroll
+  for (int k = 0; k < BITS; ++k) w[k] = 0;
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+#pragma unroll
+  for (int q4 = 0; q4 < kChunk / 8; ++q4) {
+    const uint4 v = xv[q4];
+    const uint32_t pair[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = q4 * 8 + j;
+      const uint16_t bits = (uint16_t)(j & 1 ? pair[j >> 1] >> 16 : pair[j >> 1] & 0xFFFFu);
+      const uint32_t code = (excl >> i) & 1u ? 0u : quant_code(h2f(bits), grp(i), L);
+      const int b = i * BITS;
+      w[b >> 5] |= code << (b & 31);
+      if ((b & 31) + BITS > 32) w[(b >> 5) + 1] |= code >> (32 - (b & 31));
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < BITS; ++k) out[k] = w[k];
+}
+
 template <int BK, int BV>
-__global__ void __launch_bounds__(kQuantThreads) quantize_pages_kernel(const QuantizeParams p) {
+__global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const QuantizeParams p) {
   const int page = blockIdx.x;
   const int unit = blockIdx.y;
   const int D = p.D, R = p.R, G = p.G, nsp = p.nsp;
@@ -86,15 +139,14 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pages_kernel(const Qua
   constexpr int LK = (1 << BK) - 1, LV = (1 << BV) - 1;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t* kt = reinterpret_cast<uint16_t*>(smem);              // [R][D]
-  uint16_t* vt = kt + R * D;                                      // [R][D]
-  uint8_t* kc8 = reinterpret_cast<uint8_t*>(vt + R * D);          // [R][D]
-  uint8_t* vc8 = kc8 + R * D;                                     // [R][D]
-  float* kzs = reinterpret_cast<float*>(vc8 + R * D);             // [R/G][D][2]
-  uint8_t* sidx = reinterpret_cast<uint8_t*>(kzs + 2 * (R / G) * D);  // [R][kMaxSparse]
-  uint8_t* pg = sidx + R * kMaxSparse;                            // page image (16-byte aligned: see smem size)
+  const QuantSmem sm = quant_smem(R, D, G, p.lay.bytes);
+  uint16_t* kt = reinterpret_cast<uint16_t*>(smem + sm.kt);  // [R][D]
+  uint16_t* vt = reinterpret_cast<uint16_t*>(smem + sm.vt);  // [R][D]
+  GroupQ* kq = reinterpret_cast<GroupQ*>(smem + sm.kq);      // [R/G][D]
+  GroupQ* vq = reinterpret_cast<GroupQ*>(smem + sm.vq);      // [R][D/G]
+  uint8_t* sidx = smem + sm.sidx;                            // [R][kMaxSparse]
+  uint8_t* pg = smem + sm.pg;                                // page image
   __shared__ __align__(8) uint64_t bar;
-  __shared__ int failed;
 
   const int64_t tok0 = p.src_tok0 + (int64_t)page * R;
   const uint16_t* ksrc = p.k_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
@@ -102,7 +154,6 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pages_kernel(const Qua
   uint8_t* dst = p.pages + (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)p.lay.bytes;
 
   if (tid == 0) {
-    failed = 0;
     mbar_init(&bar, 1);
     fence_mbar_init();
   }
@@ -176,19 +227,21 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pages_kernel(const Qua
     for (int i = sv_used + tid; i < p.lay.bytes - p.lay.off_sv; i += kQuantThreads) pg[p.lay.off_sv + i] = 0;
     __syncthreads();
   }
+  auto excluded = [&](int t, int c) {
+    if (nsp == 0) return false;
+    bool ex = false;
+    for (int k = 0; k < nsp; ++k) ex |= sidx[t * kMaxSparse + k] == c;
+    return ex;
+  };
 
-  // ---- keys: one (zero point, scale) per (G-token group, channel)
+  // ---- keys: one quantizer per (G-token group, channel)
   const int ngk = R / G;
   for (int idx = tid; idx < ngk * D; idx += kQuantThreads) {
     const int g = idx / D, c = idx - g * D;
     bool any = false;
     float mn = 0.0f, mx = 0.0f;
     for (int t = g * G; t < g * G + G; ++t) {
-      if (nsp > 0) {
-        bool ex = false;
-        for (int k = 0; k < nsp; ++k) ex |= sidx[t * kMaxSparse + k] == c;
-        if (ex) continue;
-      }
+      if (excluded(t, c)) continue;
       const float v = h2f(kt[t * D + c]);
       if (!any) {
         mn = v;
@@ -199,26 +252,17 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pages_kernel(const Qua
         mx = v > mx ? v : mx;
       }
     }
-    const GroupQuant q = group_params(mn, mx, LK);
-    reinterpret_cast<uint32_t*>(pg + p.lay.off_km)[g * D + c] = (uint32_t)q.zb | ((uint32_t)q.sb << 16);
-    kzs[2 * idx] = q.zf;
-    kzs[2 * idx + 1] = q.sf;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < R * D; idx += kQuantThreads) {
-    const int t = idx / D, c = idx - t * D;
-    const int gi = (t / G) * D + c;
-    bool ex = false;
-    if (nsp > 0)
-      for (int k = 0; k < nsp; ++k) ex |= sidx[t * kMaxSparse + k] == c;
-    kc8[idx] = ex ? 0 : quant_code(h2f(kt[idx]), kzs[2 * gi], kzs[2 * gi + 1], LK);
+    const GroupQ q = group_params(mn, mx, LK);
+    kq[g * D + kq_slot(c)] = q;
+    reinterpret_cast<uint32_t*>(pg + p.lay.off_km)[idx] = q.bits;
   }
 
-  // ---- values: one (zero point, scale) per (token, G-channel group); a warp per token,
+  // ---- values: one quantizer per (token, G-channel group); a warp per token,
   //      4 consecutive channels per lane, G/4 lanes per group
   {
     const int lanes_per_group = G / 4;
     const int c0 = lane * 4;
+    const int ng = D / G;
     for (int t = warp; t < R; t += kQuantThreads / 32) {
       float x[4];
 #pragma unroll
@@ -235,29 +279,38 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pages_kernel(const Qua
         mn = omn < mn ? omn : mn;
         mx = omx > mx ? omx : mx;
       }
-      const GroupQuant q = group_params(mn, mx, LV);
       if ((lane & (lanes_per_group - 1)) == 0) {
+        const GroupQ q = group_params(mn, mx, LV);
         const int g = c0 / G;
-        reinterpret_cast<uint32_t*>(pg + p.lay.off_vm)[t * (D / G) + g] = (uint32_t)q.zb | ((uint32_t)q.sb << 16);
+        vq[t * ng + g] = q;
+        reinterpret_cast<uint32_t*>(pg + p.lay.off_vm)[t * ng + g] = q.bits;
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) vc8[t * D + c0 + i] = quant_code(x[i], q.zf, q.sf, LV);
     }
   }
   __syncthreads();
 
-  // ---- pack both code planes into their bitstreams
+  // ---- codes, computed and packed a 32-channel chunk (BITS words) at a time
   {
+    constexpr int NCH = kHeadDim / kChunk;
     constexpr int WKW = kHeadDim * BK / 32, WVW = kHeadDim * BV / 32;
     uint32_t* kc = reinterpret_cast<uint32_t*>(pg + p.lay.off_kc);
     uint32_t* vc = reinterpret_cast<uint32_t*>(pg + p.lay.off_vc);
-    for (int idx = tid; idx < R * WKW; idx += kQuantThreads) {
-      const int t = idx / WKW, w = idx - t * WKW;
-      kc[idx] = pack_word<BK>(kc8 + t * D, w);
+    for (int idx = tid; idx < R * NCH; idx += kQuantThreads) {
+      const int t = idx / NCH, ch = idx - t * NCH;
+      uint32_t excl = 0;
+      for (int k = 0; k < nsp; ++k) {
+        const int c = sidx[t * kMaxSparse + k] - ch * kChunk;
+        if (c >= 0 && c < kChunk) excl |= 1u << c;
+      }
+      const GroupQ* gq = kq + (t / G) * D + ch;
+      pack_chunk<BK>(kt + t * D + ch * kChunk, [&](int i) -> const GroupQ& { return gq[i * NCH]; }, excl,
+                     kc + t * WKW + ch * BK);
     }
-    for (int idx = tid; idx < R * WVW; idx += kQuantThreads) {
-      const int t = idx / WVW, w = idx - t * WVW;
-      vc[idx] = pack_word<BV>(vc8 + t * D, w);
+    const int ng = D / G;
+    for (int idx = tid; idx < R * NCH; idx += kQuantThreads) {
+      const int t = idx / NCH, ch = idx - t * NCH;
+      const GroupQ& gq = vq[t * ng + (ch * kChunk) / G];
+      pack_chunk<BV>(vt + t * D + ch * kChunk, [&](int) -> const GroupQ& { return gq; }, 0u, vc + t * WVW + ch * BV);
     }
   }
   fence_proxy_async_smem();
@@ -284,7 +337,7 @@ __global__ void copy_tokens_kernel(const CopyTokensParams p) {
 
 template <int BK, int BV>
 cudaError_t launch_quantize_t(const QuantizeParams& p, int n_pages, cudaStream_t s) {
-  const size_t smem = quantize_smem_bytes(p.R, p.D, p.lay);
+  const size_t smem = quantize_smem_bytes(p.R, p.D, p.G, p.lay);
   auto kern = quantize_pages_kernel<BK, BV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -295,12 +348,7 @@ cudaError_t launch_quantize_t(const QuantizeParams& p, int n_pages, cudaStream_t
 
 }  // namespace
 
-size_t quantize_smem_bytes(int R, int D, const PageLayout& lay) {
-  // fp16 tiles, byte codes, per-group (z, s) floats, sparse index table, page image
-  size_t b = (size_t)R * D * 2 * 2 + (size_t)R * D * 2 + (size_t)2 * R * D * 4 / 32 + (size_t)R * kMaxSparse;
-  b = (b + 15) & ~(size_t)15;
-  return b + (size_t)lay.bytes;
-}
+size_t quantize_smem_bytes(int R, int D, int G, const PageLayout& lay) { return quant_smem(R, D, G, lay.bytes).total; }
 
 bool quantize_supported(int bk, int bv) { return bk >= 2 && bk <= 4 && bv >= 2 && bv <= 4; }
 

@@ -192,3 +192,46 @@ def test_append_on_empty_cache_acts_as_prefill():
             check_attention(w, units, q, out, f"t={t}")
     assert cache.state() == (200, 128, 72)
     cache.close()
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_quantizer_rounding_ties(bits):
+    """Values exactly on half steps, and one fp16 ulp either side, quantize as the oracle's true division."""
+    kvq = _kvq()
+    L = 2 ** bits - 1
+    D, R, G = 128, 128, 32
+    T = R + 1
+    rng = np.random.default_rng(bits)
+    K = np.zeros((T, D), np.float64)
+    V = np.zeros((T, D), np.float64)
+    for c in range(D):
+        z = float(rng.integers(-64, 64)) * 0.25
+        s = [1.0, 0.5, 2.0, 0.125][c % 4]
+        k = rng.integers(0, L, T)
+        vals = z + s * (k + 0.5)                       # exact ties
+        nudge = rng.integers(-1, 2, T)                 # -1, 0, +1 ulp
+        vals = np.where(nudge == 0, vals, np.nextafter(vals.astype(np.float16), np.where(nudge > 0, np.inf, -np.inf)
+                                                       ).astype(np.float64))
+        vals[::G] = z                                  # every group holds its min and max
+        vals[1::G] = z + s * L
+        K[:, c] = vals
+    for t in range(T):
+        z = float(rng.integers(-64, 64)) * 0.25
+        s = [1.0, 0.5, 0.25, 2.0][t % 4]
+        k = rng.integers(0, L, D)
+        vals = z + s * (k + 0.5)
+        vals[::G] = z
+        vals[1::G] = z + s * L
+        V[t] = vals
+    K16 = K.astype(np.float16).reshape(1, 1, T, D)
+    V16 = V.astype(np.float16).reshape(1, 1, T, D)
+    w = synth.WORKLOADS[0].scaled(batch=1, kv_heads=1, q_heads=1, prefill_tokens=T, decode_steps=1,
+                                  k_bits=bits, v_bits=bits)
+    cache = kvq.KVCache.for_workload(w)
+    cache.prefill_quantize(_dev(K16), _dev(V16))
+    u = oracle.OracleUnit.for_workload(w)
+    u.prefill(K16[0, 0], V16[0, 0])
+    compare_stores(cache, {(0, 0): u}, 0, 0, f"ties {bits}-bit")
+    # the crafted values really do sit on ties: the oracle's codes are even there
+    assert cache.sync_status() == 0
+    cache.close()
