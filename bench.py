@@ -351,12 +351,7 @@ def run_ours(args, dist):
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak = peaks.get("hbm_gbs", 6800.0)
     achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
-    traffic_path = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    traffic = None
-    if os.path.exists(traffic_path):
-        t = _json.load(open(traffic_path))
-        if t.get("workload") == w.name and t.get("kernel_rev") == kernel_revision():
-            traffic = t.get("bytes_per_launch")
+    traffic = decode_traffic(w)
 
     # ---------------- end to end through the C ABI from pinned host memory
     e2e = run_e2e(args, w, dist, caches, stream) if args.e2e_steps > 0 else None
@@ -369,7 +364,7 @@ def run_ours(args, dist):
     return {
         "value": value, "ms_per_step": ms_step, "gpu_launches": int(n_launch),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": "decode attention (decode_split_kernel)",
+                     "traffic": traffic, "kernel": "decode attention (decode_kernel)",
                      "bytes_per_launch": dec_bytes, "ms_per_launch": dec_ms,
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6.8 TB/s"},
         "decode_only": {"value": B * statistics.mean(T0 + 1 + i for i in range(S)) / (dec_ms * 1e-3),
@@ -379,14 +374,38 @@ def run_ours(args, dist):
     }
 
 
+DECODE_SOURCES = ("kvq_decode.cu", "kvq_ptx.cuh", "kvq_internal.h")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
+
+
 def kernel_revision():
-    """Hash of the CUDA sources: traffic counters are only valid for the kernel they were taken on."""
+    """Hash of the decode kernel's sources: DRAM counters are valid only for the kernel they were taken on."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_asymmetric_kv_kvq_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in DECODE_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def decode_traffic(w):
+    """DRAM read+write bytes per decode launch from the committed ncu summary, or None.
+
+    The summary holds `key: value` lines; its figure counts only when it was taken
+    on this workload and on the current decode kernel sources."""
+    if not os.path.exists(TRAFFIC_SUMMARY):
+        return None
+    kv = {}
+    for line in open(TRAFFIC_SUMMARY):
+        if ":" in line and not line.startswith((" ", "#")):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("workload") != w.name or kv.get("kernel_rev") != kernel_revision():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def run_e2e(args, w, dist, caches, stream):
