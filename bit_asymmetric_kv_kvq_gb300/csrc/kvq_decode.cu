@@ -55,25 +55,34 @@ __device__ __forceinline__ float code_to_float(uint32_t code) {
   return __uint_as_float(0x4B000000u | code) - 8388608.0f;
 }
 
-// Codes of one 32-bit word of a B-bit bitstream as floats without a shift per
-// code: OR-ing the masked code into the mantissa of 2^23 gives 2^23 + 2^(B*p)*code
-// exactly for the first NDIRECT positions p; the rest are read the same way
-// from the word shifted right by NDIRECT*B.  Callers subtract 2^23 (exact) and
-// fold 2^(-B*p) into the other factor.
+// Power of two that the fast paths keep their products scaled by (see MaskCodes).
+constexpr int kCodeExp = 64;
+
+// Codes of one 32-bit word of a B-bit bitstream as fp32 subnormals, one logic
+// op per code: masking the code at position p in place gives the float
+// code * 2^(B*p) * 2^-149 exactly for the first NDIRECT positions (they fit in
+// the 23 mantissa bits); the rest are read the same way from the word shifted
+// right by NDIRECT*B.  The factor each code multiplies carries
+// scale_in(p) = 2^(149 - kCodeExp - B*p), so every product is
+// code * factor * 2^-kCodeExp, a normal number, with no offset to remove;
+// scale_out(p) = 2^(kCodeExp - B*p) undoes the position scale of an
+// accumulator that summed subnormal codes against unscaled factors.
 template <int BITS>
 struct MaskCodes {
   static constexpr int PER_WORD = 32 / BITS;
   static constexpr int NDIRECT = BITS == 2 ? 11 : 5;  // (2^B - 1) * 2^(B*(n-1)) < 2^23
   static constexpr uint32_t MASK = (1u << BITS) - 1u;
   __device__ static constexpr int pos(int i) { return i < NDIRECT ? i : i - NDIRECT; }
-  // 2^(-B*p) for the code at index i of a word
-  __device__ static float unscale(int i) { return __uint_as_float((uint32_t)(127 - BITS * pos(i)) << 23); }
+  __device__ static float scale_in(int i) {
+    return __uint_as_float((uint32_t)(127 + 149 - kCodeExp - BITS * pos(i)) << 23);
+  }
+  __device__ static float scale_out(int i) { return __uint_as_float((uint32_t)(127 + kCodeExp - BITS * pos(i)) << 23); }
   __device__ __forceinline__ static void to_float(uint32_t w, float (&f)[PER_WORD]) {
     const uint32_t ws = w >> (NDIRECT * BITS);
 #pragma unroll
     for (int i = 0; i < PER_WORD; ++i) {
       const uint32_t src = i < NDIRECT ? w : ws;
-      f[i] = __uint_as_float((src & (MASK << (BITS * pos(i)))) | 0x4B000000u);
+      f[i] = __uint_as_float(src & (MASK << (BITS * pos(i))));
     }
   }
 };
@@ -266,7 +275,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
   float k_unscale[D / 32];
 #pragma unroll
   for (int j = 0; j < D / 32; ++j)
-    k_unscale[j] = S::FAST_K ? MaskCodes<S::KBITS_FAST>::unscale((lane + 32 * j) % MaskCodes<S::KBITS_FAST>::PER_WORD)
+    k_unscale[j] = S::FAST_K ? MaskCodes<S::KBITS_FAST>::scale_in((lane + 32 * j) % MaskCodes<S::KBITS_FAST>::PER_WORD)
                              : 1.0f;
 
   LaneState<HG, CPL> st;
@@ -308,7 +317,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
     for (int h = 0; h < HG; ++h)
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
-        if constexpr (S::FAST_V) st.acc[h][i] *= MaskCodes<S::FAST_V ? BV : 2>::unscale(i % MaskCodes<S::FAST_V ? BV : 2>::PER_WORD);
+        if constexpr (S::FAST_V) st.acc[h][i] *= MaskCodes<S::FAST_V ? BV : 2>::scale_out(i % MaskCodes<S::FAST_V ? BV : 2>::PER_WORD);
         st.acc[h][i] += st.zsum[h];
       }
     st.folded = true;
@@ -519,7 +528,6 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
               // four independent partial sums keep the packed FMA chains short
               float2 a2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
                               make_float2(0.0f, 0.0f)};
-              const float2 magic = make_float2(-8388608.0f, -8388608.0f);
 #pragma unroll
               for (int wi = 0; wi < NW; ++wi) {
                 float f[MC::PER_WORD];
@@ -527,13 +535,13 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
 #pragma unroll
                 for (int m = 0; m < MC::PER_WORD / 2; ++m) {
                   const int i = wi * MC::PER_WORD + 2 * m;
-                  const float2 v = __fadd2_rn(make_float2(f[2 * m], f[2 * m + 1]), magic);
-                  a2[m & 3] = __ffma2_rn(v, make_float2(qp[0][i], qp[0][i + 1]), a2[m & 3]);
+                  a2[m & 3] = __ffma2_rn(make_float2(f[2 * m], f[2 * m + 1]), make_float2(qp[0][i], qp[0][i + 1]),
+                                         a2[m & 3]);
                 }
               }
               const float2 s01 = __fadd2_rn(a2[0], a2[1]), s23 = __fadd2_rn(a2[2], a2[3]);
               const float2 s03 = __fadd2_rn(s01, s23);
-              sc[j][0] = s03.x + s03.y;
+              sc[j][0] = (s03.x + s03.y) * __uint_as_float((uint32_t)(127 + kCodeExp) << 23);
             } else {
               uint32_t codes[CPL];
               load_codes<BK, CPL>(kc + tt * (D * BK / 32), kc_lo * BK, codes);
@@ -545,14 +553,20 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
                 sc[j][h] = a;
               }
             }
+          }
+          if (p.nsp > 0) {
             // sparse entries: the dense code there is 0 (value z); add q_c (x_c - z_c)
-            for (int k = 0; k < p.nsp; ++k) {
-              const int c = si[tt * p.nsp + k];
-              if (c >= kc_lo && c < kc_lo + CPL) {
-                const float z = h2f((uint16_t)(km[g * D + c] & 0xFFFFu));
-                const float xv = h2f(sv[tt * p.nsp + k]);
 #pragma unroll
-                for (int h = 0; h < HG; ++h) sc[j][h] = fmaf(q_s[h][c], xv - z, sc[j][h]);
+            for (int j = 0; j < TPL; ++j) {
+              const int tt = stt * 32 + tau + TAU * j;
+              for (int k = 0; k < p.nsp; ++k) {
+                const int c = si[tt * p.nsp + k];
+                if (c >= kc_lo && c < kc_lo + CPL) {
+                  const float z = h2f((uint16_t)(km[g * D + c] & 0xFFFFu));
+                  const float xv = h2f(sv[tt * p.nsp + k]);
+#pragma unroll
+                  for (int h = 0; h < HG; ++h) sc[j][h] = fmaf(q_s[h][c], xv - z, sc[j][h]);
+                }
               }
             }
           }
@@ -648,9 +662,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
             const float pw = sc[j][0];
             st.l[0] += pw;
             st.zsum[0] = fmaf(pw, z, st.zsum[0]);
-            const float ps = pw * s;
+            // subnormal codes against p*s*2^(149-kCodeExp): acc[i] gathers code*p*s*2^(B*pos-kCodeExp)
+            const float ps = pw * (s * __uint_as_float((uint32_t)(127 + 149 - kCodeExp) << 23));
             const float2 ps2 = make_float2(ps, ps);
-            const float2 magic = make_float2(-8388608.0f, -8388608.0f);
 #pragma unroll
             for (int wi = 0; wi < NW; ++wi) {
               float f[MC::PER_WORD];
@@ -658,8 +672,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
 #pragma unroll
               for (int m = 0; m < MC::PER_WORD / 2; ++m) {
                 const int i = wi * MC::PER_WORD + 2 * m;
-                const float2 v = __fadd2_rn(make_float2(f[2 * m], f[2 * m + 1]), magic);
-                const float2 r = __ffma2_rn(v, ps2, make_float2(st.acc[0][i], st.acc[0][i + 1]));
+                const float2 r = __ffma2_rn(make_float2(f[2 * m], f[2 * m + 1]), ps2,
+                                            make_float2(st.acc[0][i], st.acc[0][i + 1]));
                 st.acc[0][i] = r.x;
                 st.acc[0][i + 1] = r.y;
               }
