@@ -117,12 +117,18 @@ int64_t decode_grid(const kvq_cache* c) {
   int64_t g;
   if (c->forced_splits > 0) {
     g = c->n_units * c->forced_splits;
-  } else if (c->resident >= 2 * c->n_units) {
-    // whole units per CTA group: every unit is cut into the same number of slices,
-    // so a CTA never straddles two units (costs at most a third of the slots)
-    g = c->n_units * (c->resident / c->n_units);
   } else {
+    // Every resident CTA takes an equal contiguous slice of the item list.  When at least two
+    // CTAs fit per unit, cutting every unit into the same number of slices keeps a CTA inside
+    // one unit but can leave up to a third of the slots idle: take it only when its largest
+    // slice is no longer than the plain split's.
     g = c->resident;
+    const int64_t k = c->resident / c->n_units;
+    if (k >= 2) {
+      const int64_t per_aligned = (wpu + k - 1) / k;
+      const int64_t per_plain = (total + c->resident - 1) / c->resident;
+      if (per_aligned <= per_plain) g = c->n_units * k;
+    }
   }
   if (g > total) g = total;
   return g < 1 ? 1 : g;

@@ -44,7 +44,7 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kDecodeThreads = kConsumerThreads + 32;
+constexpr int kDecodeThreads = kConsumerThreads;  // every warp computes; copies are issued by whichever warp frees a stage
 constexpr int kStages = 4;
 constexpr float kLazyRescale = 8.0f;
 
@@ -99,11 +99,8 @@ struct Shape {
   static constexpr bool FAST_K = HG == 1 && !ROPE && (BK == 2 || BK == 4);
   static constexpr bool FAST_V = HG == 1 && (BV == 2 || BV == 4);
   static constexpr int KBITS_FAST = (BK == 2 || BK == 4) ? BK : 2;
-#ifndef KVQ_MHA_MIN_BLOCKS
-#define KVQ_MHA_MIN_BLOCKS 3
-#endif
-  // resident CTAs per SM the register budget is sized for
-  static constexpr int MIN_BLOCKS = ROPE ? (HG == 1 ? 2 : 1) : (HG == 1 ? KVQ_MHA_MIN_BLOCKS : (HG == 2 ? 3 : 1));
+  // resident CTAs per SM the register budget is sized for (128 threads each)
+  static constexpr int MIN_BLOCKS = ROPE ? (HG == 1 ? 3 : 2) : (HG == 4 ? 2 : 4);
 };
 
 // Extract N codes of BITS bits starting at bit `bit0` of a token record held
@@ -138,6 +135,38 @@ __device__ __forceinline__ void load_codes(const uint32_t* rec, int bit0, uint32
       uint32_t v = wds[wi] >> o;
       if (o + BITS > 32) v |= wds[wi + 1] << (32 - o);
       codes[i] = v & MASK;
+    }
+  }
+}
+
+// N consecutive fp16 values (N a multiple of 4, src aligned to 2N bytes up to 16) as floats,
+// in 8- or 16-byte loads.
+template <int N>
+__device__ __forceinline__ void load_halves(const uint16_t* src, float (&dst)[N]) {
+  static_assert(N % 4 == 0, "rows are read in groups of four");
+  if constexpr (N % 8 == 0) {
+#pragma unroll
+    for (int v = 0; v < N / 8; ++v) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + v);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ws[i]));
+        dst[8 * v + 2 * i] = f.x;
+        dst[8 * v + 2 * i + 1] = f.y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int v = 0; v < N / 4; ++v) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(src) + v);
+      const uint32_t ws[2] = {w.x, w.y};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ws[i]));
+        dst[4 * v + 2 * i] = f.x;
+        dst[4 * v + 2 * i + 1] = f.y;
+      }
     }
   }
 }
@@ -191,75 +220,69 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ int stage_cnt[kStages];  // warps that finished each stage (mod kConsumerWarps: the last one refills)
   __shared__ __align__(16) uint16_t q_stage[2][HG * D];  // fp16 query rows of the next units
   __shared__ __align__(8) uint64_t q_full[2];
-  __shared__ __align__(8) uint64_t q_empty[2];
   __shared__ float q_s[HG][D];
   __shared__ __align__(16) float qp_s[kConsumerWarps][HG][D];
   __shared__ float wacc[kConsumerWarps][HG][D];
   __shared__ float wml[kConsumerWarps][HG][2];
   __shared__ int abort_flag;
   __shared__ int last_cta;
+  __shared__ int stage_issued[kStages];  // copies issued into each stage / query buffer so far
+  __shared__ int qbuf_issued[2];
+
+  // Page items of this slice, numbered k = 0, 1, ... in list order.  Before item x the list
+  // holds unit(x) * n_pages + min(loc(x), n_pages) page items, so page k of the slice is global
+  // page P_begin + k: unit (P_begin + k) / n_pages, page (P_begin + k) % n_pages of that unit.
+  auto pages_before = [&](int64_t x) -> int64_t {
+    const int64_t u = x / wpu, l = x - u * wpu;
+    return u * p.n_pages + (l < p.n_pages ? l : p.n_pages);
+  };
+  const int64_t P_begin = pages_before(w_begin);
+  const int n_pg = (int)(pages_before(w_end) - P_begin);
+  const int64_t unit_first = w_begin / wpu;
+  const int n_cta_units = w_end > w_begin ? (int)((w_end - 1) / wpu - unit_first + 1) : 0;
+  const uint32_t q_bytes = (uint32_t)(HG * D * 2);
+
+  // page k of the slice into stage k % kStages (one thread)
+  auto issue_page = [&](int k) {
+    // 32-bit division: a cache never holds 2^32 pages
+    const uint32_t P = (uint32_t)(P_begin + k), np = (uint32_t)p.n_pages;
+    const uint32_t u = P / np, loc = P - u * np;
+    const int st = k % kStages;
+    mbar_arrive_expect_tx(&full_bar[st], (uint32_t)page_bytes);
+    bulk_g2s(stage_mem + (size_t)st * page_bytes, p.pages + (int64_t)u * p.unit_page_stride + (int64_t)loc * page_bytes,
+             (uint32_t)page_bytes, &full_bar[st]);
+    stage_issued[st] = k / kStages + 1;
+  };
+  // query rows q[b][kvh*HG .. kvh*HG+HG-1][:] (contiguous) of the slice's j-th unit into buffer j % 2 (one thread)
+  auto issue_q = [&](int j) {
+    const int64_t u = unit_first + j;
+    const int64_t b = u / p.Hkv, kvh = u - b * p.Hkv;
+    mbar_arrive_expect_tx(&q_full[j & 1], q_bytes);
+    bulk_g2s(q_stage[j & 1], p.q + (b * p.Hq + kvh * HG) * D, q_bytes, &q_full[j & 1]);
+    qbuf_issued[j & 1] = (j >> 1) + 1;
+  };
 
   if (tid == 0) {
     abort_flag = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kConsumerWarps);
+      stage_cnt[i] = 0;
+      stage_issued[i] = 0;
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
+      qbuf_issued[i] = 0;
     }
     fence_mbar_init();
   }
   __syncthreads();
-
-  if (warp == kConsumerWarps) {
-    // ---------------- producer: one bulk copy per page item into the stage ring
-    if (lane == 0) {
-      int issued = 0;
-      int q_issued = 0;
-      int64_t unit = w_begin / wpu;
-      int loc = (int)(w_begin - unit * wpu);
-      const uint32_t q_bytes = (uint32_t)(HG * D * 2);
-      for (int64_t x = w_begin; x < w_end; ++x, ++loc) {
-        if (loc == wpu) {
-          loc = 0;
-          ++unit;
-        }
-        if (x == w_begin || loc == 0) {
-          // query rows of this unit (q[b][kvh*HG .. kvh*HG+HG-1][:], contiguous) into a double buffer
-          const int qs = q_issued & 1, qk = q_issued >> 1;
-          if (qk > 0 && !mbar_wait(&q_empty[qs], (qk - 1) & 1)) {
-            report_error(p.err, kDevWaitTimeout);
-            atomicExch(&abort_flag, 1);
-            break;
-          }
-          const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
-          mbar_arrive_expect_tx(&q_full[qs], q_bytes);
-          bulk_g2s(q_stage[qs], p.q + (b * p.Hq + kvh * HG) * D, q_bytes, &q_full[qs]);
-          ++q_issued;
-        }
-        if (loc >= p.n_pages) continue;  // window item: read by the consumers directly
-        const int st = issued % kStages, k = issued / kStages;
-        if (k > 0 && !mbar_wait(&empty_bar[st], (k - 1) & 1)) {
-          report_error(p.err, kDevWaitTimeout);
-          atomicExch(&abort_flag, 1);
-          break;
-        }
-        if (*(volatile int*)&abort_flag) break;
-        mbar_arrive_expect_tx(&full_bar[st], (uint32_t)page_bytes);
-        bulk_g2s(stage_mem + (size_t)st * page_bytes, p.pages + unit * p.unit_page_stride + (int64_t)loc * page_bytes,
-                 (uint32_t)page_bytes, &full_bar[st]);
-        ++issued;
-      }
-      // never leave with a copy in flight: wait (bounded) for the last copy of every buffer
-      for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-        mbar_wait(&full_bar[i % kStages], (i / kStages) & 1);
-      for (int i = (q_issued > 2 ? q_issued - 2 : 0); i < q_issued; ++i) mbar_wait(&q_full[i & 1], (i >> 1) & 1);
-    }
-    return;
+  if (tid == 0) {
+    for (int k = 0; k < n_pg && k < kStages; ++k) issue_page(k);
+    for (int j = 0; j < n_cta_units && j < 2; ++j) issue_q(j);
   }
 
   // ---------------- consumers
@@ -335,7 +358,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
       q_s[h][c] = h2f(q_stage[qs][i]);
     }
     named_barrier_sync(1, kConsumerThreads);
-    if (tid == 0) mbar_arrive(&q_empty[qs]);
+    // buffer qs is free again: fetch the unit after next into it
+    if (tid == 0 && q_seq + 2 < n_cta_units && !*(volatile int*)&abort_flag) issue_q(q_seq + 2);
     ++q_seq;
   };
 
@@ -694,7 +718,19 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[stg]);
+      if (lane == 0) {
+        // release the stage; the last warp to release it refills it with page pg_seq + kStages
+        mbar_arrive(&empty_bar[stg]);
+        if (atomicAdd(&stage_cnt[stg], 1) % kConsumerWarps == kConsumerWarps - 1 && pg_seq + kStages < n_pg &&
+            !*(volatile int*)&abort_flag) {
+          if (mbar_wait(&empty_bar[stg], (pg_seq / kStages) & 1)) {
+            issue_page(pg_seq + kStages);
+          } else {
+            report_error(p.err, kDevWaitTimeout);
+            atomicExch(&abort_flag, 1);
+          }
+        }
+      }
       ++pg_seq;
     } else {
       // ---------------- the fp16 window: tokens Tq .. Tq + n_r - 1, read directly
@@ -718,17 +754,21 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
 #pragma unroll
           for (int h = 0; h < HG; ++h) a[h] = 0.0f;
           if constexpr (!ROPE) {
+            float xk[CPL];
+            load_halves<CPL>(kr + kc_lo, xk);
 #pragma unroll
             for (int i = 0; i < CPL; ++i) {
-              const float xv = h2f(kr[kc_lo + i]);
 #pragma unroll
-              for (int h = 0; h < HG; ++h) a[h] = fmaf(q_s[h][kc_lo + i], xv, a[h]);
+              for (int h = 0; h < HG; ++h) a[h] = fmaf(q_s[h][kc_lo + i], xk[i], a[h]);
             }
           } else {
             const uint32_t tpos = (uint32_t)(tq + tt);
+            float xlo[S::HALF], xhi[S::HALF];
+            load_halves<S::HALF>(kr + kc_lo, xlo);
+            load_halves<S::HALF>(kr + kc_lo + D / 2, xhi);
 #pragma unroll
             for (int i = 0; i < S::HALF; ++i) {
-              const float xl = h2f(kr[kc_lo + i]), xh = h2f(kr[kc_lo + D / 2 + i]);
+              const float xl = xlo[i], xh = xhi[i];
               float cs, sn;
               rope_cs(p.rope_turns[kc_lo + i], tpos, cs, sn);
               const float rl = xl * cs - xh * sn, rh = xh * cs + xl * sn;
@@ -756,19 +796,29 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
         for (int j = 0; j < TPL; ++j) {
           const int tt = stt * 32 + tau + TAU * j;
           if (tt >= p.n_r) continue;
-          const uint16_t* vr = wv + (int64_t)tt * D;
+          float xv[CPL];
+          load_halves<CPL>(wv + (int64_t)tt * D + vc_lo, xv);
 #pragma unroll
           for (int h = 0; h < HG; ++h) {
             const float pw = sc[j][h];
             st.l[h] += pw;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) st.acc[h][i] = fmaf(pw, h2f(vr[vc_lo + i]), st.acc[h][i]);
+            for (int i = 0; i < CPL; ++i) st.acc[h][i] = fmaf(pw, xv[i], st.acc[h][i]);
           }
         }
       }
     }
   }
   if (cur >= 0) epilogue(cur, done);
+  // never leave with a copy in flight (only possible after an abort): wait, bounded, for the
+  // last copy issued into every stage and query buffer
+  __syncthreads();
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i)
+      if (stage_issued[i] > 0) mbar_wait(&full_bar[i], (stage_issued[i] - 1) & 1);
+    for (int i = 0; i < 2; ++i)
+      if (qbuf_issued[i] > 0) mbar_wait(&q_full[i], (qbuf_issued[i] - 1) & 1);
+  }
 }
 
 template <int BK, int BV, int HG, bool ROPE>
