@@ -36,6 +36,7 @@ struct kvq_cache {
   int32_t max_slots = 1;      // partial slots per query head
   int32_t forced_splits = 0;  // 0: grid = resident CTAs; n: grid = n CTAs per unit
   int64_t resident = 1;       // decode CTAs resident on the whole GPU
+  int32_t decode_warps = 1;   // warps of one decode CTA
   int64_t T = 0, Tq = 0;
   int32_t n_r = 0;
   bool prefilled = false;
@@ -109,29 +110,42 @@ kvq_status validate(const kvq_config& k) {
 
 constexpr int32_t kMaxForcedSplits = 16;
 
-// Grid of the decode launch: the resident CTA count (or n per unit when forced),
-// never more than the work items.
+// Grid of the decode launch: the resident CTAs (one per SM), or n per unit when forced; never
+// more CTAs than work items.
 int64_t decode_grid(const kvq_cache* c) {
   const int64_t wpu = c->Tq / c->cfg.residual + (c->n_r > 0 ? 1 : 0);
   const int64_t total = c->n_units * wpu;
-  int64_t g;
-  if (c->forced_splits > 0) {
-    g = c->n_units * c->forced_splits;
-  } else {
-    // Every resident CTA takes an equal contiguous slice of the item list.  When at least two
-    // CTAs fit per unit, cutting every unit into the same number of slices keeps a CTA inside
-    // one unit but can leave up to a third of the slots idle: take it only when its largest
-    // slice is no longer than the plain split's.
-    g = c->resident;
-    const int64_t k = c->resident / c->n_units;
-    if (k >= 2) {
-      const int64_t per_aligned = (wpu + k - 1) / k;
-      const int64_t per_plain = (total + c->resident - 1) / c->resident;
-      if (per_aligned <= per_plain) g = c->n_units * k;
-    }
-  }
+  int64_t g = c->forced_splits > 0 ? c->n_units * c->forced_splits : c->resident;
   if (g > total) g = total;
   return g < 1 ? 1 : g;
+}
+
+// Partial slots one query head needs for a grid of `grid` CTAs: every warp of every CTA whose
+// slice meets the unit may leave one, and fewer than ceil(grid / units) + 2 slices meet a unit.
+int64_t slots_for_grid(const kvq_cache* c, int64_t grid) {
+  return (int64_t)c->decode_warps * ((grid + c->n_units - 1) / c->n_units + 2);
+}
+
+// Grow the partial buffers to `slots` per query head (never shrinks).
+cudaError_t ensure_slots(kvq_cache* c, int64_t slots) {
+  if (slots <= c->max_slots) return cudaSuccess;
+  const int64_t heads = (int64_t)c->cfg.batch * c->cfg.num_q_heads;
+  float *ml = nullptr, *acc = nullptr;
+  cudaError_t e = cudaMalloc((void**)&ml, (size_t)(heads * slots * 2 * sizeof(float)));
+  if (e == cudaSuccess) e = cudaMalloc((void**)&acc, (size_t)(heads * slots * c->cfg.head_dim * sizeof(float)));
+  if (e != cudaSuccess) {
+    cudaFree(ml);
+    cudaFree(acc);
+    return e;
+  }
+  // the buffers may still be read by work in flight on any stream
+  cudaDeviceSynchronize();
+  cudaFree(c->part_ml);
+  cudaFree(c->part_acc);
+  c->part_ml = ml;
+  c->part_acc = acc;
+  c->max_slots = (int32_t)slots;
+  return cudaSuccess;
 }
 
 // 0.64 fixed-point turns per token of frequency i: theta_i / (2 pi), theta_i = base^(-2i/D).
@@ -219,20 +233,17 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   c->n_pages_cap = quantized_tokens(cfg->max_tokens, R) / R;
   c->unit_page_stride = c->n_pages_cap * (int64_t)c->lay.bytes;
   const int hg = cfg->num_q_heads / cfg->num_kv_heads;
-  const int per_sm = kvq::decode_resident_ctas_per_sm(cfg->k_bits, cfg->v_bits, hg, cfg->rope != 0, c->lay.bytes);
+  int warps = 0;
+  const int per_sm = kvq::decode_resident_ctas_per_sm(cfg->k_bits, cfg->v_bits, hg, cfg->rope != 0, cfg->residual,
+                                                     cfg->k_sparse, c->lay.bytes, &warps);
   if (per_sm < 1) {
     cudaGetLastError();
     delete c;
     return KVQ_ERR_UNSUPPORTED;
   }
   c->resident = (int64_t)per_sm * c->sm_count;
-  {
-    // a unit's items meet at most ceil(2*grid/units) + 2 CTA slices (and at most its item count)
-    const int64_t grid_cap = c->resident > c->n_units * kMaxForcedSplits ? c->resident : c->n_units * kMaxForcedSplits;
-    int64_t ms = (2 * grid_cap + c->n_units - 1) / c->n_units + 2;
-    if (ms > c->n_pages_cap + 1) ms = c->n_pages_cap + 1;
-    c->max_slots = (int32_t)(ms < 1 ? 1 : ms);
-  }
+  c->decode_warps = warps;
+  c->max_slots = (int32_t)slots_for_grid(c, c->resident);
 
   const int64_t heads = (int64_t)cfg->batch * cfg->num_q_heads;
   cudaError_t e = cudaSuccess;
@@ -244,11 +255,11 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   alloc((void**)&c->wv, (size_t)(c->n_units * R * D * 2));
   alloc((void**)&c->part_ml, (size_t)(heads * c->max_slots * 2 * sizeof(float)));
   alloc((void**)&c->part_acc, (size_t)(heads * c->max_slots * D * sizeof(float)));
-  alloc((void**)&c->counters, (size_t)c->n_units * sizeof(int));
+  alloc((void**)&c->counters, (size_t)c->n_units * 2 * sizeof(int));  // tickets, then slot counts
   alloc((void**)&c->err, sizeof(int));
   alloc((void**)&c->rope_turns, (size_t)(D / 2) * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(c->err, 0, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)c->n_units * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)c->n_units * 2 * sizeof(int));
   if (e == cudaSuccess) {
     std::vector<unsigned long long> turns(D / 2);
     for (int i = 0; i < D / 2; ++i) turns[i] = rope_turn_fraction(cfg->rope ? cfg->rope_base : 10000.0, i, D);
@@ -298,7 +309,17 @@ kvq_status kvq_reset(kvq_cache* c) {
 
 kvq_status kvq_set_splits(kvq_cache* c, int32_t splits) {
   if (!c || splits < 0) return KVQ_ERR_INVALID_ARG;
-  c->forced_splits = splits > kMaxForcedSplits ? kMaxForcedSplits : splits;
+  const int32_t n = splits > kMaxForcedSplits ? kMaxForcedSplits : splits;
+  if (n > 0) {
+    DeviceGuard g(c->device);
+    if (!g.ok) return fail_cuda(c);
+    const cudaError_t e = ensure_slots(c, slots_for_grid(c, c->n_units * n));
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return e == cudaErrorMemoryAllocation ? KVQ_ERR_OOM : fail_cuda(c);
+    }
+  }
+  c->forced_splits = n;
   return KVQ_OK;
 }
 
@@ -452,6 +473,7 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, void* st
   dp.part_ml = c->part_ml;
   dp.part_acc = c->part_acc;
   dp.counters = c->counters;
+  dp.nslot = c->counters + c->n_units;
   dp.out = static_cast<uint16_t*>(out);
   dp.err = c->err;
   bool supported = false;

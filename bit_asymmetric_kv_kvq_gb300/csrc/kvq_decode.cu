@@ -4,20 +4,22 @@
 // geometry problem, not a bit problem", section "Why the KV cache is a
 // problem"), so the kernel is built around streaming pages at full bandwidth:
 //
-//  * Work list.  Every (batch, kv head) unit contributes n_pages page items
-//    and, when the fp16 window is not empty, one window item.  The items of
+//  * Work list.  Every (batch, kv head) unit contributes, when the fp16
+//    window is not empty, one window item, then n_pages page items.  The items of
 //    all units are laid end to end and the grid (sized to the resident CTA
 //    count) takes equal contiguous slices of that list, so every SM streams
 //    the same number of pages whatever the batch/head/length mix, and a CTA
 //    crosses from one unit into the next without a new launch.
-//  * Streaming.  A producer warp issues one bulk (TMA) copy per page into a
-//    ring of shared-memory stages guarded by mbarriers; four consumer warps
-//    take one 32-token sub-tile of each page and dequantize in registers.
+//  * Streaming.  Pages arrive by one bulk (TMA) copy each into a ring of
+//    shared-memory stages guarded by mbarriers; the four warps of a CTA each
+//    take one 32-token sub-tile of every page and dequantize in registers, and
+//    the last warp to finish with a stage issues the copy that refills it (no
+//    warp is set aside to issue copies).
 //  * Merge.  Each CTA writes one unnormalised partial (m, l, acc[D]) per
 //    query head for every unit it touched; the CTA that completes a unit's
-//    item count (an atomic ticket, no waiting) merges the unit's partials
-//    with log-sum-exp weights and writes the fp16 output.  A unit covered by
-//    one CTA is written directly.
+//    item count (an acquire-release atomic ticket, no waiting) merges the
+//    unit's partials with log-sum-exp weights in one pass and writes the fp16
+//    output.  A unit covered by one CTA is written directly.
 //
 // Keys are quantized per channel over G-token groups, so inside a group the
 // score is linear in the codes:
@@ -42,10 +44,8 @@ namespace kvq {
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kDecodeThreads = kConsumerThreads;  // every warp computes; copies are issued by whichever warp frees a stage
-constexpr int kStages = 4;
+constexpr int kMaxStages = 16;  // shared-memory page stages per CTA (a power of two, sized per launch)
+constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLazyRescale = 8.0f;
 
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
@@ -66,7 +66,8 @@ constexpr int kCodeExp = 64;
 // scale_in(p) = 2^(149 - kCodeExp - B*p), so every product is
 // code * factor * 2^-kCodeExp, a normal number, with no offset to remove;
 // scale_out(p) = 2^(kCodeExp - B*p) undoes the position scale of an
-// accumulator that summed subnormal codes against unscaled factors.
+// accumulator that summed subnormal codes against unscaled factors, and
+// scale_back(p) = 1 / scale_out(p) puts real-valued sums into those units.
 template <int BITS>
 struct MaskCodes {
   static constexpr int PER_WORD = 32 / BITS;
@@ -77,6 +78,7 @@ struct MaskCodes {
     return __uint_as_float((uint32_t)(127 + 149 - kCodeExp - BITS * pos(i)) << 23);
   }
   __device__ static float scale_out(int i) { return __uint_as_float((uint32_t)(127 + kCodeExp - BITS * pos(i)) << 23); }
+  __device__ static float scale_back(int i) { return __uint_as_float((uint32_t)(127 - kCodeExp + BITS * pos(i)) << 23); }
   __device__ __forceinline__ static void to_float(uint32_t w, float (&f)[PER_WORD]) {
     const uint32_t ws = w >> (NDIRECT * BITS);
 #pragma unroll
@@ -99,8 +101,8 @@ struct Shape {
   static constexpr bool FAST_K = HG == 1 && !ROPE && (BK == 2 || BK == 4);
   static constexpr bool FAST_V = HG == 1 && (BV == 2 || BV == 4);
   static constexpr int KBITS_FAST = (BK == 2 || BK == 4) ? BK : 2;
-  // resident CTAs per SM the register budget is sized for (128 threads each)
-  static constexpr int MIN_BLOCKS = ROPE ? (HG == 1 ? 3 : 2) : (HG == 4 ? 2 : 4);
+  // warps of the one CTA per SM: as many as the register budget of the path allows
+  static constexpr int WARPS = ROPE ? (HG == 1 ? 12 : 8) : (HG == 4 ? 8 : 16);
 };
 
 // Extract N codes of BITS bits starting at bit `bit0` of a token record held
@@ -180,16 +182,10 @@ __device__ __forceinline__ void rope_cs(unsigned long long F, uint32_t t, float&
   sincospif(x, &s, &c);
 }
 
-// The CTA whose slice of the work list holds item x (slices [k*total/grid, (k+1)*total/grid)).
-__device__ __forceinline__ int cta_of(int64_t x, int64_t total, int grid) {
-  return (int)(((x + 1) * (int64_t)grid - 1) / total);
-}
-
 // Running softmax state of one lane for the current unit.
 template <int HG, int CPL>
 struct LaneState {
   float m[HG], l[HG], zsum[HG], acc[HG][CPL];
-  bool folded;
   __device__ __forceinline__ void reset() {
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
@@ -199,15 +195,22 @@ struct LaneState {
 #pragma unroll
       for (int i = 0; i < CPL; ++i) acc[h][i] = 0.0f;
     }
-    folded = false;
   }
 };
 
-template <int BK, int BV, int HG, bool ROPE>
-__global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_BLOCKS))
-    decode_kernel(const DecodeParams p) {
+// One CTA per SM.  The CTA streams a contiguous slice of the work list through a ring of
+// shared-memory page stages; its warps take the slice's 32-token sub-tiles one at a time from a
+// shared counter, so a warp that the scheduler serves less often simply takes fewer of them.
+// Every warp keeps its own online-softmax state per unit and, when it leaves a unit, writes one
+// partial (m, l, acc) into the next free slot of that unit; the warp whose ticket completes the
+// unit merges the unit's partials.  There is no CTA-wide barrier after the start.
+//
+// LEAN: one query head per kv head, 2- or 4-bit K and V, pages of 128 tokens, no sparse
+// entries -- the common case, with a page path that has no per-token branches.
+template <int BK, int BV, int HG, bool ROPE, bool LEAN>
+__global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode_kernel(const DecodeParams p) {
   using S = Shape<BK, BV, HG, ROPE>;
-  constexpr int D = S::D, CPL = S::CPL, KAPPA = S::KAPPA, TAU = S::TAU, TPL = S::TPL;
+  constexpr int D = S::D, CPL = S::CPL, KAPPA = S::KAPPA, TAU = S::TAU, TPL = S::TPL, W = S::WARPS;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = blockIdx.x, grid = gridDim.x;
@@ -216,93 +219,83 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
   const int64_t w_begin = (int64_t)cta * total / grid;
   const int64_t w_end = (int64_t)(cta + 1) * total / grid;
   const int page_bytes = p.lay.bytes;
+  const int log2S = p.log2_stages, n_stages = 1 << log2S;
+  const int SPP = p.R / 32;  // sub-tiles per item (1..4)
+  const int n_sub = (int)(w_end - w_begin) * SPP;
 
   extern __shared__ __align__(128) uint8_t stage_mem[];
-  __shared__ __align__(8) uint64_t full_bar[kStages];
-  __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ int stage_cnt[kStages];  // warps that finished each stage (mod kConsumerWarps: the last one refills)
-  __shared__ __align__(16) uint16_t q_stage[2][HG * D];  // fp16 query rows of the next units
-  __shared__ __align__(8) uint64_t q_full[2];
-  __shared__ float q_s[HG][D];
-  __shared__ __align__(16) float qp_s[kConsumerWarps][HG][D];
-  __shared__ float wacc[kConsumerWarps][HG][D];
-  __shared__ float wml[kConsumerWarps][HG][2];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ int stage_cnt[kMaxStages];     // sub-tiles released per stage (mod SPP: the last refills)
+  __shared__ int stage_issued[kMaxStages];  // copies issued into each stage so far
+  __shared__ __align__(16) float qw_s[W][HG][D];  // each warp's query rows (fp32) for its unit
+  __shared__ __align__(16) float qp_s[W][HG][D];  // each warp's q' for its key group
+  __shared__ int next_sub;
   __shared__ int abort_flag;
-  __shared__ int last_cta;
-  __shared__ int stage_issued[kStages];  // copies issued into each stage / query buffer so far
-  __shared__ int qbuf_issued[2];
 
-  // Page items of this slice, numbered k = 0, 1, ... in list order.  Before item x the list
-  // holds unit(x) * n_pages + min(loc(x), n_pages) page items, so page k of the slice is global
-  // page P_begin + k: unit (P_begin + k) / n_pages, page (P_begin + k) % n_pages of that unit.
+  // A unit's items are its window item (when the window holds tokens) followed by its pages.
+  // Page items of this slice are numbered k = 0, 1, ... in list order.  Before item x the list
+  // holds unit(x) * n_pages + max(loc(x) - hw, 0) page items (hw = 1 with a window item), so page
+  // k of the slice is global page P_begin + k: unit (P_begin + k) / n_pages, page
+  // (P_begin + k) % n_pages of that unit.
+  const int hw = (int)(wpu - p.n_pages);
   auto pages_before = [&](int64_t x) -> int64_t {
     const int64_t u = x / wpu, l = x - u * wpu;
-    return u * p.n_pages + (l < p.n_pages ? l : p.n_pages);
+    return u * p.n_pages + (l > hw ? l - hw : 0);
   };
   const int64_t P_begin = pages_before(w_begin);
   const int n_pg = (int)(pages_before(w_end) - P_begin);
-  const int64_t unit_first = w_begin / wpu;
-  const int n_cta_units = w_end > w_begin ? (int)((w_end - 1) / wpu - unit_first + 1) : 0;
-  const uint32_t q_bytes = (uint32_t)(HG * D * 2);
 
-  // page k of the slice into stage k % kStages (one thread)
+  // page k of the slice into stage k % n_stages (one thread)
   auto issue_page = [&](int k) {
     // 32-bit division: a cache never holds 2^32 pages
     const uint32_t P = (uint32_t)(P_begin + k), np = (uint32_t)p.n_pages;
     const uint32_t u = P / np, loc = P - u * np;
-    const int st = k % kStages;
+    const int st = k & (n_stages - 1);
     mbar_arrive_expect_tx(&full_bar[st], (uint32_t)page_bytes);
     bulk_g2s(stage_mem + (size_t)st * page_bytes, p.pages + (int64_t)u * p.unit_page_stride + (int64_t)loc * page_bytes,
              (uint32_t)page_bytes, &full_bar[st]);
-    stage_issued[st] = k / kStages + 1;
-  };
-  // query rows q[b][kvh*HG .. kvh*HG+HG-1][:] (contiguous) of the slice's j-th unit into buffer j % 2 (one thread)
-  auto issue_q = [&](int j) {
-    const int64_t u = unit_first + j;
-    const int64_t b = u / p.Hkv, kvh = u - b * p.Hkv;
-    mbar_arrive_expect_tx(&q_full[j & 1], q_bytes);
-    bulk_g2s(q_stage[j & 1], p.q + (b * p.Hq + kvh * HG) * D, q_bytes, &q_full[j & 1]);
-    qbuf_issued[j & 1] = (j >> 1) + 1;
+    stage_issued[st] = (k >> log2S) + 1;
   };
 
   if (tid == 0) {
     abort_flag = 0;
-    for (int i = 0; i < kStages; ++i) {
+    next_sub = 0;
+    for (int i = 0; i < n_stages; ++i) {
       mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], kConsumerWarps);
+      mbar_init(&empty_bar[i], SPP);
       stage_cnt[i] = 0;
       stage_issued[i] = 0;
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&q_full[i], 1);
-      qbuf_issued[i] = 0;
     }
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) {
-    for (int k = 0; k < n_pg && k < kStages; ++k) issue_page(k);
-    for (int j = 0; j < n_cta_units && j < 2; ++j) issue_q(j);
-  }
+  if (tid == 0)
+    for (int k = 0; k < n_pg && k < n_stages; ++k) issue_page(k);
 
-  // ---------------- consumers
+  // ---------------- per-warp work
   const int kap = lane % KAPPA;  // channel chunk
   const int tau = lane / KAPPA;  // token slot
   // key channels of this lane: a contiguous chunk, or (rope) half a chunk in each half of the head
   const int kc_lo = ROPE ? kap * S::HALF : kap * CPL;
   const int vc_lo = kap * CPL;
-  const int sub_tiles = p.R / 32;
   const int ng = D >> p.log2G;
   const int gv = vc_lo >> p.log2G;
-  // fast key path: 2^(-B*p) of the channels this lane prepares for the group products
+  // fast key path: 2^(149-kCodeExp-B*pos) of the channels this lane prepares for the group products
   float k_unscale[D / 32];
 #pragma unroll
   for (int j = 0; j < D / 32; ++j)
     k_unscale[j] = S::FAST_K ? MaskCodes<S::KBITS_FAST>::scale_in((lane + 32 * j) % MaskCodes<S::KBITS_FAST>::PER_WORD)
                              : 1.0f;
+  float (*qs)[D] = qw_s[warp];
 
   LaneState<HG, CPL> st;
   st.reset();
+
+  // lean page path: words per token and per lane-chunk of the key / value codes
+  constexpr int LKW = D * (S::FAST_K ? BK : 2) / 32, LVW = D * (S::FAST_V ? BV : 2) / 32;
+  constexpr int LNWK = CPL * (S::FAST_K ? BK : 2) / 32, LNWV = CPL * (S::FAST_V ? BV : 2) / 32;
+  float lean_qs[4], lean_qz[4];  // q_c * scale_in(c) and q_c for channels 4*lane .. 4*lane+3
 
   // Online-softmax update of one sub-tile: sc[j][h] are final scores (log2 units) of the
   // lane's tokens (-inf for masked ones); returns the weights in sc.
@@ -315,9 +308,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
       // the running maximum only moves when a score passes it by the lazy threshold: a vote
       // settles the common case without a reduction
       const bool over = tmax > st.m[h] + kLazyRescale || (st.m[h] == -INFINITY && tmax != -INFINITY);
-      if (__any_sync(0xffffffffu, over)) {
+      if (__any_sync(kFull, over)) {
 #pragma unroll
-        for (int off = KAPPA; off < 32; off <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+        for (int off = KAPPA; off < 32; off <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, off));
         const float mnew = fmaxf(tmax, st.m[h]);
         const float f = st.m[h] == -INFINITY ? 0.0f : exp2f(st.m[h] - mnew);
         st.l[h] *= f;
@@ -332,169 +325,158 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
     }
   };
 
-  // undo the per-position code scale of the fast value path and add the value
-  // zero-point sums (quantized tokens only); done once per unit, before any fp16 token
-  auto fold = [&]() {
-    if (st.folded) return;
+  // this warp's query rows q[b][kvh*HG .. kvh*HG+HG-1][:] (contiguous fp16) as floats
+  auto load_q = [&](int64_t unit) {
+    constexpr int PERL = HG * D / 32;
+    const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
+    float v[PERL];
+    load_halves<PERL>(p.q + (b * p.Hq + kvh * HG) * D + lane * PERL, v);
+    __syncwarp();  // every lane is done with the previous unit's rows
+#pragma unroll
+    for (int i = 0; i < PERL; ++i) (&qs[0][0])[lane * PERL + i] = v[i];
+    __syncwarp();
+    if constexpr (LEAN) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        lean_qz[i] = v[i];
+        lean_qs[i] = v[i] * MaskCodes<S::KBITS_FAST>::scale_in((4 * lane + i) % MaskCodes<S::KBITS_FAST>::PER_WORD);
+      }
+    }
+  };
+
+  // This warp leaves `unit` after `done` of its sub-tiles: one partial into the unit's next free
+  // slot, then a ticket; the warp completing the unit merges every slot and writes the output.
+  auto epilogue = [&](int64_t unit, int done) {
+    constexpr int NOUT = CPL / TAU;  // channels per head a lane holds after the reduction
+    static_assert(NOUT == 4, "the partial of a lane is one float4 per head");
+    // l and the value zero-point sums over the warp's token slots (lanes of one slot hold copies)
 #pragma unroll
     for (int h = 0; h < HG; ++h)
 #pragma unroll
-      for (int i = 0; i < CPL; ++i) {
-        if constexpr (S::FAST_V) st.acc[h][i] *= MaskCodes<S::FAST_V ? BV : 2>::scale_out(i % MaskCodes<S::FAST_V ? BV : 2>::PER_WORD);
-        st.acc[h][i] += st.zsum[h];
+      for (int off = KAPPA; off < 32; off <<= 1) {
+        st.l[h] += __shfl_xor_sync(kFull, st.l[h], off);
+        st.zsum[h] += __shfl_xor_sync(kFull, st.zsum[h], off);
       }
-    st.folded = true;
-  };
-
-  int q_seq = 0;
-  auto load_q = [&]() {
-    const int qs = q_seq & 1;
-    if (!mbar_wait(&q_full[qs], (q_seq >> 1) & 1)) {
-      report_error(p.err, kDevWaitTimeout);
-      atomicExch(&abort_flag, 1);
-    }
-    for (int i = tid; i < HG * D; i += kConsumerThreads) {
-      const int h = i / D, c = i - h * D;
-      q_s[h][c] = h2f(q_stage[qs][i]);
-    }
-    named_barrier_sync(1, kConsumerThreads);
-    // buffer qs is free again: fetch the unit after next into it
-    if (tid == 0 && q_seq + 2 < n_cta_units && !*(volatile int*)&abort_flag) issue_q(q_seq + 2);
-    ++q_seq;
-  };
-
-  // Partial of this CTA for `unit` (covering `done` of its items); merges when it completes the unit.
-  auto epilogue = [&](int64_t unit, int done) {
-    fold();
+    // reduce-scatter of acc over the token slots: each step keeps the half of the chunk that the
+    // lane's slot bit selects, so the lane ends with channels vc_lo + NOUT*tau .. + NOUT - 1
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
 #pragma unroll
-      for (int off = KAPPA; off < 32; off <<= 1) {
-        st.l[h] += __shfl_xor_sync(0xffffffffu, st.l[h], off);
+      for (int half = CPL / 2, bit = TAU / 2; half >= NOUT; half >>= 1, bit >>= 1) {
+        const bool up = (tau & bit) != 0;
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) st.acc[h][i] += __shfl_xor_sync(0xffffffffu, st.acc[h][i], off);
-      }
-    }
-    if (tau == 0) {
-#pragma unroll
-      for (int h = 0; h < HG; ++h)
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) wacc[warp][h][vc_lo + i] = st.acc[h][i];
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        wml[warp][h][0] = st.m[h];
-        wml[warp][h][1] = st.l[h];
-      }
-    }
-    named_barrier_sync(1, kConsumerThreads);
-    constexpr int PER = HG * D / kConsumerThreads;
-    float pa[PER], pm[PER], pl[PER];
-#pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int i = tid + k * kConsumerThreads;
-      const int h = i / D, c = i - h * D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wml[w][h][0]);
-      float a = 0.0f, L = 0.0f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          if (wml[w][h][0] == -INFINITY) continue;
-          const float f = exp2f(wml[w][h][0] - M);
-          a = fmaf(f, wacc[w][h][c], a);
-          L = fmaf(f, wml[w][h][1], L);
+        for (int i = 0; i < half; ++i) {
+          const float send = up ? st.acc[h][i] : st.acc[h][i + half];
+          const float keep = up ? st.acc[h][i + half] : st.acc[h][i];
+          st.acc[h][i] = keep + __shfl_xor_sync(kFull, send, bit * KAPPA);
         }
       }
-      pa[k] = a;
-      pm[k] = M;
-      pl[k] = L;
     }
+    // undo the per-position code scale of the fast value path; add the value zero-point sums
+#pragma unroll
+    for (int h = 0; h < HG; ++h)
+#pragma unroll
+      for (int i = 0; i < NOUT; ++i) {
+        float a = st.acc[h][i];
+        if constexpr (S::FAST_V) a *= MaskCodes<S::FAST_V ? BV : 2>::scale_out((vc_lo + NOUT * tau + i) % (32 / BV));
+        st.acc[h][i] = a + st.zsum[h];
+      }
     const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
     const int64_t bh0 = b * p.Hq + kvh * HG;
-    const int k_first = cta_of(unit * wpu, total, grid);
-    const int k_last = cta_of(unit * wpu + wpu - 1, total, grid);
-    if (k_first == k_last) {
+    int slot = 0;
+    if (lane == 0) slot = atomicAdd(p.nslot + unit, 1);
+    slot = __shfl_sync(kFull, slot, 0);
+    if (slot < p.max_slots) {
 #pragma unroll
-      for (int k = 0; k < PER; ++k) {
-        const int i = tid + k * kConsumerThreads;
-        p.out[bh0 * D + i] = __half_as_ushort(__float2half_rn(pa[k] / pl[k]));
-      }
-    } else {
-      const int slot = cta - k_first;
-#pragma unroll
-      for (int k = 0; k < PER; ++k) {
-        const int i = tid + k * kConsumerThreads;
-        const int h = i / D, c = i - h * D;
+      for (int h = 0; h < HG; ++h) {
         const int64_t so = (bh0 + h) * p.max_slots + slot;
-        p.part_acc[so * D + c] = pa[k];
-        if (c == 0) {
-          p.part_ml[so * 2] = pm[k];
-          p.part_ml[so * 2 + 1] = pl[k];
-        }
+        *reinterpret_cast<float4*>(p.part_acc + so * D + vc_lo + NOUT * tau) =
+            make_float4(st.acc[h][0], st.acc[h][1], st.acc[h][2], st.acc[h][3]);
+        if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + so * 2) = make_float2(st.m[h], st.l[h]);
       }
-      __threadfence();
-      named_barrier_sync(1, kConsumerThreads);
-      if (tid == 0) last_cta = atomicAdd(&p.counters[unit], done) + done == wpu;
-      named_barrier_sync(1, kConsumerThreads);
-      if (last_cta) {
-        __threadfence();
-        const int nslots = k_last - k_first + 1;
+    } else if (lane == 0) {
+      report_error(p.err, kDevBadArgument);  // slots are sized for the grid: not reached
+    }
+    // __syncwarp orders the lanes' partial stores before lane 0's release; the warp whose ticket
+    // completes the unit acquires every other warp's partials the same way
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      int prev;
+      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(prev) : "l"(p.counters + unit), "r"(done)
+                   : "memory");
+      last = prev + done == (int)(wpu * SPP);
+    }
+    last = __shfl_sync(kFull, last, 0);
+    if (last) {
+      int n = 0;
+      if (lane == 0) n = __ldcg(p.nslot + unit);
+      n = __shfl_sync(kFull, n, 0);
+      if (n > p.max_slots) n = p.max_slots;
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-          const int i = tid + k * kConsumerThreads;
-          const int h = i / D, c = i - h * D;
-          const float* ml = p.part_ml + (bh0 + h) * p.max_slots * 2;
-          const float* pacc = p.part_acc + (bh0 + h) * p.max_slots * D + c;
-          float M = -INFINITY;
+      for (int h = 0; h < HG; ++h) {
+        const float* ml = p.part_ml + (bh0 + h) * p.max_slots * 2;
+        const float* pacc = p.part_acc + (bh0 + h) * p.max_slots * D + 4 * lane;
+        float M = -INFINITY;
+        for (int sp = lane; sp < n; sp += 32) M = fmaxf(M, __ldcg(ml + 2 * sp));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+        float L = 0.0f, a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll 4
-          for (int sp = 0; sp < nslots; ++sp) M = fmaxf(M, __ldcg(ml + 2 * sp));
-          float a = 0.0f, L = 0.0f;
-#pragma unroll 4
-          for (int sp = 0; sp < nslots; ++sp) {
-            const float m = __ldcg(ml + 2 * sp);
-            if (m == -INFINITY) continue;
-            const float f = exp2f(m - M);
-            L = fmaf(f, __ldcg(ml + 2 * sp + 1), L);
-            a = fmaf(f, __ldcg(pacc + (int64_t)sp * D), a);
-          }
-          p.out[bh0 * D + i] = __half_as_ushort(__float2half_rn(a / L));
+        for (int sp = 0; sp < n; ++sp) {
+          const float2 mlv = __ldcg(reinterpret_cast<const float2*>(ml + 2 * sp));
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(pacc + (int64_t)sp * D));
+          if (mlv.x == -INFINITY) continue;
+          const float f = exp2f(mlv.x - M);
+          L = fmaf(f, mlv.y, L);
+          a0 = fmaf(f, v.x, a0);
+          a1 = fmaf(f, v.y, a1);
+          a2 = fmaf(f, v.z, a2);
+          a3 = fmaf(f, v.w, a3);
         }
-        if (tid == 0) p.counters[unit] = 0;  // ready for the next call on this stream
+        const float inv = 1.0f / L;
+        const __half2 o01 = __floats2half2_rn(a0 * inv, a1 * inv), o23 = __floats2half2_rn(a2 * inv, a3 * inv);
+        uint2 packed;
+        packed.x = *reinterpret_cast<const uint32_t*>(&o01);
+        packed.y = *reinterpret_cast<const uint32_t*>(&o23);
+        *reinterpret_cast<uint2*>(p.out + (bh0 + h) * D + 4 * lane) = packed;
+      }
+      if (lane == 0) {  // ready for the next call on this stream
+        p.counters[unit] = 0;
+        p.nslot[unit] = 0;
       }
     }
-    named_barrier_sync(1, kConsumerThreads);  // shared scratch is free again
   };
 
-  int64_t cur = -1;
+  int64_t cur = -1, ustart = 0;
   int done = 0;
-  int pg_seq = 0;
-  int64_t unit = w_begin / wpu;
-  int loc = (int)(w_begin - unit * wpu);
-  for (int64_t x = w_begin; x < w_end; ++x, ++loc) {
-    if (loc == wpu) {
-      loc = 0;
-      ++unit;
-    }
-    if (unit != cur) {
+  while (true) {
+    int s = 0;
+    if (lane == 0) s = atomicAdd(&next_sub, 1);
+    s = __shfl_sync(kFull, s, 0);
+    if (s >= n_sub || *(volatile int*)&abort_flag) break;
+    const int sx = SPP == 4 ? s >> 2 : SPP == 2 ? s >> 1 : SPP == 1 ? s : s / 3;
+    const int stt = s - sx * SPP;  // sub-tile: tokens 32*stt .. 32*stt+31 of the item
+    const int64_t x = w_begin + sx;
+    if (cur < 0 || x >= ustart + wpu) {
       if (cur >= 0) epilogue(cur, done);
-      cur = unit;
+      cur = x / wpu;
+      ustart = cur * wpu;
       done = 0;
       st.reset();
-      load_q();
+      load_q(cur);
     }
     ++done;
-    if (*(volatile int*)&abort_flag) continue;
+    const int loc = (int)(x - ustart);
 
-    if (loc < p.n_pages) {
-      // ---------------- a page of quantized tokens
-      const int stg = pg_seq % kStages;
-      if (!mbar_wait(&full_bar[stg], (pg_seq / kStages) & 1)) {
+    if (loc >= hw) {
+      // ---------------- a sub-tile of a page of quantized tokens
+      const int kpg = (int)(cur * p.n_pages + (loc - hw) - P_begin);
+      const int stg = kpg & (n_stages - 1);
+      if (!mbar_wait(&full_bar[stg], (kpg >> log2S) & 1)) {
         report_error(p.err, kDevWaitTimeout);
         atomicExch(&abort_flag, 1);
-        continue;
+        break;
       }
       const uint8_t* pgm = stage_mem + (size_t)stg * page_bytes;
       const uint32_t* kc = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_kc);
@@ -503,9 +485,135 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
       const uint32_t* vm = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vm);
       const uint8_t* si = pgm + p.lay.off_si;
       const uint16_t* sv = reinterpret_cast<const uint16_t*>(pgm + p.lay.off_sv);
-      const int64_t page_tok0 = loc * (int64_t)p.R;
+      const int64_t page_tok0 = (loc - hw) * (int64_t)p.R;
 
-      for (int stt = warp; stt < sub_tiles; stt += kConsumerWarps) {
+      if constexpr (LEAN) {
+        using MK = MaskCodes<S::KBITS_FAST>;
+        using MV = MaskCodes<S::FAST_V ? BV : 2>;
+        // byte offsets in the page of this lane's key / value words and value scales for token
+        // slot 0 (tokens 32*stt + tau + 8*j), and of the four key scales it turns into q'
+        const int lean_kc = p.lay.off_kc + ((32 * stt + tau) * LKW + kap * LNWK) * 4;
+        const int lean_vc = p.lay.off_vc + ((32 * stt + tau) * LVW + kap * LNWV) * 4;
+        const int lean_vm = p.lay.off_vm + ((32 * stt + tau) * ng + gv) * 4;
+        const int lean_vm_step = 8 * ng * 4;
+        const int lean_km = p.lay.off_km + ((((32 * stt) >> p.log2G) * D) + 4 * lane) * 4;
+        // q'_c = q_c s_c 2^(149-kCodeExp-B*pos) for the warp's key group, four channels per lane,
+        // gathered back as the lane's 32 channels; Z = sum_c q_c z_c
+        const uint4 mz = *reinterpret_cast<const uint4*>(pgm + lean_km);
+        const uint32_t mzw[4] = {mz.x, mz.y, mz.z, mz.w};
+        float qn[4], zp = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(&mzw[i]));
+          qn[i] = lean_qs[i] * zs.y;
+          zp = fmaf(lean_qz[i], zs.x, zp);
+        }
+        __syncwarp();
+        *reinterpret_cast<float4*>(&qp_s[warp][0][4 * lane]) = make_float4(qn[0], qn[1], qn[2], qn[3]);
+        __syncwarp();
+        float qp[CPL];
+#pragma unroll
+        for (int i = 0; i < CPL / 4; ++i) {
+          const float4 v = reinterpret_cast<const float4*>(&qp_s[warp][0][kap * CPL])[i];
+          qp[4 * i] = v.x;
+          qp[4 * i + 1] = v.y;
+          qp[4 * i + 2] = v.z;
+          qp[4 * i + 3] = v.w;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) zp += __shfl_xor_sync(0xffffffffu, zp, off);
+
+        // key scores of the lane's four tokens, partial over its 32 channels
+        float sc[TPL][1];
+#pragma unroll
+        for (int j = 0; j < TPL; ++j) {
+          const uint32_t* rec = reinterpret_cast<const uint32_t*>(pgm + lean_kc) + j * 8 * LKW;
+          uint32_t wds[LNWK];
+          if constexpr (LNWK == 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(rec);
+            wds[0] = v.x;
+            wds[1] = v.y;
+          } else {
+#pragma unroll
+            for (int i = 0; i < LNWK / 4; ++i) {
+              const uint4 v = reinterpret_cast<const uint4*>(rec)[i];
+              wds[4 * i] = v.x;
+              wds[4 * i + 1] = v.y;
+              wds[4 * i + 2] = v.z;
+              wds[4 * i + 3] = v.w;
+            }
+          }
+          float2 a2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                          make_float2(0.0f, 0.0f)};
+#pragma unroll
+          for (int wi = 0; wi < LNWK; ++wi) {
+            float f[MK::PER_WORD];
+            MK::to_float(wds[wi], f);
+#pragma unroll
+            for (int m = 0; m < MK::PER_WORD / 2; ++m) {
+              const int i = wi * MK::PER_WORD + 2 * m;
+              a2[m & 3] = __ffma2_rn(make_float2(f[2 * m], f[2 * m + 1]), make_float2(qp[i], qp[i + 1]), a2[m & 3]);
+            }
+          }
+          const float2 s01 = __fadd2_rn(a2[0], a2[1]), s23 = __fadd2_rn(a2[2], a2[3]);
+          const float2 s03 = __fadd2_rn(s01, s23);
+          sc[j][0] = s03.x + s03.y;
+        }
+        // sum the four channel chunks of every token; scale back by 2^kCodeExp, add Z
+        const float kscale = __uint_as_float((uint32_t)(127 + kCodeExp) << 23) * p.qk_scale_log2;
+        const float zscaled = zp * p.qk_scale_log2;
+#pragma unroll
+        for (int j = 0; j < TPL; ++j) {
+          float a = sc[j][0];
+#pragma unroll
+          for (int off = 1; off < KAPPA; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+          sc[j][0] = fmaf(a, kscale, zscaled);
+        }
+
+        softmax_update(sc);
+
+        // P.V: subnormal value codes against p*s*2^(149-kCodeExp)
+        const float pscale = __uint_as_float((uint32_t)(127 + 149 - kCodeExp) << 23);
+#pragma unroll
+        for (int j = 0; j < TPL; ++j) {
+          const uint32_t mv = *reinterpret_cast<const uint32_t*>(pgm + lean_vm + j * lean_vm_step);
+          const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(&mv));
+          const float pw = sc[j][0];
+          st.l[0] += pw;
+          st.zsum[0] = fmaf(pw, zs.x, st.zsum[0]);
+          const float ps = pw * (zs.y * pscale);
+          const float2 ps2 = make_float2(ps, ps);
+          const uint32_t* rec = reinterpret_cast<const uint32_t*>(pgm + lean_vc) + j * 8 * LVW;
+          uint32_t wds[LNWV];
+          if constexpr (LNWV == 2) {
+            const uint2 v = *reinterpret_cast<const uint2*>(rec);
+            wds[0] = v.x;
+            wds[1] = v.y;
+          } else {
+#pragma unroll
+            for (int i = 0; i < LNWV / 4; ++i) {
+              const uint4 v = reinterpret_cast<const uint4*>(rec)[i];
+              wds[4 * i] = v.x;
+              wds[4 * i + 1] = v.y;
+              wds[4 * i + 2] = v.z;
+              wds[4 * i + 3] = v.w;
+            }
+          }
+#pragma unroll
+          for (int wi = 0; wi < LNWV; ++wi) {
+            float f[MV::PER_WORD];
+            MV::to_float(wds[wi], f);
+#pragma unroll
+            for (int m = 0; m < MV::PER_WORD / 2; ++m) {
+              const int i = wi * MV::PER_WORD + 2 * m;
+              const float2 r = __ffma2_rn(make_float2(f[2 * m], f[2 * m + 1]), ps2,
+                                          make_float2(st.acc[0][i], st.acc[0][i + 1]));
+              st.acc[0][i] = r.x;
+              st.acc[0][i + 1] = r.y;
+            }
+          }
+        }
+      } else {
         const int g = (stt * 32) >> p.log2G;  // key group of this sub-tile (G >= 32)
         float sc[TPL][HG];
 
@@ -523,8 +631,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
             const float s = h2f((uint16_t)(mz >> 16)) * k_unscale[j];
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
-              qp_s[warp][h][c] = q_s[h][c] * s;
-              zp[h] = fmaf(q_s[h][c], z, zp[h]);
+              qp_s[warp][h][c] = qs[h][c] * s;
+              zp[h] = fmaf(qs[h][c], z, zp[h]);
             }
           }
           __syncwarp();
@@ -589,7 +697,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
                   const float z = h2f((uint16_t)(km[g * D + c] & 0xFFFFu));
                   const float xv = h2f(sv[tt * p.nsp + k]);
 #pragma unroll
-                  for (int h = 0; h < HG; ++h) sc[j][h] = fmaf(q_s[h][c], xv - z, sc[j][h]);
+                  for (int h = 0; h < HG; ++h) sc[j][h] = fmaf(qs[h][c], xv - z, sc[j][h]);
                 }
               }
             }
@@ -655,7 +763,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
               const float rh = kh[i] * cs + kl[i] * sn;
 #pragma unroll
               for (int h = 0; h < HG; ++h)
-                a[h] = fmaf(q_s[h][kc_lo + i], rl, fmaf(q_s[h][kc_lo + D / 2 + i], rh, a[h]));
+                a[h] = fmaf(qs[h][kc_lo + i], rl, fmaf(qs[h][kc_lo + D / 2 + i], rh, a[h]));
             }
 #pragma unroll
             for (int h = 0; h < HG; ++h) sc[j][h] = a[h];
@@ -719,27 +827,26 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
       }
       __syncwarp();
       if (lane == 0) {
-        // release the stage; the last warp to release it refills it with page pg_seq + kStages
+        // release this sub-tile of the stage; the warp releasing its last sub-tile refills the
+        // stage with page kpg + n_stages of the slice
         mbar_arrive(&empty_bar[stg]);
-        if (atomicAdd(&stage_cnt[stg], 1) % kConsumerWarps == kConsumerWarps - 1 && pg_seq + kStages < n_pg &&
+        if (atomicAdd(&stage_cnt[stg], 1) % SPP == SPP - 1 && kpg + n_stages < n_pg &&
             !*(volatile int*)&abort_flag) {
-          if (mbar_wait(&empty_bar[stg], (pg_seq / kStages) & 1)) {
-            issue_page(pg_seq + kStages);
+          if (mbar_wait(&empty_bar[stg], (kpg >> log2S) & 1)) {
+            issue_page(kpg + n_stages);
           } else {
             report_error(p.err, kDevWaitTimeout);
             atomicExch(&abort_flag, 1);
           }
         }
       }
-      ++pg_seq;
     } else {
-      // ---------------- the fp16 window: tokens Tq .. Tq + n_r - 1, read directly
-      fold();
+      // ---------------- the fp16 window: tokens Tq .. Tq + n_r - 1, read directly.  It is the
+      // unit's first item, so its loads overlap the prefetch of the unit's pages.
       const int64_t tq = p.n_pages * (int64_t)p.R;
-      const uint16_t* wk = p.wk + unit * p.win_unit_stride;
-      const uint16_t* wv = p.wv + unit * p.win_unit_stride;
-      const int wtiles = (p.n_r + 31) / 32;
-      for (int stt = warp; stt < wtiles; stt += kConsumerWarps) {
+      const uint16_t* wk = p.wk + cur * p.win_unit_stride;
+      const uint16_t* wv = p.wv + cur * p.win_unit_stride;
+      if (32 * stt < p.n_r) {
         float sc[TPL][HG];
 #pragma unroll
         for (int j = 0; j < TPL; ++j) {
@@ -759,7 +866,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
 #pragma unroll
             for (int i = 0; i < CPL; ++i) {
 #pragma unroll
-              for (int h = 0; h < HG; ++h) a[h] = fmaf(q_s[h][kc_lo + i], xk[i], a[h]);
+              for (int h = 0; h < HG; ++h) a[h] = fmaf(qs[h][kc_lo + i], xk[i], a[h]);
             }
           } else {
             const uint32_t tpos = (uint32_t)(tq + tt);
@@ -774,7 +881,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
               const float rl = xl * cs - xh * sn, rh = xh * cs + xl * sn;
 #pragma unroll
               for (int h = 0; h < HG; ++h)
-                a[h] = fmaf(q_s[h][kc_lo + i], rl, fmaf(q_s[h][kc_lo + D / 2 + i], rh, a[h]));
+                a[h] = fmaf(qs[h][kc_lo + i], rl, fmaf(qs[h][kc_lo + D / 2 + i], rh, a[h]));
             }
           }
 #pragma unroll
@@ -803,7 +910,12 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
             const float pw = sc[j][h];
             st.l[h] += pw;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) st.acc[h][i] = fmaf(pw, xv[i], st.acc[h][i]);
+            for (int i = 0; i < CPL; ++i) {
+              // in the units of the fast value path (exact powers of two), undone by the fold
+              const float sb = S::FAST_V ? MaskCodes<S::FAST_V ? BV : 2>::scale_back((vc_lo + i) % (32 / (S::FAST_V ? BV : 2)))
+                                         : 1.0f;
+              st.acc[h][i] = fmaf(pw * sb, xv[i], st.acc[h][i]);
+            }
           }
         }
       }
@@ -811,33 +923,60 @@ __global__ void __launch_bounds__(kDecodeThreads, (Shape<BK, BV, HG, ROPE>::MIN_
   }
   if (cur >= 0) epilogue(cur, done);
   // never leave with a copy in flight (only possible after an abort): wait, bounded, for the
-  // last copy issued into every stage and query buffer
+  // last copy issued into every stage
   __syncthreads();
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i)
+    for (int i = 0; i < n_stages; ++i)
       if (stage_issued[i] > 0) mbar_wait(&full_bar[i], (stage_issued[i] - 1) & 1);
-    for (int i = 0; i < 2; ++i)
-      if (qbuf_issued[i] > 0) mbar_wait(&q_full[i], (qbuf_issued[i] - 1) & 1);
   }
 }
 
-template <int BK, int BV, int HG, bool ROPE>
+// Page stages of one CTA: the largest power of two up to kMaxStages whose pages fit the opt-in
+// shared memory beside the kernel's static arrays; -1 when not even one fits.
+template <int BK, int BV, int HG, bool ROPE, bool LEAN>
+int log2_stages_t(int page_bytes) {
+  auto kern = decode_kernel<BK, BV, HG, ROPE, LEAN>;
+  static int static_smem = -1, optin = -1;
+  if (static_smem < 0) {
+    cudaFuncAttributes a{};
+    int dev = 0;
+    if (cudaFuncGetAttributes(&a, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return -1;
+    static_smem = (int)a.sharedSizeBytes;
+  }
+  const int avail = optin - static_smem;
+  int l = 4;  // kMaxStages = 16
+  while (l >= 0 && ((int64_t)page_bytes << l) > avail) --l;
+  return l;
+}
+
+template <int BK, int BV, int HG, bool ROPE, bool LEAN>
 cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t s) {
-  const size_t smem = (size_t)kStages * p.lay.bytes;
-  auto kern = decode_kernel<BK, BV, HG, ROPE>;
+  const int l = log2_stages_t<BK, BV, HG, ROPE, LEAN>(p.lay.bytes);
+  if (l < 0) return cudaErrorInvalidValue;
+  DecodeParams q = p;
+  q.log2_stages = l;
+  const size_t smem = (size_t)p.lay.bytes << l;
+  auto kern = decode_kernel<BK, BV, HG, ROPE, LEAN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kDecodeThreads, smem, s>>>(p);
+  kern<<<grid, Shape<BK, BV, HG, ROPE>::WARPS * 32, smem, s>>>(q);
   return cudaGetLastError();
 }
 
-template <int BK, int BV, int HG, bool ROPE>
-int resident_t(int page_bytes) {
-  const size_t smem = (size_t)kStages * page_bytes;
-  auto kern = decode_kernel<BK, BV, HG, ROPE>;
+template <int BK, int BV, int HG, bool ROPE, bool LEAN>
+int resident_t(int page_bytes, int* warps) {
+  *warps = Shape<BK, BV, HG, ROPE>::WARPS;
+  const int l = log2_stages_t<BK, BV, HG, ROPE, LEAN>(page_bytes);
+  if (l < 0) return 0;
+  const size_t smem = (size_t)page_bytes << l;
+  auto kern = decode_kernel<BK, BV, HG, ROPE, LEAN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDecodeThreads, smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape<BK, BV, HG, ROPE>::WARPS * 32, smem) !=
+      cudaSuccess)
+    return 0;
   return n;
 }
 
@@ -849,6 +988,9 @@ int resident_t(int page_bytes) {
   X(2, 2, 1, true) X(2, 2, 4, true) X(3, 3, 1, true) X(3, 3, 4, true) X(4, 2, 1, true) X(4, 2, 4, true)       \
   X(4, 4, 1, true) X(4, 4, 4, true)
 
+// configurations with a lean page path instantiated
+#define KVQ_LEAN_CASES(X) X(2, 2) X(4, 2) X(4, 4)
+
 bool decode_supported(int bk, int bv, int hg, bool rope) {
 #define KVQ_SUP(BKV, BVV, HGV, RP) \
   if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return true;
@@ -857,9 +999,25 @@ bool decode_supported(int bk, int bv, int hg, bool rope) {
   return false;
 }
 
-int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int page_bytes) {
+bool decode_lean(int bk, int bv, int hg, bool rope, int R, int nsp) {
+  if (hg != 1 || rope || R != 128 || nsp != 0) return false;
+#define KVQ_L(BKV, BVV) \
+  if (bk == BKV && bv == BVV) return true;
+  KVQ_LEAN_CASES(KVQ_L)
+#undef KVQ_L
+  return false;
+}
+
+int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int R, int nsp, int page_bytes, int* warps) {
+  *warps = 0;
+  if (decode_lean(bk, bv, hg, rope, R, nsp)) {
+#define KVQ_LRES(BKV, BVV) \
+    if (bk == BKV && bv == BVV) return resident_t<BKV, BVV, 1, false, true>(page_bytes, warps);
+    KVQ_LEAN_CASES(KVQ_LRES)
+#undef KVQ_LRES
+  }
 #define KVQ_RES(BKV, BVV, HGV, RP) \
-  if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return resident_t<BKV, BVV, HGV, RP>(page_bytes);
+  if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return resident_t<BKV, BVV, HGV, RP, false>(page_bytes, warps);
   KVQ_DECODE_CASES(KVQ_RES)
 #undef KVQ_RES
   return 0;
@@ -868,8 +1026,14 @@ int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int page_byte
 cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool rope, int grid, cudaStream_t s,
                           bool* supported) {
   *supported = true;
+  if (decode_lean(bk, bv, hg, rope, p.R, p.nsp)) {
+#define KVQ_LDEC(BKV, BVV) \
+    if (bk == BKV && bv == BVV) return launch_decode_t<BKV, BVV, 1, false, true>(p, grid, s);
+    KVQ_LEAN_CASES(KVQ_LDEC)
+#undef KVQ_LDEC
+  }
 #define KVQ_DEC(BKV, BVV, HGV, RP) \
-  if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return launch_decode_t<BKV, BVV, HGV, RP>(p, grid, s);
+  if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return launch_decode_t<BKV, BVV, HGV, RP, false>(p, grid, s);
   KVQ_DECODE_CASES(KVQ_DEC)
 #undef KVQ_DEC
   *supported = false;

@@ -80,6 +80,7 @@ struct DecodeParams {
   int32_t work_per_unit;    // n_pages + (n_r > 0): page items then the window item
   int32_t n_r;              // window tokens
   int32_t max_slots;        // partial slots per query head
+  int32_t log2_stages;      // page stages per CTA (set by the launcher)
   int32_t Hkv, Hq, D, G, R, nsp;
   int32_t log2G;            // G = 1 << log2G
   PageLayout lay;
@@ -87,7 +88,8 @@ struct DecodeParams {
   const unsigned long long* rope_turns;  // [D/2] theta_i / (2*pi) as 0.64 fixed point (rope only)
   float* part_ml;           // [B*Hq][max_slots][2]  (running max in log2 units, sum)
   float* part_acc;          // [B*Hq][max_slots][D]
-  int* counters;            // [B*Hkv] items finished per unit, zero between calls
+  int* counters;            // [B*Hkv] sub-tiles finished per unit, zero between calls
+  int* nslot;               // [B*Hkv] partial slots taken per unit, zero between calls
   uint16_t* out;            // [B][Hq][D] fp16 bits
   int* err;
 };
@@ -97,7 +99,11 @@ cudaError_t launch_quantize(const QuantizeParams& p, int bk, int bv, int n_pages
 cudaError_t launch_copy_tokens(const CopyTokensParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool rope, int grid, cudaStream_t s,
                           bool* supported);
-int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int page_bytes);
+// Decode CTAs resident per SM (0: unsupported), and in *warps the warps of one CTA: the partial
+// slots a unit needs are warps * (CTAs whose slices meet the unit).
+int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int R, int nsp, int page_bytes, int* warps);
+// true when decode runs the lean page path (one query head per kv head, 2/4-bit, R = 128, no sparse)
+bool decode_lean(int bk, int bv, int hg, bool rope, int R, int nsp);
 bool decode_supported(int bk, int bv, int hg, bool rope);
 bool quantize_supported(int bk, int bv);
 size_t quantize_smem_bytes(int R, int D, int G, const PageLayout& lay);

@@ -73,36 +73,41 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   }
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return KVQ_ERR_CUDA;
-  const int per_sm = kvq::decode_resident_ctas_per_sm(cfg->k_bits, cfg->v_bits, hg, cfg->rope != 0, lay.bytes);
+  int warps = 0;
+  const int per_sm = kvq::decode_resident_ctas_per_sm(cfg->k_bits, cfg->v_bits, hg, cfg->rope != 0, cfg->residual,
+                                                     cfg->k_sparse, lay.bytes, &warps);
   if (per_sm < 1) {
     cudaGetLastError();
     return KVQ_ERR_UNSUPPORTED;
   }
 
-  // Scratch layout: the RoPE turn table, per-unit counters, then (m, l) and acc[D] per query
-  // head and slice.
-  // Each unit is cut into k equal slices (k CTAs), k >= 2, as many as the scratch and the
-  // resident CTAs allow; a size whose two slices per unit do not fit is refused.
+  // Scratch layout: the RoPE turn table, per-unit tickets and slot counts, then (m, l) and acc[D]
+  // per query head and partial slot.  The grid is the resident CTA count, lowered until the
+  // slots it needs (warps * (ceil(grid / units) + 2) per query head) fit; a size that does not
+  // fit even one CTA is refused.
   const int64_t wpu = n_pages + (n_tokens - tq > 0 ? 1 : 0);
   const size_t rope_bytes = 256 * 8;  // room for the RoPE turn table (D/2 entries)
-  const size_t counter_bytes = rope_bytes + ((size_t)n_units * sizeof(int) + 255) / 256 * 256;
-  const size_t per_slot = (size_t)heads * (2 + D) * sizeof(float);
-  if (counter_bytes + 2 * per_slot > kScratchBytes) return KVQ_ERR_CAPACITY;
-  int64_t k = (int64_t)per_sm * sms / n_units;
-  if (k < 2) k = 2;
-  const int64_t k_fit = (int64_t)((kScratchBytes - counter_bytes) / per_slot);
-  if (k > k_fit) k = k_fit;
-  if (k > wpu) k = wpu;
-  if (k < 1) k = 1;
+  const size_t counter_bytes = rope_bytes + ((size_t)n_units * 2 * sizeof(int) + 255) / 256 * 256;
+  auto slots_for = [&](int64_t g) { return (int64_t)warps * ((g + n_units - 1) / n_units + 2); };
+  auto ml_bytes_for = [&](int64_t sl) { return ((size_t)heads * sl * 2 * sizeof(float) + 255) / 256 * 256; };
+  auto bytes_for = [&](int64_t g) {
+    const int64_t sl = slots_for(g);
+    return counter_bytes + ml_bytes_for(sl) + (size_t)heads * sl * D * sizeof(float);
+  };
+  int64_t grid = (int64_t)per_sm * sms;
+  if (grid > n_units * wpu) grid = n_units * wpu;
+  while (grid > 1 && bytes_for(grid) > kScratchBytes) grid = grid * 3 / 4;
+  if (bytes_for(grid) > kScratchBytes) return KVQ_ERR_CAPACITY;
+  const int64_t slots = slots_for(grid);
 
   unsigned char* base = static_cast<unsigned char*>(scratch);
   unsigned long long* rope_turns = reinterpret_cast<unsigned long long*>(base);
   int* counters = reinterpret_cast<int*>(base + rope_bytes);
   float* part_ml = reinterpret_cast<float*>(base + counter_bytes);
-  float* part_acc = part_ml + (size_t)heads * k * 2;
+  float* part_acc = reinterpret_cast<float*>(base + counter_bytes + ml_bytes_for(slots));
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   // the counters must start at zero; a call that stopped early may have left them set
-  if (cudaMemsetAsync(counters, 0, (size_t)n_units * sizeof(int), s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaMemsetAsync(counters, 0, (size_t)n_units * 2 * sizeof(int), s) != cudaSuccess) return KVQ_ERR_CUDA;
   if (cfg->rope) {
     // pageable source: the copy has taken the table by the time the call returns
     unsigned long long table[kvq::kHeadDim / 2];
@@ -122,7 +127,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   dp.n_pages = n_pages;
   dp.work_per_unit = (int32_t)wpu;
   dp.n_r = (int32_t)(n_tokens - tq);
-  dp.max_slots = (int32_t)k;
+  dp.max_slots = (int32_t)slots;
   dp.Hkv = cfg->num_kv_heads;
   dp.Hq = cfg->num_q_heads;
   dp.D = D;
@@ -136,10 +141,10 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   dp.part_ml = part_ml;
   dp.part_acc = part_acc;
   dp.counters = counters;
+  dp.nslot = counters + n_units;
   dp.out = static_cast<uint16_t*>(out_f16);
   dp.err = nullptr;
   bool supported = false;
-  const int64_t grid = n_units * k;  // k <= items per unit: every CTA has work
   if (kvq::launch_decode(dp, cfg->k_bits, cfg->v_bits, hg, cfg->rope != 0, (int)grid, s, &supported) != cudaSuccess)
     return supported ? KVQ_ERR_CUDA : KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
