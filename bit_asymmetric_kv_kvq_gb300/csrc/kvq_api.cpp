@@ -168,9 +168,10 @@ void rope_table(double base, int D, unsigned long long* out) {
   for (int i = 0; i < D / 2; ++i) out[i] = rope_turn_fraction(base, i, D);
 }
 
-PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp) {
+PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp, bool rope) {
   auto r16 = [](int64_t x) { return (int32_t)((x + 15) / 16 * 16); };
   PageLayout l{};
+  l.frag = (bk == 2 || bk == 4) && (bv == 2 || bv == 4) && !rope ? 1 : 0;
   l.off_kc = 0;
   l.off_km = l.off_kc + r16((int64_t)R * D * bk / 8);
   l.off_vc = l.off_km + r16((int64_t)(R / G) * D * 4);
@@ -224,7 +225,7 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   }
   c->sm_count = prop.multiProcessorCount;
   const int D = cfg->head_dim, R = cfg->residual, G = cfg->group_size;
-  c->lay = kvq::make_layout(R, D, G, cfg->k_bits, cfg->v_bits, cfg->k_sparse);
+  c->lay = kvq::make_layout(R, D, G, cfg->k_bits, cfg->v_bits, cfg->k_sparse, cfg->rope != 0);
   if (kvq::quantize_smem_bytes(R, D, G, c->lay) > (size_t)prop.sharedMemPerBlockOptin) {
     delete c;
     return KVQ_ERR_UNSUPPORTED;
@@ -526,10 +527,50 @@ kvq_status kvq_export_unit(kvq_cache* c, int32_t b, int32_t kvh, kvq_unit_view* 
                          cudaSuccess)
     return fail_cuda(c);
   const int64_t kc_row = (int64_t)D * bk / 8, vc_row = (int64_t)D * bv / 8;
+  // code of (token, channel) into a token-major bitstream of `bits`-bit codes
+  auto put = [](uint8_t* rows, int64_t row_bytes, int bits, int token, int ch, uint32_t code) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(rows + token * row_bytes);
+    const int b = ch * bits;
+    w[b >> 5] |= code << (b & 31);
+    if ((b & 31) + bits > 32) w[(b >> 5) + 1] |= code >> (32 - (b & 31));
+  };
   for (int64_t p = 0; p < n_pages; ++p) {
     const uint8_t* src = pg.data() + p * L.bytes;
-    if (dst->kcodes) std::memcpy((uint8_t*)dst->kcodes + p * R * kc_row, src + L.off_kc, (size_t)(R * kc_row));
-    if (dst->vcodes) std::memcpy((uint8_t*)dst->vcodes + p * R * vc_row, src + L.off_vc, (size_t)(R * vc_row));
+    if (!L.frag) {
+      if (dst->kcodes) std::memcpy((uint8_t*)dst->kcodes + p * R * kc_row, src + L.off_kc, (size_t)(R * kc_row));
+      if (dst->vcodes) std::memcpy((uint8_t*)dst->vcodes + p * R * vc_row, src + L.off_vc, (size_t)(R * vc_row));
+    } else {
+      // fragment order (see frag_key_pair / frag_value_pair) back to token-major bitstreams
+      const uint32_t* kw = reinterpret_cast<const uint32_t*>(src + L.off_kc);
+      const uint32_t* vw = reinterpret_cast<const uint32_t*>(src + L.off_vc);
+      uint8_t* kout = dst->kcodes ? (uint8_t*)dst->kcodes + p * R * kc_row : nullptr;
+      uint8_t* vout = dst->vcodes ? (uint8_t*)dst->vcodes + p * R * vc_row : nullptr;
+      if (kout) std::memset(kout, 0, (size_t)(R * kc_row));
+      if (vout) std::memset(vout, 0, (size_t)(R * vc_row));
+      for (int tile = 0; tile < R / 16; ++tile)
+        for (int lane = 0; lane < 32; ++lane) {
+          for (int w = 0; w < 2 * bk && kout; ++w) {
+            const uint32_t word = kw[((int64_t)tile * 32 + lane) * 2 * bk + w];
+            for (int j = 0; j < 16 / bk; ++j) {
+              int tok, c0;
+              kvq::frag_key_pair(bk, tile, lane, w, j, &tok, &c0);
+              const uint32_t m = (1u << bk) - 1u;
+              put(kout, kc_row, bk, tok, c0, (word >> (bk * j)) & m);
+              put(kout, kc_row, bk, tok, c0 + 1, (word >> (16 + bk * j)) & m);
+            }
+          }
+          for (int w = 0; w < 2 * bv && vout; ++w) {
+            const uint32_t word = vw[((int64_t)tile * 32 + lane) * 2 * bv + w];
+            for (int j = 0; j < 16 / bv; ++j) {
+              int tok, ch;
+              kvq::frag_value_pair(bv, tile, lane, w, j, &tok, &ch);
+              const uint32_t m = (1u << bv) - 1u;
+              put(vout, vc_row, bv, tok, ch, (word >> (bv * j)) & m);
+              put(vout, vc_row, bv, tok + 1, ch, (word >> (16 + bv * j)) & m);
+            }
+          }
+        }
+    }
     const uint32_t* km = reinterpret_cast<const uint32_t*>(src + L.off_km);
     for (int64_t i = 0; i < (int64_t)(R / G) * D; ++i) {
       const int64_t o = p * (R / G) * D + i;

@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ int stage_cnt[kMaxStages];     // sub-tiles released per stage (mod SPP: the last refills)
   __shared__ int stage_issued[kMaxStages];  // copies issued into each stage so far
+  __shared__ int stage_page[kMaxStages];    // page of the slice a stage holds or is being filled with
   __shared__ __align__(16) float qw_s[W][HG][D];  // each warp's query rows (fp32) for its unit
   __shared__ __align__(16) float qp_s[W][HG][D];  // each warp's q' for its key group
   __shared__ int next_sub;
@@ -256,6 +257,22 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
     bulk_g2s(stage_mem + (size_t)st * page_bytes, p.pages + (int64_t)u * p.unit_page_stride + (int64_t)loc * page_bytes,
              (uint32_t)page_bytes, &full_bar[st]);
     stage_issued[st] = (k >> log2S) + 1;
+    stage_page[st] = k;
+  };
+  // A warp may have taken a sub-tile of page k while a stage still serves page k - n_stages
+  // (or an older one: warps run ahead of a warp that holds a page while it merges a unit), and a
+  // parity wait cannot tell phases 2*n_stages pages apart.  So wait until the stage is assigned
+  // page k, then for its copy.  Bounded like every wait here.
+  auto wait_page = [&](int k) -> bool {
+    const int st = k & (n_stages - 1);
+    if (*(volatile int*)&stage_page[st] != k) {
+      const unsigned long long t0 = global_ns();
+      while (*(volatile int*)&stage_page[st] != k) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(128);
+      }
+    }
+    return mbar_wait(&full_bar[st], (k >> log2S) & 1);
   };
 
   if (tid == 0) {
@@ -266,6 +283,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       mbar_init(&empty_bar[i], SPP);
       stage_cnt[i] = 0;
       stage_issued[i] = 0;
+      stage_page[i] = -1;
     }
     fence_mbar_init();
   }
@@ -473,7 +491,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       // ---------------- a sub-tile of a page of quantized tokens
       const int kpg = (int)(cur * p.n_pages + (loc - hw) - P_begin);
       const int stg = kpg & (n_stages - 1);
-      if (!mbar_wait(&full_bar[stg], (kpg >> log2S) & 1)) {
+      if (!wait_page(kpg)) {
         report_error(p.err, kDevWaitTimeout);
         atomicExch(&abort_flag, 1);
         break;
@@ -945,6 +963,7 @@ int log2_stages_t(int page_bytes) {
       return -1;
     static_smem = (int)a.sharedSizeBytes;
   }
+  if (static_smem > 48 * 1024) return -1;  // more static shared memory than a kernel may declare
   const int avail = optin - static_smem;
   int l = 4;  // kMaxStages = 16
   while (l >= 0 && ((int64_t)page_bytes << l) > avail) --l;
@@ -982,16 +1001,17 @@ int resident_t(int page_bytes, int* warps) {
 
 }  // namespace
 
-#define KVQ_DECODE_CASES(X)                                                                                 \
-  X(2, 2, 1, false) X(2, 2, 2, false) X(2, 2, 4, false) X(4, 2, 1, false) X(4, 2, 2, false) X(4, 2, 4, false) \
-  X(3, 3, 1, false) X(3, 3, 2, false) X(3, 3, 4, false) X(4, 4, 1, false) X(4, 4, 2, false) X(4, 4, 4, false) \
-  X(2, 2, 1, true) X(2, 2, 4, true) X(3, 3, 1, true) X(3, 3, 4, true) X(4, 2, 1, true) X(4, 2, 4, true)       \
-  X(4, 4, 1, true) X(4, 4, 4, true)
+// configurations the CUDA-core kernel serves: codes of 3 bits, or keys rotated at decode
+#define KVQ_DECODE_CASES(X)                                                                                      \
+  X(3, 3, 1, false) X(3, 3, 2, false) X(3, 3, 4, false) X(2, 2, 1, true) X(2, 2, 4, true) X(3, 3, 1, true)       \
+  X(3, 3, 4, true) X(4, 2, 1, true) X(4, 2, 4, true) X(4, 4, 1, true) X(4, 4, 4, true)
 
-// configurations with a lean page path instantiated
-#define KVQ_LEAN_CASES(X) X(2, 2) X(4, 2) X(4, 4)
+namespace {
+bool frag_codes(int bk, int bv, bool rope) { return (bk == 2 || bk == 4) && (bv == 2 || bv == 4) && !rope; }
+}  // namespace
 
 bool decode_supported(int bk, int bv, int hg, bool rope) {
+  if (frag_codes(bk, bv, rope)) return decode_mma_supported(bk, bv, hg);
 #define KVQ_SUP(BKV, BVV, HGV, RP) \
   if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return true;
   KVQ_DECODE_CASES(KVQ_SUP)
@@ -999,23 +1019,11 @@ bool decode_supported(int bk, int bv, int hg, bool rope) {
   return false;
 }
 
-bool decode_lean(int bk, int bv, int hg, bool rope, int R, int nsp) {
-  if (hg != 1 || rope || R != 128 || nsp != 0) return false;
-#define KVQ_L(BKV, BVV) \
-  if (bk == BKV && bv == BVV) return true;
-  KVQ_LEAN_CASES(KVQ_L)
-#undef KVQ_L
-  return false;
-}
-
 int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int R, int nsp, int page_bytes, int* warps) {
+  (void)R;
+  (void)nsp;
   *warps = 0;
-  if (decode_lean(bk, bv, hg, rope, R, nsp)) {
-#define KVQ_LRES(BKV, BVV) \
-    if (bk == BKV && bv == BVV) return resident_t<BKV, BVV, 1, false, true>(page_bytes, warps);
-    KVQ_LEAN_CASES(KVQ_LRES)
-#undef KVQ_LRES
-  }
+  if (frag_codes(bk, bv, rope)) return decode_mma_resident(bk, bv, hg, page_bytes, warps);
 #define KVQ_RES(BKV, BVV, HGV, RP) \
   if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return resident_t<BKV, BVV, HGV, RP, false>(page_bytes, warps);
   KVQ_DECODE_CASES(KVQ_RES)
@@ -1025,13 +1033,9 @@ int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int R, int ns
 
 cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool rope, int grid, cudaStream_t s,
                           bool* supported) {
-  *supported = true;
-  if (decode_lean(bk, bv, hg, rope, p.R, p.nsp)) {
-#define KVQ_LDEC(BKV, BVV) \
-    if (bk == BKV && bv == BVV) return launch_decode_t<BKV, BVV, 1, false, true>(p, grid, s);
-    KVQ_LEAN_CASES(KVQ_LDEC)
-#undef KVQ_LDEC
-  }
+  *supported = decode_supported(bk, bv, hg, rope);
+  if (!*supported) return cudaErrorInvalidValue;
+  if (p.lay.frag) return launch_decode_mma(p, bk, bv, hg, grid, s);
 #define KVQ_DEC(BKV, BVV, HGV, RP) \
   if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return launch_decode_t<BKV, BVV, HGV, RP, false>(p, grid, s);
   KVQ_DECODE_CASES(KVQ_DEC)

@@ -1,0 +1,753 @@
+// Decode attention on the tensor cores, for pages whose codes are stored in
+// fragment order (2- or 4-bit keys and values, keys stored after RoPE).
+//
+// Both halves of decode attention are small matrix products per 16-token tile
+// ("KV cache has a geometry problem, not a bit problem", section "Why the KV
+// cache is a problem": every generated token reads the whole cache):
+//
+//   scores  S[token][head]   = sum_c code_k[token][c] * q'_h[c]  + Z_h,
+//           q'_h[c] = q_h[c] s_c, Z_h = sum_c q_h[c] z_c   (keys per channel over G tokens)
+//   values  O[c][head]      += sum_t code_v[t][c] * p_h[t] s_{t,g(c)}  (+ sum_t p_h[t] z_{t,g(c)})
+//                                                          (values per token over G channels)
+//
+// Each is issued as mma.sync m16n8k16 (fp16 in, fp32 accumulate) with the codes
+// as the A operand.  A code pair is turned into an A register with one AND:
+// masked in place, the two codes are exact fp16 subnormals code * 2^(B*p) * 2^-24
+// (see frag_key_pair / frag_value_pair for where each lane's codes sit).  The
+// position scale 2^(B*p) is folded into the B operand for keys (the B row of
+// that k-slot) and into the output scale for values (one position per M-tile).
+// B values are split into a high and a low fp16 part (two of the eight N
+// columns per head), which keeps them to about 22 significant bits.
+//
+// Scheduling is that of the CUDA-core kernel: one CTA per SM streams a
+// contiguous slice of the (window, pages) work list through a ring of page
+// stages, its warps take 32-token sub-tiles from a shared counter, keep their
+// own online-softmax state per unit, and leave one partial per unit they
+// touched; the warp completing a unit merges its partials.  A window sub-tile
+// (fp16 tokens not yet quantized) is computed on the CUDA cores as a
+// partial of its own.
+#include <cuda_fp16.h>
+
+#include "kvq_internal.h"
+#include "kvq_ptx.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kMmaWarps = 16;
+constexpr int kMmaMaxStages = 16;
+constexpr unsigned kAll = 0xffffffffu;
+constexpr float kLazy = 8.0f;  // the running maximum moves only when a score passes it by 8 (log2 units)
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }  // |e| <= 126
+
+// Code pairs of one fragment word (B-bit codes): pair j read in place for j < DIR, from the
+// word shifted down by SHIFT bits otherwise; pos(j) is the exponent of its position scale.
+template <int B>
+struct Pairs {
+  static constexpr int PER = 16 / B;
+  static constexpr int DIR = 10 / B;
+  static constexpr int SHIFT = B * DIR;
+  __host__ __device__ static constexpr int pos(int j) { return B * (j < DIR ? j : j - DIR); }
+  __device__ __forceinline__ static uint32_t get(uint32_t w, uint32_t ws, int j) {
+    const uint32_t m = ((((1u << B) - 1u) * 0x00010001u) << pos(j));
+    return (j < DIR ? w : ws) & m;
+  }
+};
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// v as fp16 high part (hl = 0) or the fp16 rounding of what the high part leaves (hl = 1)
+__device__ __forceinline__ float split_part(float v, int hl) {
+  const float hi = __half2float(__float2half_rn(v));
+  return hl ? v - hi : hi;
+}
+
+template <int BK, int BV, int HG>
+__global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const DecodeParams p) {
+  constexpr int D = kHeadDim, W = kMmaWarps;
+  constexpr int NCOL = 2 * HG;   // B columns per value group: (head, high/low)
+  constexpr int GPB = 8 / NCOL;  // value groups per B fragment
+  constexpr int KPW = 8 / BK;    // key k-chunks per fragment word
+  using PK = Pairs<BK>;
+  using PV = Pairs<BV>;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g8 = lane >> 2, t4 = lane & 3;  // mma fragment coordinates
+  const int cta = blockIdx.x, grid = gridDim.x;
+  const int64_t wpu = p.work_per_unit;
+  const int64_t total = p.n_units * wpu;
+  const int64_t w_begin = (int64_t)cta * total / grid;
+  const int64_t w_end = (int64_t)(cta + 1) * total / grid;
+  const int page_bytes = p.lay.bytes;
+  const int log2S = p.log2_stages, n_stages = 1 << log2S;
+  const int SPP = p.R / 32;
+  const int n_sub = (int)(w_end - w_begin) * SPP;
+  const int ng = D >> p.log2G;             // value groups per token
+  const int NB = (ng + GPB - 1) / GPB;     // B fragments for the values of one tile
+
+  // dynamic shared memory: the page stages, then each warp's query rows (fp32) and key B
+  // fragments (static arrays stay small: static shared memory is limited to 48 KB)
+  extern __shared__ __align__(128) uint8_t stage_mem[];
+  float(*qw_s)[HG][D] = reinterpret_cast<float(*)[HG][D]>(stage_mem + ((size_t)p.lay.bytes << p.log2_stages));
+  uint32_t(*bk_s)[NCOL][4][16] = reinterpret_cast<uint32_t(*)[NCOL][4][16]>(qw_s + W);
+  __shared__ __align__(8) uint64_t full_bar[kMmaMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMmaMaxStages];
+  __shared__ int stage_cnt[kMmaMaxStages];
+  __shared__ int stage_issued[kMmaMaxStages];
+  __shared__ int stage_page[kMmaMaxStages];     // page of the slice a stage holds or is being filled with
+  __shared__ int next_sub;
+  __shared__ int abort_flag;
+
+  const int hw = (int)(wpu - p.n_pages);
+  auto pages_before = [&](int64_t x) -> int64_t {
+    const int64_t u = x / wpu, l = x - u * wpu;
+    return u * p.n_pages + (l > hw ? l - hw : 0);
+  };
+  const int64_t P_begin = pages_before(w_begin);
+  const int n_pg = (int)(pages_before(w_end) - P_begin);
+  auto issue_page = [&](int k) {
+    const uint32_t P = (uint32_t)(P_begin + k), np = (uint32_t)p.n_pages;
+    const uint32_t u = P / np, loc = P - u * np;
+    const int st = k & (n_stages - 1);
+    mbar_arrive_expect_tx(&full_bar[st], (uint32_t)page_bytes);
+    bulk_g2s(stage_mem + (size_t)st * page_bytes, p.pages + (int64_t)u * p.unit_page_stride + (int64_t)loc * page_bytes,
+             (uint32_t)page_bytes, &full_bar[st]);
+    stage_issued[st] = (k >> log2S) + 1;
+    stage_page[st] = k;
+  };
+  // A warp may have taken a sub-tile of page k while a stage still serves page k - n_stages
+  // (or an older one: warps run ahead of a warp that holds a page while it merges a unit), and a
+  // parity wait cannot tell phases 2*n_stages pages apart.  So wait until the stage is assigned
+  // page k, then for its copy.  Bounded like every wait here.
+  auto wait_page = [&](int k) -> bool {
+    const int st = k & (n_stages - 1);
+    if (*(volatile int*)&stage_page[st] != k) {
+      const unsigned long long t0 = global_ns();
+      while (*(volatile int*)&stage_page[st] != k) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(128);
+      }
+    }
+    return mbar_wait(&full_bar[st], (k >> log2S) & 1);
+  };
+
+  if (tid == 0) {
+    abort_flag = 0;
+    next_sub = 0;
+    for (int i = 0; i < n_stages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], SPP);
+      stage_cnt[i] = 0;
+      stage_issued[i] = 0;
+      stage_page[i] = -1;
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int k = 0; k < n_pg && k < n_stages; ++k) issue_page(k);
+
+  float (*qs)[D] = qw_s[warp];
+  const int hcol = (g8 % NCOL) / 2;  // head of this lane's B column g8
+  const int hl = g8 & 1;             // high (0) or low (1) part in that column
+  const int gl = g8 / NCOL;          // value group of that column within a B fragment
+  const int hmine = t4 % HG;         // head of this lane's D columns 2*t4, 2*t4 + 1
+  const int gmine = t4 / HG;         // value group of those columns within a B fragment
+
+  // ---- per-warp state for the current unit
+  float dv[8][4];            // value accumulators, one m16n8 tile per 16 channels
+  float mrun;                // running maximum of head hmine (log2 units)
+  float lacc, zacc[4];       // sum of p (column owners) and p*z per B fragment
+  int es;                    // exponent bound of the value scales seen (B values carry 2^(6-es));
+                             // starts below every fp16 scale (>= 2^-24)
+  auto reset = [&]() {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dv[i][j] = 0.0f;
+    mrun = -INFINITY;
+    lacc = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) zacc[i] = 0.0f;
+    es = -30;
+  };
+
+  auto load_q = [&](int64_t unit) {
+    constexpr int PERL = HG * D / 32;
+    const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
+    const uint16_t* src = p.q + (b * p.Hq + kvh * HG) * D + lane * PERL;
+    float v[PERL];
+#pragma unroll
+    for (int i = 0; i < PERL; i += 4) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(src + i));
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+      const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+      v[i] = a.x;
+      v[i + 1] = a.y;
+      v[i + 2] = c.x;
+      v[i + 3] = c.y;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < PERL; ++i) (&qs[0][0])[lane * PERL + i] = v[i];
+    __syncwarp();
+  };
+
+  auto slot_of = [&](int64_t unit) {
+    int slot = 0;
+    if (lane == 0) slot = atomicAdd(p.nslot + unit, 1);
+    return __shfl_sync(kAll, slot, 0);
+  };
+
+  // the ticket; the warp completing the unit merges every partial and writes the output
+  auto finish = [&](int64_t unit, int done) {
+    const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
+    const int64_t bh0 = b * p.Hq + kvh * HG;
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      int prev;
+      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(prev) : "l"(p.counters + unit), "r"(done)
+                   : "memory");
+      last = prev + done == (int)(wpu * SPP);
+    }
+    last = __shfl_sync(kAll, last, 0);
+    if (!last) return;
+    int n = 0;
+    if (lane == 0) n = __ldcg(p.nslot + unit);
+    n = __shfl_sync(kAll, n, 0);
+    if (n > p.max_slots) n = p.max_slots;
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      const float* ml = p.part_ml + (bh0 + h) * p.max_slots * 2;
+      const float* pacc = p.part_acc + (bh0 + h) * p.max_slots * D + 4 * lane;
+      float M = -INFINITY;
+      for (int sp = lane; sp < n; sp += 32) M = fmaxf(M, __ldcg(ml + 2 * sp));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, off));
+      float L = 0.0f, a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll 8
+      for (int sp = 0; sp < n; ++sp) {
+        const float2 mlv = __ldcg(reinterpret_cast<const float2*>(ml + 2 * sp));
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(pacc + (int64_t)sp * D));
+        const float f = mlv.x == -INFINITY ? 0.0f : exp2f(mlv.x - M);
+        L = fmaf(f, mlv.y, L);
+        a0 = fmaf(f, v.x, a0);
+        a1 = fmaf(f, v.y, a1);
+        a2 = fmaf(f, v.z, a2);
+        a3 = fmaf(f, v.w, a3);
+      }
+      const float inv = 1.0f / L;
+      uint2 packed;
+      packed.x = pack_half2(a0 * inv, a1 * inv);
+      packed.y = pack_half2(a2 * inv, a3 * inv);
+      *reinterpret_cast<uint2*>(p.out + (bh0 + h) * D + 4 * lane) = packed;
+    }
+    if (lane == 0) {
+      p.counters[unit] = 0;
+      p.nslot[unit] = 0;
+    }
+  };
+
+  // This warp leaves `unit`: its partial (m, l, acc) per head into a fresh slot, then the ticket.
+  auto epilogue = [&](int64_t unit, int done) {
+    const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
+    const int64_t bh0 = b * p.Hq + kvh * HG;
+    // column owners' sums over the four lanes of a fragment row (t4)
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+      lacc += __shfl_xor_sync(kAll, lacc, off);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) zacc[i] += __shfl_xor_sync(kAll, zacc[i], off);
+    }
+    const int slot = slot_of(unit);
+    if (slot < p.max_slots) {
+      // zero-point sums of this lane's (group, head): owned by the lanes of column 2*t4
+      float zs[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) zs[i] = __shfl_sync(kAll, zacc[i], 4 * (2 * t4));
+      const float osc = pow2f(24 - (6 - es));
+#pragma unroll
+      for (int mc = 0; mc < 8; ++mc) {
+        const int grp = (16 * mc) >> p.log2G;
+        if (grp % GPB != gmine) continue;
+        const float s = osc * pow2f(-PV::pos(mc % PV::PER));
+        float z = zs[0];
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+          if (grp / GPB == i) z = zs[i];
+        float* dst = p.part_acc + ((bh0 + hmine) * p.max_slots + slot) * D + 16 * mc + g8;
+        dst[0] = fmaf(dv[mc][0] + dv[mc][1], s, z);
+        dst[8] = fmaf(dv[mc][2] + dv[mc][3], s, z);
+      }
+      // (m, l) of head h: m from lane h, l from the owners of column 2h (lane 8h)
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        const float mh = __shfl_sync(kAll, mrun, h);
+        const float lh = __shfl_sync(kAll, lacc, 8 * h);
+        if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + ((bh0 + h) * p.max_slots + slot) * 2) = make_float2(mh, lh);
+      }
+    } else if (lane == 0) {
+      report_error(p.err, kDevBadArgument);  // slots are sized for the grid: not reached
+    }
+    finish(unit, done);
+  };
+
+  // A window sub-tile (fp16 tokens Tq + 32*stt .. ) as a partial of its own: lane l scores
+  // token 32*stt + l, then owns channels 4l .. 4l+3 of the weighted sum.
+  auto window_subtile = [&](int64_t unit, int stt) {
+    const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
+    const int64_t bh0 = b * p.Hq + kvh * HG;
+    const uint16_t* wk = p.wk + unit * p.win_unit_stride;
+    const uint16_t* wv = p.wv + unit * p.win_unit_stride;
+    const int tok = 32 * stt + lane;
+    const bool live = tok < p.n_r;
+    float s[HG];
+#pragma unroll
+    for (int h = 0; h < HG; ++h) s[h] = 0.0f;
+    if (live) {
+      const uint4* row = reinterpret_cast<const uint4*>(wk + (int64_t)tok * D);
+#pragma unroll 4
+      for (int v = 0; v < D / 8; ++v) {
+        const uint4 w = __ldg(row + v);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ws[i]));
+#pragma unroll
+          for (int h = 0; h < HG; ++h) s[h] = fmaf(qs[h][8 * v + 2 * i], f.x, fmaf(qs[h][8 * v + 2 * i + 1], f.y, s[h]));
+        }
+      }
+    }
+    const int slot = slot_of(unit);
+    const int nt = min(32, p.n_r - 32 * stt);
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      const float sc = live ? s[h] * p.qk_scale_log2 : -INFINITY;
+      float m = sc;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kAll, m, off));
+      const float pw = live ? exp2f(sc - m) : 0.0f;
+      float l = pw;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(kAll, l, off);
+      float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+      for (int j = 0; j < nt; ++j) {
+        const float pj = __shfl_sync(kAll, pw, j);
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(wv + (int64_t)(32 * stt + j) * D + 4 * lane));
+        const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+        const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+        a0 = fmaf(pj, x01.x, a0);
+        a1 = fmaf(pj, x01.y, a1);
+        a2 = fmaf(pj, x23.x, a2);
+        a3 = fmaf(pj, x23.y, a3);
+      }
+      if (slot < p.max_slots) {
+        const int64_t so = (bh0 + h) * p.max_slots + slot;
+        *reinterpret_cast<float4*>(p.part_acc + so * D + 4 * lane) = make_float4(a0, a1, a2, a3);
+        if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + so * 2) = make_float2(m, l);
+      }
+    }
+  };
+
+  int64_t cur = -1, ustart = 0;
+  int done = 0;
+  bool touched = false;  // the warp has state (page sub-tiles) for the current unit
+  while (true) {
+    int s = 0;
+    if (lane == 0) s = atomicAdd(&next_sub, 1);
+    s = __shfl_sync(kAll, s, 0);
+    if (s >= n_sub || *(volatile int*)&abort_flag) break;
+    const int sx = SPP == 4 ? s >> 2 : SPP == 2 ? s >> 1 : SPP == 1 ? s : s / 3;
+    const int stt = s - sx * SPP;
+    const int64_t x = w_begin + sx;
+    if (cur < 0 || x >= ustart + wpu) {
+      if (cur >= 0) {
+        if (touched) epilogue(cur, done);
+        else finish(cur, done);
+      }
+      cur = x / wpu;
+      ustart = cur * wpu;
+      done = 0;
+      touched = false;
+      reset();
+      load_q(cur);
+    }
+    ++done;
+    const int loc = (int)(x - ustart);
+    if (loc < hw) {
+      if (32 * stt < p.n_r) window_subtile(cur, stt);
+      continue;
+    }
+
+    // ---------------- a sub-tile of a page: tokens 32*stt .. 32*stt+31
+    touched = true;
+    const int kpg = (int)(cur * p.n_pages + (loc - hw) - P_begin);
+    const int stg = kpg & (n_stages - 1);
+    if (!wait_page(kpg)) {
+      report_error(p.err, kDevWaitTimeout);
+      atomicExch(&abort_flag, 1);
+      break;
+    }
+    const uint8_t* pgm = stage_mem + (size_t)stg * page_bytes;
+    const uint32_t* km = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_km);
+    const uint32_t* vm = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vm);
+    const int gk = (32 * stt) >> p.log2G;  // key group
+
+    // -- key B fragments: q'_h[c] 2^(sig_h - pos) split high/low, four channels per lane
+    float zk[HG], sigk[HG];
+    {
+      const uint4 mz = *reinterpret_cast<const uint4*>(km + gk * D + 4 * lane);
+      const uint32_t mzw[4] = {mz.x, mz.y, mz.z, mz.w};
+      float zc[4], sc4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(&mzw[i]));
+        zc[i] = zs.x;
+        sc4[i] = zs.y;
+      }
+      // channel c = 4*lane + i = 16*kk + 8*hh + 2*tt + e
+      const int kk = lane >> 2, hh = (lane >> 1) & 1;
+      const int pk = PK::pos(2 * (kk % KPW) + hh);
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        const float4 q4 = *reinterpret_cast<const float4*>(&qs[h][4 * lane]);
+        const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+        float qp[4], z = 0.0f, mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          qp[i] = qv[i] * sc4[i];
+          z = fmaf(qv[i], zc[i], z);
+          mx = fmaxf(mx, fabsf(qp[i]));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          z += __shfl_xor_sync(kAll, z, off);
+          mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, off));
+        }
+        zk[h] = z;
+        // largest |B| below 2^15: scale by 2^(14 - floor(log2 max))
+        const int emax = mx > 0.0f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+        const int sig = min(max(14 - emax, -90), 90);
+        sigk[h] = pow2f(24 - sig);  // score = D * 2^(24 - sig)
+        const float sc = pow2f(sig - pk);
+        const int tt0 = 2 * (lane & 1);
+#pragma unroll
+        for (int hlp = 0; hlp < 2; ++hlp) {
+          const float v0 = split_part(qp[0] * sc, hlp), v1 = split_part(qp[1] * sc, hlp);
+          const float v2 = split_part(qp[2] * sc, hlp), v3 = split_part(qp[3] * sc, hlp);
+          bk_s[warp][2 * h + hlp][tt0][2 * kk + hh] = pack_half2(v0, v1);
+          bk_s[warp][2 * h + hlp][tt0 + 1][2 * kk + hh] = pack_half2(v2, v3);
+        }
+      }
+    }
+    __syncwarp();
+    uint32_t bf[16];
+    if (g8 < NCOL) {
+      const uint4* src = reinterpret_cast<const uint4*>(&bk_s[warp][g8][t4][0]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = src[i];
+        bf[4 * i] = v.x;
+        bf[4 * i + 1] = v.y;
+        bf[4 * i + 2] = v.z;
+        bf[4 * i + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) bf[i] = 0u;
+    }
+    __syncwarp();  // bk_s is free for the next sub-tile
+
+    // -- scores of the two 16-token tiles: lane (g8, t4 < HG) gets head t4 of tokens g8, g8 + 8
+    float sc[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int tile = 2 * stt + mt;
+      uint32_t wd[2 * BK];
+      const uint4* wsrc = reinterpret_cast<const uint4*>(pgm + p.lay.off_kc) + ((int64_t)tile * 32 + lane) * (2 * BK / 4);
+#pragma unroll
+      for (int i = 0; i < 2 * BK / 4; ++i) {
+        const uint4 v = wsrc[i];
+        wd[4 * i] = v.x;
+        wd[4 * i + 1] = v.y;
+        wd[4 * i + 2] = v.z;
+        wd[4 * i + 3] = v.w;
+      }
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int u = 0; u < BK; ++u) {
+        const uint32_t X = wd[u], Y = wd[BK + u];
+        const uint32_t Xs = X >> PK::SHIFT, Ys = Y >> PK::SHIFT;
+#pragma unroll
+        for (int jj = 0; jj < KPW; ++jj) {
+          const int kk = u * KPW + jj;
+          mma16816(d, PK::get(X, Xs, 2 * jj), PK::get(Y, Ys, 2 * jj), PK::get(X, Xs, 2 * jj + 1),
+                   PK::get(Y, Ys, 2 * jj + 1), bf[2 * kk], bf[2 * kk + 1]);
+        }
+      }
+      float s0 = -INFINITY, s1 = -INFINITY;
+      if (t4 < HG) {
+        float sgk = sigk[0], zz = zk[0];
+#pragma unroll
+        for (int h = 1; h < HG; ++h)
+          if (t4 == h) {
+            sgk = sigk[h];
+            zz = zk[h];
+          }
+        s0 = fmaf(d[0] + d[1], sgk, zz);
+        s1 = fmaf(d[2] + d[3], sgk, zz);
+        if (p.nsp > 0) {
+          // sparse entries: the dense code there is 0 (value z); add q_c (x_c - z_c)
+          const uint8_t* si = pgm + p.lay.off_si;
+          const uint16_t* sv = reinterpret_cast<const uint16_t*>(pgm + p.lay.off_sv);
+#pragma unroll
+          for (int rh = 0; rh < 2; ++rh) {
+            const int tok = 32 * stt + 16 * mt + g8 + 8 * rh;
+            float add = 0.0f;
+            for (int k = 0; k < p.nsp; ++k) {
+              const int c = si[tok * p.nsp + k];
+              const float xv = __half2float(__ushort_as_half(sv[tok * p.nsp + k]));
+              const float z = __half2float(__ushort_as_half((uint16_t)(km[gk * D + c] & 0xFFFFu)));
+              add = fmaf(qs[t4][c], xv - z, add);
+            }
+            if (rh == 0) s0 += add;
+            else s1 += add;
+          }
+        }
+        s0 *= p.qk_scale_log2;
+        s1 *= p.qk_scale_log2;
+      }
+      sc[mt][0] = s0;
+      sc[mt][1] = s1;
+    }
+
+    // -- online softmax (lazy maximum), per head over lanes t4 = head
+    {
+      const float tmax = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      const bool over = tmax > mrun + kLazy || (mrun == -INFINITY && tmax != -INFINITY);
+      if (__any_sync(kAll, over)) {
+        float mx = tmax;
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, off));
+        mx = __shfl_sync(kAll, mx, (lane & ~3) | hmine);  // the maximum of this lane's head
+        const float mnew = fmaxf(mx, mrun);
+        const float f = mrun == -INFINITY ? 0.0f : exp2f(mrun - mnew);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dv[i][j] *= f;
+        // lacc and zacc belong to head hcol
+        const float fc = __shfl_sync(kAll, f, hcol);
+        lacc *= fc;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) zacc[i] *= fc;
+        mrun = mnew;
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int rh = 0; rh < 2; ++rh) sc[mt][rh] = t4 < HG ? exp2f(sc[mt][rh] - mrun) : 0.0f;
+    }
+
+    // -- values, one 16-token tile (k-chunk) at a time
+#pragma unroll
+    for (int kc = 0; kc < 2; ++kc) {
+      const int tile = 2 * stt + kc;
+      // p of head hcol for tokens 2t4, 2t4+1, 2t4+8, 2t4+9 of the tile
+      const int la = 4 * (2 * t4) + hcol, lb = 4 * (2 * t4 + 1) + hcol;
+      const float p0 = __shfl_sync(kAll, sc[kc][0], la), p1 = __shfl_sync(kAll, sc[kc][0], lb);
+      const float p2 = __shfl_sync(kAll, sc[kc][1], la), p3 = __shfl_sync(kAll, sc[kc][1], lb);
+      const int tb = 16 * tile + 2 * t4;  // page token of p0
+      // value scales and zero points of the lane's column groups
+      float vs[4][4], vz[4][4];
+      float smax = 0.0f;
+#pragma unroll
+      for (int bi = 0; bi < 4; ++bi) {
+        const int grp = bi * GPB + gl;
+        const bool ok = bi < NB && grp < ng;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = tb + (i & 1) + 8 * (i >> 1);
+          float2 zsv = make_float2(0.0f, 0.0f);
+          if (ok) zsv = __half22float2(*reinterpret_cast<const __half2*>(vm + tok * ng + grp));
+          vz[bi][i] = zsv.x;
+          vs[bi][i] = zsv.y;
+          smax = fmaxf(smax, zsv.y);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) smax = fmaxf(smax, __shfl_xor_sync(kAll, smax, off));
+      const int enew = smax > 0.0f ? (int)((__float_as_uint(smax) >> 23) & 0xFF) - 127 : -30;
+      if (enew > es) {  // larger scales: lower the B scale, rescale what is accumulated (exact)
+        const float f = pow2f(es - enew);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dv[i][j] *= f;
+        es = enew;
+      }
+      const float bscale = pow2f(6 - es);  // p <= 2^8 and s < 2^(es+1): |B| < 2^15
+      uint32_t bv[4][2];
+#pragma unroll
+      for (int bi = 0; bi < 4; ++bi) {
+        const float v0 = p0 * vs[bi][0] * bscale, v1 = p1 * vs[bi][1] * bscale;
+        const float v2 = p2 * vs[bi][2] * bscale, v3 = p3 * vs[bi][3] * bscale;
+        bv[bi][0] = pack_half2(split_part(v0, hl), split_part(v1, hl));
+        bv[bi][1] = pack_half2(split_part(v2, hl), split_part(v3, hl));
+        if (hl == 0) zacc[bi] = fmaf(p0, vz[bi][0], fmaf(p1, vz[bi][1], fmaf(p2, vz[bi][2], fmaf(p3, vz[bi][3], zacc[bi]))));
+      }
+      if (hl == 0 && gl == 0) lacc += (p0 + p1) + (p2 + p3);
+
+      uint32_t wd[2 * BV];
+      const uint4* wsrc = reinterpret_cast<const uint4*>(pgm + p.lay.off_vc) + ((int64_t)tile * 32 + lane) * (2 * BV / 4);
+#pragma unroll
+      for (int i = 0; i < 2 * BV / 4; ++i) {
+        const uint4 v = wsrc[i];
+        wd[4 * i] = v.x;
+        wd[4 * i + 1] = v.y;
+        wd[4 * i + 2] = v.z;
+        wd[4 * i + 3] = v.w;
+      }
+      uint32_t wsh[2 * BV];
+#pragma unroll
+      for (int i = 0; i < 2 * BV; ++i) wsh[i] = wd[i] >> PV::SHIFT;
+#pragma unroll
+      for (int mc = 0; mc < 8; ++mc) {
+        const int u = mc / PV::PER, j = mc % PV::PER;
+        constexpr int WPR = BV / 2;  // words per register slot
+        const int bi = ((16 * mc) >> p.log2G) / GPB;
+        uint32_t b0 = bv[0][0], b1 = bv[0][1];
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+          if (bi == i) {
+            b0 = bv[i][0];
+            b1 = bv[i][1];
+          }
+        mma16816(dv[mc], PV::get(wd[0 * WPR + u], wsh[0 * WPR + u], j), PV::get(wd[1 * WPR + u], wsh[1 * WPR + u], j),
+                 PV::get(wd[2 * WPR + u], wsh[2 * WPR + u], j), PV::get(wd[3 * WPR + u], wsh[3 * WPR + u], j), b0, b1);
+      }
+    }
+
+    // -- release the sub-tile; the warp releasing a stage's last sub-tile refills it
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&empty_bar[stg]);
+      if (atomicAdd(&stage_cnt[stg], 1) % SPP == SPP - 1 && kpg + n_stages < n_pg && !*(volatile int*)&abort_flag) {
+        if (mbar_wait(&empty_bar[stg], (kpg >> log2S) & 1)) {
+          issue_page(kpg + n_stages);
+        } else {
+          report_error(p.err, kDevWaitTimeout);
+          atomicExch(&abort_flag, 1);
+        }
+      }
+    }
+  }
+  if (cur >= 0) {
+    if (touched) epilogue(cur, done);
+    else finish(cur, done);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int i = 0; i < n_stages; ++i)
+      if (stage_issued[i] > 0) mbar_wait(&full_bar[i], (stage_issued[i] - 1) & 1);
+  }
+}
+
+// Per-warp buffers in dynamic shared memory (bytes per CTA): query rows and key B fragments.
+template <int HG>
+constexpr size_t warp_bufs_bytes() {
+  return (size_t)kMmaWarps * (HG * kHeadDim * sizeof(float) + 2 * HG * 4 * 16 * sizeof(uint32_t));
+}
+
+// Page stages of one CTA: the largest power of two up to kMmaMaxStages whose pages fit the
+// opt-in shared memory beside the static arrays and the per-warp buffers; -1 when none fits
+// (or the static arrays exceed the 48 KB a kernel may declare).
+template <int BK, int BV, int HG>
+int log2_stages_mma(int page_bytes) {
+  auto kern = decode_mma_kernel<BK, BV, HG>;
+  static int static_smem = -1, optin = -1;
+  if (static_smem < 0) {
+    cudaFuncAttributes a{};
+    int dev = 0;
+    if (cudaFuncGetAttributes(&a, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return -1;
+    static_smem = (int)a.sharedSizeBytes;
+  }
+  if (static_smem > 48 * 1024) return -1;
+  const int64_t avail = (int64_t)optin - static_smem - (int64_t)warp_bufs_bytes<HG>();
+  int l = 4;  // kMmaMaxStages = 16
+  while (l >= 0 && ((int64_t)page_bytes << l) > avail) --l;
+  return l;
+}
+
+template <int BK, int BV, int HG>
+cudaError_t launch_mma_t(const DecodeParams& p, int grid, cudaStream_t s) {
+  const int l = log2_stages_mma<BK, BV, HG>(p.lay.bytes);
+  if (l < 0) return cudaErrorInvalidValue;
+  DecodeParams q = p;
+  q.log2_stages = l;
+  const size_t smem = ((size_t)p.lay.bytes << l) + warp_bufs_bytes<HG>();
+  auto kern = decode_mma_kernel<BK, BV, HG>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kMmaWarps * 32, smem, s>>>(q);
+  return cudaGetLastError();
+}
+
+template <int BK, int BV, int HG>
+int resident_mma_t(int page_bytes) {
+  const int l = log2_stages_mma<BK, BV, HG>(page_bytes);
+  if (l < 0) return 0;
+  const size_t smem = ((size_t)page_bytes << l) + warp_bufs_bytes<HG>();
+  auto kern = decode_mma_kernel<BK, BV, HG>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kMmaWarps * 32, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+
+#define KVQ_MMA_CASES(X) X(2, 2, 1) X(2, 2, 2) X(2, 2, 4) X(4, 2, 1) X(4, 2, 2) X(4, 2, 4) X(4, 4, 1) X(4, 4, 2) X(4, 4, 4)
+
+bool decode_mma_supported(int bk, int bv, int hg) {
+#define KVQ_MS(BKV, BVV, HGV) \
+  if (bk == BKV && bv == BVV && hg == HGV) return true;
+  KVQ_MMA_CASES(KVQ_MS)
+#undef KVQ_MS
+  return false;
+}
+
+int decode_mma_resident(int bk, int bv, int hg, int page_bytes, int* warps) {
+  *warps = kMmaWarps;
+#define KVQ_MR(BKV, BVV, HGV) \
+  if (bk == BKV && bv == BVV && hg == HGV) return resident_mma_t<BKV, BVV, HGV>(page_bytes);
+  KVQ_MMA_CASES(KVQ_MR)
+#undef KVQ_MR
+  return 0;
+}
+
+cudaError_t launch_decode_mma(const DecodeParams& p, int bk, int bv, int hg, int grid, cudaStream_t s) {
+#define KVQ_ML(BKV, BVV, HGV) \
+  if (bk == BKV && bv == BVV && hg == HGV) return launch_mma_t<BKV, BVV, HGV>(p, grid, s);
+  KVQ_MMA_CASES(KVQ_ML)
+#undef KVQ_ML
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvq

@@ -26,9 +26,36 @@ constexpr int kHeadDim = 128;
 
 struct PageLayout {
   int32_t off_kc, off_km, off_vc, off_vm, off_si, off_sv, bytes;
+  int32_t frag;  // 1: key and value codes in tensor-core fragment order (see below), 0: bitstreams
 };
 
-PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp);
+// Fragment order is used when both code widths are 2 or 4 bits and keys are stored after
+// RoPE (no rotation at decode); otherwise codes are token-major bitstreams.
+PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp, bool rope);
+
+// Fragment order of the codes of a page (D = 128, B = 2 or 4 bits).  Both sections are cut
+// into 16-token tiles; in each tile every lane l = 4g + t (g = l / 4, t = l % 4) of a warp
+// owns 2B consecutive 32-bit words (word index (tile*32 + l)*2B + w).  A word holds 16/B code
+// pairs; pair j keeps its first code at bits [B*j, B*j + B) and its second at bits
+// [16 + B*j, 16 + B*j + B), so masking a pair in place leaves two fp16 subnormals
+// code * 2^(B*j) * 2^-24 (pairs j >= 10/B are first shifted down by B*(10/B) bits).
+//
+// Keys, tile = tokens 16m .. 16m+15: word w = r*B + u holds token 16m + g + 8r; its pair j
+// covers channels c and c + 1 with c = 16*(u*(8/B) + j/2) + 8*(j%2) + 2t.
+__host__ __device__ inline void frag_key_pair(int bits, int tile, int lane, int w, int j, int* token, int* c0) {
+  const int g = lane >> 2, t = lane & 3;
+  const int r = w / bits, u = w % bits;
+  *token = 16 * tile + g + 8 * r;
+  *c0 = 16 * (u * (8 / bits) + j / 2) + 8 * (j % 2) + 2 * t;
+}
+// Values, tile = tokens 16k .. 16k+15: word w = r*(B/2) + u, r = 0..3; its pair j covers
+// channel 16*(u*(16/B) + j) + g + 8*(r%2) of tokens s and s + 1, s = 16k + 8*(r/2) + 2t.
+__host__ __device__ inline void frag_value_pair(int bits, int tile, int lane, int w, int j, int* tok0, int* ch) {
+  const int g = lane >> 2, t = lane & 3;
+  const int r = w / (bits / 2), u = w % (bits / 2);
+  *ch = 16 * (u * (16 / bits) + j) + g + 8 * (r % 2);
+  *tok0 = 16 * tile + 8 * (r / 2) + 2 * t;
+}
 
 // Host-side validation of a configuration (the checks kvq_create applies).
 kvq_status check_config(const kvq_config& cfg);
@@ -102,8 +129,10 @@ cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool ro
 // Decode CTAs resident per SM (0: unsupported), and in *warps the warps of one CTA: the partial
 // slots a unit needs are warps * (CTAs whose slices meet the unit).
 int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int R, int nsp, int page_bytes, int* warps);
-// true when decode runs the lean page path (one query head per kv head, 2/4-bit, R = 128, no sparse)
-bool decode_lean(int bk, int bv, int hg, bool rope, int R, int nsp);
+// Tensor-core decode over fragment-ordered pages (2/4-bit codes, keys without RoPE).
+bool decode_mma_supported(int bk, int bv, int hg);
+int decode_mma_resident(int bk, int bv, int hg, int page_bytes, int* warps);
+cudaError_t launch_decode_mma(const DecodeParams& p, int bk, int bv, int hg, int grid, cudaStream_t s);
 bool decode_supported(int bk, int bv, int hg, bool rope);
 bool quantize_supported(int bk, int bv);
 size_t quantize_smem_bytes(int R, int D, int G, const PageLayout& lay);

@@ -62,7 +62,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   const int hg = cfg->num_q_heads / cfg->num_kv_heads;
   const int64_t n_units = (int64_t)cfg->batch * cfg->num_kv_heads;
   const int64_t heads = (int64_t)cfg->batch * cfg->num_q_heads;
-  const kvq::PageLayout lay = kvq::make_layout(R, D, G, cfg->k_bits, cfg->v_bits, cfg->k_sparse);
+  const kvq::PageLayout lay = kvq::make_layout(R, D, G, cfg->k_bits, cfg->v_bits, cfg->k_sparse, cfg->rope != 0);
 
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return KVQ_ERR_CUDA;

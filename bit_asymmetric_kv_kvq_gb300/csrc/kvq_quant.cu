@@ -289,8 +289,47 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
   }
   __syncthreads();
 
-  // ---- codes, computed and packed a 32-channel chunk (BITS words) at a time
-  {
+  // ---- codes in fragment order (2- and 4-bit codes, keys without RoPE): one word per thread
+  //      and step, its code pairs placed as frag_key_pair / frag_value_pair describe
+  if (p.lay.frag) {
+    constexpr int KB = (BK == 2 || BK == 4) ? BK : 2, VB = (BV == 2 || BV == 4) ? BV : 2;
+    uint32_t* kc = reinterpret_cast<uint32_t*>(pg + p.lay.off_kc);
+    uint32_t* vc = reinterpret_cast<uint32_t*>(pg + p.lay.off_vc);
+    const int kwords = (R / 16) * 32 * 2 * KB;
+    for (int idx = tid; idx < kwords; idx += kQuantThreads) {
+      const int w = idx % (2 * KB), ln = (idx / (2 * KB)) % 32, tile = idx / (64 * KB);
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < 16 / KB; ++j) {
+        int tok, c0;
+        frag_key_pair(KB, tile, ln, w, j, &tok, &c0);
+        const uint32_t xx = *reinterpret_cast<const uint32_t*>(kt + tok * D + c0);
+        const GroupQ* gq = kq + (tok / G) * D;
+        const uint32_t a = excluded(tok, c0) ? 0u : quant_code(h2f((uint16_t)(xx & 0xFFFFu)), gq[kq_slot(c0)], LK);
+        const uint32_t b = excluded(tok, c0 + 1) ? 0u : quant_code(h2f((uint16_t)(xx >> 16)), gq[kq_slot(c0 + 1)], LK);
+        word |= (a << (KB * j)) | (b << (16 + KB * j));
+      }
+      kc[idx] = word;
+    }
+    const int ng = D / G;
+    const int vwords = (R / 16) * 32 * 2 * VB;
+    for (int idx = tid; idx < vwords; idx += kQuantThreads) {
+      const int w = idx % (2 * VB), ln = (idx / (2 * VB)) % 32, tile = idx / (64 * VB);
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < 16 / VB; ++j) {
+        int tok, ch;
+        frag_value_pair(VB, tile, ln, w, j, &tok, &ch);
+        const GroupQ& q0 = vq[tok * ng + ch / G];
+        const GroupQ& q1 = vq[(tok + 1) * ng + ch / G];
+        const uint32_t a = quant_code(h2f(vt[tok * D + ch]), q0, LV);
+        const uint32_t b = quant_code(h2f(vt[(tok + 1) * D + ch]), q1, LV);
+        word |= (a << (VB * j)) | (b << (16 + VB * j));
+      }
+      vc[idx] = word;
+    }
+  } else {
+    // ---- codes as token-major bitstreams, computed and packed a 32-channel chunk (BITS words) at a time
     constexpr int NCH = kHeadDim / kChunk;
     constexpr int WKW = kHeadDim * BK / 32, WVW = kHeadDim * BV / 32;
     uint32_t* kc = reinterpret_cast<uint32_t*>(pg + p.lay.off_kc);

@@ -154,12 +154,22 @@ kvq_status kvq_reset(kvq_cache* cache);
  *   cfg            a configuration kvq_create would accept
  *   pages          device, [B*Hkv][pages_per_unit][page_bytes]; page p of a unit
  *                  holds tokens [p*R, p*R+R) as consecutive sections, each padded
- *                  to a multiple of 16 bytes: key codes [R][D*k_bits/32] u32
- *                  (token-major bitstream as in kvq_unit_view), key zero
- *                  point/scale [R/G][D] u32 (fp16 zero point in the low half,
- *                  scale in the high half), value codes [R][D*v_bits/32] u32,
- *                  value zero point/scale [R][D/G] u32, sparse channels [R][k_sparse]
- *                  u8, sparse values [R][k_sparse] fp16
+ *                  to a multiple of 16 bytes: key codes (R*D*k_bits/32 u32), key
+ *                  zero point/scale [R/G][D] u32 (fp16 zero point in the low half,
+ *                  scale in the high half), value codes (R*D*v_bits/32 u32), value
+ *                  zero point/scale [R][D/G] u32, sparse channels [R][k_sparse] u8,
+ *                  sparse values [R][k_sparse] fp16.
+ *                  Codes are token-major bitstreams [R][D*bits/32] (as in
+ *                  kvq_unit_view) unless both widths are 2 or 4 bits and rope = 0;
+ *                  then both code sections are in tensor-core fragment order: per
+ *                  16-token tile m and lane l = 4g + t (g = l/4, t = l%4), 2B
+ *                  consecutive words (word index (m*32 + l)*2B + w), each holding
+ *                  16/B code pairs; pair j has its first code at bits [B*j, B*j+B)
+ *                  and its second at bits [16+B*j, 16+B*j+B).  Keys: word
+ *                  w = r*B + u, token 16m + g + 8r, channels c and c+1 with
+ *                  c = 16*(u*(8/B) + j/2) + 8*(j%2) + 2t.  Values: word
+ *                  w = r*(B/2) + u (r = 0..3), channel 16*(u*(16/B) + j) + g + 8*(r%2)
+ *                  of tokens s and s+1 with s = 16m + 8*(r/2) + 2t.
  *   window_k/_v    device fp16 [B*Hkv][R][D]; slots 0..n_r-1 hold the newest tokens
  *   n_tokens       cached tokens T >= 1: Tq = R*floor((T-1)/R) are in the pages,
  *                  n_r = T - Tq in the window

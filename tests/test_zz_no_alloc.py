@@ -25,6 +25,45 @@ def _r16(x):
     return (x + 15) // 16 * 16
 
 
+def _unpack_rows(words, n, bits):
+    """Token-major bitstream rows [T][n*bits/32] u32 -> codes [T][n]."""
+    out = np.zeros((words.shape[0], n), np.uint32)
+    for c in range(n):
+        b = c * bits
+        v = words[:, b // 32] >> np.uint32(b % 32)
+        if b % 32 + bits > 32:
+            v = v | (words[:, b // 32 + 1] << np.uint32(32 - b % 32))
+        out[:, c] = v & np.uint32((1 << bits) - 1)
+    return out
+
+
+def _fragment_words(codes, bits, keys):
+    """Codes of one page [R][128] in the fragment order include/kvq.h describes for 2- and
+    4-bit codes: per 16-token tile and lane l = 4g + t, 2*bits words; pair j of a word holds
+    its first code at bits [bits*j, ...) and its second at [16 + bits*j, ...)."""
+    R = codes.shape[0]
+    words = np.zeros((R // 16, 32, 2 * bits), np.uint32)
+    for tile in range(R // 16):
+        for lane in range(32):
+            g, t = lane // 4, lane % 4
+            for w in range(2 * bits):
+                word = 0
+                for j in range(16 // bits):
+                    if keys:  # word w = r*bits + u: token 16*tile + g + 8r, channels c, c + 1
+                        r, u = divmod(w, bits)
+                        tok = 16 * tile + g + 8 * r
+                        c = 16 * (u * (8 // bits) + j // 2) + 8 * (j % 2) + 2 * t
+                        first, second = codes[tok, c], codes[tok, c + 1]
+                    else:  # word w = r*(bits/2) + u: channel ch of tokens s, s + 1
+                        r, u = divmod(w, bits // 2)
+                        ch = 16 * (u * (16 // bits) + j) + g + 8 * (r % 2)
+                        s = 16 * tile + 8 * (r // 2) + 2 * t
+                        first, second = codes[s, ch], codes[s + 1, ch]
+                    word |= int(first) << (bits * j) | int(second) << (16 + bits * j)
+                words[tile, lane, w] = word
+    return words.reshape(-1)
+
+
 def _pages_and_window(cache, w):
     """Caller-owned copies of the cache: pages [units][Tq/R][page_bytes] and window [units][R][D]."""
     T, Tq, n_r = cache.state()
@@ -40,16 +79,22 @@ def _pages_and_window(cache, w):
     pages = np.zeros((units, max(n_pages, 1), page_bytes), np.uint8)
     win_k = np.zeros((units, R, D), np.uint16)
     win_v = np.zeros((units, R, D), np.uint16)
+    frag = bk in (2, 4) and bv in (2, 4) and not w.rope
     for u in range(units):
         b, kvh = divmod(u, w.kv_heads)
         st = cache.export_unit(b, kvh)
         for p in range(n_pages):
             pg = pages[u, p]
-            pg[0:R * D * bk // 8] = st["kcodes"][p * R:(p + 1) * R].view(np.uint8).ravel()
+            kc = st["kcodes"][p * R:(p + 1) * R]
+            vc = st["vcodes"][p * R:(p + 1) * R]
+            if frag:
+                kc = _fragment_words(_unpack_rows(kc, D, bk), bk, keys=True)
+                vc = _fragment_words(_unpack_rows(vc, D, bv), bv, keys=False)
+            pg[0:R * D * bk // 8] = kc.view(np.uint8).ravel()
             km = st["kz"][p * R // G:(p + 1) * R // G].astype(np.uint32) | (
                 st["ks"][p * R // G:(p + 1) * R // G].astype(np.uint32) << 16)
             pg[off_km:off_km + km.nbytes] = km.view(np.uint8).ravel()
-            pg[off_vc:off_vc + R * D * bv // 8] = st["vcodes"][p * R:(p + 1) * R].view(np.uint8).ravel()
+            pg[off_vc:off_vc + R * D * bv // 8] = vc.view(np.uint8).ravel()
             vm = st["vz"][p * R:(p + 1) * R].astype(np.uint32) | (st["vs"][p * R:(p + 1) * R].astype(np.uint32) << 16)
             pg[off_vm:off_vm + vm.nbytes] = vm.view(np.uint8).ravel()
             if nsp:
