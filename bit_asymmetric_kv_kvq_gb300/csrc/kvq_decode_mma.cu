@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
   constexpr int D = kHeadDim, W = kMmaWarps;
   constexpr int NCOL = 2 * HG;   // B columns per value group: (head, high/low)
   constexpr int GPB = 8 / NCOL;  // value groups per B fragment
+  constexpr int NBM = (D / 32 + GPB - 1) / GPB;  // B fragments per value tile at most (G = 32)
   constexpr int KPW = 8 / BK;    // key k-chunks per fragment word
   using PK = Pairs<BK>;
   using PV = Pairs<BV>;
@@ -96,7 +97,6 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
   const int SPP = p.R / 32;
   const int n_sub = (int)(w_end - w_begin) * SPP;
   const int ng = D >> p.log2G;             // value groups per token
-  const int NB = (ng + GPB - 1) / GPB;     // B fragments for the values of one tile
 
   // dynamic shared memory: the page stages, then each warp's query rows (fp32) and key B
   // fragments (static arrays stay small: static shared memory is limited to 48 KB)
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
   // ---- per-warp state for the current unit
   float dv[8][4];            // value accumulators, one m16n8 tile per 16 channels
   float mrun;                // running maximum of head hmine (log2 units)
-  float lacc, zacc[4];       // sum of p (column owners) and p*z per B fragment
+  float lacc, zacc[NBM];     // sum of p (column owners) and p*z per B fragment
   int es;                    // exponent bound of the value scales seen (B values carry 2^(6-es));
                              // starts below every fp16 scale (>= 2^-24)
   auto reset = [&]() {
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     mrun = -INFINITY;
     lacc = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) zacc[i] = 0.0f;
+    for (int i = 0; i < NBM; ++i) zacc[i] = 0.0f;
     es = -30;
   };
 
@@ -271,14 +271,14 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     for (int off = 1; off < 4; off <<= 1) {
       lacc += __shfl_xor_sync(kAll, lacc, off);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) zacc[i] += __shfl_xor_sync(kAll, zacc[i], off);
+      for (int i = 0; i < NBM; ++i) zacc[i] += __shfl_xor_sync(kAll, zacc[i], off);
     }
     const int slot = slot_of(unit);
     if (slot < p.max_slots) {
       // zero-point sums of this lane's (group, head): owned by the lanes of column 2*t4
-      float zs[4];
+      float zs[NBM];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) zs[i] = __shfl_sync(kAll, zacc[i], 4 * (2 * t4));
+      for (int i = 0; i < NBM; ++i) zs[i] = __shfl_sync(kAll, zacc[i], 4 * (2 * t4));
       const float osc = pow2f(24 - (6 - es));
 #pragma unroll
       for (int mc = 0; mc < 8; ++mc) {
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
         const float s = osc * pow2f(-PV::pos(mc % PV::PER));
         float z = zs[0];
 #pragma unroll
-        for (int i = 1; i < 4; ++i)
+        for (int i = 1; i < NBM; ++i)
           if (grp / GPB == i) z = zs[i];
         float* dst = p.part_acc + ((bh0 + hmine) * p.max_slots + slot) * D + 16 * mc + g8;
         dst[0] = fmaf(dv[mc][0] + dv[mc][1], s, z);
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
         const float fc = __shfl_sync(kAll, f, hcol);
         lacc *= fc;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) zacc[i] *= fc;
+        for (int i = 0; i < NBM; ++i) zacc[i] *= fc;
         mrun = mnew;
       }
 #pragma unroll
@@ -563,30 +563,26 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
         for (int rh = 0; rh < 2; ++rh) sc[mt][rh] = t4 < HG ? exp2f(sc[mt][rh] - mrun) : 0.0f;
     }
 
-    // -- values, one 16-token tile (k-chunk) at a time
-#pragma unroll
-    for (int kc = 0; kc < 2; ++kc) {
-      const int tile = 2 * stt + kc;
-      // p of head hcol for tokens 2t4, 2t4+1, 2t4+8, 2t4+9 of the tile
-      const int la = 4 * (2 * t4) + hcol, lb = 4 * (2 * t4 + 1) + hcol;
-      const float p0 = __shfl_sync(kAll, sc[kc][0], la), p1 = __shfl_sync(kAll, sc[kc][0], lb);
-      const float p2 = __shfl_sync(kAll, sc[kc][1], la), p3 = __shfl_sync(kAll, sc[kc][1], lb);
-      const int tb = 16 * tile + 2 * t4;  // page token of p0
-      // value scales and zero points of the lane's column groups
-      float vs[4][4], vz[4][4];
+    // -- values: scales and zero points of the lane's column groups for the 8 tokens it feeds
+    //    (tokens 2t4, 2t4+1, 2t4+8, 2t4+9 of both 16-token tiles)
+    float vs[2][NBM][4], vz[2][NBM][4];
+    {
       float smax = 0.0f;
 #pragma unroll
-      for (int bi = 0; bi < 4; ++bi) {
-        const int grp = bi * GPB + gl;
-        const bool ok = bi < NB && grp < ng;
+      for (int kc = 0; kc < 2; ++kc) {
+        const int tb = 16 * (2 * stt + kc) + 2 * t4;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tok = tb + (i & 1) + 8 * (i >> 1);
-          float2 zsv = make_float2(0.0f, 0.0f);
-          if (ok) zsv = __half22float2(*reinterpret_cast<const __half2*>(vm + tok * ng + grp));
-          vz[bi][i] = zsv.x;
-          vs[bi][i] = zsv.y;
-          smax = fmaxf(smax, zsv.y);
+        for (int bi = 0; bi < NBM; ++bi) {
+          const int grp = bi * GPB + gl;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tok = tb + (i & 1) + 8 * (i >> 1);
+            float2 zsv = make_float2(0.0f, 0.0f);
+            if (grp < ng) zsv = __half22float2(*reinterpret_cast<const __half2*>(vm + tok * ng + grp));
+            vz[kc][bi][i] = zsv.x;
+            vs[kc][bi][i] = zsv.y;
+            smax = fmaxf(smax, zsv.y);
+          }
         }
       }
 #pragma unroll
@@ -600,15 +596,25 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
           for (int j = 0; j < 4; ++j) dv[i][j] *= f;
         es = enew;
       }
-      const float bscale = pow2f(6 - es);  // p <= 2^8 and s < 2^(es+1): |B| < 2^15
-      uint32_t bv[4][2];
+    }
+    const float bscale = pow2f(6 - es);  // p <= 2^8 and s < 2^(es+1): |B| < 2^15
+
+    // -- values, one 16-token tile (k-chunk) at a time
 #pragma unroll
-      for (int bi = 0; bi < 4; ++bi) {
-        const float v0 = p0 * vs[bi][0] * bscale, v1 = p1 * vs[bi][1] * bscale;
-        const float v2 = p2 * vs[bi][2] * bscale, v3 = p3 * vs[bi][3] * bscale;
-        bv[bi][0] = pack_half2(split_part(v0, hl), split_part(v1, hl));
-        bv[bi][1] = pack_half2(split_part(v2, hl), split_part(v3, hl));
-        if (hl == 0) zacc[bi] = fmaf(p0, vz[bi][0], fmaf(p1, vz[bi][1], fmaf(p2, vz[bi][2], fmaf(p3, vz[bi][3], zacc[bi]))));
+    for (int kc = 0; kc < 2; ++kc) {
+      const int tile = 2 * stt + kc;
+      // p of head hcol for tokens 2t4, 2t4+1, 2t4+8, 2t4+9 of the tile
+      const int la = 4 * (2 * t4) + hcol, lb = 4 * (2 * t4 + 1) + hcol;
+      const float p0 = __shfl_sync(kAll, sc[kc][0], la), p1 = __shfl_sync(kAll, sc[kc][0], lb);
+      const float p2 = __shfl_sync(kAll, sc[kc][1], la), p3 = __shfl_sync(kAll, sc[kc][1], lb);
+      const float pb0 = p0 * bscale, pb1 = p1 * bscale, pb2 = p2 * bscale, pb3 = p3 * bscale;
+      uint32_t bv[NBM][2];
+#pragma unroll
+      for (int bi = 0; bi < NBM; ++bi) {
+        bv[bi][0] = pack_half2(split_part(pb0 * vs[kc][bi][0], hl), split_part(pb1 * vs[kc][bi][1], hl));
+        bv[bi][1] = pack_half2(split_part(pb2 * vs[kc][bi][2], hl), split_part(pb3 * vs[kc][bi][3], hl));
+        if (hl == 0)
+          zacc[bi] = fmaf(p0, vz[kc][bi][0], fmaf(p1, vz[kc][bi][1], fmaf(p2, vz[kc][bi][2], fmaf(p3, vz[kc][bi][3], zacc[bi]))));
       }
       if (hl == 0 && gl == 0) lacc += (p0 + p1) + (p2 + p3);
 
@@ -629,14 +635,16 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
       for (int mc = 0; mc < 8; ++mc) {
         const int u = mc / PV::PER, j = mc % PV::PER;
         constexpr int WPR = BV / 2;  // words per register slot
-        const int bi = ((16 * mc) >> p.log2G) / GPB;
         uint32_t b0 = bv[0][0], b1 = bv[0][1];
+        if constexpr (NBM > 1) {
+          const int bi = ((16 * mc) >> p.log2G) / GPB;
 #pragma unroll
-        for (int i = 1; i < 4; ++i)
-          if (bi == i) {
-            b0 = bv[i][0];
-            b1 = bv[i][1];
-          }
+          for (int i = 1; i < NBM; ++i)
+            if (bi == i) {
+              b0 = bv[i][0];
+              b1 = bv[i][1];
+            }
+        }
         mma16816(dv[mc], PV::get(wd[0 * WPR + u], wsh[0 * WPR + u], j), PV::get(wd[1 * WPR + u], wsh[1 * WPR + u], j),
                  PV::get(wd[2 * WPR + u], wsh[2 * WPR + u], j), PV::get(wd[3 * WPR + u], wsh[3 * WPR + u], j), b0, b1);
       }
