@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 
 #include "kvq_internal.h"
+#include "kvq_merge.cuh"
 #include "kvq_ptx.cuh"
 
 namespace kvq {
@@ -431,34 +432,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       if (lane == 0) n = __ldcg(p.nslot + unit);
       n = __shfl_sync(kFull, n, 0);
       if (n > p.max_slots) n = p.max_slots;
-#pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        const float* ml = p.part_ml + (bh0 + h) * p.max_slots * 2;
-        const float* pacc = p.part_acc + (bh0 + h) * p.max_slots * D + 4 * lane;
-        float M = -INFINITY;
-        for (int sp = lane; sp < n; sp += 32) M = fmaxf(M, __ldcg(ml + 2 * sp));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-        float L = 0.0f, a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll 4
-        for (int sp = 0; sp < n; ++sp) {
-          const float2 mlv = __ldcg(reinterpret_cast<const float2*>(ml + 2 * sp));
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(pacc + (int64_t)sp * D));
-          if (mlv.x == -INFINITY) continue;
-          const float f = exp2f(mlv.x - M);
-          L = fmaf(f, mlv.y, L);
-          a0 = fmaf(f, v.x, a0);
-          a1 = fmaf(f, v.y, a1);
-          a2 = fmaf(f, v.z, a2);
-          a3 = fmaf(f, v.w, a3);
-        }
-        const float inv = 1.0f / L;
-        const __half2 o01 = __floats2half2_rn(a0 * inv, a1 * inv), o23 = __floats2half2_rn(a2 * inv, a3 * inv);
-        uint2 packed;
-        packed.x = *reinterpret_cast<const uint32_t*>(&o01);
-        packed.y = *reinterpret_cast<const uint32_t*>(&o23);
-        *reinterpret_cast<uint2*>(p.out + (bh0 + h) * D + 4 * lane) = packed;
-      }
+      merge_partials<HG>(p, bh0, n, lane);
       if (lane == 0) {  // ready for the next call on this stream
         p.counters[unit] = 0;
         p.nslot[unit] = 0;

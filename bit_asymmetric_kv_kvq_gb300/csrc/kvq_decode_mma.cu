@@ -29,6 +29,7 @@
 #include <cuda_fp16.h>
 
 #include "kvq_internal.h"
+#include "kvq_merge.cuh"
 #include "kvq_ptx.cuh"
 
 namespace kvq {
@@ -230,32 +231,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     if (lane == 0) n = __ldcg(p.nslot + unit);
     n = __shfl_sync(kAll, n, 0);
     if (n > p.max_slots) n = p.max_slots;
-#pragma unroll
-    for (int h = 0; h < HG; ++h) {
-      const float* ml = p.part_ml + (bh0 + h) * p.max_slots * 2;
-      const float* pacc = p.part_acc + (bh0 + h) * p.max_slots * D + 4 * lane;
-      float M = -INFINITY;
-      for (int sp = lane; sp < n; sp += 32) M = fmaxf(M, __ldcg(ml + 2 * sp));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, off));
-      float L = 0.0f, a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll 8
-      for (int sp = 0; sp < n; ++sp) {
-        const float2 mlv = __ldcg(reinterpret_cast<const float2*>(ml + 2 * sp));
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(pacc + (int64_t)sp * D));
-        const float f = mlv.x == -INFINITY ? 0.0f : exp2f(mlv.x - M);
-        L = fmaf(f, mlv.y, L);
-        a0 = fmaf(f, v.x, a0);
-        a1 = fmaf(f, v.y, a1);
-        a2 = fmaf(f, v.z, a2);
-        a3 = fmaf(f, v.w, a3);
-      }
-      const float inv = 1.0f / L;
-      uint2 packed;
-      packed.x = pack_half2(a0 * inv, a1 * inv);
-      packed.y = pack_half2(a2 * inv, a3 * inv);
-      *reinterpret_cast<uint2*>(p.out + (bh0 + h) * D + 4 * lane) = packed;
-    }
+    merge_partials<HG>(p, bh0, n, lane);
     if (lane == 0) {
       p.counters[unit] = 0;
       p.nslot[unit] = 0;
@@ -487,7 +463,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
         wd[4 * i + 2] = v.z;
         wd[4 * i + 3] = v.w;
       }
-      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // four independent accumulator chains (k-chunks kk % 4) keep the mma latency off the path
+      float da[4][4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) da[c][e] = 0.0f;
 #pragma unroll
       for (int u = 0; u < BK; ++u) {
         const uint32_t X = wd[u], Y = wd[BK + u];
@@ -495,10 +476,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
 #pragma unroll
         for (int jj = 0; jj < KPW; ++jj) {
           const int kk = u * KPW + jj;
-          mma16816(d, PK::get(X, Xs, 2 * jj), PK::get(Y, Ys, 2 * jj), PK::get(X, Xs, 2 * jj + 1),
+          mma16816(da[kk & 3], PK::get(X, Xs, 2 * jj), PK::get(Y, Ys, 2 * jj), PK::get(X, Xs, 2 * jj + 1),
                    PK::get(Y, Ys, 2 * jj + 1), bf[2 * kk], bf[2 * kk + 1]);
         }
       }
+      float d[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[e] = (da[0][e] + da[1][e]) + (da[2][e] + da[3][e]);
       float s0 = -INFINITY, s1 = -INFINITY;
       if (t4 < HG) {
         float sgk = sigk[0], zz = zk[0];

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
       }
     }
     const GroupQ q = group_params(mn, mx, LK);
-    kq[g * D + kq_slot(c)] = q;
+    kq[g * D + (p.lay.frag ? c : kq_slot(c))] = q;  // fragment packing reads them channel by channel
     reinterpret_cast<uint32_t*>(pg + p.lay.off_km)[idx] = q.bits;
   }
 
@@ -295,38 +295,63 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
     constexpr int KB = (BK == 2 || BK == 4) ? BK : 2, VB = (BV == 2 || BV == 4) ? BV : 2;
     uint32_t* kc = reinterpret_cast<uint32_t*>(pg + p.lay.off_kc);
     uint32_t* vc = reinterpret_cast<uint32_t*>(pg + p.lay.off_vc);
-    const int kwords = (R / 16) * 32 * 2 * KB;
-    for (int idx = tid; idx < kwords; idx += kQuantThreads) {
-      const int w = idx % (2 * KB), ln = (idx / (2 * KB)) % 32, tile = idx / (64 * KB);
-      uint32_t word = 0;
-#pragma unroll
-      for (int j = 0; j < 16 / KB; ++j) {
-        int tok, c0;
-        frag_key_pair(KB, tile, ln, w, j, &tok, &c0);
-        const uint32_t xx = *reinterpret_cast<const uint32_t*>(kt + tok * D + c0);
-        const GroupQ* gq = kq + (tok / G) * D;
-        const uint32_t a = excluded(tok, c0) ? 0u : quant_code(h2f((uint16_t)(xx & 0xFFFFu)), gq[kq_slot(c0)], LK);
-        const uint32_t b = excluded(tok, c0 + 1) ? 0u : quant_code(h2f((uint16_t)(xx >> 16)), gq[kq_slot(c0 + 1)], LK);
-        word |= (a << (KB * j)) | (b << (16 + KB * j));
-      }
-      kc[idx] = word;
-    }
     const int ng = D / G;
-    const int vwords = (R / 16) * 32 * 2 * VB;
-    for (int idx = tid; idx < vwords; idx += kQuantThreads) {
-      const int w = idx % (2 * VB), ln = (idx / (2 * VB)) % 32, tile = idx / (64 * VB);
-      uint32_t word = 0;
+    // one thread per (16-token tile, lane) owns that lane's 2B words of the tile
+    for (int idx = tid; idx < (R / 16) * 32; idx += kQuantThreads) {
+      const int tile = idx >> 5, ln = idx & 31, g = ln >> 2, t = ln & 3;
+      {
+        // keys: tokens 16*tile + g (+8), channels 16kk + 8h + 2t (+1); one key group per tile
+        const int tk0 = 16 * tile + g;
+        const GroupQ* gq = kq + (tk0 / G) * D;
+        uint32_t wk[2 * KB];
 #pragma unroll
-      for (int j = 0; j < 16 / VB; ++j) {
-        int tok, ch;
-        frag_value_pair(VB, tile, ln, w, j, &tok, &ch);
-        const GroupQ& q0 = vq[tok * ng + ch / G];
-        const GroupQ& q1 = vq[(tok + 1) * ng + ch / G];
-        const uint32_t a = quant_code(h2f(vt[tok * D + ch]), q0, LV);
-        const uint32_t b = quant_code(h2f(vt[(tok + 1) * D + ch]), q1, LV);
-        word |= (a << (VB * j)) | (b << (16 + VB * j));
+        for (int i = 0; i < 2 * KB; ++i) wk[i] = 0;
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c0 = 16 * kk + 8 * h + 2 * t;
+            const GroupQ q0 = gq[c0], q1 = gq[c0 + 1];
+            const int j = 2 * (kk % (8 / KB)) + h;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int tok = tk0 + 8 * r;
+              const uint32_t xx = *reinterpret_cast<const uint32_t*>(kt + tok * D + c0);
+              const uint32_t a = excluded(tok, c0) ? 0u : quant_code(h2f((uint16_t)(xx & 0xFFFFu)), q0, LK);
+              const uint32_t b = excluded(tok, c0 + 1) ? 0u : quant_code(h2f((uint16_t)(xx >> 16)), q1, LK);
+              wk[r * KB + kk / (8 / KB)] |= (a << (KB * j)) | (b << (16 + KB * j));
+            }
+          }
+        uint4* dstk = reinterpret_cast<uint4*>(kc + (size_t)idx * 2 * KB);
+#pragma unroll
+        for (int i = 0; i < 2 * KB / 4; ++i) dstk[i] = make_uint4(wk[4 * i], wk[4 * i + 1], wk[4 * i + 2], wk[4 * i + 3]);
       }
-      vc[idx] = word;
+      {
+        // values: tokens s, s+1 with s = 16*tile + 8*tb + 2t; channel 16mc + g + 8rr; one
+        // quantizer per (token, channel group), used for every channel of the lane in that group
+        uint32_t wv[2 * VB];
+#pragma unroll
+        for (int i = 0; i < 2 * VB; ++i) wv[i] = 0;
+#pragma unroll
+        for (int tb = 0; tb < 2; ++tb) {
+          const int s0 = 16 * tile + 8 * tb + 2 * t;
+          for (int grp = 0; grp < ng; ++grp) {
+            const GroupQ q0 = vq[s0 * ng + grp], q1 = vq[(s0 + 1) * ng + grp];
+            for (int mc = grp * (G / 16); mc < (grp + 1) * (G / 16); ++mc)
+#pragma unroll
+              for (int rr = 0; rr < 2; ++rr) {
+                const int ch = 16 * mc + g + 8 * rr;
+                const uint32_t a = quant_code(h2f(vt[s0 * D + ch]), q0, LV);
+                const uint32_t b = quant_code(h2f(vt[(s0 + 1) * D + ch]), q1, LV);
+                const int r = 2 * tb + rr, j = mc % (16 / VB);
+                wv[r * (VB / 2) + mc / (16 / VB)] |= (a << (VB * j)) | (b << (16 + VB * j));
+              }
+          }
+        }
+        uint4* dstv = reinterpret_cast<uint4*>(vc + (size_t)idx * 2 * VB);
+#pragma unroll
+        for (int i = 0; i < 2 * VB / 4; ++i) dstv[i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+      }
     }
   } else {
     // ---- codes as token-major bitstreams, computed and packed a 32-channel chunk (BITS words) at a time
