@@ -3,9 +3,10 @@
 
 Workload (one step): for each of L layer caches (default 4) of the
 Llama-2-7B-shaped layer (B=8, 32 KV = 32 query heads, D=128, K2V2, G=32,
-R=128): prefill 4096 tokens (quantize-and-pack), then 64 decode steps, each
-an append of one token (the first one flushes the full fp16 window into a
-page) followed by decode attention over the whole cache.  Layers are visited
+R=128): prefill 4096 tokens (quantize-and-pack), then 64 fused decode steps
+(kvq_decode_step): each appends one token and runs decode attention over the
+whole cache in one launch (the first one flushes the full fp16 window into a
+page before it).  Layers are visited
 in turn inside each decode step, as a model does, so the 101-109 MB cache of
 one layer is never L2-resident when it is read again (4 caches > 129 MB L2).
 
@@ -16,7 +17,8 @@ e2e    = the same metric through the public C-ABI calls with the inputs in
          tokens and queries host->device and reads every output back.
 roofline: the dominant kernel (decode attention) against the measured HBM
          copy bandwidth: algorithmic bytes per launch (packed codes + scales
-         and zero points + fp16 window + q + out) / mean launch time.
+         and zero points + fp16 window + q + out + the new token's window
+         store) / mean launch time of the steps that do not flush.
 
 `--impl reference` times the CPU oracle (the plain fp64/fp32 C reference the
 tests check against) on a bounded sample of the same workload.
@@ -120,6 +122,11 @@ def decode_bytes(w, T):
     return w.batch * w.kv_heads * per_unit + 2 * w.batch * w.q_heads * D * 2
 
 
+def decode_step_bytes(w, T):
+    """decode_bytes plus the store of the new token's key and value into the window (a fused step)."""
+    return decode_bytes(w, T) + w.batch * w.kv_heads * w.head_dim * 4
+
+
 def step_tokens(w, layers):
     T0 = w.prefill_tokens
     return layers * sum(w.batch * (T0 + i) for i in range(1, w.decode_steps + 1))
@@ -133,7 +140,7 @@ def workload_config(w, layers, graph, world):
         "prefill_tokens": w.prefill_tokens, "decode_steps": w.decode_steps,
         "k_bits": w.k_bits, "v_bits": w.v_bits, "group": w.group, "residual": w.residual,
         "step": f"{layers} layers x (prefill {w.prefill_tokens}) + {w.decode_steps} x {layers} layers x "
-                f"(append + decode attention)",
+                f"fused decode step (append + decode attention, one launch)",
         "l2": f"inputs larger than L2: {layers} layer caches of "
               f"{decode_bytes(w, w.prefill_tokens + 1) / 1e6:.0f} MB visited in turn",
         "launch": "one CUDA graph per step" if graph else "direct C-ABI calls",
@@ -276,10 +283,9 @@ def run_ours(args, dist):
         n = 0
         for i in range(S):
             for l, h in enumerate(handles):
-                check(Lb.kvq_append(h, knp[i], vnp[i], sh), "append")
                 if events is not None:
                     events[n][0].record(stream)
-                check(Lb.kvq_decode_attention(h, qp[i], op[l][i], sh), "decode")
+                check(Lb.kvq_decode_step(h, knp[i], vnp[i], qp[i], op[l][i], sh), "decode step")
                 if events is not None:
                     events[n][1].record(stream)
                 n += 1
@@ -335,7 +341,8 @@ def run_ours(args, dist):
             raise RuntimeError("device-side error in the timed region")
     ms_step = dist.max(ms_total / args.steps)
 
-    # ---------------- per-launch timing of decode attention (direct calls, CUDA events on the launch stream)
+    # ---------------- per-launch timing of decode attention (direct calls, CUDA events on the launch stream);
+    # decode steps 1..S-1 are one launch each (step 0 also flushes the window and is left out)
     n_dec = S * L
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dec)]
     durs = []
@@ -343,9 +350,9 @@ def run_ours(args, dist):
         for _ in range(args.timing_steps):
             step(evs)
             torch.cuda.synchronize(dev)
-            durs.extend(a.elapsed_time(b) for a, b in evs)
+            durs.extend(a.elapsed_time(b) for a, b in evs[L:])
     dec_ms = statistics.mean(durs) if durs else float("nan")
-    dec_bytes = statistics.mean(decode_bytes(w, T0 + 1 + i) for i in range(S))
+    dec_bytes = statistics.mean(decode_step_bytes(w, T0 + 1 + i) for i in range(1, S))
     import json as _json
     peaks = _json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
@@ -367,7 +374,7 @@ def run_ours(args, dist):
                      "traffic": traffic, "kernel": "decode attention (decode_mma_kernel, tensor cores)",
                      "bytes_per_launch": dec_bytes, "ms_per_launch": dec_ms,
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6.8 TB/s"},
-        "decode_only": {"value": B * statistics.mean(T0 + 1 + i for i in range(S)) / (dec_ms * 1e-3),
+        "decode_only": {"value": B * statistics.mean(T0 + 1 + i for i in range(1, S)) / (dec_ms * 1e-3),
                         "unit": UNIT, "ms_per_launch": dec_ms},
         "clocks": clock_info, "e2e": e2e,
         "config": workload_config(w, L, graph is not None, dist.world),
@@ -445,8 +452,7 @@ def run_e2e(args, w, dist, caches, stream):
             dq[i].copy_(hq[i], non_blocking=True)
             h2d += hkn[i].nbytes + hvn[i].nbytes + hq[i].nbytes
             for l, c in enumerate(caches):
-                c.append(dkn[i], dvn[i], stream=stream)
-                c.decode_attention(dq[i], dout[l, i], stream=stream)
+                c.decode_step(dkn[i], dvn[i], dq[i], dout[l, i], stream=stream)
         hout.copy_(dout, non_blocking=True)
         d2h += hout.nbytes
 

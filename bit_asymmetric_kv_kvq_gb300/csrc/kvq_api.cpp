@@ -184,6 +184,79 @@ PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp, bool rope) 
 
 }  // namespace kvq
 
+// The full window of every unit becomes page Tq/R (the flush of an append that finds n_r = R).
+cudaError_t flush_window(kvq_cache* c, cudaStream_t s) {
+  const int R = c->cfg.residual, D = c->cfg.head_dim;
+  kvq::QuantizeParams qp{};
+  qp.k_src = c->wk;
+  qp.v_src = c->wv;
+  qp.src_unit_stride = (int64_t)R * D;
+  qp.src_tok0 = 0;
+  qp.pages = c->pages;
+  qp.unit_page_stride = c->unit_page_stride;
+  qp.page0 = c->Tq / R;
+  qp.n_units = (int32_t)c->n_units;
+  qp.Hkv = c->cfg.num_kv_heads;
+  qp.D = D;
+  qp.G = c->cfg.group_size;
+  qp.R = R;
+  qp.nsp = c->cfg.k_sparse;
+  qp.lay = c->lay;
+  qp.err = c->err;
+  const cudaError_t e = kvq::launch_quantize(qp, c->cfg.k_bits, c->cfg.v_bits, 1, s);
+  if (e == cudaSuccess) {
+    c->launches++;
+    c->Tq += R;
+    c->n_r = 0;
+  }
+  return e;
+}
+
+// Decode attention over the cache's current state.  k_new/v_new are null, or hold the window's
+// newest token (slot n_r - 1), which the kernel then reads from there and stores into the window.
+kvq_status launch_decode_for(kvq_cache* c, const void* q, void* out, const void* k_new, const void* v_new,
+                             cudaStream_t s) {
+  const int R = c->cfg.residual;
+  const int64_t grid = decode_grid(c);
+  const int hg = c->cfg.num_q_heads / c->cfg.num_kv_heads;
+  kvq::DecodeParams dp{};
+  dp.q = static_cast<const uint16_t*>(q);
+  dp.pages = c->pages;
+  dp.unit_page_stride = c->unit_page_stride;
+  dp.wk = c->wk;
+  dp.wv = c->wv;
+  dp.win_unit_stride = (int64_t)R * c->cfg.head_dim;
+  dp.k_new = static_cast<const uint16_t*>(k_new);
+  dp.v_new = static_cast<const uint16_t*>(v_new);
+  dp.n_units = c->n_units;
+  dp.n_pages = c->Tq / R;
+  dp.work_per_unit = (int32_t)(dp.n_pages + (c->n_r > 0 ? 1 : 0));
+  dp.n_r = c->n_r;
+  dp.max_slots = c->max_slots;
+  dp.Hkv = c->cfg.num_kv_heads;
+  dp.Hq = c->cfg.num_q_heads;
+  dp.D = c->cfg.head_dim;
+  dp.G = c->cfg.group_size;
+  dp.log2G = c->cfg.group_size == 64 ? 6 : 5;
+  dp.R = R;
+  dp.nsp = c->cfg.k_sparse;
+  dp.lay = c->lay;
+  dp.qk_scale_log2 = c->cfg.softmax_scale * 1.4426950408889634f;
+  dp.rope_turns = c->rope_turns;
+  dp.part_ml = c->part_ml;
+  dp.part_acc = c->part_acc;
+  dp.counters = c->counters;
+  dp.nslot = c->counters + c->n_units;
+  dp.out = static_cast<uint16_t*>(out);
+  dp.err = c->err;
+  bool supported = false;
+  if (kvq::launch_decode(dp, c->cfg.k_bits, c->cfg.v_bits, hg, c->cfg.rope != 0, (int)grid, s, &supported) !=
+      cudaSuccess)
+    return supported ? fail_cuda(c) : KVQ_ERR_UNSUPPORTED;
+  c->launches++;
+  return KVQ_OK;
+}
+
 extern "C" {
 
 int32_t kvq_version(void) { return (1 << 16) | 0; }
@@ -395,29 +468,7 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, void* stream) 
   if (!g.ok) return fail_cuda(c);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int R = c->cfg.residual, D = c->cfg.head_dim;
-  if (c->n_r == R) {
-    // flush: the full window becomes page Tq/R
-    kvq::QuantizeParams qp{};
-    qp.k_src = c->wk;
-    qp.v_src = c->wv;
-    qp.src_unit_stride = (int64_t)R * D;
-    qp.src_tok0 = 0;
-    qp.pages = c->pages;
-    qp.unit_page_stride = c->unit_page_stride;
-    qp.page0 = c->Tq / R;
-    qp.n_units = (int32_t)c->n_units;
-    qp.Hkv = c->cfg.num_kv_heads;
-    qp.D = D;
-    qp.G = c->cfg.group_size;
-    qp.R = R;
-    qp.nsp = c->cfg.k_sparse;
-    qp.lay = c->lay;
-    qp.err = c->err;
-    if (kvq::launch_quantize(qp, c->cfg.k_bits, c->cfg.v_bits, 1, s) != cudaSuccess) return fail_cuda(c);
-    c->launches++;
-    c->Tq += R;
-    c->n_r = 0;
-  }
+  if (c->n_r == R && flush_window(c, s) != cudaSuccess) return fail_cuda(c);
   kvq::CopyTokensParams cp{};
   cp.k_src = static_cast<const uint16_t*>(k);
   cp.v_src = static_cast<const uint16_t*>(v);
@@ -445,44 +496,23 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, void* st
   if (c->T < 1) return KVQ_ERR_STATE;
   DeviceGuard g(c->device);
   if (!g.ok) return fail_cuda(c);
+  return launch_decode_for(c, q, out, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_decode_step(kvq_cache* c, const void* k, const void* v, const void* q, void* out, void* stream) {
+  if (!c || !k || !v || !q || !out) return KVQ_ERR_INVALID_ARG;
+  if (c->broken) return KVQ_ERR_CUDA;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
+  if (c->T + 1 > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail_cuda(c);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int R = c->cfg.residual;
-  const int64_t grid = decode_grid(c);
-  const int hg = c->cfg.num_q_heads / c->cfg.num_kv_heads;
-  kvq::DecodeParams dp{};
-  dp.q = static_cast<const uint16_t*>(q);
-  dp.pages = c->pages;
-  dp.unit_page_stride = c->unit_page_stride;
-  dp.wk = c->wk;
-  dp.wv = c->wv;
-  dp.win_unit_stride = (int64_t)R * c->cfg.head_dim;
-  dp.n_units = c->n_units;
-  dp.n_pages = c->Tq / R;
-  dp.work_per_unit = (int32_t)(dp.n_pages + (c->n_r > 0 ? 1 : 0));
-  dp.n_r = c->n_r;
-  dp.max_slots = c->max_slots;
-  dp.Hkv = c->cfg.num_kv_heads;
-  dp.Hq = c->cfg.num_q_heads;
-  dp.D = c->cfg.head_dim;
-  dp.G = c->cfg.group_size;
-  dp.log2G = c->cfg.group_size == 64 ? 6 : 5;
-  dp.R = R;
-  dp.nsp = c->cfg.k_sparse;
-  dp.lay = c->lay;
-  dp.qk_scale_log2 = c->cfg.softmax_scale * 1.4426950408889634f;
-  dp.rope_turns = c->rope_turns;
-  dp.part_ml = c->part_ml;
-  dp.part_acc = c->part_acc;
-  dp.counters = c->counters;
-  dp.nslot = c->counters + c->n_units;
-  dp.out = static_cast<uint16_t*>(out);
-  dp.err = c->err;
-  bool supported = false;
-  if (kvq::launch_decode(dp, c->cfg.k_bits, c->cfg.v_bits, hg, c->cfg.rope != 0, (int)grid, s, &supported) !=
-      cudaSuccess)
-    return supported ? fail_cuda(c) : KVQ_ERR_UNSUPPORTED;
-  c->launches++;
-  return KVQ_OK;
+  if (c->n_r == c->cfg.residual && flush_window(c, s) != cudaSuccess) return fail_cuda(c);
+  // the new token is window slot n_r; the decode launch stores it there as it reads it
+  c->n_r += 1;
+  c->T += 1;
+  c->prefilled = true;
+  return launch_decode_for(c, q, out, k, v, s);
 }
 
 kvq_status kvq_sync_status(kvq_cache* c, void* stream) {

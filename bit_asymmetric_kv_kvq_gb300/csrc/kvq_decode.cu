@@ -838,6 +838,14 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       const int64_t tq = p.n_pages * (int64_t)p.R;
       const uint16_t* wk = p.wk + cur * p.win_unit_stride;
       const uint16_t* wv = p.wv + cur * p.win_unit_stride;
+      // the newest token comes from the caller's buffers when the step appends it; the warp
+      // that covers it also stores it into its window slot
+      const int newest = p.k_new ? p.n_r - 1 : -1;
+      if (newest >= 32 * stt && newest < 32 * stt + 32) {
+        const uint16_t* src = lane < 16 ? p.k_new + cur * D : p.v_new + cur * D;
+        uint16_t* dst = const_cast<uint16_t*>(lane < 16 ? wk : wv) + (int64_t)newest * D;
+        reinterpret_cast<uint4*>(dst)[lane & 15] = __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15));
+      }
       if (32 * stt < p.n_r) {
         float sc[TPL][HG];
 #pragma unroll
@@ -848,7 +856,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
             for (int h = 0; h < HG; ++h) sc[j][h] = 0.0f;
             continue;
           }
-          const uint16_t* kr = wk + (int64_t)tt * D;
+          const uint16_t* kr = tt == newest ? p.k_new + cur * D : wk + (int64_t)tt * D;
           float a[HG];
 #pragma unroll
           for (int h = 0; h < HG; ++h) a[h] = 0.0f;
@@ -896,7 +904,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
           const int tt = stt * 32 + tau + TAU * j;
           if (tt >= p.n_r) continue;
           float xv[CPL];
-          load_halves<CPL>(wv + (int64_t)tt * D + vc_lo, xv);
+          load_halves<CPL>((tt == newest ? p.v_new + cur * D : wv + (int64_t)tt * D) + vc_lo, xv);
 #pragma unroll
           for (int h = 0; h < HG; ++h) {
             const float pw = sc[j][h];

@@ -291,11 +291,14 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     const uint16_t* wv = p.wv + unit * p.win_unit_stride;
     const int tok = 32 * stt + lane;
     const bool live = tok < p.n_r;
+    // the newest token comes from the caller's buffers when the step appends it (stored below)
+    const int newest = p.k_new ? p.n_r - 1 : -1;
     float s[HG];
 #pragma unroll
     for (int h = 0; h < HG; ++h) s[h] = 0.0f;
     if (live) {
-      const uint4* row = reinterpret_cast<const uint4*>(wk + (int64_t)tok * D);
+      const uint4* row =
+          reinterpret_cast<const uint4*>(tok == newest ? p.k_new + unit * D : wk + (int64_t)tok * D);
 #pragma unroll 4
       for (int v = 0; v < D / 8; ++v) {
         const uint4 w = __ldg(row + v);
@@ -323,7 +326,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
       float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
       for (int j = 0; j < nt; ++j) {
         const float pj = __shfl_sync(kAll, pw, j);
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(wv + (int64_t)(32 * stt + j) * D + 4 * lane));
+        const uint16_t* vrow = 32 * stt + j == newest ? p.v_new + unit * D : wv + (int64_t)(32 * stt + j) * D;
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(vrow + 4 * lane));
         const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
         const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
         a0 = fmaf(pj, x01.x, a0);
@@ -336,6 +340,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
         *reinterpret_cast<float4*>(p.part_acc + so * D + 4 * lane) = make_float4(a0, a1, a2, a3);
         if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + so * 2) = make_float2(m, l);
       }
+    }
+    if (newest >= 32 * stt && newest < 32 * stt + 32) {
+      // store the appended token into its window slot: lanes 0-15 the key row, 16-31 the value row
+      const uint16_t* src = lane < 16 ? p.k_new + unit * D : p.v_new + unit * D;
+      uint16_t* dst = const_cast<uint16_t*>(lane < 16 ? wk : wv) + (int64_t)newest * D;
+      reinterpret_cast<uint4*>(dst)[lane & 15] = __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15));
     }
   };
 

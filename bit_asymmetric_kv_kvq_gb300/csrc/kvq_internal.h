@@ -102,6 +102,8 @@ struct DecodeParams {
   const uint16_t* wk;       // window [units][R][D]
   const uint16_t* wv;
   int64_t win_unit_stride;  // elements
+  const uint16_t* k_new;    // null, or [B*Hkv][D] fp16: the window's newest token (slot n_r - 1),
+  const uint16_t* v_new;    //   read from here and stored into the window by the decode kernel
   int64_t n_units;          // B * Hkv
   int64_t n_pages;          // quantized pages per unit (Tq / R)
   int32_t work_per_unit;    // n_pages + (n_r > 0): page items then the window item

@@ -63,6 +63,7 @@ SIGNATURES = {
     "kvq_prefill_quantize": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, _P]),
     "kvq_append": (ctypes.c_int, [_P, _P, _P, _P]),
     "kvq_decode_attention": (ctypes.c_int, [_P, _P, _P, _P]),
+    "kvq_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "kvq_reset": (ctypes.c_int, [_P]),
     "kvq_decode_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(kvq_config), _P, ctypes.c_int64, _P, _P,
                                                     ctypes.c_int64, _P, _P, _P]),
@@ -156,6 +157,10 @@ def kvq_append(handle, k, v, stream=None) -> None:
 
 def kvq_decode_attention(handle, q, out, stream=None) -> None:
     _check(lib().kvq_decode_attention(handle, _ptr(q), _ptr(out), _stream(stream)), "kvq_decode_attention")
+
+
+def kvq_decode_step(handle, k, v, q, out, stream=None) -> None:
+    _check(lib().kvq_decode_step(handle, _ptr(k), _ptr(v), _ptr(q), _ptr(out), _stream(stream)), "kvq_decode_step")
 
 
 def kvq_decode_attention_noalloc(cfg: kvq_config, pages, pages_per_unit: int, window_k, window_v, n_tokens: int,
@@ -258,6 +263,19 @@ class KVCache:
             out = torch.empty_like(q)
         self._need(out, (c.batch, c.num_q_heads, c.head_dim), "out")
         kvq_decode_attention(self.handle, q, out, _stream(stream, self.device))
+        return out
+
+    def decode_step(self, k, v, q, out=None, stream=None):
+        """append(k, v) then decode_attention(q) in one call (one launch, two on a flush)."""
+        import torch
+        c = self.cfg
+        self._need(k, (c.batch, c.num_kv_heads, c.head_dim), "k")
+        self._need(v, (c.batch, c.num_kv_heads, c.head_dim), "v")
+        self._need(q, (c.batch, c.num_q_heads, c.head_dim), "q")
+        if out is None:
+            out = torch.empty_like(q)
+        self._need(out, (c.batch, c.num_q_heads, c.head_dim), "out")
+        kvq_decode_step(self.handle, k, v, q, out, _stream(stream, self.device))
         return out
 
     def reset(self):

@@ -131,6 +131,21 @@ kvq_status kvq_append(kvq_cache* cache, const void* k_f16, const void* v_f16, vo
 kvq_status kvq_decode_attention(kvq_cache* cache, const void* q_f16, void* out_f16, void* cuda_stream);
 
 /*
+ * One decode step of a layer in one call: kvq_append(k, v) followed by
+ * kvq_decode_attention(q, out), with identical results (the same cache state
+ * and bit-identical outputs).  The append's flush, when the window is full,
+ * is its own launch; the new token is read by the attention launch straight
+ * from k and v and stored into its window slot by that launch, so a step costs
+ * one launch (two on a flush) instead of two (three).  Buffers as for
+ * kvq_append and kvq_decode_attention; the same errors (KVQ_ERR_CAPACITY
+ * before any work when the cache is full).  unite.ai page, section "System
+ * tax": each generated token appends to the window, flushes a full window as
+ * one block, and reads the whole cache.
+ */
+kvq_status kvq_decode_step(kvq_cache* cache, const void* k_f16, const void* v_f16, const void* q_f16, void* out_f16,
+                           void* cuda_stream);
+
+/*
  * Forget every cached token so the cache can take a new batch of sequences
  * (the next call may be a prefill).  Host-only: no device work, no memory
  * is freed or cleared; the pages are simply overwritten by later calls.
