@@ -14,7 +14,8 @@ machine and the canonical packed stores the CUDA library exports:
   vz, vs  uint16 [Tq][D/G]        value zero point / scale, per token per G-channel group
   sp_idx  uint8  [Tq][nsp]        sparse key entries: channel, ascending
   sp_val  uint16 [Tq][nsp]        sparse key entries: exact fp16 value
-  wk, wv  uint16 [n_r][D]         fp16 residual window (tokens Tq .. Tq+n_r)
+  wk, wv  uint16 [n_r][D]         fp16 residual window (tokens S+Tq .. S+Tq+n_r)
+  sk, sv  uint16 [n_s][D]         fp16 attention-sink tokens (tokens 0 .. n_s)
 
 State machine (unite.ai page, "System tax"; KIVI summary page, "Method"):
 the most recent tokens stay in an fp16 window of at most R tokens and are
@@ -22,6 +23,15 @@ quantized as one block when the window is full.  Reading: an append that
 finds the window full first quantizes those R tokens, then stores the new
 token, so for T >= 1 tokens the window holds n_r in [1, R] tokens and
 Tq = R*floor((T-1)/R).
+
+Attention sinks (unite.ai page and dothoosh.com page, sections on research
+directions, on InnerQ): besides the recent window, the first tokens of the
+sequence are kept in fp16 too.  Reading: with S sink tokens, the first
+n_s = min(T, S) tokens go to the sink store and are never quantized; the
+state machine above runs on the tokens after them (T - n_s of them), so
+Tq = R*floor((T-n_s-1)/R).  Positions (for RoPE) stay absolute: sink tokens
+0..n_s, quantized tokens n_s..n_s+Tq, window after them.  S = 0 is the plain
+cache.
 """
 from __future__ import annotations
 
@@ -61,7 +71,8 @@ class _Unit(ctypes.Structure):
     _fields_ = [("D", _I), ("G", _I), ("nsp", _I), ("rope", _I), ("rope_base", ctypes.c_double),
                 ("Tq", _I64), ("n_r", _I64),
                 ("kcodes", _P), ("kz", _P), ("ks", _P), ("sp_idx", _P), ("sp_val", _P),
-                ("vcodes", _P), ("vz", _P), ("vs", _P), ("wk", _P), ("wv", _P)]
+                ("vcodes", _P), ("vz", _P), ("vs", _P), ("wk", _P), ("wv", _P),
+                ("n_s", _I64), ("sk", _P), ("sv", _P)]
 
 
 def lib():
@@ -255,9 +266,9 @@ def quantized_tokens(T: int, R: int) -> int:
 class OracleUnit:
     """Cache state of one (batch, kv-head) sequence, driven like the library."""
 
-    def __init__(self, head_dim, k_bits, v_bits, group, residual, k_sparse=0, rope=0, rope_base=10000.0):
+    def __init__(self, head_dim, k_bits, v_bits, group, residual, k_sparse=0, rope=0, rope_base=10000.0, sink=0):
         self.D, self.bk, self.bv, self.G, self.R = head_dim, k_bits, v_bits, group, residual
-        self.nsp, self.rope, self.rope_base = k_sparse, rope, rope_base
+        self.nsp, self.rope, self.rope_base, self.S = k_sparse, rope, rope_base, sink
         D = head_dim
         self.kcodes = np.zeros((0, D), np.uint8)
         self.kz = np.zeros((0, D), np.uint16)
@@ -269,11 +280,14 @@ class OracleUnit:
         self.vs = np.zeros((0, D // group), np.uint16)
         self.wk = np.zeros((0, D), np.uint16)
         self.wv = np.zeros((0, D), np.uint16)
+        self.sk = np.zeros((0, D), np.uint16)
+        self.sv = np.zeros((0, D), np.uint16)
         self.prefilled = False
 
     @classmethod
     def for_workload(cls, w):
-        return cls(w.head_dim, w.k_bits, w.v_bits, w.group, w.residual, w.k_sparse, w.rope, w.rope_base)
+        return cls(w.head_dim, w.k_bits, w.v_bits, w.group, w.residual, w.k_sparse, w.rope, w.rope_base,
+                   getattr(w, "sink", 0))
 
     @property
     def Tq(self):
@@ -284,8 +298,12 @@ class OracleUnit:
         return self.wk.shape[0]
 
     @property
+    def n_s(self):
+        return self.sk.shape[0]
+
+    @property
     def T(self):
-        return self.Tq + self.n_r
+        return self.n_s + self.Tq + self.n_r
 
     def _quantize_block(self, K16, V16):
         kc, kz, ks, si, sv = quantize_keys(K16, self.G, self.bk, self.nsp)
@@ -300,10 +318,14 @@ class OracleUnit:
         self.vs = np.concatenate([self.vs, vs])
 
     def prefill(self, K16, V16):
-        """Cache T prompt tokens: quantize the first R*floor((T-1)/R), keep the rest fp16."""
+        """Cache T prompt tokens: the first min(T, S) go to the sink; of the rest, quantize the first
+        R*floor((T'-1)/R) and keep the others in the fp16 window."""
         if self.prefilled or self.T:
             raise RuntimeError("prefill is allowed once, on an empty cache")
         K, V = f16_bits(K16), f16_bits(V16)
+        ns = min(K.shape[0], self.S)
+        self.sk, self.sv = K[:ns].copy(), V[:ns].copy()
+        K, V = K[ns:], V[ns:]
         T = K.shape[0]
         Tq = quantized_tokens(T, self.R)
         if Tq:
@@ -313,9 +335,14 @@ class OracleUnit:
         self.prefilled = True
 
     def append(self, k16, v16):
-        """One decode token: flush a full window as one quantized block, then store the token."""
+        """One decode token: into the sink while it has room; otherwise flush a full window as one
+        quantized block, then store the token in the window."""
         k = f16_bits(k16).reshape(1, self.D)
         v = f16_bits(v16).reshape(1, self.D)
+        if self.n_s < self.S:
+            self.sk = np.concatenate([self.sk, k])
+            self.sv = np.concatenate([self.sv, v])
+            return
         if self.n_r == self.R:
             self._quantize_block(self.wk, self.wv)
             self.wk = np.zeros((0, self.D), np.uint16)
@@ -327,14 +354,17 @@ class OracleUnit:
         """Canonical packed stores (the layout the library exports)."""
         return dict(kcodes=pack_rows(self.kcodes, self.bk), kz=self.kz.copy(), ks=self.ks.copy(),
                     vcodes=pack_rows(self.vcodes, self.bv), vz=self.vz.copy(), vs=self.vs.copy(),
-                    sp_idx=self.sp_idx.copy(), sp_val=self.sp_val.copy(), wk=self.wk.copy(), wv=self.wv.copy())
+                    sp_idx=self.sp_idx.copy(), sp_val=self.sp_val.copy(), wk=self.wk.copy(), wv=self.wv.copy(),
+                    sk=self.sk.copy(), sv=self.sv.copy())
 
     def _struct(self):
         keep = [_c(self.kcodes, np.uint8), _c(self.kz, np.uint16), _c(self.ks, np.uint16),
                 _c(self.sp_idx, np.uint8), _c(self.sp_val, np.uint16), _c(self.vcodes, np.uint8),
                 _c(self.vz, np.uint16), _c(self.vs, np.uint16), _c(self.wk, np.uint16), _c(self.wv, np.uint16)]
+        sink = [_c(self.sk, np.uint16), _c(self.sv, np.uint16)]
         u = _Unit(self.D, self.G, self.nsp, self.rope, float(self.rope_base), self.Tq, self.n_r,
-                  *[_ptr(a) for a in keep])
+                  *[_ptr(a) for a in keep], self.n_s, *[_ptr(a) for a in sink])
+        keep += sink
         return u, keep
 
     def dequant(self, t: int):

@@ -333,14 +333,29 @@ typedef struct {
   const uint8_t* vcodes;  /* [Tq][D] */
   const uint16_t* vz;     /* [Tq][D/G] */
   const uint16_t* vs;
-  const uint16_t* wk;     /* [n_r][D] fp16 window keys (tokens Tq..Tq+n_r) */
+  const uint16_t* wk;     /* [n_r][D] fp16 window keys (tokens n_s+Tq .. n_s+Tq+n_r) */
   const uint16_t* wv;
+  int64_t n_s;            /* attention-sink tokens kept fp16 (tokens 0 .. n_s) */
+  const uint16_t* sk;     /* [n_s][D] */
+  const uint16_t* sv;
 } kvqo_unit;
 
-/* Key of token t as the decoder sees it: z + s*code (exact in fp64), sparse
-   entries restored, window keys as stored, then RoPE at position t if asked. */
+/* Token order: the n_s sink tokens, then the Tq quantized tokens, then the
+   n_r window tokens; t is the absolute position, which is also the RoPE
+   position. */
+
+/* Key of token t as the decoder sees it: sink and window keys as stored,
+   quantized keys z + s*code (exact in fp64) with their sparse entries
+   restored, then RoPE at position t if asked. */
 static void key_of(const kvqo_unit* u, int64_t t, double* k) {
   const int D = u->D;
+  if (t < u->n_s) {
+    for (int c = 0; c < D; ++c) k[c] = kvqo_half_to_double(u->sk[t * D + c]);
+    if (u->rope) kvqo_rope(k, D, (double)t, u->rope_base);
+    return;
+  }
+  const int64_t abs_t = t;
+  t -= u->n_s;
   if (t < u->Tq) {
     const int64_t g = t / u->G;
     for (int c = 0; c < D; ++c)
@@ -350,11 +365,16 @@ static void key_of(const kvqo_unit* u, int64_t t, double* k) {
   } else {
     for (int c = 0; c < D; ++c) k[c] = kvqo_half_to_double(u->wk[(t - u->Tq) * D + c]);
   }
-  if (u->rope) kvqo_rope(k, D, (double)t, u->rope_base);
+  if (u->rope) kvqo_rope(k, D, (double)abs_t, u->rope_base);
 }
 
 static void value_of(const kvqo_unit* u, int64_t t, double* v) {
   const int D = u->D, ng = D / u->G;
+  if (t < u->n_s) {
+    for (int c = 0; c < D; ++c) v[c] = kvqo_half_to_double(u->sv[t * D + c]);
+    return;
+  }
+  t -= u->n_s;
   if (t < u->Tq) {
     for (int c = 0; c < D; ++c) {
       const int j = c / u->G;
@@ -366,7 +386,7 @@ static void value_of(const kvqo_unit* u, int64_t t, double* v) {
 }
 
 int kvqo_dequant_token(const kvqo_unit* u, int64_t t, double* k, double* v) {
-  if (t < 0 || t >= u->Tq + u->n_r) return -1;
+  if (t < 0 || t >= u->n_s + u->Tq + u->n_r) return -1;
   if (k) key_of(u, t, k);
   if (v) value_of(u, t, v);
   return 0;
@@ -387,7 +407,7 @@ int kvqo_dequant_token(const kvqo_unit* u, int64_t t, double* k, double* v) {
 int kvqo_attention_partial(const kvqo_unit* u, const uint16_t* q, int Hg, float softmax_scale,
                            int64_t t_begin, int64_t t_end, double* m, double* l, double* acc) {
   const int D = u->D;
-  const int64_t T = u->Tq + u->n_r;
+  const int64_t T = u->n_s + u->Tq + u->n_r;
   if (t_begin < 0 || t_end > T || t_begin > t_end || Hg <= 0) return -1;
   const int64_t n = t_end - t_begin;
   const double scale = (double)softmax_scale;
@@ -449,7 +469,7 @@ int kvqo_combine(int S, int D, const double* m, const double* l, const double* a
   return 0;
 }
 
-/* Full decode attention of Hg heads over all T = Tq + n_r tokens. */
+/* Full decode attention of Hg heads over all T = n_s + Tq + n_r tokens. */
 int kvqo_attention(const kvqo_unit* u, const uint16_t* q, int Hg, float softmax_scale, double* out) {
   const int D = u->D;
   double* m = (double*)malloc(sizeof(double) * Hg);
@@ -459,7 +479,7 @@ int kvqo_attention(const kvqo_unit* u, const uint16_t* q, int Hg, float softmax_
     free(m); free(l); free(acc);
     return -2;
   }
-  int rc = kvqo_attention_partial(u, q, Hg, softmax_scale, 0, u->Tq + u->n_r, m, l, acc);
+  int rc = kvqo_attention_partial(u, q, Hg, softmax_scale, 0, u->n_s + u->Tq + u->n_r, m, l, acc);
   for (int h = 0; rc == 0 && h < Hg; ++h) rc = kvqo_combine(1, D, m + h, l + h, acc + h * D, out + h * D);
   free(m);
   free(l);
