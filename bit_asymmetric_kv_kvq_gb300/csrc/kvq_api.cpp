@@ -7,6 +7,11 @@
 // as one page (the flush) and then stores the new token.  So for T >= 1
 // cached tokens the window holds n_r in [1, R] tokens and Tq = R*floor((T-1)/R)
 // tokens are quantized.  All counts live on the host: no call reads the GPU.
+//
+// Attention sinks (unite.ai page and dothoosh.com page, research-direction sections: InnerQ keeps
+// the attention-sink tokens in high precision as well as the recent ones): with sink_tokens = S
+// the first n_s = min(T, S) tokens are stored fp16 in a sink store and never quantized; the
+// window/flush machine above runs on the tokens after them, so Tq = R*floor((T-n_s-1)/R).
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -28,6 +33,8 @@ struct kvq_cache {
   uint8_t* pages = nullptr;
   uint16_t* wk = nullptr;
   uint16_t* wv = nullptr;
+  uint16_t* sk = nullptr;     // sink tokens [units][S][D]
+  uint16_t* sv = nullptr;
   float* part_ml = nullptr;
   float* part_acc = nullptr;
   int* counters = nullptr;
@@ -39,6 +46,7 @@ struct kvq_cache {
   int32_t decode_warps = 1;   // warps of one decode CTA
   int64_t T = 0, Tq = 0;
   int32_t n_r = 0;
+  int32_t n_s = 0;            // sink tokens held (<= S)
   bool prefilled = false;
   bool broken = false;
   int64_t launches = 0;
@@ -71,6 +79,8 @@ void free_all(kvq_cache* c) {
   cudaFree(c->pages);
   cudaFree(c->wk);
   cudaFree(c->wv);
+  cudaFree(c->sk);
+  cudaFree(c->sv);
   cudaFree(c->part_ml);
   cudaFree(c->part_acc);
   cudaFree(c->counters);
@@ -78,6 +88,7 @@ void free_all(kvq_cache* c) {
   cudaFree(c->rope_turns);
   c->pages = nullptr;
   c->wk = c->wv = nullptr;
+  c->sk = c->sv = nullptr;
   c->part_ml = c->part_acc = nullptr;
   c->err = nullptr;
   c->counters = nullptr;
@@ -94,12 +105,13 @@ kvq_status validate(const kvq_config& k) {
   if (k.head_dim % k.group_size || k.residual % k.group_size) return KVQ_ERR_INVALID_ARG;
   if (!(k.softmax_scale > 0.0f) || !std::isfinite(k.softmax_scale)) return KVQ_ERR_INVALID_ARG;
   if (k.rope && (!(k.rope_base > 1.0f) || !std::isfinite(k.rope_base))) return KVQ_ERR_INVALID_ARG;
-  if (k.k_sparse > k.head_dim) return KVQ_ERR_INVALID_ARG;
+  if (k.k_sparse > k.head_dim || k.sink_tokens < 0) return KVQ_ERR_INVALID_ARG;
   // what this build implements
   if (k.head_dim != kvq::kHeadDim) return KVQ_ERR_UNSUPPORTED;
   if (k.group_size != 32 && k.group_size != 64) return KVQ_ERR_UNSUPPORTED;
   if (k.residual % 32 || k.residual > 128) return KVQ_ERR_UNSUPPORTED;
   if (k.k_sparse > 4) return KVQ_ERR_UNSUPPORTED;
+  if (k.sink_tokens > k.residual) return KVQ_ERR_UNSUPPORTED;
   if ((int64_t)k.batch * k.num_q_heads > (int64_t)1 << 30) return KVQ_ERR_UNSUPPORTED;
   if (k.max_tokens >= ((int64_t)1 << 31)) return KVQ_ERR_UNSUPPORTED;
   const int hg = k.num_q_heads / k.num_kv_heads;
@@ -112,8 +124,10 @@ constexpr int32_t kMaxForcedSplits = 16;
 
 // Grid of the decode launch: the resident CTAs (one per SM), or n per unit when forced; never
 // more CTAs than work items.
+int64_t fp16_items(const kvq_cache* c) { return (c->n_s + c->n_r + c->cfg.residual - 1) / c->cfg.residual; }
+
 int64_t decode_grid(const kvq_cache* c) {
-  const int64_t wpu = c->Tq / c->cfg.residual + (c->n_r > 0 ? 1 : 0);
+  const int64_t wpu = c->Tq / c->cfg.residual + fp16_items(c);
   const int64_t total = c->n_units * wpu;
   int64_t g = c->forced_splits > 0 ? c->n_units * c->forced_splits : c->resident;
   if (g > total) g = total;
@@ -212,6 +226,31 @@ cudaError_t flush_window(kvq_cache* c, cudaStream_t s) {
   return e;
 }
 
+// Copy n_tok tokens (from token src_tok0 of a [units][src_tokens][D] pair of buffers) into the sink
+// store at slot n_s.
+cudaError_t copy_to_sink(kvq_cache* c, const void* k, const void* v, int64_t src_tokens, int64_t src_tok0,
+                         int32_t n_tok, cudaStream_t s) {
+  const int D = c->cfg.head_dim;
+  kvq::CopyTokensParams cp{};
+  cp.k_src = static_cast<const uint16_t*>(k);
+  cp.v_src = static_cast<const uint16_t*>(v);
+  cp.src_unit_stride = src_tokens * D;
+  cp.src_tok0 = src_tok0;
+  cp.k_dst = c->sk;
+  cp.v_dst = c->sv;
+  cp.dst_unit_stride = (int64_t)c->cfg.sink_tokens * D;
+  cp.dst_tok0 = c->n_s;
+  cp.n_tok = n_tok;
+  cp.n_units = (int32_t)c->n_units;
+  cp.D = D;
+  const cudaError_t e = kvq::launch_copy_tokens(cp, s);
+  if (e == cudaSuccess) {
+    c->launches++;
+    c->n_s += n_tok;
+  }
+  return e;
+}
+
 // Decode attention over the cache's current state.  k_new/v_new are null, or hold the window's
 // newest token (slot n_r - 1), which the kernel then reads from there and stores into the window.
 kvq_status launch_decode_for(kvq_cache* c, const void* q, void* out, const void* k_new, const void* v_new,
@@ -228,10 +267,15 @@ kvq_status launch_decode_for(kvq_cache* c, const void* q, void* out, const void*
   dp.win_unit_stride = (int64_t)R * c->cfg.head_dim;
   dp.k_new = static_cast<const uint16_t*>(k_new);
   dp.v_new = static_cast<const uint16_t*>(v_new);
+  dp.sk = c->sk;
+  dp.sv = c->sv;
+  dp.sink_unit_stride = (int64_t)c->cfg.sink_tokens * c->cfg.head_dim;
   dp.n_units = c->n_units;
   dp.n_pages = c->Tq / R;
-  dp.work_per_unit = (int32_t)(dp.n_pages + (c->n_r > 0 ? 1 : 0));
+  dp.work_per_unit = (int32_t)(dp.n_pages + fp16_items(c));
   dp.n_r = c->n_r;
+  dp.n_s = c->n_s;
+  dp.n_w = c->n_s + c->n_r;
   dp.max_slots = c->max_slots;
   dp.Hkv = c->cfg.num_kv_heads;
   dp.Hq = c->cfg.num_q_heads;
@@ -327,6 +371,8 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   alloc((void**)&c->pages, (size_t)(c->n_units * c->unit_page_stride));
   alloc((void**)&c->wk, (size_t)(c->n_units * R * D * 2));
   alloc((void**)&c->wv, (size_t)(c->n_units * R * D * 2));
+  alloc((void**)&c->sk, (size_t)(c->n_units * cfg->sink_tokens * D * 2));
+  alloc((void**)&c->sv, (size_t)(c->n_units * cfg->sink_tokens * D * 2));
   alloc((void**)&c->part_ml, (size_t)(heads * c->max_slots * 2 * sizeof(float)));
   alloc((void**)&c->part_acc, (size_t)(heads * c->max_slots * D * sizeof(float)));
   alloc((void**)&c->counters, (size_t)c->n_units * 2 * sizeof(int));  // tickets, then slot counts
@@ -377,6 +423,7 @@ kvq_status kvq_reset(kvq_cache* c) {
   c->T = 0;
   c->Tq = 0;
   c->n_r = 0;
+  c->n_s = 0;
   c->prefilled = false;
   return KVQ_OK;
 }
@@ -414,7 +461,10 @@ kvq_status kvq_prefill_quantize(kvq_cache* c, const void* k, const void* v, int6
   if (!g.ok) return fail_cuda(c);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int R = c->cfg.residual, D = c->cfg.head_dim;
-  const int64_t Tq = quantized_tokens(n_tokens, R);
+  // the first min(n_tokens, S) tokens go to the sink; the window machine takes the rest
+  const int64_t ns = n_tokens < c->cfg.sink_tokens ? n_tokens : c->cfg.sink_tokens;
+  if (ns > 0 && copy_to_sink(c, k, v, n_tokens, 0, (int32_t)ns, s) != cudaSuccess) return fail_cuda(c);
+  const int64_t Tq = quantized_tokens(n_tokens - ns, R);
   const int64_t n_pages = Tq / R;
   // one launch per at most 65535 pages in grid.x
   for (int64_t p0 = 0; p0 < n_pages; p0 += 65535) {
@@ -423,7 +473,7 @@ kvq_status kvq_prefill_quantize(kvq_cache* c, const void* k, const void* v, int6
     qp.k_src = static_cast<const uint16_t*>(k);
     qp.v_src = static_cast<const uint16_t*>(v);
     qp.src_unit_stride = n_tokens * D;
-    qp.src_tok0 = p0 * R;
+    qp.src_tok0 = ns + p0 * R;
     qp.pages = c->pages;
     qp.unit_page_stride = c->unit_page_stride;
     qp.page0 = p0;
@@ -442,19 +492,21 @@ kvq_status kvq_prefill_quantize(kvq_cache* c, const void* k, const void* v, int6
   cp.k_src = static_cast<const uint16_t*>(k);
   cp.v_src = static_cast<const uint16_t*>(v);
   cp.src_unit_stride = n_tokens * D;
-  cp.src_tok0 = Tq;
+  cp.src_tok0 = ns + Tq;
   cp.k_dst = c->wk;
   cp.v_dst = c->wv;
   cp.dst_unit_stride = (int64_t)R * D;
   cp.dst_tok0 = 0;
-  cp.n_tok = (int32_t)(n_tokens - Tq);
+  cp.n_tok = (int32_t)(n_tokens - ns - Tq);
   cp.n_units = (int32_t)c->n_units;
   cp.D = D;
-  if (kvq::launch_copy_tokens(cp, s) != cudaSuccess) return fail_cuda(c);
-  c->launches++;
+  if (cp.n_tok > 0) {
+    if (kvq::launch_copy_tokens(cp, s) != cudaSuccess) return fail_cuda(c);
+    c->launches++;
+  }
   c->T = n_tokens;
   c->Tq = Tq;
-  c->n_r = (int32_t)(n_tokens - Tq);
+  c->n_r = (int32_t)(n_tokens - ns - Tq);
   c->prefilled = true;
   return KVQ_OK;
 }
@@ -468,6 +520,12 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, void* stream) 
   if (!g.ok) return fail_cuda(c);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int R = c->cfg.residual, D = c->cfg.head_dim;
+  if (c->n_s < c->cfg.sink_tokens) {  // the sink still has room
+    if (copy_to_sink(c, k, v, 1, 0, 1, s) != cudaSuccess) return fail_cuda(c);
+    c->T += 1;
+    c->prefilled = true;
+    return KVQ_OK;
+  }
   if (c->n_r == R && flush_window(c, s) != cudaSuccess) return fail_cuda(c);
   kvq::CopyTokensParams cp{};
   cp.k_src = static_cast<const uint16_t*>(k);
@@ -507,6 +565,12 @@ kvq_status kvq_decode_step(kvq_cache* c, const void* k, const void* v, const voi
   DeviceGuard g(c->device);
   if (!g.ok) return fail_cuda(c);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c->n_s < c->cfg.sink_tokens) {  // the token goes to the sink: a copy, then plain decode
+    if (copy_to_sink(c, k, v, 1, 0, 1, s) != cudaSuccess) return fail_cuda(c);
+    c->T += 1;
+    c->prefilled = true;
+    return launch_decode_for(c, q, out, nullptr, nullptr, s);
+  }
   if (c->n_r == c->cfg.residual && flush_window(c, s) != cudaSuccess) return fail_cuda(c);
   // the new token is window slot n_r; the decode launch stores it there as it reads it
   c->n_r += 1;
@@ -537,6 +601,7 @@ kvq_status kvq_unit_sizes(const kvq_cache* c, kvq_unit_view* v) {
   v->sp_idx_bytes = Tq * nsp;
   v->sp_val_bytes = Tq * nsp * 2;
   v->window_bytes = (int64_t)c->n_r * D * 2;
+  v->sink_bytes = (int64_t)c->n_s * D * 2;
   return KVQ_OK;
 }
 
@@ -623,6 +688,14 @@ kvq_status kvq_export_unit(kvq_cache* c, int32_t b, int32_t kvh, kvq_unit_view* 
     if (dst->wk && cudaMemcpy(dst->wk, c->wk + unit * R * D, wbytes, cudaMemcpyDeviceToHost) != cudaSuccess)
       return fail_cuda(c);
     if (dst->wv && cudaMemcpy(dst->wv, c->wv + unit * R * D, wbytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return fail_cuda(c);
+  }
+  const size_t sbytes = (size_t)c->n_s * D * 2;
+  const int64_t S = c->cfg.sink_tokens;
+  if (sbytes) {
+    if (dst->sk && cudaMemcpy(dst->sk, c->sk + unit * S * D, sbytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return fail_cuda(c);
+    if (dst->sv && cudaMemcpy(dst->sv, c->sv + unit * S * D, sbytes, cudaMemcpyDeviceToHost) != cudaSuccess)
       return fail_cuda(c);
   }
   return KVQ_OK;

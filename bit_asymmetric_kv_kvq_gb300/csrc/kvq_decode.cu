@@ -235,9 +235,9 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
   __shared__ int next_sub;
   __shared__ int abort_flag;
 
-  // A unit's items are its window item (when the window holds tokens) followed by its pages.
-  // Page items of this slice are numbered k = 0, 1, ... in list order.  Before item x the list
-  // holds unit(x) * n_pages + max(loc(x) - hw, 0) page items (hw = 1 with a window item), so page
+  // A unit's items are its fp16 items (hw = ceil(n_w / R) of them: the sink rows, then the window
+  // rows) followed by its pages.  Page items of this slice are numbered k = 0, 1, ... in list
+  // order.  Before item x the list holds unit(x) * n_pages + max(loc(x) - hw, 0) page items, so page
   // k of the slice is global page P_begin + k: unit (P_begin + k) / n_pages, page
   // (P_begin + k) % n_pages of that unit.
   const int hw = (int)(wpu - p.n_pages);
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       const uint32_t* vm = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vm);
       const uint8_t* si = pgm + p.lay.off_si;
       const uint16_t* sv = reinterpret_cast<const uint16_t*>(pgm + p.lay.off_sv);
-      const int64_t page_tok0 = (loc - hw) * (int64_t)p.R;
+      const int64_t page_tok0 = p.n_s + (loc - hw) * (int64_t)p.R;
 
       if constexpr (LEAN) {
         using MK = MaskCodes<S::KBITS_FAST>;
@@ -833,30 +833,36 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
         }
       }
     } else {
-      // ---------------- the fp16 window: tokens Tq .. Tq + n_r - 1, read directly.  It is the
-      // unit's first item, so its loads overlap the prefetch of the unit's pages.
+      // ---------------- the fp16 rows, read directly: the n_s sink tokens (positions 0..n_s),
+      // then the n_r window tokens (positions n_s + Tq ..).  They are the unit's first items, so
+      // their loads overlap the prefetch of the unit's pages.
       const int64_t tq = p.n_pages * (int64_t)p.R;
       const uint16_t* wk = p.wk + cur * p.win_unit_stride;
       const uint16_t* wv = p.wv + cur * p.win_unit_stride;
+      const uint16_t* sk = p.sk + cur * p.sink_unit_stride;
+      const uint16_t* sv = p.sv + cur * p.sink_unit_stride;
+      const int f = loc * SPP + stt;  // sub-tile of the unit's fp16 rows
       // the newest token comes from the caller's buffers when the step appends it; the warp
       // that covers it also stores it into its window slot
-      const int newest = p.k_new ? p.n_r - 1 : -1;
-      if (newest >= 32 * stt && newest < 32 * stt + 32) {
+      const int newest = p.k_new ? p.n_w - 1 : -1;
+      if (newest >= 32 * f && newest < 32 * f + 32) {
         const uint16_t* src = lane < 16 ? p.k_new + cur * D : p.v_new + cur * D;
-        uint16_t* dst = const_cast<uint16_t*>(lane < 16 ? wk : wv) + (int64_t)newest * D;
+        uint16_t* dst = const_cast<uint16_t*>(lane < 16 ? wk : wv) + (int64_t)(newest - p.n_s) * D;
         reinterpret_cast<uint4*>(dst)[lane & 15] = __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15));
       }
-      if (32 * stt < p.n_r) {
+      if (32 * f < p.n_w) {
         float sc[TPL][HG];
 #pragma unroll
         for (int j = 0; j < TPL; ++j) {
-          const int tt = stt * 32 + tau + TAU * j;
-          if (tt >= p.n_r) {
+          const int tt = f * 32 + tau + TAU * j;
+          if (tt >= p.n_w) {
 #pragma unroll
             for (int h = 0; h < HG; ++h) sc[j][h] = 0.0f;
             continue;
           }
-          const uint16_t* kr = tt == newest ? p.k_new + cur * D : wk + (int64_t)tt * D;
+          const uint16_t* kr = tt == newest ? p.k_new + cur * D
+                               : tt < p.n_s ? sk + (int64_t)tt * D
+                                            : wk + (int64_t)(tt - p.n_s) * D;
           float a[HG];
 #pragma unroll
           for (int h = 0; h < HG; ++h) a[h] = 0.0f;
@@ -869,7 +875,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
               for (int h = 0; h < HG; ++h) a[h] = fmaf(qs[h][kc_lo + i], xk[i], a[h]);
             }
           } else {
-            const uint32_t tpos = (uint32_t)(tq + tt);
+            const uint32_t tpos = (uint32_t)(tt < p.n_s ? tt : tq + tt);
             float xlo[S::HALF], xhi[S::HALF];
             load_halves<S::HALF>(kr + kc_lo, xlo);
             load_halves<S::HALF>(kr + kc_lo + D / 2, xhi);
@@ -889,22 +895,25 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
         }
 #pragma unroll
         for (int j = 0; j < TPL; ++j) {
-          const int tt = stt * 32 + tau + TAU * j;
+          const int tt = f * 32 + tau + TAU * j;
 #pragma unroll
           for (int h = 0; h < HG; ++h) {
             float a = sc[j][h];
 #pragma unroll
             for (int off = 1; off < KAPPA; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-            sc[j][h] = tt < p.n_r ? a * p.qk_scale_log2 : -INFINITY;
+            sc[j][h] = tt < p.n_w ? a * p.qk_scale_log2 : -INFINITY;
           }
         }
         softmax_update(sc);
 #pragma unroll
         for (int j = 0; j < TPL; ++j) {
-          const int tt = stt * 32 + tau + TAU * j;
-          if (tt >= p.n_r) continue;
+          const int tt = f * 32 + tau + TAU * j;
+          if (tt >= p.n_w) continue;
           float xv[CPL];
-          load_halves<CPL>((tt == newest ? p.v_new + cur * D : wv + (int64_t)tt * D) + vc_lo, xv);
+          const uint16_t* vr = tt == newest ? p.v_new + cur * D
+                               : tt < p.n_s ? sv + (int64_t)tt * D
+                                            : wv + (int64_t)(tt - p.n_s) * D;
+          load_halves<CPL>(vr + vc_lo, xv);
 #pragma unroll
           for (int h = 0; h < HG; ++h) {
             const float pw = sc[j][h];

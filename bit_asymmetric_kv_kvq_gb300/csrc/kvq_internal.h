@@ -104,10 +104,15 @@ struct DecodeParams {
   int64_t win_unit_stride;  // elements
   const uint16_t* k_new;    // null, or [B*Hkv][D] fp16: the window's newest token (slot n_r - 1),
   const uint16_t* v_new;    //   read from here and stored into the window by the decode kernel
+  const uint16_t* sk;       // attention-sink tokens [units][S][D] (null when S = 0)
+  const uint16_t* sv;
+  int64_t sink_unit_stride; // elements (S * D)
   int64_t n_units;          // B * Hkv
   int64_t n_pages;          // quantized pages per unit (Tq / R)
-  int32_t work_per_unit;    // n_pages + (n_r > 0): page items then the window item
+  int32_t work_per_unit;    // ceil(n_w / R) fp16 items, then the n_pages page items
   int32_t n_r;              // window tokens
+  int32_t n_s;              // sink tokens; positions: sink 0..n_s, pages n_s.., window n_s + Tq..
+  int32_t n_w;              // fp16 rows n_s + n_r: the sink rows, then the window rows
   int32_t max_slots;        // partial slots per query head
   int32_t log2_stages;      // page stages per CTA (set by the launcher)
   int32_t Hkv, Hq, D, G, R, nsp;

@@ -127,6 +127,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   dp.n_pages = n_pages;
   dp.work_per_unit = (int32_t)wpu;
   dp.n_r = (int32_t)(n_tokens - tq);
+  dp.n_w = dp.n_r;  // no sink tokens here
   dp.max_slots = (int32_t)slots;
   dp.Hkv = cfg->num_kv_heads;
   dp.Hq = cfg->num_q_heads;

@@ -42,14 +42,15 @@ class kvq_config(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("max_tokens", ctypes.c_int64), ("k_bits", ctypes.c_int32),
                 ("v_bits", ctypes.c_int32), ("group_size", ctypes.c_int32), ("residual", ctypes.c_int32),
                 ("k_sparse", ctypes.c_int32), ("rope", ctypes.c_int32), ("rope_base", ctypes.c_float),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("sink_tokens", ctypes.c_int32)]
 
 
 class kvq_unit_view(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("kcodes", "kz", "ks", "vcodes", "vz", "vs", "sp_idx", "sp_val",
                                                "wk", "wv")] + \
                [(n, ctypes.c_int64) for n in ("kcodes_bytes", "kmeta_bytes", "vcodes_bytes", "vmeta_bytes",
-                                              "sp_idx_bytes", "sp_val_bytes", "window_bytes")]
+                                              "sp_idx_bytes", "sp_val_bytes", "window_bytes")] + \
+               [("sk", ctypes.c_void_p), ("sv", ctypes.c_void_p), ("sink_bytes", ctypes.c_int64)]
 
 
 _P = ctypes.c_void_p
@@ -128,11 +129,11 @@ def _stream(stream, device=None):
 
 
 def make_config(batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits, v_bits, group_size, residual,
-                k_sparse=0, rope=0, rope_base=10000.0, softmax_scale=None) -> kvq_config:
+                k_sparse=0, rope=0, rope_base=10000.0, softmax_scale=None, sink_tokens=0) -> kvq_config:
     if softmax_scale is None:
         softmax_scale = 1.0 / float(head_dim) ** 0.5
     return kvq_config(batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits, v_bits, group_size, residual,
-                      k_sparse, rope, rope_base, softmax_scale)
+                      k_sparse, rope, rope_base, softmax_scale, sink_tokens)
 
 
 # ------------------------------------------------------------------ C-ABI named functions
@@ -204,6 +205,7 @@ def kvq_export_unit(handle, b: int, kvh: int, cfg: kvq_config, stream=None) -> d
     sizes = kvq_unit_view()
     _check(lib().kvq_unit_sizes(handle, ctypes.byref(sizes)), "kvq_unit_sizes")
     t, tq, nr = kvq_get_state(handle)
+    ns = t - tq - nr
     D, G, nsp = cfg.head_dim, cfg.group_size, cfg.k_sparse
     out = dict(
         kcodes=np.zeros((tq, D * cfg.k_bits // 32), np.uint32), kz=np.zeros((tq // G, D), np.uint16),
@@ -211,8 +213,12 @@ def kvq_export_unit(handle, b: int, kvh: int, cfg: kvq_config, stream=None) -> d
         vz=np.zeros((tq, D // G), np.uint16), vs=np.zeros((tq, D // G), np.uint16),
         sp_idx=np.zeros((tq, nsp), np.uint8), sp_val=np.zeros((tq, nsp), np.uint16),
         wk=np.zeros((nr, D), np.uint16), wv=np.zeros((nr, D), np.uint16))
+    sink = dict(sk=np.zeros((ns, D), np.uint16), sv=np.zeros((ns, D), np.uint16))
     assert out["kcodes"].nbytes == sizes.kcodes_bytes and out["wk"].nbytes == sizes.window_bytes
-    view = kvq_unit_view(*[a.ctypes.data if a.size else None for a in out.values()])
+    assert sink["sk"].nbytes == sizes.sink_bytes
+    ptr = lambda a: a.ctypes.data if a.size else None  # noqa: E731
+    view = kvq_unit_view(*[ptr(a) for a in out.values()], *[0] * 7, ptr(sink["sk"]), ptr(sink["sv"]), 0)
+    out.update(sink)
     _check(lib().kvq_export_unit(handle, b, kvh, ctypes.byref(view), _stream(stream)), "kvq_export_unit")
     return out
 
@@ -223,16 +229,17 @@ class KVCache:
     """One layer's quantized KV cache on one GPU (torch tensors in, torch tensors out)."""
 
     def __init__(self, batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits=2, v_bits=2, group_size=32,
-                 residual=128, k_sparse=0, rope=0, rope_base=10000.0, softmax_scale=None, device=0):
+                 residual=128, k_sparse=0, rope=0, rope_base=10000.0, softmax_scale=None, device=0, sink_tokens=0):
         self.cfg = make_config(batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits, v_bits, group_size,
-                               residual, k_sparse, rope, rope_base, softmax_scale)
+                               residual, k_sparse, rope, rope_base, softmax_scale, sink_tokens)
         self.device = device
         self.handle = kvq_create(self.cfg, device)
 
     @classmethod
     def for_workload(cls, w, device=0, max_tokens=None):
         return cls(w.batch, w.kv_heads, w.q_heads, w.head_dim, max_tokens or w.max_tokens, w.k_bits, w.v_bits,
-                   w.group, w.residual, w.k_sparse, w.rope, w.rope_base, w.softmax_scale, device)
+                   w.group, w.residual, w.k_sparse, w.rope, w.rope_base, w.softmax_scale, device,
+                   getattr(w, "sink", 0))
 
     def _need(self, t, shape, name):
         import torch

@@ -79,6 +79,10 @@ typedef struct {
                             position = absolute token index) */
   float rope_base;       /* RoPE base, e.g. 10000 (used when rope = 1) */
   float softmax_scale;   /* scale applied to q.k, e.g. 1/sqrt(D) */
+  int32_t sink_tokens;   /* S, 0..R: the first S tokens of every sequence are kept fp16 (attention sinks)
+                            and never quantized; 0 = no sinks.  unite.ai page and dothoosh.com page,
+                            research-direction sections (InnerQ keeps high-precision windows for the
+                            recent tokens and for the attention-sink tokens). */
 } kvq_config;
 
 typedef struct kvq_cache kvq_cache; /* opaque */
@@ -99,10 +103,12 @@ kvq_status kvq_destroy(kvq_cache* cache);
 /*
  * Prefill: cache the prompt's keys and values, k and v device fp16
  * [B][Hkv][n_tokens][D], 1 <= n_tokens <= max_tokens.  The first
- * Tq = R*floor((n_tokens-1)/R) tokens are quantized into packed pages (keys
- * per channel over G-token groups, values per token over G-channel groups, the
- * sparse outliers first when k_sparse > 0); the last n_tokens - Tq tokens
- * (1..R) are copied into the fp16 window.  Allowed once, on an empty cache
+ * n_s = min(n_tokens, S) tokens are copied into the fp16 sink store (S =
+ * sink_tokens, usually 0); of the T' = n_tokens - n_s tokens after them the
+ * first Tq = R*floor((T'-1)/R) are quantized into packed pages (keys per
+ * channel over G-token groups, values per token over G-channel groups, the
+ * sparse outliers first when k_sparse > 0) and the last T' - Tq (1..R, or 0
+ * when T' = 0) are copied into the fp16 window.  Allowed once, on an empty cache
  * (otherwise KVQ_ERR_STATE).  KIVI summary page, section "Method"; unite.ai
  * page, sections "Keys", "Values", "System tax".
  */
@@ -110,9 +116,10 @@ kvq_status kvq_prefill_quantize(kvq_cache* cache, const void* k_f16, const void*
                                 void* cuda_stream);
 
 /*
- * Append one decode token: k and v device fp16 [B][Hkv][D].  If the window
- * already holds R tokens it is first quantized as one block (the flush), then
- * the new token is stored in the window.  An append on an empty cache acts as
+ * Append one decode token: k and v device fp16 [B][Hkv][D].  While the sink
+ * store holds fewer than S tokens the token goes there.  Otherwise, if the
+ * window already holds R tokens it is first quantized as one block (the
+ * flush), then the new token is stored in the window.  An append on an empty cache acts as
  * a prefill of one token.  KVQ_ERR_CAPACITY when the cache already holds
  * max_tokens tokens.  unite.ai page, section "System tax".
  */
@@ -224,7 +231,7 @@ kvq_status kvq_get_state(const kvq_cache* cache, int64_t* t_total, int64_t* t_qu
  *   vz, vs uint16 [Tq][D/G]          value zero point / scale
  *   sp_idx uint8  [Tq][k_sparse]     sparse key channels, ascending
  *   sp_val uint16 [Tq][k_sparse]     sparse key values (exact fp16)
- *   wk, wv uint16 [n_r][D]           fp16 window (tokens Tq .. Tq+n_r-1)
+ *   wk, wv uint16 [n_r][D]           fp16 window (tokens n_s+Tq .. n_s+Tq+n_r-1)
  */
 typedef struct {
   void* kcodes; void* kz; void* ks;
@@ -232,6 +239,8 @@ typedef struct {
   void* sp_idx; void* sp_val;
   void* wk; void* wv;
   int64_t kcodes_bytes, kmeta_bytes, vcodes_bytes, vmeta_bytes, sp_idx_bytes, sp_val_bytes, window_bytes;
+  void* sk; void* sv;    /* sink tokens uint16 [n_s][D] (fp16 bits), n_s = T - Tq - n_r */
+  int64_t sink_bytes;
 } kvq_unit_view;
 
 /* Fill the *_bytes fields of `sizes` for the current state (pointers untouched). */

@@ -99,6 +99,7 @@ class Workload:
     key_outliers: str      # "per_head4": 4 channels per kv head ~ sign*N(40,5); "layer1pct": 1% of (head, channel) pairs ~ sign*N(50,5)
     queries: str           # "normal": N(0,1); "peaked": biased toward 8 past keys (84% of mass on 5% of tokens)
     seed: int
+    sink: int = 0          # attention-sink tokens kept fp16 (0: none)
 
     @property
     def softmax_scale(self) -> float:

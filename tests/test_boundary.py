@@ -64,6 +64,7 @@ def _status(kvq, **over):
     ("k_sparse", -1, -1), ("rope", 2, -1), ("softmax_scale", 0.0, -1), ("softmax_scale", float("inf"), -1),
     ("head_dim", 64, -2), ("group_size", 16, -2), ("residual", 256, -2), ("k_sparse", 5, -2),
     ("num_q_heads", 32, -2),  # 8 query heads per kv head: not in this build
+    ("sink_tokens", -1, -1), ("sink_tokens", 129, -2),  # more sink tokens than R: not in this build
 ])
 def test_bad_configs_are_rejected_on_the_host(kvq, field, value, expect):
     assert _status(kvq, **{field: value}) == expect
