@@ -234,6 +234,8 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
   __shared__ __align__(16) float qp_s[W][HG][D];  // each warp's q' for its key group
   __shared__ int next_sub;
   __shared__ int abort_flag;
+  // rope: the turn of frequency i over TAU tokens (cos, sin), the step between a lane's tokens
+  __shared__ float2 rope_step[ROPE ? kHeadDim / 2 : 1];
 
   // A unit's items are its fp16 items (hw = ceil(n_w / R) of them: the sink rows, then the window
   // rows) followed by its pages.  Page items of this slice are numbered k = 0, 1, ... in list
@@ -287,6 +289,13 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       stage_page[i] = -1;
     }
     fence_mbar_init();
+  }
+  if constexpr (ROPE) {
+    for (int i = tid; i < D / 2; i += blockDim.x) {
+      float c, s;
+      rope_cs(p.rope_turns[i], (uint32_t)S::TAU, c, s);
+      rope_step[i] = make_float2(c, s);
+    }
   }
   __syncthreads();
   if (tid == 0)
@@ -721,6 +730,12 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
             zh[i] = h2f((uint16_t)(c2 & 0xFFFFu));
             sh[i] = h2f((uint16_t)(c2 >> 16));
           }
+          // cos/sin of the lane's first token, exact from the turn count, then turned by TAU
+          // tokens per step (angle addition; a few fp32 roundings per step)
+          float rc[HF], rs[HF];
+#pragma unroll
+          for (int i = 0; i < HF; ++i)
+            rope_cs(p.rope_turns[kc_lo + i], (uint32_t)(page_tok0 + stt * 32 + tau), rc[i], rs[i]);
 #pragma unroll
           for (int j = 0; j < TPL; ++j) {
             const int tt = stt * 32 + tau + TAU * j;
@@ -743,19 +758,22 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
                 if (c == kc_lo + D / 2 + i) kh[i] = xv;
               }
             }
-            const uint32_t tpos = (uint32_t)(page_tok0 + tt);
             float a[HG];
 #pragma unroll
             for (int h = 0; h < HG; ++h) a[h] = 0.0f;
 #pragma unroll
             for (int i = 0; i < HF; ++i) {
-              float cs, sn;
-              rope_cs(p.rope_turns[kc_lo + i], tpos, cs, sn);
+              const float cs = rc[i], sn = rs[i];
               const float rl = kl[i] * cs - kh[i] * sn;
               const float rh = kh[i] * cs + kl[i] * sn;
 #pragma unroll
               for (int h = 0; h < HG; ++h)
                 a[h] = fmaf(qs[h][kc_lo + i], rl, fmaf(qs[h][kc_lo + D / 2 + i], rh, a[h]));
+              if (j + 1 < TPL) {
+                const float2 st = rope_step[kc_lo + i];
+                rc[i] = cs * st.x - sn * st.y;
+                rs[i] = sn * st.x + cs * st.y;
+              }
             }
 #pragma unroll
             for (int h = 0; h < HG; ++h) sc[j][h] = a[h];
