@@ -60,7 +60,13 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--sink", type=int, default=0, help="attention-sink tokens kept fp16 (0: none)")
     return ap.parse_args(argv)
+
+
+def workload_of(args):
+    w = synth.WORKLOADS[args.workload]
+    return w.scaled(sink=args.sink) if args.sink else w
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -115,10 +121,11 @@ def quantized_tokens(T, R):
 def decode_bytes(w, T):
     """Algorithmic bytes of one decode launch over T cached tokens (all units), plus q and out."""
     D, G = w.head_dim, w.group
-    Tq = quantized_tokens(T, w.residual)
-    n_r = T - Tq
+    n_s = min(T, w.sink)
+    Tq = quantized_tokens(T - n_s, w.residual)
+    n_r = T - n_s - Tq
     per_unit = (Tq * D * (w.k_bits + w.v_bits) // 8 + (Tq // G) * D * 4 + Tq * (D // G) * 4
-                + Tq * w.k_sparse * 3 + n_r * D * 4)
+                + Tq * w.k_sparse * 3 + (n_r + n_s) * D * 4)
     return w.batch * w.kv_heads * per_unit + 2 * w.batch * w.q_heads * D * 2
 
 
@@ -139,6 +146,7 @@ def workload_config(w, layers, graph, world):
         "batch": w.batch, "kv_heads": w.kv_heads, "q_heads": w.q_heads, "head_dim": w.head_dim,
         "prefill_tokens": w.prefill_tokens, "decode_steps": w.decode_steps,
         "k_bits": w.k_bits, "v_bits": w.v_bits, "group": w.group, "residual": w.residual,
+        **({"sink_tokens": w.sink} if w.sink else {}),
         "step": f"{layers} layers x (prefill {w.prefill_tokens}) + {w.decode_steps} x {layers} layers x "
                 f"fused decode step (append + decode attention, one launch)",
         "l2": f"inputs larger than L2: {layers} layer caches of "
@@ -242,7 +250,7 @@ def run_ours(args, dist):
 
     if _build.stale():
         _build.build()
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     L = args.layers
     dev = torch.device(f"cuda:{dist.local_rank}")
     torch.cuda.set_device(dev)
@@ -477,7 +485,7 @@ def run_e2e(args, w, dist, caches, stream):
 # ------------------------------------------------------------------ reference arm: the CPU oracle
 
 def run_reference(args, dist):
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     L = args.layers
     # each step: a bounded sample of the workload through the oracle
     per = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
@@ -520,7 +528,7 @@ def main(argv=None):
             "config": res["config"], "e2e": res["e2e"], "roofline": res["roofline"],
             "decode_only": res["decode_only"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"]}
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(synth.WORKLOADS[args.workload], args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(workload_of(args), args.cpu_seconds)
     if dist.rank == 0:
         print(json.dumps(line))
     dist.close()

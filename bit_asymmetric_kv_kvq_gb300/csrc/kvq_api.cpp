@@ -10,8 +10,10 @@
 //
 // Attention sinks (unite.ai page and dothoosh.com page, research-direction sections: InnerQ keeps
 // the attention-sink tokens in high precision as well as the recent ones): with sink_tokens = S
-// the first n_s = min(T, S) tokens are stored fp16 in a sink store and never quantized; the
-// window/flush machine above runs on the tokens after them, so Tq = R*floor((T-n_s-1)/R).
+// the first n_s = min(T, S) tokens are stored fp16 and never quantized; the window/flush machine
+// above runs on the tokens after them, so Tq = R*floor((T-n_s-1)/R).  Each unit keeps its fp16
+// rows in one buffer of S + R rows: the sink rows 0 .. n_s, then the window rows S .. S + n_r.  The
+// window fills only once the sink is full, so the rows in use are always 0 .. n_s + n_r.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -31,10 +33,8 @@ struct kvq_cache {
   int64_t n_pages_cap = 0;    // pages per unit
   int64_t unit_page_stride = 0;
   uint8_t* pages = nullptr;
-  uint16_t* wk = nullptr;
+  uint16_t* wk = nullptr;     // fp16 rows [units][S + R][D]: sink rows, then window rows
   uint16_t* wv = nullptr;
-  uint16_t* sk = nullptr;     // sink tokens [units][S][D]
-  uint16_t* sv = nullptr;
   float* part_ml = nullptr;
   float* part_acc = nullptr;
   int* counters = nullptr;
@@ -79,8 +79,6 @@ void free_all(kvq_cache* c) {
   cudaFree(c->pages);
   cudaFree(c->wk);
   cudaFree(c->wv);
-  cudaFree(c->sk);
-  cudaFree(c->sv);
   cudaFree(c->part_ml);
   cudaFree(c->part_acc);
   cudaFree(c->counters);
@@ -88,7 +86,6 @@ void free_all(kvq_cache* c) {
   cudaFree(c->rope_turns);
   c->pages = nullptr;
   c->wk = c->wv = nullptr;
-  c->sk = c->sv = nullptr;
   c->part_ml = c->part_acc = nullptr;
   c->err = nullptr;
   c->counters = nullptr;
@@ -124,6 +121,8 @@ constexpr int32_t kMaxForcedSplits = 16;
 
 // Grid of the decode launch: the resident CTAs (one per SM), or n per unit when forced; never
 // more CTAs than work items.
+int64_t rows_per_unit(const kvq_cache* c) { return (int64_t)c->cfg.sink_tokens + c->cfg.residual; }
+
 int64_t fp16_items(const kvq_cache* c) { return (c->n_s + c->n_r + c->cfg.residual - 1) / c->cfg.residual; }
 
 int64_t decode_grid(const kvq_cache* c) {
@@ -202,10 +201,10 @@ PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp, bool rope) 
 cudaError_t flush_window(kvq_cache* c, cudaStream_t s) {
   const int R = c->cfg.residual, D = c->cfg.head_dim;
   kvq::QuantizeParams qp{};
-  qp.k_src = c->wk;
+  qp.k_src = c->wk;  // the window rows follow the sink rows
   qp.v_src = c->wv;
-  qp.src_unit_stride = (int64_t)R * D;
-  qp.src_tok0 = 0;
+  qp.src_unit_stride = rows_per_unit(c) * D;
+  qp.src_tok0 = c->cfg.sink_tokens;
   qp.pages = c->pages;
   qp.unit_page_stride = c->unit_page_stride;
   qp.page0 = c->Tq / R;
@@ -227,7 +226,7 @@ cudaError_t flush_window(kvq_cache* c, cudaStream_t s) {
 }
 
 // Copy n_tok tokens (from token src_tok0 of a [units][src_tokens][D] pair of buffers) into the sink
-// store at slot n_s.
+// rows from row n_s.
 cudaError_t copy_to_sink(kvq_cache* c, const void* k, const void* v, int64_t src_tokens, int64_t src_tok0,
                          int32_t n_tok, cudaStream_t s) {
   const int D = c->cfg.head_dim;
@@ -236,9 +235,9 @@ cudaError_t copy_to_sink(kvq_cache* c, const void* k, const void* v, int64_t src
   cp.v_src = static_cast<const uint16_t*>(v);
   cp.src_unit_stride = src_tokens * D;
   cp.src_tok0 = src_tok0;
-  cp.k_dst = c->sk;
-  cp.v_dst = c->sv;
-  cp.dst_unit_stride = (int64_t)c->cfg.sink_tokens * D;
+  cp.k_dst = c->wk;
+  cp.v_dst = c->wv;
+  cp.dst_unit_stride = rows_per_unit(c) * D;
   cp.dst_tok0 = c->n_s;
   cp.n_tok = n_tok;
   cp.n_units = (int32_t)c->n_units;
@@ -264,12 +263,9 @@ kvq_status launch_decode_for(kvq_cache* c, const void* q, void* out, const void*
   dp.unit_page_stride = c->unit_page_stride;
   dp.wk = c->wk;
   dp.wv = c->wv;
-  dp.win_unit_stride = (int64_t)R * c->cfg.head_dim;
+  dp.win_unit_stride = rows_per_unit(c) * c->cfg.head_dim;
   dp.k_new = static_cast<const uint16_t*>(k_new);
   dp.v_new = static_cast<const uint16_t*>(v_new);
-  dp.sk = c->sk;
-  dp.sv = c->sv;
-  dp.sink_unit_stride = (int64_t)c->cfg.sink_tokens * c->cfg.head_dim;
   dp.n_units = c->n_units;
   dp.n_pages = c->Tq / R;
   dp.work_per_unit = (int32_t)(dp.n_pages + fp16_items(c));
@@ -369,10 +365,8 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
     if (e == cudaSuccess) e = cudaMalloc(p, bytes < 16 ? 16 : bytes);
   };
   alloc((void**)&c->pages, (size_t)(c->n_units * c->unit_page_stride));
-  alloc((void**)&c->wk, (size_t)(c->n_units * R * D * 2));
-  alloc((void**)&c->wv, (size_t)(c->n_units * R * D * 2));
-  alloc((void**)&c->sk, (size_t)(c->n_units * cfg->sink_tokens * D * 2));
-  alloc((void**)&c->sv, (size_t)(c->n_units * cfg->sink_tokens * D * 2));
+  alloc((void**)&c->wk, (size_t)(c->n_units * rows_per_unit(c) * D * 2));
+  alloc((void**)&c->wv, (size_t)(c->n_units * rows_per_unit(c) * D * 2));
   alloc((void**)&c->part_ml, (size_t)(heads * c->max_slots * 2 * sizeof(float)));
   alloc((void**)&c->part_acc, (size_t)(heads * c->max_slots * D * sizeof(float)));
   alloc((void**)&c->counters, (size_t)c->n_units * 2 * sizeof(int));  // tickets, then slot counts
@@ -495,8 +489,8 @@ kvq_status kvq_prefill_quantize(kvq_cache* c, const void* k, const void* v, int6
   cp.src_tok0 = ns + Tq;
   cp.k_dst = c->wk;
   cp.v_dst = c->wv;
-  cp.dst_unit_stride = (int64_t)R * D;
-  cp.dst_tok0 = 0;
+  cp.dst_unit_stride = rows_per_unit(c) * D;
+  cp.dst_tok0 = ns;  // = S whenever window tokens remain
   cp.n_tok = (int32_t)(n_tokens - ns - Tq);
   cp.n_units = (int32_t)c->n_units;
   cp.D = D;
@@ -534,8 +528,8 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, void* stream) 
   cp.src_tok0 = 0;
   cp.k_dst = c->wk;
   cp.v_dst = c->wv;
-  cp.dst_unit_stride = (int64_t)R * D;
-  cp.dst_tok0 = c->n_r;
+  cp.dst_unit_stride = rows_per_unit(c) * D;
+  cp.dst_tok0 = c->n_s + c->n_r;  // the sink is full here: n_s = S
   cp.n_tok = 1;
   cp.n_units = (int32_t)c->n_units;
   cp.D = D;
@@ -683,19 +677,23 @@ kvq_status kvq_export_unit(kvq_cache* c, int32_t b, int32_t kvh, kvq_unit_view* 
       if (dst->sp_val) std::memcpy((uint8_t*)dst->sp_val + p * R * nsp * 2, src + L.off_sv, (size_t)(R * nsp * 2));
     }
   }
+  const int64_t S = c->cfg.sink_tokens;
   const size_t wbytes = (size_t)c->n_r * D * 2;
   if (wbytes) {
-    if (dst->wk && cudaMemcpy(dst->wk, c->wk + unit * R * D, wbytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (dst->wk && cudaMemcpy(dst->wk, c->wk + (unit * rows_per_unit(c) + S) * D, wbytes, cudaMemcpyDeviceToHost) !=
+                       cudaSuccess)
       return fail_cuda(c);
-    if (dst->wv && cudaMemcpy(dst->wv, c->wv + unit * R * D, wbytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (dst->wv && cudaMemcpy(dst->wv, c->wv + (unit * rows_per_unit(c) + S) * D, wbytes, cudaMemcpyDeviceToHost) !=
+                       cudaSuccess)
       return fail_cuda(c);
   }
   const size_t sbytes = (size_t)c->n_s * D * 2;
-  const int64_t S = c->cfg.sink_tokens;
   if (sbytes) {
-    if (dst->sk && cudaMemcpy(dst->sk, c->sk + unit * S * D, sbytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (dst->sk && cudaMemcpy(dst->sk, c->wk + unit * rows_per_unit(c) * D, sbytes, cudaMemcpyDeviceToHost) !=
+                       cudaSuccess)
       return fail_cuda(c);
-    if (dst->sv && cudaMemcpy(dst->sv, c->sv + unit * S * D, sbytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (dst->sv && cudaMemcpy(dst->sv, c->wv + unit * rows_per_unit(c) * D, sbytes, cudaMemcpyDeviceToHost) !=
+                       cudaSuccess)
       return fail_cuda(c);
   }
   return KVQ_OK;

@@ -857,15 +857,13 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       const int64_t tq = p.n_pages * (int64_t)p.R;
       const uint16_t* wk = p.wk + cur * p.win_unit_stride;
       const uint16_t* wv = p.wv + cur * p.win_unit_stride;
-      const uint16_t* sk = p.sk + cur * p.sink_unit_stride;
-      const uint16_t* sv = p.sv + cur * p.sink_unit_stride;
       const int f = loc * SPP + stt;  // sub-tile of the unit's fp16 rows
       // the newest token comes from the caller's buffers when the step appends it; the warp
       // that covers it also stores it into its window slot
       const int newest = p.k_new ? p.n_w - 1 : -1;
       if (newest >= 32 * f && newest < 32 * f + 32) {
         const uint16_t* src = lane < 16 ? p.k_new + cur * D : p.v_new + cur * D;
-        uint16_t* dst = const_cast<uint16_t*>(lane < 16 ? wk : wv) + (int64_t)(newest - p.n_s) * D;
+        uint16_t* dst = const_cast<uint16_t*>(lane < 16 ? wk : wv) + (int64_t)newest * D;
         reinterpret_cast<uint4*>(dst)[lane & 15] = __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15));
       }
       if (32 * f < p.n_w) {
@@ -878,9 +876,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
             for (int h = 0; h < HG; ++h) sc[j][h] = 0.0f;
             continue;
           }
-          const uint16_t* kr = tt == newest ? p.k_new + cur * D
-                               : tt < p.n_s ? sk + (int64_t)tt * D
-                                            : wk + (int64_t)(tt - p.n_s) * D;
+          const uint16_t* kr = tt == newest ? p.k_new + cur * D : wk + (int64_t)tt * D;
           float a[HG];
 #pragma unroll
           for (int h = 0; h < HG; ++h) a[h] = 0.0f;
@@ -928,9 +924,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
           const int tt = f * 32 + tau + TAU * j;
           if (tt >= p.n_w) continue;
           float xv[CPL];
-          const uint16_t* vr = tt == newest ? p.v_new + cur * D
-                               : tt < p.n_s ? sv + (int64_t)tt * D
-                                            : wv + (int64_t)(tt - p.n_s) * D;
+          const uint16_t* vr = tt == newest ? p.v_new + cur * D : wv + (int64_t)tt * D;
           load_halves<CPL>(vr + vc_lo, xv);
 #pragma unroll
           for (int h = 0; h < HG; ++h) {

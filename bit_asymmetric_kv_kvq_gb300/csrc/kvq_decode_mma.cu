@@ -282,28 +282,24 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     finish(unit, done);
   };
 
-  // A sub-tile of the fp16 rows (the n_s sink tokens, then the n_r window tokens; rows
-  // 32*stt ..) as a partial of its own: lane l scores row 32*stt + l, then owns channels
-  // 4l .. 4l+3 of the weighted sum.
+  // A sub-tile of the fp16 rows (the sink tokens, then the window tokens; rows 32*stt ..) as a
+  // partial of its own: lane l scores row 32*stt + l, then owns channels 4l .. 4l+3 of the
+  // weighted sum.
   auto window_subtile = [&](int64_t unit, int stt) {
     const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
     const int64_t bh0 = b * p.Hq + kvh * HG;
     const uint16_t* wk = p.wk + unit * p.win_unit_stride;
     const uint16_t* wv = p.wv + unit * p.win_unit_stride;
-    const uint16_t* sk = p.sk + unit * p.sink_unit_stride;
-    const uint16_t* sv = p.sv + unit * p.sink_unit_stride;
     const int tok = 32 * stt + lane;
     const bool live = tok < p.n_w;
     // the newest token comes from the caller's buffers when the step appends it (stored below)
     const int newest = p.k_new ? p.n_w - 1 : -1;
-    auto krow = [&](int r) { return r < p.n_s ? sk + (int64_t)r * D : wk + (int64_t)(r - p.n_s) * D; };
-    auto vrow_of = [&](int r) { return r < p.n_s ? sv + (int64_t)r * D : wv + (int64_t)(r - p.n_s) * D; };
     float s[HG];
 #pragma unroll
     for (int h = 0; h < HG; ++h) s[h] = 0.0f;
     if (live) {
       const uint4* row =
-          reinterpret_cast<const uint4*>(tok == newest ? p.k_new + unit * D : krow(tok));
+          reinterpret_cast<const uint4*>(tok == newest ? p.k_new + unit * D : wk + (int64_t)tok * D);
 #pragma unroll 4
       for (int v = 0; v < D / 8; ++v) {
         const uint4 w = __ldg(row + v);
@@ -331,7 +327,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
       float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
       for (int j = 0; j < nt; ++j) {
         const float pj = __shfl_sync(kAll, pw, j);
-        const uint16_t* vrow = 32 * stt + j == newest ? p.v_new + unit * D : vrow_of(32 * stt + j);
+        const uint16_t* vrow = 32 * stt + j == newest ? p.v_new + unit * D : wv + (int64_t)(32 * stt + j) * D;
         const uint2 w = __ldg(reinterpret_cast<const uint2*>(vrow + 4 * lane));
         const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
         const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
@@ -349,7 +345,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     if (newest >= 32 * stt && newest < 32 * stt + 32) {
       // store the appended token into its window slot: lanes 0-15 the key row, 16-31 the value row
       const uint16_t* src = lane < 16 ? p.k_new + unit * D : p.v_new + unit * D;
-      uint16_t* dst = const_cast<uint16_t*>(lane < 16 ? wk : wv) + (int64_t)(newest - p.n_s) * D;
+      uint16_t* dst = const_cast<uint16_t*>(lane < 16 ? wk : wv) + (int64_t)newest * D;
       reinterpret_cast<uint4*>(dst)[lane & 15] = __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15));
     }
   };

@@ -99,14 +99,11 @@ struct DecodeParams {
   const uint16_t* q;        // [B][Hq][D] fp16 bits
   const uint8_t* pages;
   int64_t unit_page_stride;
-  const uint16_t* wk;       // window [units][R][D]
-  const uint16_t* wv;
+  const uint16_t* wk;       // fp16 rows [units][S + R][D]: the sink rows, then the window rows
+  const uint16_t* wv;       //   (rows 0 .. n_w are contiguous: the window fills only after the sink)
   int64_t win_unit_stride;  // elements
   const uint16_t* k_new;    // null, or [B*Hkv][D] fp16: the window's newest token (slot n_r - 1),
   const uint16_t* v_new;    //   read from here and stored into the window by the decode kernel
-  const uint16_t* sk;       // attention-sink tokens [units][S][D] (null when S = 0)
-  const uint16_t* sv;
-  int64_t sink_unit_stride; // elements (S * D)
   int64_t n_units;          // B * Hkv
   int64_t n_pages;          // quantized pages per unit (Tq / R)
   int32_t work_per_unit;    // ceil(n_w / R) fp16 items, then the n_pages page items
