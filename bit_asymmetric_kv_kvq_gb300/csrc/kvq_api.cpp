@@ -285,15 +285,14 @@ kvq_status launch_decode_for(kvq_cache* c, const void* q, void* out, const void*
   dp.rope_turns = c->rope_turns;
   dp.part_ml = c->part_ml;
   dp.part_acc = c->part_acc;
-  dp.counters = c->counters;
-  dp.nslot = c->counters + c->n_units;
+  dp.nslot = c->counters;
   dp.out = static_cast<uint16_t*>(out);
   dp.err = c->err;
   bool supported = false;
   if (kvq::launch_decode(dp, c->cfg.k_bits, c->cfg.v_bits, hg, c->cfg.rope != 0, (int)grid, s, &supported) !=
       cudaSuccess)
     return supported ? fail_cuda(c) : KVQ_ERR_UNSUPPORTED;
-  c->launches++;
+  c->launches += 2;  // the decode kernel and the merge of its partials
   return KVQ_OK;
 }
 
@@ -369,11 +368,11 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   alloc((void**)&c->wv, (size_t)(c->n_units * rows_per_unit(c) * D * 2));
   alloc((void**)&c->part_ml, (size_t)(heads * c->max_slots * 2 * sizeof(float)));
   alloc((void**)&c->part_acc, (size_t)(heads * c->max_slots * D * sizeof(float)));
-  alloc((void**)&c->counters, (size_t)c->n_units * 2 * sizeof(int));  // tickets, then slot counts
+  alloc((void**)&c->counters, (size_t)c->n_units * sizeof(int));  // partial slots taken per unit
   alloc((void**)&c->err, sizeof(int));
   alloc((void**)&c->rope_turns, (size_t)(D / 2) * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(c->err, 0, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)c->n_units * 2 * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)c->n_units * sizeof(int));
   if (e == cudaSuccess) {
     std::vector<unsigned long long> turns(D / 2);
     for (int i = 0; i < D / 2; ++i) turns[i] = rope_turn_fraction(cfg->rope ? cfg->rope_base : 10000.0, i, D);

@@ -4,22 +4,22 @@
 // geometry problem, not a bit problem", section "Why the KV cache is a
 // problem"), so the kernel is built around streaming pages at full bandwidth:
 //
-//  * Work list.  Every (batch, kv head) unit contributes, when the fp16
-//    window is not empty, one window item, then n_pages page items.  The items of
+//  * Work list.  Every (batch, kv head) unit contributes its fp16 items (sink
+//    and window rows, when there are any), then n_pages page items.  The items of
 //    all units are laid end to end and the grid (sized to the resident CTA
 //    count) takes equal contiguous slices of that list, so every SM streams
 //    the same number of pages whatever the batch/head/length mix, and a CTA
 //    crosses from one unit into the next without a new launch.
 //  * Streaming.  Pages arrive by one bulk (TMA) copy each into a ring of
-//    shared-memory stages guarded by mbarriers; the four warps of a CTA each
-//    take one 32-token sub-tile of every page and dequantize in registers, and
-//    the last warp to finish with a stage issues the copy that refills it (no
-//    warp is set aside to issue copies).
-//  * Merge.  Each CTA writes one unnormalised partial (m, l, acc[D]) per
-//    query head for every unit it touched; the CTA that completes a unit's
-//    item count (an acquire-release atomic ticket, no waiting) merges the
-//    unit's partials with log-sum-exp weights in one pass and writes the fp16
-//    output.  A unit covered by one CTA is written directly.
+//    shared-memory stages guarded by mbarriers; the warps of a CTA take the
+//    pages' 32-token sub-tiles from a shared counter and dequantize in
+//    registers, and the last warp to finish with a stage issues the copy that
+//    refills it (no warp is set aside to issue copies).
+//  * Merge.  Each warp writes one unnormalised partial (m, l, acc[D]) per
+//    query head for every unit it touched.  A small kernel launched right
+//    after (one warp per unit) combines a unit's partials with log-sum-exp
+//    weights and writes the fp16 output; merging inside the decode launch put
+//    chains of L2 round trips at the end of every CTA's slice.
 //
 // Keys are quantized per channel over G-token groups, so inside a group the
 // score is linear in the codes:
@@ -203,8 +203,8 @@ struct LaneState {
 // shared-memory page stages; its warps take the slice's 32-token sub-tiles one at a time from a
 // shared counter, so a warp that the scheduler serves less often simply takes fewer of them.
 // Every warp keeps its own online-softmax state per unit and, when it leaves a unit, writes one
-// partial (m, l, acc) into the next free slot of that unit; the warp whose ticket completes the
-// unit merges the unit's partials.  There is no CTA-wide barrier after the start.
+// partial (m, l, acc) into the next free slot of that unit; merge_kernel combines them after the
+// launch.  There is no CTA-wide barrier after the start.
 //
 // LEAN: one query head per kv head, 2- or 4-bit K and V, pages of 128 tokens, no sparse
 // entries -- the common case, with a page path that has no per-token branches.
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
     stage_page[st] = k;
   };
   // A warp may have taken a sub-tile of page k while a stage still serves page k - n_stages
-  // (or an older one: warps run ahead of a warp that holds a page while it merges a unit), and a
+  // (or an older one: warps run ahead of a warp that holds a page while it writes a partial), and a
   // parity wait cannot tell phases 2*n_stages pages apart.  So wait until the stage is assigned
   // page k, then for its copy.  Bounded like every wait here.
   auto wait_page = [&](int k) -> bool {
@@ -372,9 +372,9 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
     }
   };
 
-  // This warp leaves `unit` after `done` of its sub-tiles: one partial into the unit's next free
-  // slot, then a ticket; the warp completing the unit merges every slot and writes the output.
-  auto epilogue = [&](int64_t unit, int done) {
+  // This warp leaves `unit`: one partial into the unit's next free slot (the merge kernel that
+  // follows the launch combines the slots).
+  auto epilogue = [&](int64_t unit) {
     constexpr int NOUT = CPL / TAU;  // channels per head a lane holds after the reduction
     static_assert(NOUT == 4, "the partial of a lane is one float4 per head");
     // l and the value zero-point sums over the warp's token slots (lanes of one slot hold copies)
@@ -425,32 +425,9 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
     } else if (lane == 0) {
       report_error(p.err, kDevBadArgument);  // slots are sized for the grid: not reached
     }
-    // __syncwarp orders the lanes' partial stores before lane 0's release; the warp whose ticket
-    // completes the unit acquires every other warp's partials the same way
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      int prev;
-      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(prev) : "l"(p.counters + unit), "r"(done)
-                   : "memory");
-      last = prev + done == (int)(wpu * SPP);
-    }
-    last = __shfl_sync(kFull, last, 0);
-    if (last) {
-      int n = 0;
-      if (lane == 0) n = __ldcg(p.nslot + unit);
-      n = __shfl_sync(kFull, n, 0);
-      if (n > p.max_slots) n = p.max_slots;
-      merge_partials<HG>(p, bh0, n, lane);
-      if (lane == 0) {  // ready for the next call on this stream
-        p.counters[unit] = 0;
-        p.nslot[unit] = 0;
-      }
-    }
   };
 
   int64_t cur = -1, ustart = 0;
-  int done = 0;
   while (true) {
     int s = 0;
     if (lane == 0) s = atomicAdd(&next_sub, 1);
@@ -460,14 +437,12 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
     const int stt = s - sx * SPP;  // sub-tile: tokens 32*stt .. 32*stt+31 of the item
     const int64_t x = w_begin + sx;
     if (cur < 0 || x >= ustart + wpu) {
-      if (cur >= 0) epilogue(cur, done);
+      if (cur >= 0) epilogue(cur);
       cur = x / wpu;
       ustart = cur * wpu;
-      done = 0;
       st.reset();
       load_q(cur);
     }
-    ++done;
     const int loc = (int)(x - ustart);
 
     if (loc >= hw) {
@@ -942,7 +917,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       }
     }
   }
-  if (cur >= 0) epilogue(cur, done);
+  if (cur >= 0) epilogue(cur);
   // never leave with a copy in flight (only possible after an abort): wait, bounded, for the
   // last copy issued into every stage
   __syncthreads();
@@ -1034,10 +1009,29 @@ int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int R, int ns
   return 0;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool rope, int grid, cudaStream_t s,
-                          bool* supported) {
-  *supported = decode_supported(bk, bv, hg, rope);
-  if (!*supported) return cudaErrorInvalidValue;
+namespace {
+
+cudaError_t launch_merge(const DecodeParams& p, int hg, cudaStream_t s) {
+  const unsigned grid = (unsigned)p.n_units;
+  const size_t smem = (size_t)hg * p.max_slots * sizeof(float);  // the slot weights
+  auto run = [&](auto kern, int threads) -> cudaError_t {
+    if (smem > 32 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    kern<<<grid, threads, smem, s>>>(p);
+    return cudaGetLastError();
+  };
+  switch (hg) {
+    case 1: return run(merge_kernel<1>, 1 * kMergeWarpsPerHead * 32);
+    case 2: return run(merge_kernel<2>, 2 * kMergeWarpsPerHead * 32);
+    case 4: return run(merge_kernel<4>, 4 * kMergeWarpsPerHead * 32);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_only(const DecodeParams& p, int bk, int bv, int hg, bool rope, int grid, cudaStream_t s,
+                               bool* supported) {
   if (p.lay.frag) return launch_decode_mma(p, bk, bv, hg, grid, s);
 #define KVQ_DEC(BKV, BVV, HGV, RP) \
   if (bk == BKV && bv == BVV && hg == HGV && rope == RP) return launch_decode_t<BKV, BVV, HGV, RP, false>(p, grid, s);
@@ -1045,6 +1039,17 @@ cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool ro
 #undef KVQ_DEC
   *supported = false;
   return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool rope, int grid, cudaStream_t s,
+                          bool* supported) {
+  *supported = decode_supported(bk, bv, hg, rope);
+  if (!*supported) return cudaErrorInvalidValue;
+  const cudaError_t e = launch_decode_only(p, bk, bv, hg, rope, grid, s, supported);
+  if (e != cudaSuccess) return e;
+  return launch_merge(p, hg, s);
 }
 
 }  // namespace kvq

@@ -23,13 +23,12 @@
 // contiguous slice of the (window, pages) work list through a ring of page
 // stages, its warps take 32-token sub-tiles from a shared counter, keep their
 // own online-softmax state per unit, and leave one partial per unit they
-// touched; the warp completing a unit merges its partials.  A window sub-tile
+// touched; the merge kernel launched after combines them.  A window sub-tile
 // (fp16 tokens not yet quantized) is computed on the CUDA cores as a
 // partial of its own.
 #include <cuda_fp16.h>
 
 #include "kvq_internal.h"
-#include "kvq_merge.cuh"
 #include "kvq_ptx.cuh"
 
 namespace kvq {
@@ -130,7 +129,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     stage_page[st] = k;
   };
   // A warp may have taken a sub-tile of page k while a stage still serves page k - n_stages
-  // (or an older one: warps run ahead of a warp that holds a page while it merges a unit), and a
+  // (or an older one: warps run ahead of a warp that holds a page while it writes a partial), and a
   // parity wait cannot tell phases 2*n_stages pages apart.  So wait until the stage is assigned
   // page k, then for its copy.  Bounded like every wait here.
   auto wait_page = [&](int k) -> bool {
@@ -213,33 +212,9 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     return __shfl_sync(kAll, slot, 0);
   };
 
-  // the ticket; the warp completing the unit merges every partial and writes the output
-  auto finish = [&](int64_t unit, int done) {
-    const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
-    const int64_t bh0 = b * p.Hq + kvh * HG;
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      int prev;
-      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(prev) : "l"(p.counters + unit), "r"(done)
-                   : "memory");
-      last = prev + done == (int)(wpu * SPP);
-    }
-    last = __shfl_sync(kAll, last, 0);
-    if (!last) return;
-    int n = 0;
-    if (lane == 0) n = __ldcg(p.nslot + unit);
-    n = __shfl_sync(kAll, n, 0);
-    if (n > p.max_slots) n = p.max_slots;
-    merge_partials<HG>(p, bh0, n, lane);
-    if (lane == 0) {
-      p.counters[unit] = 0;
-      p.nslot[unit] = 0;
-    }
-  };
-
-  // This warp leaves `unit`: its partial (m, l, acc) per head into a fresh slot, then the ticket.
-  auto epilogue = [&](int64_t unit, int done) {
+  // This warp leaves `unit`: its partial (m, l, acc) per head into a fresh slot (the merge
+  // kernel that follows the launch combines the slots).
+  auto epilogue = [&](int64_t unit) {
     const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
     const int64_t bh0 = b * p.Hq + kvh * HG;
     // column owners' sums over the four lanes of a fragment row (t4)
@@ -279,7 +254,6 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     } else if (lane == 0) {
       report_error(p.err, kDevBadArgument);  // slots are sized for the grid: not reached
     }
-    finish(unit, done);
   };
 
   // A sub-tile of the fp16 rows (the sink tokens, then the window tokens; rows 32*stt ..) as a
@@ -351,7 +325,6 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
   };
 
   int64_t cur = -1, ustart = 0;
-  int done = 0;
   bool touched = false;  // the warp has state (page sub-tiles) for the current unit
   while (true) {
     int s = 0;
@@ -362,18 +335,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     const int stt = s - sx * SPP;
     const int64_t x = w_begin + sx;
     if (cur < 0 || x >= ustart + wpu) {
-      if (cur >= 0) {
-        if (touched) epilogue(cur, done);
-        else finish(cur, done);
-      }
+      if (cur >= 0 && touched) epilogue(cur);
       cur = x / wpu;
       ustart = cur * wpu;
-      done = 0;
       touched = false;
       reset();
       load_q(cur);
     }
-    ++done;
     const int loc = (int)(x - ustart);
     if (loc < hw) {
       const int f = loc * SPP + stt;  // sub-tile of the unit's fp16 rows
@@ -660,10 +628,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
       }
     }
   }
-  if (cur >= 0) {
-    if (touched) epilogue(cur, done);
-    else finish(cur, done);
-  }
+  if (cur >= 0 && touched) epilogue(cur);
   __syncthreads();
   if (tid == 0) {
     for (int i = 0; i < n_stages; ++i)

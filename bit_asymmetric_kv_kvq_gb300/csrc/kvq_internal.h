@@ -119,8 +119,8 @@ struct DecodeParams {
   const unsigned long long* rope_turns;  // [D/2] theta_i / (2*pi) as 0.64 fixed point (rope only)
   float* part_ml;           // [B*Hq][max_slots][2]  (running max in log2 units, sum)
   float* part_acc;          // [B*Hq][max_slots][D]
-  int* counters;            // [B*Hkv] sub-tiles finished per unit, zero between calls
-  int* nslot;               // [B*Hkv] partial slots taken per unit, zero between calls
+  int* nslot;               // [B*Hkv] partial slots taken per unit, zero between calls (the
+                            //   merge kernel clears them)
   uint16_t* out;            // [B][Hq][D] fp16 bits
   int* err;
 };

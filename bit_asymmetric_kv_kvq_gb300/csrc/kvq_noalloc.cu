@@ -141,8 +141,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   dp.rope_turns = rope_turns;
   dp.part_ml = part_ml;
   dp.part_acc = part_acc;
-  dp.counters = counters;
-  dp.nslot = counters + n_units;
+  dp.nslot = counters;
   dp.out = static_cast<uint16_t*>(out_f16);
   dp.err = nullptr;
   bool supported = false;
