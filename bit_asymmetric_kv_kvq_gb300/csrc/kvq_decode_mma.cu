@@ -268,52 +268,79 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     const bool live = tok < p.n_w;
     // the newest token comes from the caller's buffers when the step appends it (stored below)
     const int newest = p.k_new ? p.n_w - 1 : -1;
+    // the slot early, so the atomic's round trip overlaps the row loads
+    int slot = 0;
+    if (lane == 0) slot = atomicAdd(p.nslot + unit, 1);
+    // rows come from DRAM: keep eight 16-byte loads in flight per lane
     float s[HG];
 #pragma unroll
     for (int h = 0; h < HG; ++h) s[h] = 0.0f;
     if (live) {
       const uint4* row =
           reinterpret_cast<const uint4*>(tok == newest ? p.k_new + unit * D : wk + (int64_t)tok * D);
-#pragma unroll 4
-      for (int v = 0; v < D / 8; ++v) {
-        const uint4 w = __ldg(row + v);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ws[i]));
+      for (int v0 = 0; v0 < D / 8; v0 += 8) {
+        uint4 w[8];
 #pragma unroll
-          for (int h = 0; h < HG; ++h) s[h] = fmaf(qs[h][8 * v + 2 * i], f.x, fmaf(qs[h][8 * v + 2 * i + 1], f.y, s[h]));
+        for (int v = 0; v < 8; ++v) w[v] = __ldg(row + v0 + v);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint32_t ws[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ws[i]));
+            const int c = 8 * (v0 + v) + 2 * i;
+#pragma unroll
+            for (int h = 0; h < HG; ++h) s[h] = fmaf(qs[h][c], f.x, fmaf(qs[h][c + 1], f.y, s[h]));
+          }
         }
       }
     }
-    const int slot = slot_of(unit);
     const int nt = min(32, p.n_w - 32 * stt);
+    float m[HG], pw[HG], l[HG], a[HG][4];
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
       const float sc = live ? s[h] * p.qk_scale_log2 : -INFINITY;
-      float m = sc;
+      m[h] = sc;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kAll, m, off));
-      const float pw = live ? exp2f(sc - m) : 0.0f;
-      float l = pw;
+      for (int off = 16; off > 0; off >>= 1) m[h] = fmaxf(m[h], __shfl_xor_sync(kAll, m[h], off));
+      pw[h] = live ? exp2f(sc - m[h]) : 0.0f;
+      l[h] = pw[h];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(kAll, l, off);
-      float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-      for (int j = 0; j < nt; ++j) {
-        const float pj = __shfl_sync(kAll, pw, j);
-        const uint16_t* vrow = 32 * stt + j == newest ? p.v_new + unit * D : wv + (int64_t)(32 * stt + j) * D;
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(vrow + 4 * lane));
-        const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
-        const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
-        a0 = fmaf(pj, x01.x, a0);
-        a1 = fmaf(pj, x01.y, a1);
-        a2 = fmaf(pj, x23.x, a2);
-        a3 = fmaf(pj, x23.y, a3);
+      for (int off = 16; off > 0; off >>= 1) l[h] += __shfl_xor_sync(kAll, l[h], off);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[h][i] = 0.0f;
+    }
+    // values: lane l owns channels 4l .. 4l+3 of every row; eight rows' loads in flight
+    for (int j0 = 0; j0 < nt; j0 += 8) {
+      uint2 w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 32 * stt + j0 + i;
+        const uint16_t* vrow = r == newest ? p.v_new + unit * D : wv + (int64_t)r * D;
+        w[i] = j0 + i < nt ? __ldg(reinterpret_cast<const uint2*>(vrow + 4 * lane)) : make_uint2(0u, 0u);
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&w[i].x));
+        const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&w[i].y));
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          const float pj = __shfl_sync(kAll, pw[h], (j0 + i) & 31);  // 0 past nt: those lanes are not live
+          a[h][0] = fmaf(pj, x01.x, a[h][0]);
+          a[h][1] = fmaf(pj, x01.y, a[h][1]);
+          a[h][2] = fmaf(pj, x23.x, a[h][2]);
+          a[h][3] = fmaf(pj, x23.y, a[h][3]);
+        }
+      }
+    }
+    slot = __shfl_sync(kAll, slot, 0);
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
       if (slot < p.max_slots) {
         const int64_t so = (bh0 + h) * p.max_slots + slot;
-        *reinterpret_cast<float4*>(p.part_acc + so * D + 4 * lane) = make_float4(a0, a1, a2, a3);
-        if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + so * 2) = make_float2(m, l);
+        *reinterpret_cast<float4*>(p.part_acc + so * D + 4 * lane) = make_float4(a[h][0], a[h][1], a[h][2], a[h][3]);
+        if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + so * 2) = make_float2(m[h], l[h]);
       }
     }
     if (newest >= 32 * stt && newest < 32 * stt + 32) {
