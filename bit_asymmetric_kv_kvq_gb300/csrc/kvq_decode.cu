@@ -290,6 +290,8 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
     }
     fence_mbar_init();
   }
+  pdl_allow_next();  // the merge kernel may take SMs as this grid's CTAs leave
+  pdl_wait();        // the cache, the query, the slot counts and the RoPE table come from earlier work
   if constexpr (ROPE) {
     for (int i = tid; i < D / 2; i += blockDim.x) {
       float c, s;
@@ -958,8 +960,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t s) {
   auto kern = decode_kernel<BK, BV, HG, ROPE, LEAN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, Shape<BK, BV, HG, ROPE>::WARPS * 32, smem, s>>>(q);
-  return cudaGetLastError();
+  return launch_pdl(kern, (unsigned)grid, Shape<BK, BV, HG, ROPE>::WARPS * 32, smem, s, q);
 }
 
 template <int BK, int BV, int HG, bool ROPE, bool LEAN>
@@ -1019,8 +1020,7 @@ cudaError_t launch_merge(const DecodeParams& p, int hg, cudaStream_t s) {
       const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
     }
-    kern<<<grid, threads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, (unsigned)threads, smem, s, p);
   };
   switch (hg) {
     case 1: return run(merge_kernel<1>, 1 * kMergeWarpsPerHead * 32);

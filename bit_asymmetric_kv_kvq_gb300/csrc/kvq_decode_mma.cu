@@ -156,6 +156,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     }
     fence_mbar_init();
   }
+  pdl_allow_next();  // the merge kernel may take SMs as this grid's CTAs leave
+  pdl_wait();        // the cache, the query and the slot counts come from earlier kernels
   __syncthreads();
   if (tid == 0)
     for (int k = 0; k < n_pg && k < n_stages; ++k) issue_page(k);
@@ -701,8 +703,7 @@ cudaError_t launch_mma_t(const DecodeParams& p, int grid, cudaStream_t s) {
   auto kern = decode_mma_kernel<BK, BV, HG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kMmaWarps * 32, smem, s>>>(q);
-  return cudaGetLastError();
+  return launch_pdl(kern, (unsigned)grid, kMmaWarps * 32, smem, s, q);
 }
 
 template <int BK, int BV, int HG>

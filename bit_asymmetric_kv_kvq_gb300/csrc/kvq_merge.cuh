@@ -10,6 +10,7 @@
 #include <cuda_fp16.h>
 
 #include "kvq_internal.h"
+#include "kvq_ptx.cuh"
 
 namespace kvq {
 
@@ -31,6 +32,8 @@ __global__ void __launch_bounds__(HG * kMergeWarpsPerHead * 32) merge_kernel(con
   const int64_t unit = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = warp / WH, wh = warp % WH, ht = tid - h * WH * 32;  // head, warp and thread within it
+  pdl_allow_next();
+  pdl_wait();  // the decode launch's partials
   if (tid == 0) n_s = min(p.nslot[unit], p.max_slots);
   __syncthreads();
   const int n = n_s;

@@ -6,6 +6,8 @@
 
 #include <cstdint>
 
+#include <cuda_runtime.h>
+
 namespace kvq {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -113,6 +115,30 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
 
 __device__ __forceinline__ void report_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
+}
+
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start while the kernel
+// before it on the stream finishes (once that one allows it); pdl_wait blocks until the previous
+// kernel has completed and its writes are visible, so everything before it may touch only
+// registers, shared memory and kernel parameters.  For a kernel launched without the attribute
+// (or after one that never allows it) pdl_wait returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... Args>
+cudaError_t launch_pdl(void (*kern)(Args...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                       const Args&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 }  // namespace kvq
