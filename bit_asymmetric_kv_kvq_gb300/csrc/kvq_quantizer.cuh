@@ -1,0 +1,59 @@
+// The uniform asymmetric group quantizer on the GPU, shared by the page kernel (kvq_quant.cu) and
+// the axis-ablation kernels (kvq_ablation.cu).
+//
+// Zero point = group minimum, step = range/(2^B - 1), round to the nearest step ("KV cache has a
+// geometry problem, not a bit problem", section "Quantization error in practice"), in fp32 with
+// every rounding fixed:
+//   range = mx - mn (RN), s32 = range / L (RN, true division),
+//   z = fp16(mn), s = fp16_rn(s32), code = clamp(rint((x - z) / s), 0, L)
+// with z and s the stored fp16 values.  A zero minimum is stored as +0 and a zero range gives
+// s = +0 and codes 0.  The quotient is formed as (x - z) * (1/s) and replaced by the IEEE quotient
+// within 2^-14 of a half-integer, where the two could round differently (kvq_quant.cu explains
+// the bound), so every code equals the one the true division gives.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+namespace kvq {
+namespace {
+
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+__device__ __forceinline__ uint16_t f2h(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+// Per-group quantizer: fp32 zero point and scale as stored (fp16 widened), the
+// reciprocal of the scale, and the two fp16 bit patterns (zero low, scale high).
+struct __align__(16) GroupQ {
+  float zf, sf, inv;
+  uint32_t bits;
+};
+
+// Zero point and scale of a group from its exact min and max.
+__device__ __forceinline__ GroupQ group_params(float mn, float mx, int L) {
+  GroupQ g;
+  mn = __fadd_rn(mn, 0.0f);  // -0 -> +0
+  float range = __fsub_rn(mx, mn);
+  if (!(range > 0.0f)) range = 0.0f;
+  const float s32 = __fdiv_rn(range, (float)L);
+  const uint16_t zb = f2h(mn), sb = f2h(s32);
+  g.zf = h2f(zb);
+  g.sf = h2f(sb);
+  g.inv = g.sf > 0.0f ? __frcp_rn(g.sf) : 0.0f;
+  g.bits = (uint32_t)zb | ((uint32_t)sb << 16);
+  return g;
+}
+
+__device__ __forceinline__ uint32_t quant_code(float x, const GroupQ& g, int L) {
+  if (g.sf == 0.0f) return 0;
+  const float d = __fsub_rn(x, g.zf);
+  float r = __fmul_rn(d, g.inv);
+  const float frac = r - floorf(r);
+  if (fabsf(frac - 0.5f) <= 0x1.0p-14f) r = __fdiv_rn(d, g.sf);  // near a rounding tie: exact quotient
+  float q = rintf(r);
+  q = fminf(fmaxf(q, 0.0f), (float)L);
+  return (uint32_t)q;
+}
+
+}  // namespace
+}  // namespace kvq

@@ -78,7 +78,16 @@ SIGNATURES = {
     "kvq_launch_count": (ctypes.c_int64, [_P]),
     "kvq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kvq_version": (ctypes.c_int32, []),
+    "kvq_axis_quantize": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]),
+    "kvq_axis_dequantize": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_int32, _P, _P]),
+    "kvq_axis_attention": (ctypes.c_int, [_P, _P, ctypes.c_int32, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64,
+                                          ctypes.c_int32, ctypes.c_float, _P, _P, _P]),
 }
+
+KVQ_AXIS_TOKENS = 0    # groups of G tokens of one channel (per-channel scales)
+KVQ_AXIS_CHANNELS = 1  # groups of G channels of one token (per-token scales)
 
 
 def lib():
@@ -221,6 +230,22 @@ def kvq_export_unit(handle, b: int, kvh: int, cfg: kvq_config, stream=None) -> d
     out.update(sink)
     _check(lib().kvq_export_unit(handle, b, kvh, ctypes.byref(view), _stream(stream)), "kvq_export_unit")
     return out
+
+
+def kvq_axis_quantize(x, n_units, n_tokens, head_dim, bits, group_size, axis, codes, zero, scale, stream=None):
+    _check(lib().kvq_axis_quantize(_ptr(x), n_units, n_tokens, head_dim, bits, group_size, axis, _ptr(codes),
+                                   _ptr(zero), _ptr(scale), _stream(stream)), "kvq_axis_quantize")
+
+
+def kvq_axis_dequantize(codes, zero, scale, n_units, n_tokens, head_dim, group_size, axis, out, stream=None):
+    _check(lib().kvq_axis_dequantize(_ptr(codes), _ptr(zero), _ptr(scale), n_units, n_tokens, head_dim, group_size,
+                                     axis, _ptr(out), _stream(stream)), "kvq_axis_dequantize")
+
+
+def kvq_axis_attention(k, v, kv_f32, q, n_units, heads_per_unit, n_tokens, head_dim, softmax_scale, scores, out,
+                       stream=None):
+    _check(lib().kvq_axis_attention(_ptr(k), _ptr(v), kv_f32, _ptr(q), n_units, heads_per_unit, n_tokens, head_dim,
+                                    softmax_scale, _ptr(scores), _ptr(out), _stream(stream)), "kvq_axis_attention")
 
 
 # ------------------------------------------------------------------ owner object

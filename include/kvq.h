@@ -279,6 +279,48 @@ const char* kvq_status_string(kvq_status status);
 /* Library version, (major << 16) | minor. */
 int32_t kvq_version(void);
 
+/* ---------------- axis ablation (analysis beside the cache, not the cache) ----------------
+ *
+ * The comparison at the centre of "KV cache has a geometry problem, not a bit problem"
+ * (sections "Keys" and "Values"; restated on the dothoosh.com page): quantize keys or values
+ * with groups along either axis and measure what that does to attention scores and outputs.
+ * These calls run on device buffers the caller owns; nothing is allocated.  Errors are detected
+ * on the host before any launch (KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED); KVQ_ERR_CUDA if the
+ * launch fails.  All are asynchronous on cuda_stream.
+ */
+#define KVQ_AXIS_TOKENS 0   /* groups of G tokens of one channel ("per-channel"; the cache's keys) */
+#define KVQ_AXIS_CHANNELS 1 /* groups of G channels of one token ("per-token"; the cache's values) */
+
+/*
+ * Quantize x, device fp16 [n_units][n_tokens][head_dim] (8-byte aligned), with the cache's group
+ * quantizer (zero point = group minimum, step = range / (2^bits - 1), round to nearest; unite.ai
+ * page, section "Quantization error in practice") along `axis`.  Outputs, device:
+ * codes_u8 uint8 [n_units][n_tokens][head_dim] (4-byte aligned), one code per byte;
+ * zero_f16 and scale_f16 fp16 bits, [n_units][n_tokens/G][head_dim] for KVQ_AXIS_TOKENS
+ * (n_tokens a multiple of G, n_units <= 65535) or [n_units][n_tokens][head_dim/G] for
+ * KVQ_AXIS_CHANNELS.  bits 2..4; group_size 32 or 64; head_dim 128.
+ */
+kvq_status kvq_axis_quantize(const void* x_f16, int64_t n_units, int64_t n_tokens, int32_t head_dim, int32_t bits,
+                             int32_t group_size, int32_t axis, void* codes_u8, void* zero_f16, void* scale_f16,
+                             void* cuda_stream);
+
+/* z + s*code (one rounding) for the output of kvq_axis_quantize: out_f32 device fp32
+   [n_units][n_tokens][head_dim], 16-byte aligned. */
+kvq_status kvq_axis_dequantize(const void* codes_u8, const void* zero_f16, const void* scale_f16, int64_t n_units,
+                               int64_t n_tokens, int32_t head_dim, int32_t group_size, int32_t axis, void* out_f32,
+                               void* cuda_stream);
+
+/*
+ * Exact decode attention (fp32 arithmetic) of heads_per_unit (1, 2 or 4) query heads per unit:
+ * q_f16 device fp16 [n_units][heads_per_unit][head_dim]; k and v device [n_units][n_tokens][head_dim],
+ * fp32 when kv_f32 = 1 (16-byte aligned), fp16 when kv_f32 = 0 (8-byte aligned).  out_f32 device
+ * fp32 [n_units][heads_per_unit][head_dim] = softmax(softmax_scale * q.K^T) V; scores_f32, if not
+ * NULL, receives softmax_scale * q.k per [n_units][heads_per_unit][n_tokens].
+ */
+kvq_status kvq_axis_attention(const void* k, const void* v, int32_t kv_f32, const void* q_f16, int64_t n_units,
+                              int32_t heads_per_unit, int64_t n_tokens, int32_t head_dim, float softmax_scale,
+                              void* scores_f32, void* out_f32, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

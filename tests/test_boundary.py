@@ -92,3 +92,17 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         b.lib()
+
+
+def test_axis_calls_check_arguments_on_the_host(kvq):
+    L = kvq.lib()
+    p = 256  # any 16-byte aligned non-null address: the checks run before any launch
+    assert L.kvq_axis_quantize(None, 1, 64, 128, 2, 32, 0, p, p, p, None) == -1
+    assert L.kvq_axis_quantize(p, 1, 64, 128, 5, 32, 0, p, p, p, None) == -1   # bits
+    assert L.kvq_axis_quantize(p, 1, 64, 128, 2, 32, 2, p, p, p, None) == -1   # axis
+    assert L.kvq_axis_quantize(p, 1, 65, 128, 2, 32, 0, p, p, p, None) == -1   # tokens not a multiple of G
+    assert L.kvq_axis_quantize(p, 1, 64, 64, 2, 32, 0, p, p, p, None) == -2    # head_dim
+    assert L.kvq_axis_quantize(p, 1, 64, 128, 2, 16, 1, p, p, p, None) == -2   # group
+    assert L.kvq_axis_dequantize(p, p, p, 0, 64, 128, 32, 0, p, None) == -1
+    assert L.kvq_axis_attention(p, p, 1, p, 1, 3, 64, 128, 0.1, None, p, None) == -2  # heads per unit
+    assert L.kvq_axis_attention(p, p, 1, p, 1, 1, 64, 128, 0.0, None, p, None) == -1  # scale
