@@ -24,6 +24,11 @@ finds the window full first quantizes those R tokens, then stores the new
 token, so for T >= 1 tokens the window holds n_r in [1, R] tokens and
 Tq = R*floor((T-1)/R).
 
+Codebooks (KVQuant review, "Proposed method": the nuqX non-uniform datatype,
+here with caller-supplied levels instead of calibrated ones): a cache may map
+codes to non-uniform levels lev[c] (in steps, 0 = lev[0] < ... < lev[L] = L);
+a value then takes the nearest level and dequantizes to z + s*lev[c].
+
 Attention sinks (unite.ai page and dothoosh.com page, sections on research
 directions, on InnerQ): besides the recent window, the first tokens of the
 sequence are kept in fp16 too.  Reading: with S sink tokens, the first
@@ -72,7 +77,7 @@ class _Unit(ctypes.Structure):
                 ("Tq", _I64), ("n_r", _I64),
                 ("kcodes", _P), ("kz", _P), ("ks", _P), ("sp_idx", _P), ("sp_val", _P),
                 ("vcodes", _P), ("vz", _P), ("vs", _P), ("wk", _P), ("wv", _P),
-                ("n_s", _I64), ("sk", _P), ("sv", _P)]
+                ("n_s", _I64), ("sk", _P), ("sv", _P), ("k_lev", _P), ("v_lev", _P)]
 
 
 def lib():
@@ -89,13 +94,13 @@ def lib():
             L.kvqo_float_to_half_n.restype = None
             L.kvqo_float_to_half_n.argtypes = [_P, _I64, _P]
             L.kvqo_quantize_group.restype = None
-            L.kvqo_quantize_group.argtypes = [_P, _I64, _I, _P, _I64, _I, _P, _P, _P, _I64]
+            L.kvqo_quantize_group.argtypes = [_P, _I64, _I, _P, _I64, _I, _P, _P, _P, _I64, _P]
             L.kvqo_sparse_select.restype = None
             L.kvqo_sparse_select.argtypes = [_P, _I, _I, _P, _P]
             L.kvqo_quantize_keys.restype = _I
-            L.kvqo_quantize_keys.argtypes = [_P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P]
+            L.kvqo_quantize_keys.argtypes = [_P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]
             L.kvqo_quantize_values.restype = _I
-            L.kvqo_quantize_values.argtypes = [_P, _I64, _I, _I, _I, _P, _P, _P]
+            L.kvqo_quantize_values.argtypes = [_P, _I64, _I, _I, _I, _P, _P, _P, _P]
             L.kvqo_pack.restype = _I
             L.kvqo_pack.argtypes = [_P, _I64, _I, _P]
             L.kvqo_unpack.restype = _I
@@ -162,15 +167,16 @@ def bits_f64(b) -> np.ndarray:
 
 # ---------------------------------------------------------------- quantizer
 
-def quantize_group(x16, bits: int, excl=None):
-    """One group of fp16 values -> (z_bits, s_bits, codes u8)."""
+def quantize_group(x16, bits: int, excl=None, levels=None):
+    """One group of fp16 values -> (z_bits, s_bits, codes u8); levels: non-uniform levels in steps."""
+    lev = _levels(levels, bits)
     x = f16_bits(x16).ravel().copy()
     n = x.size
     ex = None if excl is None else _c(excl, np.uint8).ravel()
     z = np.zeros(1, np.uint16)
     s = np.zeros(1, np.uint16)
     codes = np.zeros(n, np.uint8)
-    lib().kvqo_quantize_group(_ptr(x), 1, n, _ptr(ex), 1, bits, _ptr(z), _ptr(s), _ptr(codes), 1)
+    lib().kvqo_quantize_group(_ptr(x), 1, n, _ptr(ex), 1, bits, _ptr(z), _ptr(s), _ptr(codes), 1, _ptr(lev))
     return int(z[0]), int(s[0]), codes
 
 
@@ -182,7 +188,16 @@ def sparse_select(x16, nsp: int):
     return idx, val
 
 
-def quantize_keys(K16, G: int, bits: int, nsp: int = 0):
+def _levels(levels, bits):
+    if levels is None:
+        return None
+    lev = np.ascontiguousarray(levels, dtype=np.float32)
+    if lev.shape != (1 << bits,):
+        raise ValueError("need 2^bits levels")
+    return lev
+
+
+def quantize_keys(K16, G: int, bits: int, nsp: int = 0, levels=None):
     """Keys [T][D] fp16 -> codes u8 [T][D], z/s u16 [T/G][D], sp_idx u8 [T][nsp], sp_val u16 [T][nsp]."""
     K = f16_bits(K16)
     T, D = K.shape
@@ -191,20 +206,23 @@ def quantize_keys(K16, G: int, bits: int, nsp: int = 0):
     s = np.zeros((T // G, D), np.uint16)
     si = np.zeros((T, nsp), np.uint8)
     sv = np.zeros((T, nsp), np.uint16)
-    rc = lib().kvqo_quantize_keys(_ptr(K), T, D, G, bits, nsp, _ptr(codes), _ptr(z), _ptr(s), _ptr(si), _ptr(sv))
+    lev = _levels(levels, bits)
+    rc = lib().kvqo_quantize_keys(_ptr(K), T, D, G, bits, nsp, _ptr(codes), _ptr(z), _ptr(s), _ptr(si), _ptr(sv),
+                                  _ptr(lev))
     if rc != 0:
         raise ValueError(f"kvqo_quantize_keys rejected its arguments ({rc})")
     return codes, z, s, si, sv
 
 
-def quantize_values(V16, G: int, bits: int):
+def quantize_values(V16, G: int, bits: int, levels=None):
     """Values [T][D] fp16 -> codes u8 [T][D], z/s u16 [T][D/G]."""
     V = f16_bits(V16)
     T, D = V.shape
     codes = np.zeros((T, D), np.uint8)
     z = np.zeros((T, D // G), np.uint16)
     s = np.zeros((T, D // G), np.uint16)
-    rc = lib().kvqo_quantize_values(_ptr(V), T, D, G, bits, _ptr(codes), _ptr(z), _ptr(s))
+    lev = _levels(levels, bits)
+    rc = lib().kvqo_quantize_values(_ptr(V), T, D, G, bits, _ptr(codes), _ptr(z), _ptr(s), _ptr(lev))
     if rc != 0:
         raise ValueError(f"kvqo_quantize_values rejected its arguments ({rc})")
     return codes, z, s
@@ -266,9 +284,11 @@ def quantized_tokens(T: int, R: int) -> int:
 class OracleUnit:
     """Cache state of one (batch, kv-head) sequence, driven like the library."""
 
-    def __init__(self, head_dim, k_bits, v_bits, group, residual, k_sparse=0, rope=0, rope_base=10000.0, sink=0):
+    def __init__(self, head_dim, k_bits, v_bits, group, residual, k_sparse=0, rope=0, rope_base=10000.0, sink=0,
+                 k_levels=None, v_levels=None):
         self.D, self.bk, self.bv, self.G, self.R = head_dim, k_bits, v_bits, group, residual
         self.nsp, self.rope, self.rope_base, self.S = k_sparse, rope, rope_base, sink
+        self.k_lev, self.v_lev = _levels(k_levels, k_bits), _levels(v_levels, v_bits)
         D = head_dim
         self.kcodes = np.zeros((0, D), np.uint8)
         self.kz = np.zeros((0, D), np.uint16)
@@ -287,7 +307,7 @@ class OracleUnit:
     @classmethod
     def for_workload(cls, w):
         return cls(w.head_dim, w.k_bits, w.v_bits, w.group, w.residual, w.k_sparse, w.rope, w.rope_base,
-                   getattr(w, "sink", 0))
+                   getattr(w, "sink", 0), getattr(w, "k_levels", None), getattr(w, "v_levels", None))
 
     @property
     def Tq(self):
@@ -306,8 +326,8 @@ class OracleUnit:
         return self.n_s + self.Tq + self.n_r
 
     def _quantize_block(self, K16, V16):
-        kc, kz, ks, si, sv = quantize_keys(K16, self.G, self.bk, self.nsp)
-        vc, vz, vs = quantize_values(V16, self.G, self.bv)
+        kc, kz, ks, si, sv = quantize_keys(K16, self.G, self.bk, self.nsp, self.k_lev)
+        vc, vz, vs = quantize_values(V16, self.G, self.bv, self.v_lev)
         self.kcodes = np.concatenate([self.kcodes, kc])
         self.kz = np.concatenate([self.kz, kz])
         self.ks = np.concatenate([self.ks, ks])
@@ -363,7 +383,7 @@ class OracleUnit:
                 _c(self.vz, np.uint16), _c(self.vs, np.uint16), _c(self.wk, np.uint16), _c(self.wv, np.uint16)]
         sink = [_c(self.sk, np.uint16), _c(self.sv, np.uint16)]
         u = _Unit(self.D, self.G, self.nsp, self.rope, float(self.rope_base), self.Tq, self.n_r,
-                  *[_ptr(a) for a in keep], self.n_s, *[_ptr(a) for a in sink])
+                  *[_ptr(a) for a in keep], self.n_s, *[_ptr(a) for a in sink], _ptr(self.k_lev), _ptr(self.v_lev))
         keep += sink
         return u, keep
 

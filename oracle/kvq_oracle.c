@@ -125,9 +125,27 @@ void kvqo_float_to_half_n(const float* f, int64_t n, uint16_t* out) {
  *    to fp32 (reading: codes are taken against the grid the decoder sees),
  *    a true fp32 division and rint rounding half to even.
  */
+/*
+ * Non-uniform levels (the nuqX datatype of the KVQuant review, "Proposed method", whose levels
+ * come from a calibration the page does not give: here the caller's).  Reading: the zero point
+ * and step stay those of steps 1-3; levels[0..L] are positions in steps, increasing from 0 to L;
+ * a value takes the nearest level to y = (x - z) / s (fp32 quotient), found as the number of
+ * decision thresholds t_j = fp32(levels[j] + levels[j+1]) * 0.5 (j < L) that y exceeds, so a value
+ * on a threshold takes the lower level.  levels == NULL is the uniform quantizer of step 4.
+ */
+static uint8_t level_code(float y, const float* levels, int L) {
+  uint8_t c = 0;
+  for (int j = 0; j < L; ++j) {
+    volatile float sum = levels[j] + levels[j + 1];
+    volatile float t = sum * 0.5f;
+    if (y > t) ++c;
+  }
+  return c;
+}
+
 void kvqo_quantize_group(const uint16_t* x, int64_t stride, int n, const uint8_t* excl,
                          int64_t excl_stride, int bits, uint16_t* z_out, uint16_t* s_out,
-                         uint8_t* codes, int64_t code_stride) {
+                         uint8_t* codes, int64_t code_stride, const float* levels) {
   const int L = (1 << bits) - 1;
   int any = 0;
   float mn = 0.0f, mx = 0.0f;
@@ -159,10 +177,14 @@ void kvqo_quantize_group(const uint16_t* x, int64_t stride, int n, const uint8_t
       float v = kvqo_half_to_float(x[i * stride]);
       volatile float d = v - zf;
       volatile float r = d / sf;
-      float q = rintf(r);
-      if (q < 0.0f) q = 0.0f;
-      if (q > (float)L) q = (float)L;
-      code = (uint8_t)q;
+      if (levels) {
+        code = level_code(r, levels, L);
+      } else {
+        float q = rintf(r);
+        if (q < 0.0f) q = 0.0f;
+        if (q > (float)L) q = (float)L;
+        code = (uint8_t)q;
+      }
     }
     codes[i * code_stride] = code;
   }
@@ -222,7 +244,8 @@ void kvqo_sparse_select(const uint16_t* x, int D, int nsp, uint8_t* idx, uint16_
  * entries of each token are chosen first and excluded from every group.
  */
 int kvqo_quantize_keys(const uint16_t* K, int64_t Tq, int D, int G, int bits, int nsp,
-                       uint8_t* codes, uint16_t* z, uint16_t* s, uint8_t* sp_idx, uint16_t* sp_val) {
+                       uint8_t* codes, uint16_t* z, uint16_t* s, uint8_t* sp_idx, uint16_t* sp_val,
+                       const float* levels) {
   if (Tq < 0 || G <= 0 || Tq % G || D <= 0 || D > 1024 || nsp < 0 || nsp > 64 || bits < 1 || bits > 8)
     return -1;
   uint8_t* excl = 0;
@@ -238,7 +261,7 @@ int kvqo_quantize_keys(const uint16_t* K, int64_t Tq, int D, int G, int bits, in
     for (int c = 0; c < D; ++c) {
       const int64_t off = g * G * D + c;
       kvqo_quantize_group(K + off, D, G, excl ? excl + off : 0, D, bits, z + g * D + c, s + g * D + c,
-                          codes + off, D);
+                          codes + off, D, levels);
     }
   }
   free(excl);
@@ -250,13 +273,13 @@ int kvqo_quantize_keys(const uint16_t* K, int64_t Tq, int D, int G, int bits, in
  * G channels, one (z, s): z[t*(D/G) + j].  codes[t*D + c] unpacked.
  */
 int kvqo_quantize_values(const uint16_t* V, int64_t Tq, int D, int G, int bits, uint8_t* codes,
-                         uint16_t* z, uint16_t* s) {
+                         uint16_t* z, uint16_t* s, const float* levels) {
   if (Tq < 0 || G <= 0 || D % G || bits < 1 || bits > 8) return -1;
   const int ng = D / G;
   for (int64_t t = 0; t < Tq; ++t)
     for (int j = 0; j < ng; ++j)
       kvqo_quantize_group(V + t * D + j * G, 1, G, 0, 0, bits, z + t * ng + j, s + t * ng + j,
-                          codes + t * D + j * G, 1);
+                          codes + t * D + j * G, 1, levels);
   return 0;
 }
 
@@ -338,6 +361,8 @@ typedef struct {
   int64_t n_s;            /* attention-sink tokens kept fp16 (tokens 0 .. n_s) */
   const uint16_t* sk;     /* [n_s][D] */
   const uint16_t* sv;
+  const float* k_lev;     /* non-uniform levels of the key / value codes, or NULL (uniform) */
+  const float* v_lev;
 } kvqo_unit;
 
 /* Token order: the n_s sink tokens, then the Tq quantized tokens, then the
@@ -360,7 +385,8 @@ static void key_of(const kvqo_unit* u, int64_t t, double* k) {
     const int64_t g = t / u->G;
     for (int c = 0; c < D; ++c)
       k[c] = kvqo_half_to_double(u->kz[g * D + c]) +
-             kvqo_half_to_double(u->ks[g * D + c]) * (double)u->kcodes[t * D + c];
+             kvqo_half_to_double(u->ks[g * D + c]) *
+                 (u->k_lev ? (double)u->k_lev[u->kcodes[t * D + c]] : (double)u->kcodes[t * D + c]);
     for (int j = 0; j < u->nsp; ++j) k[u->sp_idx[t * u->nsp + j]] = kvqo_half_to_double(u->sp_val[t * u->nsp + j]);
   } else {
     for (int c = 0; c < D; ++c) k[c] = kvqo_half_to_double(u->wk[(t - u->Tq) * D + c]);
@@ -378,7 +404,9 @@ static void value_of(const kvqo_unit* u, int64_t t, double* v) {
   if (t < u->Tq) {
     for (int c = 0; c < D; ++c) {
       const int j = c / u->G;
-      v[c] = kvqo_half_to_double(u->vz[t * ng + j]) + kvqo_half_to_double(u->vs[t * ng + j]) * (double)u->vcodes[t * D + c];
+      v[c] = kvqo_half_to_double(u->vz[t * ng + j]) +
+             kvqo_half_to_double(u->vs[t * ng + j]) *
+                 (u->v_lev ? (double)u->v_lev[u->vcodes[t * D + c]] : (double)u->vcodes[t * D + c]);
     }
   } else {
     for (int c = 0; c < D; ++c) v[c] = kvqo_half_to_double(u->wv[(t - u->Tq) * D + c]);
