@@ -26,6 +26,7 @@ tests check against) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -61,12 +62,27 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--sink", type=int, default=0, help="attention-sink tokens kept fp16 (0: none)")
+    ap.add_argument("--codebook", action="store_true",
+                    help="non-uniform levels (cosine-spaced, denser at the group's ends) for keys and values")
     return ap.parse_args(argv)
+
+
+def codebook_levels(bits):
+    """Cosine-spaced levels in steps: 0 and L kept, denser near both ends of the group's range."""
+    L = (1 << bits) - 1
+    lev = (L * (0.5 - 0.5 * np.cos(np.pi * np.arange(L + 1) / L))).astype(np.float32)
+    lev[0], lev[-1] = 0.0, float(L)
+    return lev
 
 
 def workload_of(args):
     w = synth.WORKLOADS[args.workload]
-    return w.scaled(sink=args.sink) if args.sink else w
+    if args.sink:
+        w = w.scaled(sink=args.sink)
+    if args.codebook:
+        w = dataclasses.replace(w, k_levels=tuple(codebook_levels(w.k_bits).tolist()),
+                                v_levels=tuple(codebook_levels(w.v_bits).tolist()))
+    return w
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -147,6 +163,7 @@ def workload_config(w, layers, graph, world):
         "prefill_tokens": w.prefill_tokens, "decode_steps": w.decode_steps,
         "k_bits": w.k_bits, "v_bits": w.v_bits, "group": w.group, "residual": w.residual,
         **({"sink_tokens": w.sink} if w.sink else {}),
+        **({"codebook": "cosine-spaced levels (non-uniform)"} if w.k_levels else {}),
         "step": f"{layers} layers x (prefill {w.prefill_tokens}) + {w.decode_steps} x {layers} layers x "
                 f"fused decode step (append + decode attention, one launch)",
         "l2": f"inputs larger than L2: {layers} layer caches of "

@@ -19,7 +19,8 @@ LIBDIR = os.path.join(PKG, "_lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "libkvq.so")
 
-SOURCES = ["kvq_api.cpp", "kvq_quant.cu", "kvq_decode.cu", "kvq_decode_mma.cu", "kvq_noalloc.cu", "kvq_ablation.cu"]
+SOURCES = ["kvq_api.cpp", "kvq_quant.cu", "kvq_decode.cu", "kvq_decode_lut.cu", "kvq_decode_mma.cu", "kvq_noalloc.cu",
+           "kvq_ablation.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -47,6 +47,9 @@ struct kvq_cache {
   int64_t T = 0, Tq = 0;
   int32_t n_r = 0;
   int32_t n_s = 0;            // sink tokens held (<= S)
+  bool lut_set = false;       // codebook caches: kvq_set_codebooks has run
+  float k_lev[16] = {}, v_lev[16] = {};  // codebook levels (in steps) and the decision thresholds
+  float k_thr[16] = {}, v_thr[16] = {};  //   between consecutive levels
   bool prefilled = false;
   bool broken = false;
   int64_t launches = 0;
@@ -103,6 +106,7 @@ kvq_status validate(const kvq_config& k) {
   if (!(k.softmax_scale > 0.0f) || !std::isfinite(k.softmax_scale)) return KVQ_ERR_INVALID_ARG;
   if (k.rope && (!(k.rope_base > 1.0f) || !std::isfinite(k.rope_base))) return KVQ_ERR_INVALID_ARG;
   if (k.k_sparse > k.head_dim || k.sink_tokens < 0) return KVQ_ERR_INVALID_ARG;
+  if (k.codebook != 0 && k.codebook != 1) return KVQ_ERR_INVALID_ARG;
   // what this build implements
   if (k.head_dim != kvq::kHeadDim) return KVQ_ERR_UNSUPPORTED;
   if (k.group_size != 32 && k.group_size != 64) return KVQ_ERR_UNSUPPORTED;
@@ -112,7 +116,7 @@ kvq_status validate(const kvq_config& k) {
   if ((int64_t)k.batch * k.num_q_heads > (int64_t)1 << 30) return KVQ_ERR_UNSUPPORTED;
   if (k.max_tokens >= ((int64_t)1 << 31)) return KVQ_ERR_UNSUPPORTED;
   const int hg = k.num_q_heads / k.num_kv_heads;
-  if (!kvq::decode_supported(k.k_bits, k.v_bits, hg, k.rope != 0)) return KVQ_ERR_UNSUPPORTED;
+  if (!kvq::decode_supported(k.k_bits, k.v_bits, hg, k.rope != 0, k.codebook != 0)) return KVQ_ERR_UNSUPPORTED;
   if (!kvq::quantize_supported(k.k_bits, k.v_bits)) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
@@ -181,10 +185,10 @@ void rope_table(double base, int D, unsigned long long* out) {
   for (int i = 0; i < D / 2; ++i) out[i] = rope_turn_fraction(base, i, D);
 }
 
-PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp, bool rope) {
+PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp, bool rope, bool codebook) {
   auto r16 = [](int64_t x) { return (int32_t)((x + 15) / 16 * 16); };
   PageLayout l{};
-  l.frag = (bk == 2 || bk == 4) && (bv == 2 || bv == 4) && !rope ? 1 : 0;
+  l.frag = (bk == 2 || bk == 4) && (bv == 2 || bv == 4) && !rope && !codebook ? 1 : 0;
   l.off_kc = 0;
   l.off_km = l.off_kc + r16((int64_t)R * D * bk / 8);
   l.off_vc = l.off_km + r16((int64_t)(R / G) * D * 4);
@@ -196,6 +200,14 @@ PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp, bool rope) 
 }
 
 }  // namespace kvq
+
+// Codebook caches quantize with the decision thresholds between their levels.
+void set_codebook(const kvq_cache* c, kvq::QuantizeParams* qp) {
+  if (!c->cfg.codebook) return;
+  qp->lut = 1;
+  std::memcpy(qp->k_thr, c->k_thr, sizeof(qp->k_thr));
+  std::memcpy(qp->v_thr, c->v_thr, sizeof(qp->v_thr));
+}
 
 // The full window of every unit becomes page Tq/R (the flush of an append that finds n_r = R).
 cudaError_t flush_window(kvq_cache* c, cudaStream_t s) {
@@ -216,6 +228,7 @@ cudaError_t flush_window(kvq_cache* c, cudaStream_t s) {
   qp.nsp = c->cfg.k_sparse;
   qp.lay = c->lay;
   qp.err = c->err;
+  set_codebook(c, &qp);
   const cudaError_t e = kvq::launch_quantize(qp, c->cfg.k_bits, c->cfg.v_bits, 1, s);
   if (e == cudaSuccess) {
     c->launches++;
@@ -288,6 +301,11 @@ kvq_status launch_decode_for(kvq_cache* c, const void* q, void* out, const void*
   dp.nslot = c->counters;
   dp.out = static_cast<uint16_t*>(out);
   dp.err = c->err;
+  if (c->cfg.codebook) {
+    dp.lut = 1;
+    std::memcpy(dp.k_lev, c->k_lev, sizeof(dp.k_lev));
+    std::memcpy(dp.v_lev, c->v_lev, sizeof(dp.v_lev));
+  }
   bool supported = false;
   if (kvq::launch_decode(dp, c->cfg.k_bits, c->cfg.v_bits, hg, c->cfg.rope != 0, (int)grid, s, &supported) !=
       cudaSuccess)
@@ -337,7 +355,7 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   }
   c->sm_count = prop.multiProcessorCount;
   const int D = cfg->head_dim, R = cfg->residual, G = cfg->group_size;
-  c->lay = kvq::make_layout(R, D, G, cfg->k_bits, cfg->v_bits, cfg->k_sparse, cfg->rope != 0);
+  c->lay = kvq::make_layout(R, D, G, cfg->k_bits, cfg->v_bits, cfg->k_sparse, cfg->rope != 0, cfg->codebook != 0);
   if (kvq::quantize_smem_bytes(R, D, G, c->lay) > (size_t)prop.sharedMemPerBlockOptin) {
     delete c;
     return KVQ_ERR_UNSUPPORTED;
@@ -348,7 +366,7 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   const int hg = cfg->num_q_heads / cfg->num_kv_heads;
   int warps = 0;
   const int per_sm = kvq::decode_resident_ctas_per_sm(cfg->k_bits, cfg->v_bits, hg, cfg->rope != 0, cfg->residual,
-                                                     cfg->k_sparse, c->lay.bytes, &warps);
+                                                     cfg->k_sparse, c->lay.bytes, &warps, cfg->codebook != 0);
   if (per_sm < 1) {
     cudaGetLastError();
     delete c;
@@ -421,6 +439,36 @@ kvq_status kvq_reset(kvq_cache* c) {
   return KVQ_OK;
 }
 
+kvq_status kvq_set_codebooks(kvq_cache* c, const float* k_levels, const float* v_levels) {
+  if (!c || !k_levels || !v_levels) return KVQ_ERR_INVALID_ARG;
+  if (!c->cfg.codebook) return KVQ_ERR_INVALID_ARG;
+  if (c->prefilled || c->T != 0) return KVQ_ERR_STATE;
+  auto check = [](const float* lev, int bits) {
+    const int L = (1 << bits) - 1;
+    if (lev[0] != 0.0f || lev[L] != (float)L) return false;
+    for (int j = 0; j < L; ++j)
+      if (!(lev[j + 1] > lev[j]) || !std::isfinite(lev[j + 1])) return false;
+    return true;
+  };
+  if (!check(k_levels, c->cfg.k_bits) || !check(v_levels, c->cfg.v_bits)) return KVQ_ERR_INVALID_ARG;
+  auto store = [](const float* lev, int bits, float* dst_lev, float* dst_thr) {
+    const int L = (1 << bits) - 1;
+    for (int j = 0; j < 16; ++j) dst_lev[j] = j <= L ? lev[j] : 0.0f;
+    for (int j = 0; j < 16; ++j) {
+      if (j < L) {
+        volatile float sum = lev[j] + lev[j + 1];  // one rounding, then an exact halving
+        dst_thr[j] = sum * 0.5f;
+      } else {
+        dst_thr[j] = 0.0f;
+      }
+    }
+  };
+  store(k_levels, c->cfg.k_bits, c->k_lev, c->k_thr);
+  store(v_levels, c->cfg.v_bits, c->v_lev, c->v_thr);
+  c->lut_set = true;
+  return KVQ_OK;
+}
+
 kvq_status kvq_set_splits(kvq_cache* c, int32_t splits) {
   if (!c || splits < 0) return KVQ_ERR_INVALID_ARG;
   const int32_t n = splits > kMaxForcedSplits ? kMaxForcedSplits : splits;
@@ -448,7 +496,7 @@ kvq_status kvq_prefill_quantize(kvq_cache* c, const void* k, const void* v, int6
   if (c->broken) return KVQ_ERR_CUDA;
   if (!aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
   if (n_tokens < 1) return KVQ_ERR_INVALID_ARG;
-  if (c->prefilled || c->T != 0) return KVQ_ERR_STATE;
+  if (c->prefilled || c->T != 0 || (c->cfg.codebook && !c->lut_set)) return KVQ_ERR_STATE;
   if (n_tokens > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
   DeviceGuard g(c->device);
   if (!g.ok) return fail_cuda(c);
@@ -478,6 +526,7 @@ kvq_status kvq_prefill_quantize(kvq_cache* c, const void* k, const void* v, int6
     qp.nsp = c->cfg.k_sparse;
     qp.lay = c->lay;
     qp.err = c->err;
+    set_codebook(c, &qp);
     if (kvq::launch_quantize(qp, c->cfg.k_bits, c->cfg.v_bits, (int)np, s) != cudaSuccess) return fail_cuda(c);
     c->launches++;
   }
@@ -508,6 +557,7 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, void* stream) 
   if (!c || !k || !v) return KVQ_ERR_INVALID_ARG;
   if (c->broken) return KVQ_ERR_CUDA;
   if (!aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
+  if (c->cfg.codebook && !c->lut_set) return KVQ_ERR_STATE;
   if (c->T + 1 > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
   DeviceGuard g(c->device);
   if (!g.ok) return fail_cuda(c);
@@ -554,6 +604,7 @@ kvq_status kvq_decode_step(kvq_cache* c, const void* k, const void* v, const voi
   if (!c || !k || !v || !q || !out) return KVQ_ERR_INVALID_ARG;
   if (c->broken) return KVQ_ERR_CUDA;
   if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
+  if (c->cfg.codebook && !c->lut_set) return KVQ_ERR_STATE;
   if (c->T + 1 > c->cfg.max_tokens) return KVQ_ERR_CAPACITY;
   DeviceGuard g(c->device);
   if (!g.ok) return fail_cuda(c);

@@ -31,7 +31,7 @@ struct PageLayout {
 
 // Fragment order is used when both code widths are 2 or 4 bits and keys are stored after
 // RoPE (no rotation at decode); otherwise codes are token-major bitstreams.
-PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp, bool rope);
+PageLayout make_layout(int R, int D, int G, int bk, int bv, int nsp, bool rope, bool codebook = false);
 
 // Fragment order of the codes of a page (D = 128, B = 2 or 4 bits).  Both sections are cut
 // into 16-token tiles; in each tile every lane l = 4g + t (g = l / 4, t = l % 4) of a warp
@@ -81,6 +81,9 @@ struct QuantizeParams {
   int32_t n_units, Hkv, D, G, R, nsp;
   PageLayout lay;
   int* err;
+  int32_t lut;               // 1: codes are codebook indices chosen by the thresholds below
+  float k_thr[16];           // decision thresholds between consecutive key / value levels
+  float v_thr[16];
 };
 
 struct CopyTokensParams {
@@ -123,6 +126,9 @@ struct DecodeParams {
                             //   merge kernel clears them)
   uint16_t* out;            // [B][Hq][D] fp16 bits
   int* err;
+  int32_t lut;              // 1: codebook cache (the CUDA-core kernel with level lookups)
+  float k_lev[16];          // codebook caches: the level (in steps) of each key / value code
+  float v_lev[16];
 };
 
 // Launchers (return cudaGetLastError() after the launch).
@@ -132,12 +138,17 @@ cudaError_t launch_decode(const DecodeParams& p, int bk, int bv, int hg, bool ro
                           bool* supported);
 // Decode CTAs resident per SM (0: unsupported), and in *warps the warps of one CTA: the partial
 // slots a unit needs are warps * (CTAs whose slices meet the unit).
-int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int R, int nsp, int page_bytes, int* warps);
+int decode_resident_ctas_per_sm(int bk, int bv, int hg, bool rope, int R, int nsp, int page_bytes, int* warps,
+                                bool codebook = false);
 // Tensor-core decode over fragment-ordered pages (2/4-bit codes, keys without RoPE).
 bool decode_mma_supported(int bk, int bv, int hg);
 int decode_mma_resident(int bk, int bv, int hg, int page_bytes, int* warps);
 cudaError_t launch_decode_mma(const DecodeParams& p, int bk, int bv, int hg, int grid, cudaStream_t s);
-bool decode_supported(int bk, int bv, int hg, bool rope);
+// CUDA-core decode of codebook caches (kvq_decode_lut.cu).
+bool decode_lut_supported(int bk, int bv, int hg, bool rope);
+int decode_lut_resident(int bk, int bv, int hg, bool rope, int page_bytes, int* warps);
+cudaError_t launch_decode_lut(const DecodeParams& p, int bk, int bv, int hg, bool rope, int grid, cudaStream_t s);
+bool decode_supported(int bk, int bv, int hg, bool rope, bool codebook = false);
 bool quantize_supported(int bk, int bv);
 size_t quantize_smem_bytes(int R, int D, int G, const PageLayout& lay);
 

@@ -53,6 +53,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   const kvq_status st = kvq::check_config(*cfg);
   if (st != KVQ_OK) return st;
   if (n_tokens < 1 || n_tokens > cfg->max_tokens || pages_per_unit < 0) return KVQ_ERR_INVALID_ARG;
+  if (cfg->sink_tokens != 0 || cfg->codebook != 0) return KVQ_ERR_UNSUPPORTED;  // the buffers hold neither
   if (!aligned16(pages) || !aligned16(window_k) || !aligned16(window_v) || !aligned16(q_f16) || !aligned16(out_f16))
     return KVQ_ERR_INVALID_ARG;
   const int D = cfg->head_dim, R = cfg->residual, G = cfg->group_size;

@@ -70,7 +70,8 @@ __device__ __forceinline__ int kq_slot(int c) { return (c % kChunk) * (kHeadDim 
 // packed into BITS words of the token's bitstream.  grp(i) is the quantizer of channel
 // i of the chunk; excl has bit i set for an excluded channel (code 0).
 template <int BITS, class Params>
-__device__ __forceinline__ void pack_chunk(const uint16_t* x, const Params& grp, uint32_t excl, uint32_t* out) {
+__device__ __forceinline__ void pack_chunk(const uint16_t* x, const Params& grp, uint32_t excl, uint32_t* out,
+                                           const float* thr) {
   constexpr int L = (1 << BITS) - 1;
   uint32_t w[BITS];
 #pragma unroll
@@ -84,7 +85,7 @@ __device__ __forceinline__ void pack_chunk(const uint16_t* x, const Params& grp,
     for (int j = 0; j < 8; ++j) {
       const int i = q4 * 8 + j;
       const uint16_t bits = (uint16_t)(j & 1 ? pair[j >> 1] >> 16 : pair[j >> 1] & 0xFFFFu);
-      const uint32_t code = (excl >> i) & 1u ? 0u : quant_code(h2f(bits), grp(i), L);
+      const uint32_t code = (excl >> i) & 1u ? 0u : code_of(h2f(bits), grp(i), L, thr);
       const int b = i * BITS;
       w[b >> 5] |= code << (b & 31);
       if ((b & 31) + BITS > 32) w[(b >> 5) + 1] |= code >> (32 - (b & 31));
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
   uint8_t* sidx = smem + sm.sidx;                            // [R][kMaxSparse]
   uint8_t* pg = smem + sm.pg;                                // page image
   __shared__ __align__(8) uint64_t bar;
+  __shared__ float thr_s[2][16];  // codebook decision thresholds (keys, values)
 
   const int64_t tok0 = p.src_tok0 + (int64_t)page * R;
   const uint16_t* ksrc = p.k_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
@@ -122,7 +124,13 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
     mbar_init(&bar, 1);
     fence_mbar_init();
   }
+  if (tid < 16) {
+    thr_s[0][tid] = p.k_thr[tid];
+    thr_s[1][tid] = p.v_thr[tid];
+  }
   __syncthreads();
+  const float* kthr = p.lut ? thr_s[0] : nullptr;
+  const float* vthr = p.lut ? thr_s[1] : nullptr;
   const uint32_t tile_bytes = (uint32_t)(R * D * 2);
   if (tid == 0) {
     mbar_arrive_expect_tx(&bar, 2 * tile_bytes);
@@ -333,13 +341,14 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
       }
       const GroupQ* gq = kq + (t / G) * D + ch;
       pack_chunk<BK>(kt + t * D + ch * kChunk, [&](int i) -> const GroupQ& { return gq[i * NCH]; }, excl,
-                     kc + t * WKW + ch * BK);
+                     kc + t * WKW + ch * BK, kthr);
     }
     const int ng = D / G;
     for (int idx = tid; idx < R * NCH; idx += kQuantThreads) {
       const int t = idx / NCH, ch = idx - t * NCH;
       const GroupQ& gq = vq[t * ng + (ch * kChunk) / G];
-      pack_chunk<BV>(vt + t * D + ch * kChunk, [&](int) -> const GroupQ& { return gq; }, 0u, vc + t * WVW + ch * BV);
+      pack_chunk<BV>(vt + t * D + ch * kChunk, [&](int) -> const GroupQ& { return gq; }, 0u, vc + t * WVW + ch * BV,
+                     vthr);
     }
   }
   fence_proxy_async_smem();

@@ -55,5 +55,19 @@ __device__ __forceinline__ uint32_t quant_code(float x, const GroupQ& g, int L) 
   return (uint32_t)q;
 }
 
+// Codebook quantizer (non-uniform levels, "nuqX" without its calibration): the same zero point and
+// step, then the nearest of the caller's levels lev[0..L] (in steps, 0 = lev[0] < ... < lev[L] = L).
+// y = (x - z) / s is the IEEE quotient and the code is the number of decision thresholds
+// thr[j] = fp32((lev[j] + lev[j+1]) * 0.5) that y exceeds, so a value on a threshold takes the lower
+// level.  thr == nullptr selects the uniform quantizer.
+__device__ __forceinline__ uint32_t code_of(float x, const GroupQ& g, int L, const float* thr) {
+  if (!thr) return quant_code(x, g, L);
+  if (g.sf == 0.0f) return 0;
+  const float y = __fdiv_rn(__fsub_rn(x, g.zf), g.sf);
+  uint32_t c = 0;
+  for (int j = 0; j < L; ++j) c += y > thr[j] ? 1u : 0u;
+  return c;
+}
+
 }  // namespace
 }  // namespace kvq

@@ -42,7 +42,7 @@ class kvq_config(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("max_tokens", ctypes.c_int64), ("k_bits", ctypes.c_int32),
                 ("v_bits", ctypes.c_int32), ("group_size", ctypes.c_int32), ("residual", ctypes.c_int32),
                 ("k_sparse", ctypes.c_int32), ("rope", ctypes.c_int32), ("rope_base", ctypes.c_float),
-                ("softmax_scale", ctypes.c_float), ("sink_tokens", ctypes.c_int32)]
+                ("softmax_scale", ctypes.c_float), ("sink_tokens", ctypes.c_int32), ("codebook", ctypes.c_int32)]
 
 
 class kvq_unit_view(ctypes.Structure):
@@ -66,6 +66,7 @@ SIGNATURES = {
     "kvq_decode_attention": (ctypes.c_int, [_P, _P, _P, _P]),
     "kvq_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "kvq_reset": (ctypes.c_int, [_P]),
+    "kvq_set_codebooks": (ctypes.c_int, [_P, _P, _P]),
     "kvq_decode_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(kvq_config), _P, ctypes.c_int64, _P, _P,
                                                     ctypes.c_int64, _P, _P, _P]),
     "kvq_get_state": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
@@ -138,11 +139,11 @@ def _stream(stream, device=None):
 
 
 def make_config(batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits, v_bits, group_size, residual,
-                k_sparse=0, rope=0, rope_base=10000.0, softmax_scale=None, sink_tokens=0) -> kvq_config:
+                k_sparse=0, rope=0, rope_base=10000.0, softmax_scale=None, sink_tokens=0, codebook=0) -> kvq_config:
     if softmax_scale is None:
         softmax_scale = 1.0 / float(head_dim) ** 0.5
     return kvq_config(batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits, v_bits, group_size, residual,
-                      k_sparse, rope, rope_base, softmax_scale, sink_tokens)
+                      k_sparse, rope, rope_base, softmax_scale, sink_tokens, codebook)
 
 
 # ------------------------------------------------------------------ C-ABI named functions
@@ -232,6 +233,13 @@ def kvq_export_unit(handle, b: int, kvh: int, cfg: kvq_config, stream=None) -> d
     return out
 
 
+def kvq_set_codebooks(handle, k_levels, v_levels) -> None:
+    """Non-uniform levels (in steps) of a codebook cache: host sequences of 2^k_bits and 2^v_bits floats."""
+    k = np.ascontiguousarray(k_levels, dtype=np.float32)
+    v = np.ascontiguousarray(v_levels, dtype=np.float32)
+    _check(lib().kvq_set_codebooks(handle, k.ctypes.data, v.ctypes.data), "kvq_set_codebooks")
+
+
 def kvq_axis_quantize(x, n_units, n_tokens, head_dim, bits, group_size, axis, codes, zero, scale, stream=None):
     _check(lib().kvq_axis_quantize(_ptr(x), n_units, n_tokens, head_dim, bits, group_size, axis, _ptr(codes),
                                    _ptr(zero), _ptr(scale), _stream(stream)), "kvq_axis_quantize")
@@ -254,17 +262,21 @@ class KVCache:
     """One layer's quantized KV cache on one GPU (torch tensors in, torch tensors out)."""
 
     def __init__(self, batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits=2, v_bits=2, group_size=32,
-                 residual=128, k_sparse=0, rope=0, rope_base=10000.0, softmax_scale=None, device=0, sink_tokens=0):
+                 residual=128, k_sparse=0, rope=0, rope_base=10000.0, softmax_scale=None, device=0, sink_tokens=0,
+                 k_levels=None, v_levels=None):
         self.cfg = make_config(batch, num_kv_heads, num_q_heads, head_dim, max_tokens, k_bits, v_bits, group_size,
-                               residual, k_sparse, rope, rope_base, softmax_scale, sink_tokens)
+                               residual, k_sparse, rope, rope_base, softmax_scale, sink_tokens,
+                               0 if k_levels is None else 1)
         self.device = device
         self.handle = kvq_create(self.cfg, device)
+        if k_levels is not None:
+            kvq_set_codebooks(self.handle, k_levels, v_levels)
 
     @classmethod
     def for_workload(cls, w, device=0, max_tokens=None):
         return cls(w.batch, w.kv_heads, w.q_heads, w.head_dim, max_tokens or w.max_tokens, w.k_bits, w.v_bits,
                    w.group, w.residual, w.k_sparse, w.rope, w.rope_base, w.softmax_scale, device,
-                   getattr(w, "sink", 0))
+                   getattr(w, "sink", 0), getattr(w, "k_levels", None) or None, getattr(w, "v_levels", None) or None)
 
     def _need(self, t, shape, name):
         import torch

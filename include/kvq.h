@@ -83,6 +83,12 @@ typedef struct {
                             and never quantized; 0 = no sinks.  unite.ai page and dothoosh.com page,
                             research-direction sections (InnerQ keeps high-precision windows for the
                             recent tokens and for the attention-sink tokens). */
+  int32_t codebook;      /* 0: uniform levels (code c stands for z + c*s).  1: non-uniform levels (the
+                            nuqX datatype of the KVQuant review, "Proposed method", without its
+                            calibration): code c stands for z + lev[c]*s with per-cache key and value
+                            levels set by kvq_set_codebooks before the first prefill or append;
+                            rope = 0 with (k_bits, v_bits) in {(2,2), (3,3), (4,4), (4,2)} and 1 or 4
+                            query heads per kv head, or rope = 1 with 3/3 bits and 4. */
 } kvq_config;
 
 typedef struct kvq_cache kvq_cache; /* opaque */
@@ -151,6 +157,19 @@ kvq_status kvq_decode_attention(kvq_cache* cache, const void* q_f16, void* out_f
  */
 kvq_status kvq_decode_step(kvq_cache* cache, const void* k_f16, const void* v_f16, const void* q_f16, void* out_f16,
                            void* cuda_stream);
+
+/*
+ * Codebooks of a cache created with codebook = 1: k_levels[0 .. 2^k_bits) and v_levels[0 .. 2^v_bits),
+ * host fp32 arrays (copied), the level of each code in quantization steps, strictly increasing from
+ * lev[0] = 0 to lev[L] = L (L = 2^bits - 1), so a group's minimum and maximum stay exact.  A value
+ * x of a group with zero point z and step s takes the code of the nearest level to
+ * y = (x - z) / s (fp32 quotient): the number of thresholds fp32((lev[j] + lev[j+1]) * 0.5),
+ * j < L, that y exceeds (a value on a threshold takes the lower level).  lev[c] = c is the
+ * uniform quantizer except on exact ties.  Must run before the first prefill or append
+ * (KVQ_ERR_STATE otherwise; those calls return KVQ_ERR_STATE until it has run); kvq_reset keeps
+ * the codebooks.  KVQ_ERR_INVALID_ARG for a uniform cache or levels that break the rules above.
+ */
+kvq_status kvq_set_codebooks(kvq_cache* cache, const float* k_levels, const float* v_levels);
 
 /*
  * Forget every cached token so the cache can take a new batch of sequences

@@ -307,7 +307,7 @@ class OracleUnit:
     @classmethod
     def for_workload(cls, w):
         return cls(w.head_dim, w.k_bits, w.v_bits, w.group, w.residual, w.k_sparse, w.rope, w.rope_base,
-                   getattr(w, "sink", 0), getattr(w, "k_levels", None), getattr(w, "v_levels", None))
+                   getattr(w, "sink", 0), getattr(w, "k_levels", None) or None, getattr(w, "v_levels", None) or None)
 
     @property
     def Tq(self):

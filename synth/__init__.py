@@ -100,6 +100,8 @@ class Workload:
     queries: str           # "normal": N(0,1); "peaked": biased toward 8 past keys (84% of mass on 5% of tokens)
     seed: int
     sink: int = 0          # attention-sink tokens kept fp16 (0: none)
+    k_levels: tuple = ()   # non-uniform codebook levels in steps (empty: uniform codes)
+    v_levels: tuple = ()
 
     @property
     def softmax_scale(self) -> float:
