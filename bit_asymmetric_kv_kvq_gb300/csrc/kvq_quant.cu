@@ -209,25 +209,45 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
 
   // ---- keys: one quantizer per (G-token group, channel)
   const int ngk = R / G;
-  for (int idx = tid; idx < ngk * D; idx += kQuantThreads) {
-    const int g = idx / D, c = idx - g * D;
-    bool any = false;
-    float mn = 0.0f, mx = 0.0f;
-    for (int t = g * G; t < g * G + G; ++t) {
-      if (excluded(t, c)) continue;
-      const float v = h2f(kt[t * D + c]);
-      if (!any) {
-        mn = v;
-        mx = v;
-        any = true;
-      } else {
-        mn = v < mn ? v : mn;
-        mx = v > mx ? v : mx;
+  if (nsp == 0) {
+    // two channels per thread: fp16 minimum and maximum are exact, so the scan runs on half2
+    for (int idx = tid; idx < ngk * D / 2; idx += kQuantThreads) {
+      const int g = idx / (D / 2), c = 2 * (idx - g * (D / 2));
+      const __half2* col = reinterpret_cast<const __half2*>(kt + (g * G) * D + c);
+      __half2 mn = col[0], mx = mn;
+#pragma unroll 8
+      for (int t = 1; t < G; ++t) {
+        const __half2 v = col[t * (D / 2)];
+        mn = __hmin2(mn, v);
+        mx = __hmax2(mx, v);
       }
+      const float2 fmn = __half22float2(mn), fmx = __half22float2(mx);
+      const GroupQ q0 = group_params(fmn.x, fmx.x, LK), q1 = group_params(fmn.y, fmx.y, LK);
+      kq[g * D + (p.lay.frag ? c : kq_slot(c))] = q0;  // fragment packing reads them channel by channel
+      kq[g * D + (p.lay.frag ? c + 1 : kq_slot(c + 1))] = q1;
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint32_t*>(pg + p.lay.off_km) + g * D + c) = make_uint2(q0.bits, q1.bits);
     }
-    const GroupQ q = group_params(mn, mx, LK);
-    kq[g * D + (p.lay.frag ? c : kq_slot(c))] = q;  // fragment packing reads them channel by channel
-    reinterpret_cast<uint32_t*>(pg + p.lay.off_km)[idx] = q.bits;
+  } else {
+    for (int idx = tid; idx < ngk * D; idx += kQuantThreads) {
+      const int g = idx / D, c = idx - g * D;
+      bool any = false;
+      float mn = 0.0f, mx = 0.0f;
+      for (int t = g * G; t < g * G + G; ++t) {
+        if (excluded(t, c)) continue;
+        const float v = h2f(kt[t * D + c]);
+        if (!any) {
+          mn = v;
+          mx = v;
+          any = true;
+        } else {
+          mn = v < mn ? v : mn;
+          mx = v > mx ? v : mx;
+        }
+      }
+      const GroupQ q = group_params(mn, mx, LK);
+      kq[g * D + (p.lay.frag ? c : kq_slot(c))] = q;
+      reinterpret_cast<uint32_t*>(pg + p.lay.off_km)[idx] = q.bits;
+    }
   }
 
   // ---- values: one quantizer per (token, G-channel group); a warp per token,
@@ -238,8 +258,15 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
     const int ng = D / G;
     for (int t = warp; t < R; t += kQuantThreads / 32) {
       float x[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) x[i] = h2f(vt[t * D + c0 + i]);
+      {
+        const uint2 w = *reinterpret_cast<const uint2*>(vt + t * D + c0);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+        x[0] = a.x;
+        x[1] = a.y;
+        x[2] = b.x;
+        x[3] = b.y;
+      }
       float mn = x[0], mx = x[0];
 #pragma unroll
       for (int i = 1; i < 4; ++i) {
