@@ -31,6 +31,7 @@ import json
 import math
 import os
 import statistics
+import tempfile
 import subprocess
 import sys
 import time
@@ -186,8 +187,15 @@ class Clocks:
         if not enabled:
             return
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            # samples go to a file of their own; KVQ_CLOCKS_DIR keeps it (default: a temporary file)
+            keep = os.environ.get("KVQ_CLOCKS_DIR")
+            if keep:
+                os.makedirs(keep, exist_ok=True)
+                self.path = os.path.join(keep, f"clocks_bench_{os.getpid()}.csv")
+            else:
+                fd, self.path = tempfile.mkstemp(prefix="clocks_bench_", suffix=".csv")
+                os.close(fd)
+            self.keep = bool(keep)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
@@ -218,6 +226,8 @@ class Clocks:
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+        if not self.keep:
+            os.remove(self.path)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
