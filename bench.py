@@ -16,9 +16,11 @@ e2e    = the same metric through the public C-ABI calls with the inputs in
          pinned host memory: every step copies its prefill inputs, appended
          tokens and queries host->device and reads every output back.
 roofline: the dominant kernel (decode attention) against the measured HBM
-         copy bandwidth: algorithmic bytes per launch (packed codes + scales
+         copy bandwidth: algorithmic bytes per call (packed codes + scales
          and zero points + fp16 window + q + out + the new token's window
-         store) / mean launch time of the steps that do not flush.
+         store) / mean time of the decode steps that do not flush, each timed
+         with CUDA events around the whole call (the decode kernel and the
+         small kernel that merges its partials, launched back to back).
 
 `--impl reference` times the CPU oracle (the plain fp64/fp32 C reference the
 tests check against) on a bounded sample of the same workload.
@@ -406,7 +408,7 @@ def run_ours(args, dist):
     return {
         "value": value, "ms_per_step": ms_step, "gpu_launches": int(n_launch),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": "decode attention (decode_mma_kernel, tensor cores)",
+                     "traffic": traffic, "kernel": "decode attention call: decode_mma_kernel (tensor cores) + merge_kernel",
                      "bytes_per_launch": dec_bytes, "ms_per_launch": dec_ms,
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6.8 TB/s"},
         "decode_only": {"value": B * statistics.mean(T0 + 1 + i for i in range(1, S)) / (dec_ms * 1e-3),
