@@ -85,7 +85,8 @@ __device__ __forceinline__ void pack_chunk(const uint16_t* x, const Params& grp,
     for (int j = 0; j < 8; ++j) {
       const int i = q4 * 8 + j;
       const uint16_t bits = (uint16_t)(j & 1 ? pair[j >> 1] >> 16 : pair[j >> 1] & 0xFFFFu);
-      const uint32_t code = (excl >> i) & 1u ? 0u : code_of(h2f(bits), grp(i), L, thr);
+      const uint32_t c = code_of(h2f(bits), grp(i), L, thr);  // then masked: no branch per code
+      const uint32_t code = (excl >> i) & 1u ? 0u : c;
       const int b = i * BITS;
       w[b >> 5] |= code << (b & 31);
       if ((b & 31) + BITS > 32) w[(b >> 5) + 1] |= code >> (32 - (b & 31));
@@ -317,8 +318,12 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
             for (int r = 0; r < 2; ++r) {
               const int tok = tk0 + 8 * r;
               const uint32_t xx = *reinterpret_cast<const uint32_t*>(kt + tok * D + c0);
-              const uint32_t a = excluded(tok, c0) ? 0u : quant_code(h2f((uint16_t)(xx & 0xFFFFu)), q0, LK);
-              const uint32_t b = excluded(tok, c0 + 1) ? 0u : quant_code(h2f((uint16_t)(xx >> 16)), q1, LK);
+              uint32_t a = quant_code(h2f((uint16_t)(xx & 0xFFFFu)), q0, LK);
+              uint32_t b = quant_code(h2f((uint16_t)(xx >> 16)), q1, LK);
+              if (nsp > 0) {
+                a = excluded(tok, c0) ? 0u : a;
+                b = excluded(tok, c0 + 1) ? 0u : b;
+              }
               wk[r * KB + kk / (8 / KB)] |= (a << (KB * j)) | (b << (16 + KB * j));
             }
           }

@@ -44,12 +44,17 @@ __device__ __forceinline__ GroupQ group_params(float mn, float mx, int L) {
   return g;
 }
 
+// Branch-free in the common case: a zero step has inv = 0, so r = 0 and the code is 0; the exact
+// quotient is taken only when some lane of the warp is within 2^-14 of a half-integer (about one
+// warp step in 300), so the warp pays one vote instead of a divergent branch per code.
 __device__ __forceinline__ uint32_t quant_code(float x, const GroupQ& g, int L) {
-  if (g.sf == 0.0f) return 0;
   const float d = __fsub_rn(x, g.zf);
   float r = __fmul_rn(d, g.inv);
   const float frac = r - floorf(r);
-  if (fabsf(frac - 0.5f) <= 0x1.0p-14f) r = __fdiv_rn(d, g.sf);  // near a rounding tie: exact quotient
+  const bool near = fabsf(frac - 0.5f) <= 0x1.0p-14f;
+  if (__any_sync(__activemask(), near)) {
+    if (near) r = __fdiv_rn(d, g.sf);  // near a rounding tie: the exact quotient (s > 0 here)
+  }
   float q = rintf(r);
   q = fminf(fmaxf(q, 0.0f), (float)L);
   return (uint32_t)q;
