@@ -493,11 +493,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
 #pragma unroll
       for (int e = 0; e < 4; ++e) d[e] = (da[0][e] + da[1][e]) + (da[2][e] + da[3][e]);
       float s0 = -INFINITY, s1 = -INFINITY;
-      if (t4 < HG) {
+      {
+        // every lane computes (no branch); lanes past the heads take head 0 and are masked below
+        const int hq = t4 < HG ? t4 : 0;
         float sgk = sigk[0], zz = zk[0];
 #pragma unroll
         for (int h = 1; h < HG; ++h)
-          if (t4 == h) {
+          if (hq == h) {
             sgk = sigk[h];
             zz = zk[h];
           }
@@ -515,14 +517,14 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
               const int c = si[tok * p.nsp + k];
               const float xv = __half2float(__ushort_as_half(sv[tok * p.nsp + k]));
               const float z = __half2float(__ushort_as_half((uint16_t)(km[gk * D + c] & 0xFFFFu)));
-              add = fmaf(qs[t4][c], xv - z, add);
+              add = fmaf(qs[hq][c], xv - z, add);
             }
             if (rh == 0) s0 += add;
             else s1 += add;
           }
         }
-        s0 *= p.qk_scale_log2;
-        s1 *= p.qk_scale_log2;
+        s0 = t4 < HG ? s0 * p.qk_scale_log2 : -INFINITY;
+        s1 = t4 < HG ? s1 * p.qk_scale_log2 : -INFINITY;
       }
       sc[mt][0] = s0;
       sc[mt][1] = s1;
@@ -606,10 +608,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
       for (int bi = 0; bi < NBM; ++bi) {
         bv[bi][0] = pack_half2(split_part(pb0 * vs[kc][bi][0], hl), split_part(pb1 * vs[kc][bi][1], hl));
         bv[bi][1] = pack_half2(split_part(pb2 * vs[kc][bi][2], hl), split_part(pb3 * vs[kc][bi][3], hl));
-        if (hl == 0)
-          zacc[bi] = fmaf(p0, vz[kc][bi][0], fmaf(p1, vz[kc][bi][1], fmaf(p2, vz[kc][bi][2], fmaf(p3, vz[kc][bi][3], zacc[bi]))));
+        // (every lane accumulates; only the lanes of the high columns are read in the epilogue)
+        zacc[bi] = fmaf(p0, vz[kc][bi][0], fmaf(p1, vz[kc][bi][1], fmaf(p2, vz[kc][bi][2], fmaf(p3, vz[kc][bi][3], zacc[bi]))));
       }
-      if (hl == 0 && gl == 0) lacc += (p0 + p1) + (p2 + p3);
+      lacc += (p0 + p1) + (p2 + p3);  // read from the lanes of head h's high column (lane 8h)
 
       uint32_t wd[2 * BV];
       const uint4* wsrc = reinterpret_cast<const uint4*>(pgm + p.lay.off_vc) + ((int64_t)tile * 32 + lane) * (2 * BV / 4);
