@@ -64,15 +64,15 @@ struct Pairs {
   }
 };
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
+__device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
 
-// v as fp16 high part (hl = 0) or the fp16 rounding of what the high part leaves (hl = 1)
-__device__ __forceinline__ float split_part(float v, int hl) {
-  const float hi = __half2float(__float2half_rn(v));
-  return hl ? v - hi : hi;
+// (a, b) split into fp16 high parts and the fp16 rounding of what they leave: a = hi + lo to about
+// 22 significant bits.  Two values per conversion.
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 f = __half22float2(h);
+  hi = h2bits(h);
+  lo = h2bits(__floats2half2_rn(a - f.x, b - f.y));
 }
 
 template <int BK, int BV, int HG>
@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
   __shared__ int stage_page[kMmaMaxStages];     // page of the slice a stage holds or is being filled with
   __shared__ int next_sub;
   __shared__ int abort_flag;
+  __shared__ __align__(16) uint32_t zero_frag[4][16];  // B fragments of the unused columns
 
   const int hw = (int)(wpu - p.n_pages);
   auto pages_before = [&](int64_t x) -> int64_t {
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     return mbar_wait(&full_bar[st], (k >> log2S) & 1);
   };
 
+  if (tid < 64) (&zero_frag[0][0])[tid] = 0u;
   if (tid == 0) {
     abort_flag = 0;
     next_sub = 0;
@@ -419,30 +421,30 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
           mx = fmaxf(mx, fabsf(qp[i]));
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          z += __shfl_xor_sync(kAll, z, off);
-          mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, off));
-        }
+        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(kAll, z, off);
+        // mx >= 0: its bit pattern orders like its value, so one integer reduction finds the maximum
+        const uint32_t mxb = __reduce_max_sync(kAll, __float_as_uint(mx));
         zk[h] = z;
         // largest |B| below 2^15: scale by 2^(14 - floor(log2 max))
-        const int emax = mx > 0.0f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+        const int emax = mxb != 0u ? (int)((mxb >> 23) & 0xFF) - 127 : 0;
         const int sig = min(max(14 - emax, -90), 90);
         sigk[h] = pow2f(24 - sig);  // score = D * 2^(24 - sig)
         const float sc = pow2f(sig - pk);
         const int tt0 = 2 * (lane & 1);
-#pragma unroll
-        for (int hlp = 0; hlp < 2; ++hlp) {
-          const float v0 = split_part(qp[0] * sc, hlp), v1 = split_part(qp[1] * sc, hlp);
-          const float v2 = split_part(qp[2] * sc, hlp), v3 = split_part(qp[3] * sc, hlp);
-          bk_s[warp][2 * h + hlp][tt0][2 * kk + hh] = pack_half2(v0, v1);
-          bk_s[warp][2 * h + hlp][tt0 + 1][2 * kk + hh] = pack_half2(v2, v3);
-        }
+        uint32_t hi01, lo01, hi23, lo23;
+        split2(qp[0] * sc, qp[1] * sc, hi01, lo01);
+        split2(qp[2] * sc, qp[3] * sc, hi23, lo23);
+        bk_s[warp][2 * h][tt0][2 * kk + hh] = hi01;
+        bk_s[warp][2 * h][tt0 + 1][2 * kk + hh] = hi23;
+        bk_s[warp][2 * h + 1][tt0][2 * kk + hh] = lo01;
+        bk_s[warp][2 * h + 1][tt0 + 1][2 * kk + hh] = lo23;
       }
     }
     __syncwarp();
     uint32_t bf[16];
-    if (g8 < NCOL) {
-      const uint4* src = reinterpret_cast<const uint4*>(&bk_s[warp][g8][t4][0]);
+    {
+      // lanes of the unused B columns read a block of zeros: one path for every lane
+      const uint4* src = reinterpret_cast<const uint4*>(g8 < NCOL ? &bk_s[warp][g8][t4][0] : &zero_frag[t4][0]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 v = src[i];
@@ -451,9 +453,6 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
         bf[4 * i + 2] = v.z;
         bf[4 * i + 3] = v.w;
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) bf[i] = 0u;
     }
     __syncwarp();  // bk_s is free for the next sub-tile
 
@@ -580,9 +579,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
           }
         }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) smax = fmaxf(smax, __shfl_xor_sync(kAll, smax, off));
-      const int enew = smax > 0.0f ? (int)((__float_as_uint(smax) >> 23) & 0xFF) - 127 : -30;
+      const uint32_t smaxb = __reduce_max_sync(kAll, __float_as_uint(smax));  // scales are >= 0
+      const int enew = smaxb != 0u ? (int)((smaxb >> 23) & 0xFF) - 127 : -30;
       if (enew > es) {  // larger scales: lower the B scale, rescale what is accumulated (exact)
         const float f = pow2f(es - enew);
 #pragma unroll
@@ -606,8 +604,11 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
       uint32_t bv[NBM][2];
 #pragma unroll
       for (int bi = 0; bi < NBM; ++bi) {
-        bv[bi][0] = pack_half2(split_part(pb0 * vs[kc][bi][0], hl), split_part(pb1 * vs[kc][bi][1], hl));
-        bv[bi][1] = pack_half2(split_part(pb2 * vs[kc][bi][2], hl), split_part(pb3 * vs[kc][bi][3], hl));
+        uint32_t h0, l0, h1, l1;
+        split2(pb0 * vs[kc][bi][0], pb1 * vs[kc][bi][1], h0, l0);
+        split2(pb2 * vs[kc][bi][2], pb3 * vs[kc][bi][3], h1, l1);
+        bv[bi][0] = hl ? l0 : h0;
+        bv[bi][1] = hl ? l1 : h1;
         // (every lane accumulates; only the lanes of the high columns are read in the epilogue)
         zacc[bi] = fmaf(p0, vz[kc][bi][0], fmaf(p1, vz[kc][bi][1], fmaf(p2, vz[kc][bi][2], fmaf(p3, vz[kc][bi][3], zacc[bi]))));
       }
