@@ -456,41 +456,55 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     }
     __syncwarp();  // bk_s is free for the next sub-tile
 
-    // -- scores of the two 16-token tiles: lane (g8, t4 < HG) gets head t4 of tokens g8, g8 + 8
+    // -- scores of the two 16-token tiles: lane (g8, t4 < HG) gets head t4 of tokens g8, g8 + 8.
+    //    The tiles' products are interleaved, two accumulator chains each (k-chunks kk % 2), so four
+    //    independent chains keep the mma latency off the path.
+    float dsum[2][4];
+    {
+      uint32_t wd[2][2 * BK];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const uint4* wsrc =
+            reinterpret_cast<const uint4*>(pgm + p.lay.off_kc) + ((int64_t)(2 * stt + mt) * 32 + lane) * (2 * BK / 4);
+#pragma unroll
+        for (int i = 0; i < 2 * BK / 4; ++i) {
+          const uint4 v = wsrc[i];
+          wd[mt][4 * i] = v.x;
+          wd[mt][4 * i + 1] = v.y;
+          wd[mt][4 * i + 2] = v.z;
+          wd[mt][4 * i + 3] = v.w;
+        }
+      }
+      float da[2][2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) da[mt][c][e] = 0.0f;
+#pragma unroll
+      for (int u = 0; u < BK; ++u) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const uint32_t X = wd[mt][u], Y = wd[mt][BK + u];
+          const uint32_t Xs = X >> PK::SHIFT, Ys = Y >> PK::SHIFT;
+#pragma unroll
+          for (int jj = 0; jj < KPW; ++jj) {
+            const int kk = u * KPW + jj;
+            mma16816(da[mt][kk & 1], PK::get(X, Xs, 2 * jj), PK::get(Y, Ys, 2 * jj), PK::get(X, Xs, 2 * jj + 1),
+                     PK::get(Y, Ys, 2 * jj + 1), bf[2 * kk], bf[2 * kk + 1]);
+          }
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dsum[mt][e] = da[mt][0][e] + da[mt][1][e];
+    }
     float sc[2][2];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-      const int tile = 2 * stt + mt;
-      uint32_t wd[2 * BK];
-      const uint4* wsrc = reinterpret_cast<const uint4*>(pgm + p.lay.off_kc) + ((int64_t)tile * 32 + lane) * (2 * BK / 4);
-#pragma unroll
-      for (int i = 0; i < 2 * BK / 4; ++i) {
-        const uint4 v = wsrc[i];
-        wd[4 * i] = v.x;
-        wd[4 * i + 1] = v.y;
-        wd[4 * i + 2] = v.z;
-        wd[4 * i + 3] = v.w;
-      }
-      // four independent accumulator chains (k-chunks kk % 4) keep the mma latency off the path
-      float da[4][4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) da[c][e] = 0.0f;
-#pragma unroll
-      for (int u = 0; u < BK; ++u) {
-        const uint32_t X = wd[u], Y = wd[BK + u];
-        const uint32_t Xs = X >> PK::SHIFT, Ys = Y >> PK::SHIFT;
-#pragma unroll
-        for (int jj = 0; jj < KPW; ++jj) {
-          const int kk = u * KPW + jj;
-          mma16816(da[kk & 3], PK::get(X, Xs, 2 * jj), PK::get(Y, Ys, 2 * jj), PK::get(X, Xs, 2 * jj + 1),
-                   PK::get(Y, Ys, 2 * jj + 1), bf[2 * kk], bf[2 * kk + 1]);
-        }
-      }
-      float d[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) d[e] = (da[0][e] + da[1][e]) + (da[2][e] + da[3][e]);
+      const float* d = dsum[mt];
       float s0 = -INFINITY, s1 = -INFINITY;
       {
         // every lane computes (no branch); lanes past the heads take head 0 and are masked below
