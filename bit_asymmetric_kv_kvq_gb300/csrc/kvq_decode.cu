@@ -43,14 +43,7 @@ namespace {
 
 cudaError_t launch_merge(const DecodeParams& p, int hg, cudaStream_t s) {
   const unsigned grid = (unsigned)p.n_units;
-  const size_t smem = (size_t)hg * p.max_slots * sizeof(float);  // the slot weights
-  auto run = [&](auto kern, int threads) -> cudaError_t {
-    if (smem > 32 * 1024) {
-      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-    }
-    return launch_pdl(kern, grid, (unsigned)threads, smem, s, p);
-  };
+  auto run = [&](auto kern, int threads) -> cudaError_t { return launch_pdl(kern, grid, (unsigned)threads, 0, s, p); };
   switch (hg) {
     case 1: return run(merge_kernel<1>, 1 * kMergeWarpsPerHead * 32);
     case 2: return run(merge_kernel<2>, 2 * kMergeWarpsPerHead * 32);

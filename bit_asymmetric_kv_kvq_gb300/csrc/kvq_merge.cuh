@@ -15,23 +15,24 @@
 namespace kvq {
 
 constexpr int kMergeWarpsPerHead = 4;
+constexpr int kMergeChunk = 16;  // slots a warp loads at once
 
 // One CTA per unit, kMergeWarpsPerHead warps per query head.  The partials sit in L2, so the
-// merge is a latency problem: every (m, l) of the head is loaded at once to fix M and the weights,
-// then the head's warps split the slots and keep all their acc loads in flight, and shared memory
-// sums the warps.  Two L2 round trips per unit.  Dynamic shared memory: HG * max_slots floats.
+// merge is a latency problem: each warp takes every kMergeWarpsPerHead-th slot and loads the
+// (m, l) and acc of sixteen of them together, merging them into a running (M, L, acc) of its own;
+// shared memory then merges the head's warps.  For up to 64 slots per head that is one L2 round
+// trip after the slot count.
 template <int HG>
 __global__ void __launch_bounds__(HG * kMergeWarpsPerHead * 32) merge_kernel(const DecodeParams p) {
   constexpr int D = kHeadDim;
-  constexpr int WH = kMergeWarpsPerHead;
+  constexpr int WH = kMergeWarpsPerHead, CH = kMergeChunk;
   constexpr unsigned all = 0xffffffffu;
-  extern __shared__ float wts[];  // [HG][max_slots]
-  __shared__ float red[HG][WH][D];
-  __shared__ float hmax[HG][WH], hsum[HG][WH];
+  __shared__ float4 red[HG][WH][32];
+  __shared__ float wm[HG][WH], wl[HG][WH];
   __shared__ int n_s;
   const int64_t unit = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = warp / WH, wh = warp % WH, ht = tid - h * WH * 32;  // head, warp and thread within it
+  const int h = warp / WH, wh = warp % WH;  // head and warp within it
   pdl_allow_next();
   pdl_wait();  // the decode launch's partials
   if (tid == 0) n_s = min(p.nslot[unit], p.max_slots);
@@ -41,57 +42,69 @@ __global__ void __launch_bounds__(HG * kMergeWarpsPerHead * 32) merge_kernel(con
   const int64_t bh = b * p.Hq + kvh * HG + h;
   const float* ml = p.part_ml + bh * p.max_slots * 2;
   const float* pacc = p.part_acc + bh * p.max_slots * D + 4 * lane;
-  float* w = wts + h * p.max_slots;
 
-  // the head's maximum, the slot weights and the weighted sum of l
-  float mx = -INFINITY;
-  for (int s = ht; s < n; s += WH * 32) mx = fmaxf(mx, __ldcg(ml + 2 * s));
+  float M = -INFINITY, L = 0.0f;
+  float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int base = wh; base < n; base += WH * CH) {
+    // this chunk's slots base + WH*k, k < CH: lane k < CH loads slot k's (m, l); every lane loads
+    // its four channels of every slot's acc -- all in flight together
+    const int sl = base + WH * lane;
+    const float2 mlv = lane < CH && sl < n ? __ldcg(reinterpret_cast<const float2*>(ml + 2 * sl))
+                                            : make_float2(-INFINITY, 0.0f);
+    float4 v[CH];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(all, mx, off));
-  if (lane == 0) hmax[h][wh] = mx;
-  __syncthreads();
-  float M = hmax[h][0];
+    for (int k = 0; k < CH; ++k) {
+      const int sk = base + WH * k;
+      v[k] = sk < n ? __ldcg(reinterpret_cast<const float4*>(pacc + (int64_t)sk * D)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float cm = mlv.x;
 #pragma unroll
-  for (int i = 1; i < WH; ++i) M = fmaxf(M, hmax[h][i]);
-  float lsum = 0.0f;
-  for (int s = ht; s < n; s += WH * 32) {
-    const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + 2 * s));
-    const float f = v.x == -INFINITY ? 0.0f : exp2f(v.x - M);
-    w[s] = f;
-    lsum = fmaf(f, v.y, lsum);
+    for (int off = 1; off < CH; off <<= 1) cm = fmaxf(cm, __shfl_xor_sync(all, cm, off));
+    cm = __shfl_sync(all, cm, 0);
+    const float Mn = fmaxf(M, cm);
+    const float fo = M == -INFINITY ? 0.0f : exp2f(M - Mn);
+    const float wk = mlv.x == -INFINITY ? 0.0f : exp2f(mlv.x - Mn);
+    float lp = wk * mlv.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lp += __shfl_xor_sync(all, lp, off);
+    L = fmaf(L, fo, lp);
+    a.x *= fo;
+    a.y *= fo;
+    a.z *= fo;
+    a.w *= fo;
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      const float f = __shfl_sync(all, wk, k);
+      a.x = fmaf(f, v[k].x, a.x);
+      a.y = fmaf(f, v[k].y, a.y);
+      a.z = fmaf(f, v[k].z, a.z);
+      a.w = fmaf(f, v[k].w, a.w);
+    }
+    M = Mn;
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(all, lsum, off);
-  if (lane == 0) hsum[h][wh] = lsum;
-  __syncthreads();
-
-  // this warp's slots wh, wh + WH, ...: lane l owns channels 4l .. 4l+3
-  float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll 8
-  for (int s = wh; s < n; s += WH) {
-    const float f = w[s];
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(pacc + (int64_t)s * D));
-    a0 = fmaf(f, v.x, a0);
-    a1 = fmaf(f, v.y, a1);
-    a2 = fmaf(f, v.z, a2);
-    a3 = fmaf(f, v.w, a3);
+  red[h][wh][lane] = a;
+  if (lane == 0) {
+    wm[h][wh] = M;
+    wl[h][wh] = L;
   }
-  *reinterpret_cast<float4*>(&red[h][wh][4 * lane]) = make_float4(a0, a1, a2, a3);
   __syncthreads();
   if (wh == 0) {
-    float L = 0.0f;
+    float Mh = wm[h][0];
 #pragma unroll
-    for (int i = 0; i < WH; ++i) L += hsum[h][i];
-    float4 o = *reinterpret_cast<const float4*>(&red[h][0][4 * lane]);
+    for (int i = 1; i < WH; ++i) Mh = fmaxf(Mh, wm[h][i]);
+    float Lh = 0.0f;
+    float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-    for (int i = 1; i < WH; ++i) {
-      const float4 v = *reinterpret_cast<const float4*>(&red[h][i][4 * lane]);
-      o.x += v.x;
-      o.y += v.y;
-      o.z += v.z;
-      o.w += v.w;
+    for (int i = 0; i < WH; ++i) {
+      const float f = wm[h][i] == -INFINITY ? 0.0f : exp2f(wm[h][i] - Mh);
+      Lh = fmaf(f, wl[h][i], Lh);
+      const float4 r = red[h][i][lane];
+      o.x = fmaf(f, r.x, o.x);
+      o.y = fmaf(f, r.y, o.y);
+      o.z = fmaf(f, r.z, o.z);
+      o.w = fmaf(f, r.w, o.w);
     }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    const float inv = Lh > 0.0f ? 1.0f / Lh : 0.0f;
     const __half2 o01 = __floats2half2_rn(o.x * inv, o.y * inv), o23 = __floats2half2_rn(o.z * inv, o.w * inv);
     uint2 packed;
     packed.x = *reinterpret_cast<const uint32_t*>(&o01);
