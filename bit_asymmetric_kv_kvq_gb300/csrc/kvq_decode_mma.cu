@@ -357,13 +357,16 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
 
   int64_t cur = -1, ustart = 0;
   bool touched = false;  // the warp has state (page sub-tiles) for the current unit
+  // sub-tiles taken at a time: two (of one page) when a page has an even number of them, which
+  // halves the scheduling, page-wait and release work per sub-tile
+  const int GR = (SPP & 1) ? 1 : 2;
   while (true) {
     int s = 0;
-    if (lane == 0) s = atomicAdd(&next_sub, 1);
+    if (lane == 0) s = atomicAdd(&next_sub, GR);
     s = __shfl_sync(kAll, s, 0);
     if (s >= n_sub || *(volatile int*)&abort_flag) break;
     const int sx = SPP == 4 ? s >> 2 : SPP == 2 ? s >> 1 : SPP == 1 ? s : s / 3;
-    const int stt = s - sx * SPP;
+    const int stt0 = s - sx * SPP;
     const int64_t x = w_begin + sx;
     if (cur < 0 || x >= ustart + wpu) {
       if (cur >= 0 && touched) epilogue(cur);
@@ -375,12 +378,14 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     }
     const int loc = (int)(x - ustart);
     if (loc < hw) {
-      const int f = loc * SPP + stt;  // sub-tile of the unit's fp16 rows
-      if (32 * f < p.n_w) window_subtile(cur, f);
+      for (int qq = 0; qq < GR; ++qq) {
+        const int f = loc * SPP + stt0 + qq;  // sub-tile of the unit's fp16 rows
+        if (32 * f < p.n_w) window_subtile(cur, f);
+      }
       continue;
     }
 
-    // ---------------- a sub-tile of a page: tokens 32*stt .. 32*stt+31
+    // ---------------- sub-tiles of a page: tokens 32*stt .. 32*stt+31 for stt = stt0 .. stt0+GR-1
     touched = true;
     const int kpg = (int)(cur * p.n_pages + (loc - hw) - P_begin);
     const int stg = kpg & (n_stages - 1);
@@ -392,6 +397,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
     const uint8_t* pgm = stage_mem + (size_t)stg * page_bytes;
     const uint32_t* km = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_km);
     const uint32_t* vm = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vm);
+    for (int qq = 0; qq < GR; ++qq) {
+    const int stt = stt0 + qq;
     const int gk = (32 * stt) >> p.log2G;  // key group
 
     // -- key B fragments: q'_h[c] 2^(sig_h - pos) split high/low, four channels per lane
@@ -660,11 +667,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
       }
     }
 
-    // -- release the sub-tile; the warp releasing a stage's last sub-tile refills it
+    }  // sub-tiles of the grab
+
+    // -- release the sub-tiles; the warp releasing a stage's last sub-tile refills it
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive(&empty_bar[stg]);
-      if (atomicAdd(&stage_cnt[stg], 1) % SPP == SPP - 1 && kpg + n_stages < n_pg && !*(volatile int*)&abort_flag) {
+      for (int qq = 0; qq < GR; ++qq) mbar_arrive(&empty_bar[stg]);
+      if (atomicAdd(&stage_cnt[stg], GR) % SPP == SPP - GR && kpg + n_stages < n_pg && !*(volatile int*)&abort_flag) {
         if (mbar_wait(&empty_bar[stg], (kpg >> log2S) & 1)) {
           issue_page(kpg + n_stages);
         } else {
