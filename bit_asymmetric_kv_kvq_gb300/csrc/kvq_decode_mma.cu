@@ -75,7 +75,18 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   lo = h2bits(__floats2half2_rn(a - f.x, b - f.y));
 }
 
-template <int BK, int BV, int HG>
+// The common page shape -- R = 128 tokens, G = 32, no sparse entries -- as compile-time offsets
+// (the layout make_layout gives it); STD kernels use them so that the page addressing folds.
+template <int BK, int BV>
+struct StdPage {
+  static constexpr int kc = 0;
+  static constexpr int km = 128 * 128 * BK / 8;
+  static constexpr int vc = km + (128 / 32) * 128 * 4;
+  static constexpr int vm = vc + 128 * 128 * BV / 8;
+  static constexpr int bytes = vm + 128 * (128 / 32) * 4;
+};
+
+template <int BK, int BV, int HG, bool STD>
 __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const DecodeParams p) {
   constexpr int D = kHeadDim, W = kMmaWarps;
   constexpr int NCOL = 2 * HG;   // B columns per value group: (head, high/low)
@@ -92,16 +103,21 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
   const int64_t total = p.n_units * wpu;
   const int64_t w_begin = (int64_t)cta * total / grid;
   const int64_t w_end = (int64_t)(cta + 1) * total / grid;
-  const int page_bytes = p.lay.bytes;
+  using SP = StdPage<BK, BV>;
+  const int page_bytes = STD ? SP::bytes : p.lay.bytes;
+  const int off_kc = STD ? SP::kc : p.lay.off_kc, off_km = STD ? SP::km : p.lay.off_km;
+  const int off_vc = STD ? SP::vc : p.lay.off_vc, off_vm = STD ? SP::vm : p.lay.off_vm;
+  const int log2G = STD ? 5 : p.log2G;
+  const int nsp = STD ? 0 : p.nsp;
   const int log2S = p.log2_stages, n_stages = 1 << log2S;
-  const int SPP = p.R / 32;
+  const int SPP = STD ? 4 : p.R / 32;
   const int n_sub = (int)(w_end - w_begin) * SPP;
-  const int ng = D >> p.log2G;             // value groups per token
+  const int ng = D >> log2G;               // value groups per token
 
   // dynamic shared memory: the page stages, then each warp's query rows (fp32) and key B
   // fragments (static arrays stay small: static shared memory is limited to 48 KB)
   extern __shared__ __align__(128) uint8_t stage_mem[];
-  float(*qw_s)[HG][D] = reinterpret_cast<float(*)[HG][D]>(stage_mem + ((size_t)p.lay.bytes << p.log2_stages));
+  float(*qw_s)[HG][D] = reinterpret_cast<float(*)[HG][D]>(stage_mem + ((size_t)page_bytes << p.log2_stages));
   uint32_t(*bk_s)[NCOL][4][16] = reinterpret_cast<uint32_t(*)[NCOL][4][16]>(qw_s + W);
   __shared__ __align__(8) uint64_t full_bar[kMmaMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMmaMaxStages];
@@ -237,7 +253,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
       const float osc = pow2f(24 - (6 - es));
 #pragma unroll
       for (int mc = 0; mc < 8; ++mc) {
-        const int grp = (16 * mc) >> p.log2G;
+        const int grp = (16 * mc) >> log2G;
         if (grp % GPB != gmine) continue;
         const float s = osc * pow2f(-PV::pos(mc % PV::PER));
         float z = zs[0];
@@ -395,11 +411,11 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
       break;
     }
     const uint8_t* pgm = stage_mem + (size_t)stg * page_bytes;
-    const uint32_t* km = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_km);
-    const uint32_t* vm = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vm);
+    const uint32_t* km = reinterpret_cast<const uint32_t*>(pgm + off_km);
+    const uint32_t* vm = reinterpret_cast<const uint32_t*>(pgm + off_vm);
     for (int qq = 0; qq < GR; ++qq) {
     const int stt = stt0 + qq;
-    const int gk = (32 * stt) >> p.log2G;  // key group
+    const int gk = (32 * stt) >> log2G;  // key group
 
     // -- key B fragments: q'_h[c] 2^(sig_h - pos) split high/low, four channels per lane
     float zk[HG], sigk[HG];
@@ -472,7 +488,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const uint4* wsrc =
-            reinterpret_cast<const uint4*>(pgm + p.lay.off_kc) + ((int64_t)(2 * stt + mt) * 32 + lane) * (2 * BK / 4);
+            reinterpret_cast<const uint4*>(pgm + off_kc) + ((int64_t)(2 * stt + mt) * 32 + lane) * (2 * BK / 4);
 #pragma unroll
         for (int i = 0; i < 2 * BK / 4; ++i) {
           const uint4 v = wsrc[i];
@@ -525,7 +541,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
           }
         s0 = fmaf(d[0] + d[1], sgk, zz);
         s1 = fmaf(d[2] + d[3], sgk, zz);
-        if (p.nsp > 0) {
+        if (nsp > 0) {
           // sparse entries: the dense code there is 0 (value z); add q_c (x_c - z_c)
           const uint8_t* si = pgm + p.lay.off_si;
           const uint16_t* sv = reinterpret_cast<const uint16_t*>(pgm + p.lay.off_sv);
@@ -636,7 +652,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
       lacc += (p0 + p1) + (p2 + p3);  // read from the lanes of head h's high column (lane 8h)
 
       uint32_t wd[2 * BV];
-      const uint4* wsrc = reinterpret_cast<const uint4*>(pgm + p.lay.off_vc) + ((int64_t)tile * 32 + lane) * (2 * BV / 4);
+      const uint4* wsrc = reinterpret_cast<const uint4*>(pgm + off_vc) + ((int64_t)tile * 32 + lane) * (2 * BV / 4);
 #pragma unroll
       for (int i = 0; i < 2 * BV / 4; ++i) {
         const uint4 v = wsrc[i];
@@ -654,7 +670,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
         constexpr int WPR = BV / 2;  // words per register slot
         uint32_t b0 = bv[0][0], b1 = bv[0][1];
         if constexpr (NBM > 1) {
-          const int bi = ((16 * mc) >> p.log2G) / GPB;
+          const int bi = ((16 * mc) >> log2G) / GPB;
 #pragma unroll
           for (int i = 1; i < NBM; ++i)
             if (bi == i) {
@@ -702,7 +718,7 @@ constexpr size_t warp_bufs_bytes() {
 // (or the static arrays exceed the 48 KB a kernel may declare).
 template <int BK, int BV, int HG>
 int log2_stages_mma(int page_bytes) {
-  auto kern = decode_mma_kernel<BK, BV, HG>;
+  auto kern = decode_mma_kernel<BK, BV, HG, false>;  // both variants declare the same static arrays
   static int static_smem = -1, optin = -1;
   if (static_smem < 0) {
     cudaFuncAttributes a{};
@@ -726,7 +742,10 @@ cudaError_t launch_mma_t(const DecodeParams& p, int grid, cudaStream_t s) {
   DecodeParams q = p;
   q.log2_stages = l;
   const size_t smem = ((size_t)p.lay.bytes << l) + warp_bufs_bytes<HG>();
-  auto kern = decode_mma_kernel<BK, BV, HG>;
+  const bool std_shape = p.R == 128 && p.G == 32 && p.nsp == 0 && p.lay.bytes == StdPage<BK, BV>::bytes &&
+                         p.lay.off_km == StdPage<BK, BV>::km && p.lay.off_vc == StdPage<BK, BV>::vc &&
+                         p.lay.off_vm == StdPage<BK, BV>::vm && p.lay.off_kc == 0;
+  auto kern = std_shape ? decode_mma_kernel<BK, BV, HG, true> : decode_mma_kernel<BK, BV, HG, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, (unsigned)grid, kMmaWarps * 32, smem, s, q);
@@ -737,8 +756,11 @@ int resident_mma_t(int page_bytes) {
   const int l = log2_stages_mma<BK, BV, HG>(page_bytes);
   if (l < 0) return 0;
   const size_t smem = ((size_t)page_bytes << l) + warp_bufs_bytes<HG>();
-  auto kern = decode_mma_kernel<BK, BV, HG>;
+  auto kern = decode_mma_kernel<BK, BV, HG, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+  if (cudaFuncSetAttribute(decode_mma_kernel<BK, BV, HG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kMmaWarps * 32, smem) != cudaSuccess) return 0;
   return n;
