@@ -75,17 +75,6 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   lo = h2bits(__floats2half2_rn(a - f.x, b - f.y));
 }
 
-// The common page shape -- R = 128 tokens, G = 32, no sparse entries -- as compile-time offsets
-// (the layout make_layout gives it); STD kernels use them so that the page addressing folds.
-template <int BK, int BV>
-struct StdPage {
-  static constexpr int kc = 0;
-  static constexpr int km = 128 * 128 * BK / 8;
-  static constexpr int vc = km + (128 / 32) * 128 * 4;
-  static constexpr int vm = vc + 128 * 128 * BV / 8;
-  static constexpr int bytes = vm + 128 * (128 / 32) * 4;
-};
-
 template <int BK, int BV, int HG, bool STD>
 __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const DecodeParams p) {
   constexpr int D = kHeadDim, W = kMmaWarps;

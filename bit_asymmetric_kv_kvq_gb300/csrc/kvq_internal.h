@@ -57,6 +57,18 @@ __host__ __device__ inline void frag_value_pair(int bits, int tile, int lane, in
   *tok0 = 16 * tile + 8 * (r / 2) + 2 * t;
 }
 
+// The common page shape -- R = 128 tokens, D = 128, G = 32, no sparse entries -- as compile-time
+// offsets (the layout make_layout gives it).  The page and decode kernels have variants compiled
+// for it (chosen at launch when a cache's layout matches), in which the page addressing folds.
+template <int BK, int BV>
+struct StdPage {
+  static constexpr int kc = 0;
+  static constexpr int km = 128 * 128 * BK / 8;
+  static constexpr int vc = km + (128 / 32) * 128 * 4;
+  static constexpr int vm = vc + 128 * 128 * BV / 8;
+  static constexpr int bytes = vm + 128 * (128 / 32) * 4;
+};
+
 // Host-side validation of a configuration (the checks kvq_create applies).
 kvq_status check_config(const kvq_config& cfg);
 

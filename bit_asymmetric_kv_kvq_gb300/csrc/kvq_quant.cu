@@ -96,17 +96,23 @@ __device__ __forceinline__ void pack_chunk(const uint16_t* x, const Params& grp,
   for (int k = 0; k < BITS; ++k) out[k] = w[k];
 }
 
-template <int BK, int BV>
+template <int BK, int BV, bool STD>
 __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const QuantizeParams p) {
   const int page = blockIdx.x;
   const int unit = blockIdx.y;
-  const int D = p.D, R = p.R, G = p.G, nsp = p.nsp;
+  // STD: the common page shape (StdPage) with compile-time sizes and offsets
+  using SP = StdPage<BK, BV>;
+  const int D = STD ? kHeadDim : p.D, R = STD ? 128 : p.R, G = STD ? 32 : p.G, nsp = STD ? 0 : p.nsp;
+  const bool frag = STD ? true : p.lay.frag != 0;
+  const int lay_bytes = STD ? SP::bytes : p.lay.bytes;
+  const int off_kc = STD ? SP::kc : p.lay.off_kc, off_km = STD ? SP::km : p.lay.off_km;
+  const int off_vc = STD ? SP::vc : p.lay.off_vc, off_vm = STD ? SP::vm : p.lay.off_vm;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   constexpr int LK = (1 << BK) - 1, LV = (1 << BV) - 1;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  const QuantSmem sm = quant_smem(R, D, G, p.lay.bytes);
+  const QuantSmem sm = quant_smem(R, D, G, lay_bytes);
   uint16_t* kt = reinterpret_cast<uint16_t*>(smem + sm.kt);  // [R][D]
   uint16_t* vt = reinterpret_cast<uint16_t*>(smem + sm.vt);  // [R][D]
   GroupQ* kq = reinterpret_cast<GroupQ*>(smem + sm.kq);      // [R/G][D]
@@ -119,7 +125,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
   const int64_t tok0 = p.src_tok0 + (int64_t)page * R;
   const uint16_t* ksrc = p.k_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
   const uint16_t* vsrc = p.v_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
-  uint8_t* dst = p.pages + (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)p.lay.bytes;
+  uint8_t* dst = p.pages + (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)lay_bytes;
 
   if (tid == 0) {
     mbar_init(&bar, 1);
@@ -224,9 +230,9 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
       }
       const float2 fmn = __half22float2(mn), fmx = __half22float2(mx);
       const GroupQ q0 = group_params(fmn.x, fmx.x, LK), q1 = group_params(fmn.y, fmx.y, LK);
-      kq[g * D + (p.lay.frag ? c : kq_slot(c))] = q0;  // fragment packing reads them channel by channel
-      kq[g * D + (p.lay.frag ? c + 1 : kq_slot(c + 1))] = q1;
-      *reinterpret_cast<uint2*>(reinterpret_cast<uint32_t*>(pg + p.lay.off_km) + g * D + c) = make_uint2(q0.bits, q1.bits);
+      kq[g * D + (frag ? c : kq_slot(c))] = q0;  // fragment packing reads them channel by channel
+      kq[g * D + (frag ? c + 1 : kq_slot(c + 1))] = q1;
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint32_t*>(pg + off_km) + g * D + c) = make_uint2(q0.bits, q1.bits);
     }
   } else {
     for (int idx = tid; idx < ngk * D; idx += kQuantThreads) {
@@ -246,8 +252,8 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
         }
       }
       const GroupQ q = group_params(mn, mx, LK);
-      kq[g * D + (p.lay.frag ? c : kq_slot(c))] = q;
-      reinterpret_cast<uint32_t*>(pg + p.lay.off_km)[idx] = q.bits;
+      kq[g * D + (frag ? c : kq_slot(c))] = q;
+      reinterpret_cast<uint32_t*>(pg + off_km)[idx] = q.bits;
     }
   }
 
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
         const GroupQ q = group_params(mn, mx, LV);
         const int g = c0 / G;
         vq[t * ng + g] = q;
-        reinterpret_cast<uint32_t*>(pg + p.lay.off_vm)[t * ng + g] = q.bits;
+        reinterpret_cast<uint32_t*>(pg + off_vm)[t * ng + g] = q.bits;
       }
     }
   }
@@ -292,10 +298,10 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
 
   // ---- codes in fragment order (2- and 4-bit codes, keys without RoPE): one word per thread
   //      and step, its code pairs placed as frag_key_pair / frag_value_pair describe
-  if (p.lay.frag) {
+  if (frag) {
     constexpr int KB = (BK == 2 || BK == 4) ? BK : 2, VB = (BV == 2 || BV == 4) ? BV : 2;
-    uint32_t* kc = reinterpret_cast<uint32_t*>(pg + p.lay.off_kc);
-    uint32_t* vc = reinterpret_cast<uint32_t*>(pg + p.lay.off_vc);
+    uint32_t* kc = reinterpret_cast<uint32_t*>(pg + off_kc);
+    uint32_t* vc = reinterpret_cast<uint32_t*>(pg + off_vc);
     const int ng = D / G;
     // one thread per (16-token tile, lane) owns that lane's 2B words of the tile
     for (int idx = tid; idx < (R / 16) * 32; idx += kQuantThreads) {
@@ -362,8 +368,8 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
     // ---- codes as token-major bitstreams, computed and packed a 32-channel chunk (BITS words) at a time
     constexpr int NCH = kHeadDim / kChunk;
     constexpr int WKW = kHeadDim * BK / 32, WVW = kHeadDim * BV / 32;
-    uint32_t* kc = reinterpret_cast<uint32_t*>(pg + p.lay.off_kc);
-    uint32_t* vc = reinterpret_cast<uint32_t*>(pg + p.lay.off_vc);
+    uint32_t* kc = reinterpret_cast<uint32_t*>(pg + off_kc);
+    uint32_t* vc = reinterpret_cast<uint32_t*>(pg + off_vc);
     for (int idx = tid; idx < R * NCH; idx += kQuantThreads) {
       const int t = idx / NCH, ch = idx - t * NCH;
       uint32_t excl = 0;
@@ -386,7 +392,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
   fence_proxy_async_smem();
   __syncthreads();
   if (tid == 0) {
-    bulk_s2g(dst, pg, (uint32_t)p.lay.bytes);
+    bulk_s2g(dst, pg, (uint32_t)lay_bytes);
     bulk_commit();
     bulk_wait_all();
   }
@@ -408,7 +414,12 @@ __global__ void copy_tokens_kernel(const CopyTokensParams p) {
 template <int BK, int BV>
 cudaError_t launch_quantize_t(const QuantizeParams& p, int n_pages, cudaStream_t s) {
   const size_t smem = quantize_smem_bytes(p.R, p.D, p.G, p.lay);
-  auto kern = quantize_pages_kernel<BK, BV>;
+  using SP = StdPage<BK, BV>;
+  constexpr bool can_std = (BK == 2 || BK == 4) && (BV == 2 || BV == 4);  // fragment-order pages only
+  const bool std_shape = can_std && p.R == 128 && p.D == kHeadDim && p.G == 32 && p.nsp == 0 && p.lay.frag &&
+                         !p.lut && p.lay.bytes == SP::bytes && p.lay.off_kc == SP::kc && p.lay.off_km == SP::km &&
+                         p.lay.off_vc == SP::vc && p.lay.off_vm == SP::vm;
+  auto kern = std_shape ? quantize_pages_kernel<BK, BV, can_std> : quantize_pages_kernel<BK, BV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)n_pages, (unsigned)p.n_units);
