@@ -96,8 +96,14 @@ __device__ __forceinline__ void pack_chunk(const uint16_t* x, const Params& grp,
   for (int k = 0; k < BITS; ++k) out[k] = w[k];
 }
 
+// Threads of one page CTA: the common-shape variant runs 512 (it needs about 35 registers, and
+// its fragment packing gives keys and values to separate halves), the general one 256.
+template <bool STD>
+__host__ __device__ constexpr int quant_threads() { return STD ? 2 * kQuantThreads : kQuantThreads; }
+
 template <int BK, int BV, bool STD>
-__global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const QuantizeParams p) {
+__global__ void __launch_bounds__(quant_threads<STD>(), 2) quantize_pages_kernel(const QuantizeParams p) {
+  constexpr int NT = quant_threads<STD>();
   const int page = blockIdx.x;
   const int unit = blockIdx.y;
   // STD: the common page shape (StdPage) with compile-time sizes and offsets
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
 
   // ---- sparse outliers of each key vector: the nsp largest |x|, ties to the lower channel
   if (nsp > 0) {
-    for (int t = warp; t < R; t += kQuantThreads / 32) {
+    for (int t = warp; t < R; t += NT / 32) {
       const uint16_t* row = kt + t * D;
       float a[kHeadDim / 32];
 #pragma unroll
@@ -203,8 +209,8 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
     }
     // zero the padding of the sparse sections
     const int si_used = R * nsp, sv_used = R * nsp * 2;
-    for (int i = si_used + tid; i < p.lay.off_sv - p.lay.off_si; i += kQuantThreads) pg[p.lay.off_si + i] = 0;
-    for (int i = sv_used + tid; i < p.lay.bytes - p.lay.off_sv; i += kQuantThreads) pg[p.lay.off_sv + i] = 0;
+    for (int i = si_used + tid; i < p.lay.off_sv - p.lay.off_si; i += NT) pg[p.lay.off_si + i] = 0;
+    for (int i = sv_used + tid; i < p.lay.bytes - p.lay.off_sv; i += NT) pg[p.lay.off_sv + i] = 0;
     __syncthreads();
   }
   auto excluded = [&](int t, int c) {
@@ -218,7 +224,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
   const int ngk = R / G;
   if (nsp == 0) {
     // two channels per thread: fp16 minimum and maximum are exact, so the scan runs on half2
-    for (int idx = tid; idx < ngk * D / 2; idx += kQuantThreads) {
+    for (int idx = tid; idx < ngk * D / 2; idx += NT) {
       const int g = idx / (D / 2), c = 2 * (idx - g * (D / 2));
       const __half2* col = reinterpret_cast<const __half2*>(kt + (g * G) * D + c);
       __half2 mn = col[0], mx = mn;
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
       *reinterpret_cast<uint2*>(reinterpret_cast<uint32_t*>(pg + off_km) + g * D + c) = make_uint2(q0.bits, q1.bits);
     }
   } else {
-    for (int idx = tid; idx < ngk * D; idx += kQuantThreads) {
+    for (int idx = tid; idx < ngk * D; idx += NT) {
       const int g = idx / D, c = idx - g * D;
       bool any = false;
       float mn = 0.0f, mx = 0.0f;
@@ -263,7 +269,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
     const int lanes_per_group = G / 4;
     const int c0 = lane * 4;
     const int ng = D / G;
-    for (int t = warp; t < R; t += kQuantThreads / 32) {
+    for (int t = warp; t < R; t += NT / 32) {
       float x[4];
       {
         const uint2 w = *reinterpret_cast<const uint2*>(vt + t * D + c0);
@@ -303,10 +309,15 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
     uint32_t* kc = reinterpret_cast<uint32_t*>(pg + off_kc);
     uint32_t* vc = reinterpret_cast<uint32_t*>(pg + off_vc);
     const int ng = D / G;
-    // one thread per (16-token tile, lane) owns that lane's 2B words of the tile
-    for (int idx = tid; idx < (R / 16) * 32; idx += kQuantThreads) {
+    // one thread per (16-token tile, lane) owns that lane's 2B words of the tile; with 512 threads
+    // the first half packs the keys and the second half the values
+    const int items = (R / 16) * 32;
+    const bool split = NT >= 2 * items;
+    const int first = split && tid >= items ? items : 0;
+    for (int id2 = tid - first; id2 < items; id2 += split ? 2 * items : NT) {
+      const int idx = id2;
       const int tile = idx >> 5, ln = idx & 31, g = ln >> 2, t = ln & 3;
-      {
+      if (!split || first == 0) {
         // keys: tokens 16*tile + g (+8), channels 16kk + 8h + 2t (+1); one key group per tile
         const int tk0 = 16 * tile + g;
         const GroupQ* gq = kq + (tk0 / G) * D;
@@ -337,7 +348,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
 #pragma unroll
         for (int i = 0; i < 2 * KB / 4; ++i) dstk[i] = make_uint4(wk[4 * i], wk[4 * i + 1], wk[4 * i + 2], wk[4 * i + 3]);
       }
-      {
+      if (!split || first != 0) {
         // values: tokens s, s+1 with s = 16*tile + 8*tb + 2t; channel 16mc + g + 8rr; one
         // quantizer per (token, channel group), used for every channel of the lane in that group
         uint32_t wv[2 * VB];
@@ -370,7 +381,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
     constexpr int WKW = kHeadDim * BK / 32, WVW = kHeadDim * BV / 32;
     uint32_t* kc = reinterpret_cast<uint32_t*>(pg + off_kc);
     uint32_t* vc = reinterpret_cast<uint32_t*>(pg + off_vc);
-    for (int idx = tid; idx < R * NCH; idx += kQuantThreads) {
+    for (int idx = tid; idx < R * NCH; idx += NT) {
       const int t = idx / NCH, ch = idx - t * NCH;
       uint32_t excl = 0;
       for (int k = 0; k < nsp; ++k) {
@@ -382,7 +393,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
                      kc + t * WKW + ch * BK, kthr);
     }
     const int ng = D / G;
-    for (int idx = tid; idx < R * NCH; idx += kQuantThreads) {
+    for (int idx = tid; idx < R * NCH; idx += NT) {
       const int t = idx / NCH, ch = idx - t * NCH;
       const GroupQ& gq = vq[t * ng + (ch * kChunk) / G];
       pack_chunk<BV>(vt + t * D + ch * kChunk, [&](int) -> const GroupQ& { return gq; }, 0u, vc + t * WVW + ch * BV,
@@ -423,7 +434,7 @@ cudaError_t launch_quantize_t(const QuantizeParams& p, int n_pages, cudaStream_t
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)n_pages, (unsigned)p.n_units);
-  kern<<<grid, kQuantThreads, smem, s>>>(p);
+  kern<<<grid, std_shape ? quant_threads<can_std>() : kQuantThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
