@@ -48,6 +48,7 @@ struct QuantSmem {
   size_t kt, vt, kq, vq, sidx, pg, total;
 };
 
+// page_bytes = 0: the page is written straight to global memory (no image in shared memory).
 __host__ __device__ inline QuantSmem quant_smem(int R, int D, int G, int page_bytes) {
   QuantSmem m;
   m.kt = 0;
@@ -102,7 +103,7 @@ template <bool STD>
 __host__ __device__ constexpr int quant_threads() { return STD ? 2 * kQuantThreads : kQuantThreads; }
 
 template <int BK, int BV, bool STD>
-__global__ void __launch_bounds__(quant_threads<STD>(), 2) quantize_pages_kernel(const QuantizeParams p) {
+__global__ void __launch_bounds__(quant_threads<STD>(), STD ? 3 : 2) quantize_pages_kernel(const QuantizeParams p) {
   constexpr int NT = quant_threads<STD>();
   const int page = blockIdx.x;
   const int unit = blockIdx.y;
@@ -118,13 +119,17 @@ __global__ void __launch_bounds__(quant_threads<STD>(), 2) quantize_pages_kernel
   constexpr int LK = (1 << BK) - 1, LV = (1 << BV) - 1;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  const QuantSmem sm = quant_smem(R, D, G, lay_bytes);
+  // the common shape writes its page straight to global memory (16-byte stores, coalesced per warp),
+  // which leaves room for three CTAs per SM; the general kernel assembles it in shared memory
+  const QuantSmem sm = quant_smem(R, D, G, STD ? 0 : lay_bytes);
   uint16_t* kt = reinterpret_cast<uint16_t*>(smem + sm.kt);  // [R][D]
   uint16_t* vt = reinterpret_cast<uint16_t*>(smem + sm.vt);  // [R][D]
   GroupQ* kq = reinterpret_cast<GroupQ*>(smem + sm.kq);      // [R/G][D]
   GroupQ* vq = reinterpret_cast<GroupQ*>(smem + sm.vq);      // [R][D/G]
   uint8_t* sidx = smem + sm.sidx;                            // [R][kMaxSparse]
-  uint8_t* pg = smem + sm.pg;                                // page image
+  uint8_t* const dst_page =
+      p.pages + (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)lay_bytes;
+  uint8_t* pg = STD ? dst_page : smem + sm.pg;                // page image (or the page itself)
   __shared__ __align__(8) uint64_t bar;
   __shared__ float thr_s[2][16];  // codebook decision thresholds (keys, values)
 
@@ -400,12 +405,14 @@ __global__ void __launch_bounds__(quant_threads<STD>(), 2) quantize_pages_kernel
                      vthr);
     }
   }
-  fence_proxy_async_smem();
-  __syncthreads();
-  if (tid == 0) {
-    bulk_s2g(dst, pg, (uint32_t)lay_bytes);
-    bulk_commit();
-    bulk_wait_all();
+  if constexpr (!STD) {
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_s2g(dst, pg, (uint32_t)lay_bytes);
+      bulk_commit();
+      bulk_wait_all();
+    }
   }
 }
 
@@ -424,13 +431,13 @@ __global__ void copy_tokens_kernel(const CopyTokensParams p) {
 
 template <int BK, int BV>
 cudaError_t launch_quantize_t(const QuantizeParams& p, int n_pages, cudaStream_t s) {
-  const size_t smem = quantize_smem_bytes(p.R, p.D, p.G, p.lay);
   using SP = StdPage<BK, BV>;
   constexpr bool can_std = (BK == 2 || BK == 4) && (BV == 2 || BV == 4);  // fragment-order pages only
   const bool std_shape = can_std && p.R == 128 && p.D == kHeadDim && p.G == 32 && p.nsp == 0 && p.lay.frag &&
                          !p.lut && p.lay.bytes == SP::bytes && p.lay.off_kc == SP::kc && p.lay.off_km == SP::km &&
                          p.lay.off_vc == SP::vc && p.lay.off_vm == SP::vm;
   auto kern = std_shape ? quantize_pages_kernel<BK, BV, can_std> : quantize_pages_kernel<BK, BV, false>;
+  const size_t smem = std_shape ? quant_smem(p.R, p.D, p.G, 0).total : quantize_smem_bytes(p.R, p.D, p.G, p.lay);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)n_pages, (unsigned)p.n_units);

@@ -22,11 +22,13 @@ namespace {
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 __device__ __forceinline__ uint16_t f2h(float f) { return __half_as_ushort(__float2half_rn(f)); }
 
-// Per-group quantizer: fp32 zero point and scale as stored (fp16 widened), the
-// reciprocal of the scale, and the two fp16 bit patterns (zero low, scale high).
-struct __align__(16) GroupQ {
-  float zf, sf, inv;
+// Per-group quantizer: the reciprocal of the scale and the two fp16 bit patterns (zero point low,
+// scale high); the zero point and scale as stored are widened from the bits where they are used.
+struct __align__(8) GroupQ {
+  float inv;
   uint32_t bits;
+  __device__ __forceinline__ float zf() const { return h2f((uint16_t)(bits & 0xFFFFu)); }
+  __device__ __forceinline__ float sf() const { return h2f((uint16_t)(bits >> 16)); }
 };
 
 // Zero point and scale of a group from its exact min and max.
@@ -37,9 +39,8 @@ __device__ __forceinline__ GroupQ group_params(float mn, float mx, int L) {
   if (!(range > 0.0f)) range = 0.0f;
   const float s32 = __fdiv_rn(range, (float)L);
   const uint16_t zb = f2h(mn), sb = f2h(s32);
-  g.zf = h2f(zb);
-  g.sf = h2f(sb);
-  g.inv = g.sf > 0.0f ? __frcp_rn(g.sf) : 0.0f;
+  const float sf = h2f(sb);
+  g.inv = sf > 0.0f ? __frcp_rn(sf) : 0.0f;
   g.bits = (uint32_t)zb | ((uint32_t)sb << 16);
   return g;
 }
@@ -48,12 +49,12 @@ __device__ __forceinline__ GroupQ group_params(float mn, float mx, int L) {
 // quotient is taken only when some lane of the warp is within 2^-14 of a half-integer (about one
 // warp step in 300), so the warp pays one vote instead of a divergent branch per code.
 __device__ __forceinline__ uint32_t quant_code(float x, const GroupQ& g, int L) {
-  const float d = __fsub_rn(x, g.zf);
+  const float d = __fsub_rn(x, g.zf());
   float r = __fmul_rn(d, g.inv);
   const float frac = r - floorf(r);
   const bool near = fabsf(frac - 0.5f) <= 0x1.0p-14f;
   if (__any_sync(__activemask(), near)) {
-    if (near) r = __fdiv_rn(d, g.sf);  // near a rounding tie: the exact quotient (s > 0 here)
+    if (near) r = __fdiv_rn(d, g.sf());  // near a rounding tie: the exact quotient (s > 0 here)
   }
   float q = rintf(r);
   q = fminf(fmaxf(q, 0.0f), (float)L);
@@ -67,8 +68,9 @@ __device__ __forceinline__ uint32_t quant_code(float x, const GroupQ& g, int L) 
 // level.  thr == nullptr selects the uniform quantizer.
 __device__ __forceinline__ uint32_t code_of(float x, const GroupQ& g, int L, const float* thr) {
   if (!thr) return quant_code(x, g, L);
-  if (g.sf == 0.0f) return 0;
-  const float y = __fdiv_rn(__fsub_rn(x, g.zf), g.sf);
+  const float sf = g.sf();
+  if (sf == 0.0f) return 0;
+  const float y = __fdiv_rn(__fsub_rn(x, g.zf()), sf);
   uint32_t c = 0;
   for (int j = 0; j < L; ++j) c += y > thr[j] ? 1u : 0u;
   return c;
