@@ -108,8 +108,9 @@ struct Shape {
   static constexpr bool FAST_K = HG == 1 && !ROPE && (BK == 2 || BK == 4);
   static constexpr bool FAST_V = HG == 1 && (BV == 2 || BV == 4);
   static constexpr int KBITS_FAST = (BK == 2 || BK == 4) ? BK : 2;
-  // warps of the one CTA per SM: as many as the register budget of the path allows
-  static constexpr int WARPS = ROPE ? (HG == 1 ? 12 : 8) : (HG == 4 ? 8 : 16);
+  // warps of the one CTA per SM: as many as the register budget of the path allows (keys
+  // rotated at decode need about 255 registers: at 168, one head per kv head spilled 1.4 KB)
+  static constexpr int WARPS = ROPE ? 8 : (HG == 4 ? 8 : 16);
 };
 
 // Extract N codes of BITS bits starting at bit `bit0` of a token record held
