@@ -35,7 +35,11 @@ namespace kvq {
 
 namespace {
 
-constexpr int kMmaWarps = 16;
+// Warps of the one CTA per SM: 16 at 128 registers, except with four query heads per kv head,
+// which hold more per lane (B fragments, softmax state per head) and spilled at 128: they take
+// 12 warps at up to 168 registers.
+template <int HG>
+__host__ __device__ constexpr int mma_warps() { return HG == 4 ? 12 : 16; }
 constexpr int kMmaMaxStages = 16;
 constexpr unsigned kAll = 0xffffffffu;
 constexpr float kLazy = 8.0f;  // the running maximum moves only when a score passes it by 8 (log2 units)
@@ -76,8 +80,8 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
 }
 
 template <int BK, int BV, int HG, bool STD>
-__global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const DecodeParams p) {
-  constexpr int D = kHeadDim, W = kMmaWarps;
+__global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(const DecodeParams p) {
+  constexpr int D = kHeadDim, W = mma_warps<HG>();
   constexpr int NCOL = 2 * HG;   // B columns per value group: (head, high/low)
   constexpr int GPB = 8 / NCOL;  // value groups per B fragment
   constexpr int NBM = (D / 32 + GPB - 1) / GPB;  // B fragments per value tile at most (G = 32)
@@ -699,7 +703,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) decode_mma_kernel(const Dec
 // Per-warp buffers in dynamic shared memory (bytes per CTA): query rows and key B fragments.
 template <int HG>
 constexpr size_t warp_bufs_bytes() {
-  return (size_t)kMmaWarps * (HG * kHeadDim * sizeof(float) + 2 * HG * 4 * 16 * sizeof(uint32_t));
+  return (size_t)mma_warps<HG>() * (HG * kHeadDim * sizeof(float) + 2 * HG * 4 * 16 * sizeof(uint32_t));
 }
 
 // Page stages of one CTA: the largest power of two up to kMmaMaxStages whose pages fit the
@@ -737,7 +741,7 @@ cudaError_t launch_mma_t(const DecodeParams& p, int grid, cudaStream_t s) {
   auto kern = std_shape ? decode_mma_kernel<BK, BV, HG, true> : decode_mma_kernel<BK, BV, HG, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, (unsigned)grid, kMmaWarps * 32, smem, s, q);
+  return launch_pdl(kern, (unsigned)grid, mma_warps<HG>() * 32, smem, s, q);
 }
 
 template <int BK, int BV, int HG>
@@ -751,7 +755,7 @@ int resident_mma_t(int page_bytes) {
                            (int)smem) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kMmaWarps * 32, smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, mma_warps<HG>() * 32, smem) != cudaSuccess) return 0;
   return n;
 }
 
@@ -768,7 +772,7 @@ bool decode_mma_supported(int bk, int bv, int hg) {
 }
 
 int decode_mma_resident(int bk, int bv, int hg, int page_bytes, int* warps) {
-  *warps = kMmaWarps;
+  *warps = hg == 4 ? mma_warps<4>() : mma_warps<1>();
 #define KVQ_MR(BKV, BVV, HGV) \
   if (bk == BKV && bv == BVV && hg == HGV) return resident_mma_t<BKV, BVV, HGV>(page_bytes);
   KVQ_MMA_CASES(KVQ_MR)
