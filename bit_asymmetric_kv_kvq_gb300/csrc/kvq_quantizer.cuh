@@ -47,16 +47,17 @@ __device__ __forceinline__ GroupQ group_params(float mn, float mx, int L) {
 
 // Branch-free in the common case: a zero step has inv = 0, so r = 0 and the code is 0; the exact
 // quotient is taken only when some lane of the warp is within 2^-14 of a half-integer (about one
-// warp step in 300), so the warp pays one vote instead of a divergent branch per code.
+// warp step in 300), so the warp pays one vote instead of a divergent branch per code.  "Within
+// 2^-14 of a half-integer" is |r - rint(r)| >= 1/2 - 2^-14; the difference is exact (r and its
+// rounding are within a factor of two of each other, or the rounding is 0).
 __device__ __forceinline__ uint32_t quant_code(float x, const GroupQ& g, int L) {
   const float d = __fsub_rn(x, g.zf());
-  float r = __fmul_rn(d, g.inv);
-  const float frac = r - floorf(r);
-  const bool near = fabsf(frac - 0.5f) <= 0x1.0p-14f;
-  if (__any_sync(__activemask(), near)) {
-    if (near) r = __fdiv_rn(d, g.sf());  // near a rounding tie: the exact quotient (s > 0 here)
-  }
+  const float r = __fmul_rn(d, g.inv);
   float q = rintf(r);
+  const bool near = fabsf(__fsub_rn(r, q)) >= 0.5f - 0x1.0p-14f;
+  if (__any_sync(__activemask(), near)) {
+    if (near) q = rintf(__fdiv_rn(d, g.sf()));  // near a rounding tie: the exact quotient (s > 0 here)
+  }
   q = fminf(fmaxf(q, 0.0f), (float)L);
   return (uint32_t)q;
 }
