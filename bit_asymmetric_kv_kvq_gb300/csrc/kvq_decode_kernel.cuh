@@ -21,7 +21,7 @@
 //    refills it (no warp is set aside to issue copies).
 //  * Merge.  Each warp writes one unnormalised partial (m, l, acc[D]) per
 //    query head for every unit it touched.  A small kernel launched right
-//    after (one warp per unit) combines a unit's partials with log-sum-exp
+//    after (one CTA per unit) combines a unit's partials with log-sum-exp
 //    weights and writes the fp16 output; merging inside the decode launch put
 //    chains of L2 round trips at the end of every CTA's slice.
 //

@@ -219,8 +219,9 @@ kvq_status kvq_reset(kvq_cache* cache);
  * Errors: KVQ_ERR_INVALID_ARG (nulls, misalignment, Tq/R > pages_per_unit),
  * KVQ_ERR_UNSUPPORTED, and KVQ_ERR_CAPACITY when even the smallest launch's
  * partials do not fit the 8 MiB array: B*Hq*(D+2)*4 bytes per partial slot,
- * 3*W slots per query head for a one-CTA launch (W = 16 warps for one query
- * head per kv head, 8 for four), plus two counters per unit.  Larger sizes run
+ * 3*W slots per query head for a one-CTA launch (W = warps of one decode CTA:
+ * 16 on the tensor-core kernel, 12 there with four query heads per kv head; 8
+ * to 16 on the CUDA-core kernel), plus two counters per unit.  Larger sizes run
  * on fewer CTAs than the GPU holds, as many as the array allows.  The device is the current one.  The first call on a device looks up
  * the array's address once (a runtime symbol lookup), so make that first call
  * before any stream capture.  Every call shares the one array: it clears the
