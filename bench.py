@@ -53,19 +53,20 @@ UNIT = "KV tokens/s"
 
 
 def parse_args(argv=None):
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--layers", type=int, default=4)
-    ap.add_argument("--workload", type=int, default=1)
+    ap = argparse.ArgumentParser(description="Decode-attention throughput of the quantized KV cache (one JSON line).")
+    ap.add_argument("--gpus", type=int, default=1, help="GPUs (one process each under torchrun; replicas)")
+    ap.add_argument("--steps", type=int, default=100, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=3, help="untimed warm-up steps (at least 3)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
+                    help="the CUDA library, or the CPU oracle on a bounded sample")
+    ap.add_argument("--layers", type=int, default=4, help="layer caches visited in turn per step")
+    ap.add_argument("--workload", type=int, default=1, help="index into synth.WORKLOADS")
     ap.add_argument("--graph", type=int, default=1, help="replay each step as one CUDA graph (1) or call directly (0)")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=10, help="steps timed end to end from pinned host buffers")
     ap.add_argument("--timing-steps", type=int, default=3, help="extra direct-call steps timed per decode launch")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
     ap.add_argument("--sink", type=int, default=0, help="attention-sink tokens kept fp16 (0: none)")
     ap.add_argument("--codebook", action="store_true",
                     help="non-uniform levels (cosine-spaced, denser at the group's ends) for keys and values")
