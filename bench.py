@@ -15,8 +15,9 @@ value  = KV tokens attended per second over the whole step (sum over decodes
 e2e    = the same metric through the public C-ABI calls with the inputs in
          pinned host memory: every step copies its prefill inputs, appended
          tokens and queries host->device and reads every output back.  The
-         prefill inputs go through a copy stream into two device buffers, so
-         the copy of the next layer's prompt overlaps the current compute.
+         copies run on streams of their own into one device buffer per layer
+         (and one per step for the decode inputs), so the next step's copies
+         overlap the current step's compute.
 roofline: the dominant kernel (decode attention) against the measured HBM
          copy bandwidth: algorithmic bytes per call (packed codes + scales
          and zero points + fp16 window + q + out + the new token's window
@@ -472,14 +473,21 @@ def run_e2e(args, w, dist, caches, stream):
     hvn = pin(V[:, :, T0:T0 + S].transpose(2, 0, 1, 3))
     hq = pin(np.stack([synth.queries(w, i) for i in range(S)]))
     hout = torch.empty((L, S) + tuple(hq.shape[1:]), dtype=torch.float16).pin_memory()
-    # prefill inputs arrive on a copy stream into two device buffers, so that copying layer l + 1's
-    # (or the next step's) prompt overlaps the compute of the layers before it; every byte is still
-    # copied inside the timed region, and the compute stream waits for each copy it uses
+    # Copies run on streams of their own and overlap the compute; every byte is still copied inside
+    # the timed region, and the compute stream waits for each copy it uses.  Every layer has its own
+    # device buffer for its prompt, so all of the next step's prompts can stream in while this step
+    # decodes.  A step's decode inputs (new keys, new values, queries of all its decode steps) arrive
+    # in one transfer each on a stream of their own, before the decodes that read them: small copies
+    # issued on the compute stream between decode launches would sit in the copy queue ahead of the
+    # next step's prompts.
+    nbuf = L
     copy_streams = [torch.cuda.Stream(dev) for _ in range(COPY_STREAMS)]
-    dk = [torch.empty_like(hk, device=dev) for _ in range(2)]
-    dv = [torch.empty_like(hv, device=dev) for _ in range(2)]
-    copied = [[torch.cuda.Event() for _ in copy_streams] for _ in range(2)]
-    used = [torch.cuda.Event() for _ in range(2)]
+    dec_stream = torch.cuda.Stream(dev)
+    dk = [torch.empty_like(hk, device=dev) for _ in range(nbuf)]
+    dv = [torch.empty_like(hv, device=dev) for _ in range(nbuf)]
+    copied = [[torch.cuda.Event() for _ in copy_streams] for _ in range(nbuf)]
+    used = [torch.cuda.Event() for _ in range(nbuf)]
+    dec_copied, dec_used = torch.cuda.Event(), torch.cuda.Event()
     # the batch dimension is split across the copy streams: each takes whole sequences
     parts = np.array_split(np.arange(hk.shape[0]), len(copy_streams))
     dkn = torch.empty_like(hkn, device=dev)
@@ -492,7 +500,7 @@ def run_e2e(args, w, dist, caches, stream):
     def step():
         nonlocal h2d, d2h
         for l, c in enumerate(caches):
-            b = l % 2
+            b = l % nbuf
             for cs, part, ev in zip(copy_streams, parts, copied[b]):
                 if len(part) == 0:
                     continue
@@ -507,13 +515,18 @@ def run_e2e(args, w, dist, caches, stream):
             c.reset()
             c.prefill_quantize(dk[b], dv[b], stream=stream)
             used[b].record(stream)
+        dec_stream.wait_event(dec_used)  # the previous step's decodes have read the decode inputs
+        with torch.cuda.stream(dec_stream):
+            dkn.copy_(hkn, non_blocking=True)
+            dvn.copy_(hvn, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+        dec_copied.record(dec_stream)
+        h2d += hkn.nbytes + hvn.nbytes + hq.nbytes
+        stream.wait_event(dec_copied)
         for i in range(S):
-            dkn[i].copy_(hkn[i], non_blocking=True)
-            dvn[i].copy_(hvn[i], non_blocking=True)
-            dq[i].copy_(hq[i], non_blocking=True)
-            h2d += hkn[i].nbytes + hvn[i].nbytes + hq[i].nbytes
             for l, c in enumerate(caches):
                 c.decode_step(dkn[i], dvn[i], dq[i], dout[l, i], stream=stream)
+        dec_used.record(stream)
         hout.copy_(dout, non_blocking=True)
         d2h += hout.nbytes
 
@@ -524,7 +537,7 @@ def run_e2e(args, w, dist, caches, stream):
         dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for cs in copy_streams:
+        for cs in copy_streams + [dec_stream]:
             cs.wait_event(e0)  # no copy of the timed steps starts before the clock does
         for _ in range(args.e2e_steps):
             step()
