@@ -33,7 +33,6 @@ from __future__ import annotations
 import argparse
 import dataclasses
 import json
-import math
 import os
 import statistics
 import tempfile
@@ -462,7 +461,6 @@ COPY_STREAMS = 4  # host->device copy streams for the prefill inputs (several co
 def run_e2e(args, w, dist, caches, stream):
     import torch
 
-    import bit_asymmetric_kv_kvq_gb300 as kvq
     dev = torch.device(f"cuda:{dist.local_rank}")
     T0, S, L = w.prefill_tokens, w.decode_steps, len(caches)
     K = synth.keys(w)
