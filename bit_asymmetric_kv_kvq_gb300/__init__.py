@@ -6,11 +6,12 @@ is its Python binding.
 """
 from .kvq import (KVCache, KVQError, kvq_append, kvq_config, kvq_create, kvq_decode_attention, kvq_decode_step,
                   kvq_destroy,
-                  kvq_export_unit, kvq_get_splits, kvq_get_state, kvq_launch_count, kvq_prefill_quantize,
-                  kvq_reset, kvq_set_codebooks, kvq_set_splits, kvq_sync_status, lib, make_config, status_string)
+                  kvq_export_unit, kvq_get_splits, kvq_get_state, kvq_launch_count, kvq_page_layout,
+                  kvq_prefill_quantize, kvq_reset, kvq_set_codebooks, kvq_set_splits, kvq_sync_status, lib, make_config, status_string)
 
 __all__ = ["KVCache", "KVQError", "kvq_append", "kvq_config", "kvq_create", "kvq_decode_attention", "kvq_decode_step",
            "kvq_destroy",
-           "kvq_export_unit", "kvq_get_splits", "kvq_get_state", "kvq_launch_count", "kvq_prefill_quantize",
+           "kvq_export_unit", "kvq_get_splits", "kvq_get_state", "kvq_launch_count", "kvq_page_layout",
+           "kvq_prefill_quantize",
            "kvq_reset", "kvq_set_codebooks", "kvq_set_splits", "kvq_sync_status", "lib", "make_config",
            "status_string"]

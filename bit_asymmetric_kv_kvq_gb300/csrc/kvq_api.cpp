@@ -318,6 +318,25 @@ extern "C" {
 
 int32_t kvq_version(void) { return (1 << 16) | 0; }
 
+kvq_status kvq_page_layout(const kvq_config* cfg, kvq_page_info* info) {
+  if (!cfg || !info) return KVQ_ERR_INVALID_ARG;
+  const kvq_status st = validate(*cfg);
+  if (st != KVQ_OK) return st;
+  // the layout kvq_create gives the cache's pages
+  const kvq::PageLayout l = kvq::make_layout(cfg->residual, cfg->head_dim, cfg->group_size, cfg->k_bits, cfg->v_bits,
+                                             cfg->k_sparse, cfg->rope != 0, cfg->codebook != 0);
+  info->page_bytes = l.bytes;
+  info->kcodes_offset = l.off_kc;
+  info->kmeta_offset = l.off_km;
+  info->vcodes_offset = l.off_vc;
+  info->vmeta_offset = l.off_vm;
+  info->sp_idx_offset = l.off_si;
+  info->sp_val_offset = l.off_sv;
+  info->tokens_per_page = cfg->residual;
+  info->fragment_order = l.frag;
+  return KVQ_OK;
+}
+
 const char* kvq_status_string(kvq_status s) {
   switch (s) {
     case KVQ_OK: return "ok";

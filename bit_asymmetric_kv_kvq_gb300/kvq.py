@@ -53,6 +53,12 @@ class kvq_unit_view(ctypes.Structure):
                [("sk", ctypes.c_void_p), ("sv", ctypes.c_void_p), ("sink_bytes", ctypes.c_int64)]
 
 
+class kvq_page_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("page_bytes", "kcodes_offset", "kmeta_offset", "vcodes_offset",
+                                              "vmeta_offset", "sp_idx_offset", "sp_val_offset")] + \
+               [("tokens_per_page", ctypes.c_int32), ("fragment_order", ctypes.c_int32)]
+
+
 _P = ctypes.c_void_p
 _lock = threading.Lock()
 _lib = None
@@ -79,6 +85,7 @@ SIGNATURES = {
     "kvq_launch_count": (ctypes.c_int64, [_P]),
     "kvq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kvq_version": (ctypes.c_int32, []),
+    "kvq_page_layout": (ctypes.c_int, [ctypes.POINTER(kvq_config), ctypes.POINTER(kvq_page_info)]),
     "kvq_axis_quantize": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]),
     "kvq_axis_dequantize": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
@@ -152,6 +159,13 @@ def kvq_create(cfg: kvq_config, device: int = 0) -> int:
     h = _P()
     _check(lib().kvq_create(ctypes.byref(cfg), device, ctypes.byref(h)), "kvq_create")
     return h.value
+
+
+def kvq_page_layout(cfg: kvq_config) -> dict:
+    """Byte layout of one page of a configuration (host arithmetic, no GPU needed)."""
+    info = kvq_page_info()
+    _check(lib().kvq_page_layout(ctypes.byref(cfg), ctypes.byref(info)), "kvq_page_layout")
+    return {n: getattr(info, n) for n, _ in kvq_page_info._fields_}
 
 
 def kvq_destroy(handle) -> None:

@@ -233,6 +233,35 @@ kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const void* pages
                                         const void* window_k, const void* window_v, int64_t n_tokens,
                                         const void* q_f16, void* out_f16, void* cuda_stream);
 
+/*
+ * Page layout of a configuration, for callers that build or size the packed
+ * pages themselves (kvq_decode_attention_noalloc takes them in this layout).
+ * Host arithmetic only: no CUDA call, no device needed.  One page holds R
+ * tokens of one (batch, kv head) unit; its sections are those listed for
+ * kvq_decode_attention_noalloc, in that order, each padded to a multiple of
+ * 16 bytes; every offset is in bytes from the start of the page.
+ *   page_bytes      bytes of one page (the stride of pages within a unit)
+ *   kcodes_offset   key codes, R*D*k_bits/8 bytes
+ *   kmeta_offset    key zero point / scale, [R/G][D] u32
+ *   vcodes_offset   value codes, R*D*v_bits/8 bytes
+ *   vmeta_offset    value zero point / scale, [R][D/G] u32
+ *   sp_idx_offset   sparse key channels, [R][k_sparse] u8
+ *   sp_val_offset   sparse key values, [R][k_sparse] fp16
+ *   tokens_per_page R
+ *   fragment_order  1: both code sections in tensor-core fragment order,
+ *                   0: token-major bitstreams
+ * Errors: KVQ_ERR_INVALID_ARG (null pointer, or a configuration kvq_create
+ * refuses as invalid), KVQ_ERR_UNSUPPORTED (one it refuses as unsupported).
+ */
+typedef struct {
+  int64_t page_bytes;
+  int64_t kcodes_offset, kmeta_offset, vcodes_offset, vmeta_offset, sp_idx_offset, sp_val_offset;
+  int32_t tokens_per_page;
+  int32_t fragment_order;
+} kvq_page_info;
+
+kvq_status kvq_page_layout(const kvq_config* cfg, kvq_page_info* info);
+
 /* ---------------- helpers (not on the hot path) ---------------- */
 
 /* Host-tracked state: tokens cached, tokens quantized (Tq), tokens in the window. */

@@ -106,3 +106,40 @@ def test_axis_calls_check_arguments_on_the_host(kvq):
     assert L.kvq_axis_dequantize(p, p, p, 0, 64, 128, 32, 0, p, None) == -1
     assert L.kvq_axis_attention(p, p, 1, p, 1, 3, 64, 128, 0.1, None, p, None) == -2  # heads per unit
     assert L.kvq_axis_attention(p, p, 1, p, 1, 1, 64, 128, 0.0, None, p, None) == -1  # scale
+
+
+def _r16(x):
+    return (x + 15) // 16 * 16
+
+
+@pytest.mark.parametrize("bk,bv,G,R,nsp,rope,cb", [
+    (2, 2, 32, 128, 0, 0, 0), (4, 2, 32, 128, 0, 0, 0), (4, 4, 64, 128, 0, 0, 0), (3, 3, 64, 128, 2, 1, 0),
+    (2, 2, 32, 64, 1, 0, 0), (3, 3, 32, 96, 3, 0, 0), (2, 2, 32, 128, 0, 1, 0), (4, 4, 32, 128, 0, 0, 1),
+])
+def test_page_layout_on_the_host(kvq, bk, bv, G, R, nsp, rope, cb):
+    """kvq_page_layout: the sections the header lists, in order, each padded to 16 bytes; fragment
+    order exactly for 2/4-bit codes with keys stored after RoPE and uniform levels."""
+    hg = 4 if (rope or cb) and (bk, bv) == (3, 3) else 1
+    cfg = kvq.make_config(2, 2, 2 * hg, 128, 4096, bk, bv, G, R, k_sparse=nsp, rope=rope, codebook=cb)
+    lay = kvq.kvq.kvq_page_layout(cfg)
+    D = 128
+    sizes = [R * D * bk // 8, (R // G) * D * 4, R * D * bv // 8, R * (D // G) * 4, R * nsp, R * nsp * 2]
+    offs = [lay[k] for k in ("kcodes_offset", "kmeta_offset", "vcodes_offset", "vmeta_offset", "sp_idx_offset",
+                             "sp_val_offset")] + [lay["page_bytes"]]
+    assert offs[0] == 0
+    for i, n in enumerate(sizes):
+        assert offs[i + 1] - offs[i] == _r16(n), (i, offs, sizes)
+    assert lay["tokens_per_page"] == R
+    assert lay["fragment_order"] == int(bk in (2, 4) and bv in (2, 4) and not rope and not cb)
+
+
+def test_page_layout_errors(kvq):
+    L = kvq.lib()
+    cfg = kvq.make_config(1, 1, 1, 128, 16, 2, 2, 32, 128)
+    info = kvq.kvq.kvq_page_info()
+    assert L.kvq_page_layout(None, ctypes.byref(info)) == -1
+    assert L.kvq_page_layout(ctypes.byref(cfg), None) == -1
+    cfg.k_bits = 5
+    assert L.kvq_page_layout(ctypes.byref(cfg), ctypes.byref(info)) == -1
+    cfg.k_bits, cfg.head_dim = 2, 64
+    assert L.kvq_page_layout(ctypes.byref(cfg), ctypes.byref(info)) == -2
