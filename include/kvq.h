@@ -251,7 +251,9 @@ kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const void* pages
  *   fragment_order  1: both code sections in tensor-core fragment order,
  *                   0: token-major bitstreams
  * Errors: KVQ_ERR_INVALID_ARG (null pointer, or a configuration kvq_create
- * refuses as invalid), KVQ_ERR_UNSUPPORTED (one it refuses as unsupported).
+ * refuses as invalid), KVQ_ERR_UNSUPPORTED (a valid configuration this build
+ * does not implement).  kvq_create also checks the device's limits (shared
+ * memory, resident CTAs), which this call, having no device, does not.
  */
 typedef struct {
   int64_t page_bytes;
