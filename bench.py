@@ -1,32 +1,37 @@
 #!/usr/bin/env python
-"""Benchmark: decode-attention KV tokens/s on the Llama-2-7B-shaped 2-bit layer.
+"""Benchmark: decode-attention KV tokens/s of the 2-bit quantized KV cache (one JSON line).
 
-Workload (one step): for each of L layer caches (default 4) of the
-Llama-2-7B-shaped layer (B=8, 32 KV = 32 query heads, D=128, K2V2, G=32,
-R=128): prefill 4096 tokens (quantize-and-pack), then 64 fused decode steps
-(kvq_decode_step): each appends one token and runs decode attention over the
-whole cache in one launch (the first one flushes the full fp16 window into a
-page before it).  Layers are visited
-in turn inside each decode step, as a model does, so the 101-109 MB cache of
-one layer is never L2-resident when it is read again (4 caches > 129 MB L2).
+Default workload: the Llama-3-8B-shaped GQA layer (B=32, 8 KV / 32 query heads,
+D=128, context 32768, K2V2, G=32, R=128), the largest 2-bit workload.  One step,
+for each of L layer caches (default 4): a full prefill quantize-and-pack of the
+32768-token prompt, then the workload's fused decode steps (kvq_decode_step:
+append one token, flushing the full fp16 window into a page first, then decode
+attention over the whole cache).  Every layer reads a 4.3 GB prompt and its own
+805 MB cache, so nothing a kernel reads is L2-resident (L2 is 129 MB).  The other
+workloads run with --workload N (N = 0..4).
 
-value  = KV tokens attended per second over the whole step (sum over decodes
-         of B*T, T = 4097..4160), inputs resident in HBM.
-e2e    = the same metric through the public C-ABI calls with the inputs in
-         pinned host memory: every step copies its prefill inputs, appended
-         tokens and queries host->device and reads every output back.  The
-         copies run on streams of their own into one device buffer per layer
-         (and one per step for the decode inputs), so the next step's copies
-         overlap the current step's compute.
-roofline: the dominant kernel (decode attention) against the measured HBM
-         copy bandwidth: algorithmic bytes per call (packed codes + scales
-         and zero points + fp16 window + q + out + the new token's window
-         store) / mean time of the decode steps that do not flush, each timed
-         with CUDA events around the whole call (the decode kernel and the
-         small kernel that merges its partials, launched back to back).
+value   = KV tokens attended per second over the whole step (sum over decodes of
+          B*T), inputs resident in HBM, one CUDA graph per step.
+decode  = the decode-attention call alone (decode kernel + the kernel merging its
+          partials), timed per call with CUDA events on the launching stream over
+          at least 50 calls that rotate over the L caches: median and p90, KV
+          tokens/s = B*T / median, and HBM GB/s of its algorithmic bytes (packed
+          codes + scales and zero points + sparse entries + fp16 window + q + out).
+prefill = the prefill call alone, timed the same way.
+roofline: the kernel that takes the larger share of the step (by the medians
+          above), against the measured HBM copy bandwidth.
+e2e     = the same metric through the public C-ABI calls with the inputs in
+          pinned host memory: every step copies its prompts, appended tokens and
+          queries host->device and reads every output back.
+cpu_baseline: the CPU oracle (the plain C reference the tests check against) on
+          a bounded sample of the same workload, on one thread and on every host
+          core (one process per core, each over its own (sequence, kv head) units).
 
-`--impl reference` times the CPU oracle (the plain fp64/fp32 C reference the
-tests check against) on a bounded sample of the same workload.
+After the timed region one sampled (sequence, kv head) unit of the last step is
+checked against the oracle: its packed stores bit for bit and its attention
+output within 2e-3.
+
+`--impl reference` times the CPU oracle on every host core, step by step.
 """
 from __future__ import annotations
 
@@ -35,9 +40,9 @@ import dataclasses
 import json
 import os
 import statistics
-import tempfile
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -50,6 +55,7 @@ import synth  # noqa: E402
 
 METRIC = "decode-attention KV tokens/s and HBM GB/s (% of GB300 roofline) at 2-bit"
 UNIT = "KV tokens/s"
+DEFAULT_WORKLOAD = 3
 
 
 def parse_args(argv=None):
@@ -60,13 +66,17 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
                     help="the CUDA library, or the CPU oracle on a bounded sample")
     ap.add_argument("--layers", type=int, default=4, help="layer caches visited in turn per step")
-    ap.add_argument("--workload", type=int, default=1, help="index into synth.WORKLOADS")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, help="index into synth.WORKLOADS")
     ap.add_argument("--graph", type=int, default=1, help="replay each step as one CUDA graph (1) or call directly (0)")
-    ap.add_argument("--e2e-steps", type=int, default=10, help="steps timed end to end from pinned host buffers")
-    ap.add_argument("--timing-steps", type=int, default=3, help="extra direct-call steps timed per decode launch")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    ap.add_argument("--e2e-steps", type=int, default=5, help="steps timed end to end from pinned host buffers")
+    ap.add_argument("--decode-calls", type=int, default=64, help="decode-attention calls timed one by one (>= 50)")
+    ap.add_argument("--prefill-calls", type=int, default=12, help="prefill calls timed one by one")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0, help="oracle time of each CPU-baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-self-check", action="store_true", help="skip the post-timing check against the oracle")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (small profiling cases)")
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's prompt length")
     ap.add_argument("--sink", type=int, default=0, help="attention-sink tokens kept fp16 (0: none)")
     ap.add_argument("--codebook", action="store_true",
                     help="non-uniform levels (cosine-spaced, denser at the group's ends) for keys and values")
@@ -83,12 +93,23 @@ def codebook_levels(bits):
 
 def workload_of(args):
     w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.scaled(batch=args.batch, name=w.name + f" (batch {args.batch})")
+    if args.tokens:
+        w = w.scaled(prefill_tokens=args.tokens, name=w.name + f" (prompt {args.tokens})")
     if args.sink:
         w = w.scaled(sink=args.sink)
     if args.codebook:
         w = dataclasses.replace(w, k_levels=tuple(codebook_levels(w.k_bits).tolist()),
                                 v_levels=tuple(codebook_levels(w.v_bits).tolist()))
     return w
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -156,6 +177,18 @@ def decode_step_bytes(w, T):
     return decode_bytes(w, T) + w.batch * w.kv_heads * w.head_dim * 4
 
 
+def prefill_bytes(w, T0):
+    """Algorithmic bytes of one prefill call: the fp16 prompt read once, the packed pages and the fp16
+    sink and window rows written (packed codes + scales and zero points + sparse entries)."""
+    D, G = w.head_dim, w.group
+    n_s = min(T0, w.sink)
+    Tq = quantized_tokens(T0 - n_s, w.residual)
+    n_r = T0 - n_s - Tq
+    written = (Tq * D * (w.k_bits + w.v_bits) // 8 + (Tq // G) * D * 4 + Tq * (D // G) * 4 + Tq * w.k_sparse * 3
+               + (n_r + n_s) * D * 4)
+    return w.batch * w.kv_heads * (T0 * D * 4 + written)
+
+
 def step_tokens(w, layers):
     T0 = w.prefill_tokens
     return layers * sum(w.batch * (T0 + i) for i in range(1, w.decode_steps + 1))
@@ -168,15 +201,24 @@ def workload_config(w, layers, graph, world):
         "batch": w.batch, "kv_heads": w.kv_heads, "q_heads": w.q_heads, "head_dim": w.head_dim,
         "prefill_tokens": w.prefill_tokens, "decode_steps": w.decode_steps,
         "k_bits": w.k_bits, "v_bits": w.v_bits, "group": w.group, "residual": w.residual,
+        **({"k_sparse": w.k_sparse} if w.k_sparse else {}),
+        **({"rope": f"keys stored pre-RoPE, rotated at decode (base {w.rope_base:g})"} if w.rope else {}),
         **({"sink_tokens": w.sink} if w.sink else {}),
         **({"codebook": "cosine-spaced levels (non-uniform)"} if w.k_levels else {}),
         "step": f"{layers} layers x (prefill {w.prefill_tokens}) + {w.decode_steps} x {layers} layers x "
-                f"fused decode step (append + decode attention, one launch)",
-        "l2": f"inputs larger than L2: {layers} layer caches of "
-              f"{decode_bytes(w, w.prefill_tokens + 1) / 1e6:.0f} MB visited in turn",
+                f"fused decode step (append, flushing a full window first, + decode attention)",
+        "l2": f"inputs larger than L2: a {prefill_bytes(w, w.prefill_tokens) / 1e9:.2f} GB prefill per layer and "
+              f"{layers} layer caches of {decode_bytes(w, w.prefill_tokens + 1) / 1e6:.0f} MB visited in turn",
         "launch": "one CUDA graph per step" if graph else "direct C-ABI calls",
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
     }
+
+
+def timing_stats(ms_list):
+    """Median, p90 and mean (ms) of per-call times."""
+    a = np.asarray(ms_list, np.float64)
+    return {"median_us": float(np.median(a)) * 1e3, "p90_us": float(np.percentile(a, 90)) * 1e3,
+            "mean_us": float(a.mean()) * 1e3, "calls": int(a.size)}
 
 
 # ------------------------------------------------------------------ clocks
@@ -203,7 +245,7 @@ class Clocks:
             self.keep = bool(keep)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -217,7 +259,7 @@ class Clocks:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], [], set()
+        sm, mx, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
@@ -228,6 +270,10 @@ class Clocks:
                 mx.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
@@ -236,22 +282,23 @@ class Clocks:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sm_mhz_min": min(sm), "sm_mhz_p10": float(np.percentile(sm, 10)),
+                **({"power_w_median": statistics.median(power)} if power else {})}
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
 
-def cpu_baseline(w, seconds):
-    """The oracle as it stands, one (sequence, kv head) unit at a time: prefill, then every decode step
-    (append + fp64 attention), until `seconds` of oracle time.  One unit is 1/Hkv of a sequence's work,
-    so it is credited with sum_i T_i / Hkv tokens, in the GPU's unit.  Input generation is not timed."""
+def _oracle_units(w, units, Q, seconds):
+    """The oracle as it stands over (sequence, kv head) units in turn -- prefill, then every decode step
+    (append + fp64 attention of the unit's query heads) -- until `seconds` of oracle time.  A unit is
+    1/Hkv of its sequence's work and is credited with sum_i T_i / Hkv tokens, in the GPU's unit.
+    Input generation is not timed."""
     import oracle
     T0, steps = w.prefill_tokens, w.decode_steps
-    Q = [synth.queries(w, i) for i in range(steps)]
     busy = 0.0
     tokens = 0.0
-    units = 0
-    for unit in range(w.batch * w.kv_heads):
+    done = 0
+    for unit in units:
         b, kvh = divmod(unit, w.kv_heads)
         K = synth.keys(w, b, 1, kvh, 1)[0, 0]
         V = synth.values(w, b, 1, kvh, 1)[0, 0]
@@ -264,12 +311,76 @@ def cpu_baseline(w, seconds):
             u.attention(Q[i][b, hs], w.softmax_scale)
             tokens += (T0 + i + 1) / w.kv_heads
         busy += time.perf_counter() - t0
-        units += 1
+        done += 1
         if busy >= seconds:
             break
-    return {"value": tokens / busy, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{units} (sequence, kv head) units x (prefill {T0} + {steps} x (append + attention)), "
-                      f"single-threaded C oracle, {busy:.1f} s"}
+    return {"tokens": tokens, "busy": busy, "units": done}
+
+
+def _oracle_worker(job):
+    """One process of the all-core leg: its own units, its own generator threads set to one."""
+    wl, units, Q, seconds = job
+    return _oracle_units(wl, units, Q, seconds)
+
+
+class OraclePool:
+    """One single-threaded oracle process per host core (spawned: no CUDA state is inherited)."""
+
+    def __init__(self, cores=None):
+        import multiprocessing as mp
+        self.cores = cores or host_cores()
+        ctx = mp.get_context("spawn")
+        env_before = os.environ.get("KVQ_SYNTH_THREADS")
+        os.environ["KVQ_SYNTH_THREADS"] = "1"  # the workers' input generation stays on their own core
+        try:
+            self.pool = ctx.Pool(self.cores)
+        finally:
+            if env_before is None:
+                os.environ.pop("KVQ_SYNTH_THREADS", None)
+            else:
+                os.environ["KVQ_SYNTH_THREADS"] = env_before
+
+    def run(self, w, Q, seconds, offset=0):
+        """Every process runs the oracle over units offset+k, offset+k+C, ... for `seconds` of oracle time;
+        the throughput is the units' tokens over the longest process's oracle time."""
+        n_units = w.batch * w.kv_heads
+        jobs = []
+        for k in range(self.cores):
+            units = [(offset + k + j * self.cores) % n_units for j in range(n_units)]
+            jobs.append((w, units, Q, seconds))
+        res = self.pool.map(_oracle_worker, jobs)
+        tokens = sum(r["tokens"] for r in res)
+        wall = max(r["busy"] for r in res)
+        return {"value": tokens / wall, "tokens": tokens, "busy_max": wall, "units": sum(r["units"] for r in res)}
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def all_queries(w):
+    return [synth.queries(w, i) for i in range(w.decode_steps)]
+
+
+def cpu_baseline(w, seconds, pool=None):
+    """The oracle timed on one thread and on every host core of this machine."""
+    T0, steps = w.prefill_tokens, w.decode_steps
+    Q = all_queries(w)
+    one = _oracle_units(w, range(w.batch * w.kv_heads), Q, seconds)
+    own = pool is None
+    pool = pool or OraclePool()
+    try:
+        allc = pool.run(w, Q, seconds)
+    finally:
+        if own:
+            pool.close()
+    work = f"(sequence, kv head) units x (prefill {T0} + {steps} x (append + fp64 attention))"
+    return {"value": allc["value"], "unit": UNIT, "cores": pool.cores, "kind": "oracle",
+            "host_cores": host_cores(),
+            "sample": f"{allc['units']} {work} on {pool.cores} single-threaded oracle processes (one per core), "
+                      f"{allc['busy_max']:.1f} s of oracle time each",
+            "single_thread": {"value": one["tokens"] / one["busy"], "unit": UNIT, "cores": 1,
+                              "sample": f"{one['units']} {work}, {one['busy']:.1f} s"}}
 
 
 # ------------------------------------------------------------------ our implementation
@@ -292,13 +403,14 @@ def run_ours(args, dist):
     # inputs (same synthetic sequence for every layer; each layer has its own cache)
     K = synth.keys(w)
     V = synth.values(w)
-    Q = np.stack([synth.queries(w, i) for i in range(S)])  # [S][B][Hq][D]
+    Q = np.stack(all_queries(w))  # [S][B][Hq][D]
     k_pre = torch.from_numpy(np.ascontiguousarray(K[:, :, :T0])).to(dev)
     v_pre = torch.from_numpy(np.ascontiguousarray(V[:, :, :T0])).to(dev)
     k_new = torch.from_numpy(np.ascontiguousarray(K[:, :, T0:T0 + S].transpose(2, 0, 1, 3))).to(dev)  # [S][B][Hkv][D]
     v_new = torch.from_numpy(np.ascontiguousarray(V[:, :, T0:T0 + S].transpose(2, 0, 1, 3))).to(dev)
     q_dev = torch.from_numpy(Q).to(dev)
     out = torch.empty((L, S, B, Hq, D), dtype=torch.float16, device=dev)
+    out_dec = torch.empty((L, B, Hq, D), dtype=torch.float16, device=dev)
     caches = [kvq.KVCache.for_workload(w, device=dist.local_rank) for _ in range(L)]
     handles = [c.handle for c in caches]
     Lb = kvq.lib()
@@ -316,19 +428,16 @@ def run_ours(args, dist):
         if st != 0:
             raise kvq.KVQError(st, what)
 
-    def step(events=None):
+    def prefill(h):
+        check(Lb.kvq_reset(h), "reset")
+        check(Lb.kvq_prefill_quantize(h, kp, vp, T0, sh), "prefill")
+
+    def step():
         for h in handles:
-            check(Lb.kvq_reset(h), "reset")
-            check(Lb.kvq_prefill_quantize(h, kp, vp, T0, sh), "prefill")
-        n = 0
+            prefill(h)
         for i in range(S):
             for l, h in enumerate(handles):
-                if events is not None:
-                    events[n][0].record(stream)
                 check(Lb.kvq_decode_step(h, knp[i], vnp[i], qp[i], op[l][i], sh), "decode step")
-                if events is not None:
-                    events[n][1].record(stream)
-                n += 1
 
     def launches():
         return sum(Lb.kvq_launch_count(h) for h in handles)
@@ -381,24 +490,59 @@ def run_ours(args, dist):
             raise RuntimeError("device-side error in the timed region")
     ms_step = dist.max(ms_total / args.steps)
 
-    # ---------------- per-launch timing of decode attention (direct calls, CUDA events on the launch stream);
-    # decode steps 1..S-1 are one launch each (step 0 also flushes the window and is left out)
-    n_dec = S * L
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dec)]
-    durs = []
-    with torch.cuda.stream(stream):
-        for _ in range(args.timing_steps):
-            step(evs)
-            torch.cuda.synchronize(dev)
-            durs.extend(a.elapsed_time(b) for a, b in evs[L:])
-    dec_ms = statistics.mean(durs) if durs else float("nan")
-    dec_bytes = statistics.mean(decode_step_bytes(w, T0 + 1 + i) for i in range(1, S))
-    import json as _json
-    peaks = _json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
-        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    # ---------------- the timed path checked against the oracle: one sampled unit of the last step
+    self_check = None
+    if not args.no_self_check:
+        self_check = check_against_oracle(w, caches[0], out[0, S - 1], K, V, Q[S - 1])
+
+    # ---------------- per-call timing (CUDA events on the launching stream), rotating over the layers:
+    # decode attention over each cache's state after the step, then the prefill
+    def per_call(n, call):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for j in range(n):
+                evs[j][0].record(stream)
+                call(j)
+                evs[j][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in evs]
+
+    T_dec = T0 + S
+    n_dec = max(args.decode_calls, 1)
+    dec_ms = per_call(n_dec, lambda j: check(Lb.kvq_decode_attention(handles[j % L], qp[S - 1],
+                                                                     out_dec[j % L].data_ptr(), sh), "decode"))
+    pre_ms = per_call(max(args.prefill_calls, 1), lambda j: prefill(handles[j % L]))
+    for h in handles:
+        if Lb.kvq_sync_status(h, sh) != 0:
+            raise RuntimeError("device-side error in the per-call timing")
+    dec = timing_stats(dec_ms)
+    pre = timing_stats(pre_ms)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
     peak = peaks.get("hbm_gbs", 6800.0)
-    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = decode_traffic(w)
+    peak_source = "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6.8 TB/s"
+    dec_b = decode_bytes(w, T_dec)
+    pre_b = prefill_bytes(w, T0)
+    dec_gbs = dec_b / (dec["median_us"] * 1e-6) / 1e9
+    pre_gbs = pre_b / (pre["median_us"] * 1e-6) / 1e9
+    kernels = {
+        "decode_attention": {
+            "bound": "hbm", "achieved": dec_gbs, "peak": peak, "unit": "GB/s", "frac": dec_gbs / peak,
+            "traffic": kernel_traffic("decode", w), "bytes_per_call": dec_b, **dec, "tokens_attended": T_dec,
+            "kernel": "decode attention call: decode kernel + merge_kernel (programmatic dependent launch)"},
+        "prefill": {
+            "bound": "hbm", "achieved": pre_gbs, "peak": peak, "unit": "GB/s", "frac": pre_gbs / peak,
+            "traffic": kernel_traffic("prefill", w), "bytes_per_call": pre_b, **pre,
+            "kernel": "prefill call: quantize_pages_kernel + copy_tokens_kernel (window tail)"},
+    }
+    # the dominant kernel: the larger share of the step
+    share_pre = L * pre["median_us"]
+    share_dec = L * S * dec["median_us"]
+    dom = "prefill" if share_pre >= share_dec else "decode_attention"
+    roof = dict(kernels[dom])
+    roof["name"] = dom
+    roof["peak_source"] = peak_source
+    roof["step_share"] = (share_pre if dom == "prefill" else share_dec) / (ms_step * 1e3)
 
     # ---------------- end to end through the C ABI from pinned host memory
     e2e = run_e2e(args, w, dist, caches, stream) if args.e2e_steps > 0 else None
@@ -410,49 +554,85 @@ def run_ours(args, dist):
         c.close()
     return {
         "value": value, "ms_per_step": ms_step, "gpu_launches": int(n_launch),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": "decode attention call: decode_mma_kernel (tensor cores) + merge_kernel",
-                     "bytes_per_launch": dec_bytes, "ms_per_launch": dec_ms,
-                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6.8 TB/s"},
-        "decode_only": {"value": B * statistics.mean(T0 + 1 + i for i in range(1, S)) / (dec_ms * 1e-3),
-                        "unit": UNIT, "ms_per_launch": dec_ms},
-        "clocks": clock_info, "e2e": e2e,
+        "roofline": roof,
+        "decode_only": {"value": B * T_dec / (dec["median_us"] * 1e-6), "unit": UNIT,
+                        "hbm_gbs": dec_gbs, "frac": dec_gbs / peak, **dec},
+        "kernels": kernels,
+        "clocks": clock_info, "e2e": e2e, "self_check": self_check,
         "config": workload_config(w, L, graph is not None, dist.world),
     }
 
 
-DECODE_SOURCES = ("kvq_decode_mma.cu", "kvq_merge.cuh", "kvq_ptx.cuh", "kvq_internal.h")
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "decode_mma_kernel_traffic.txt")
+def check_against_oracle(w, cache, out_last, K, V, q_last):
+    """One sampled unit of the timed path against the oracle: stores bit for bit, attention within 2e-3."""
+    import oracle
+    T0, S = w.prefill_tokens, w.decode_steps
+    rng = np.random.default_rng(1234)
+    b = int(rng.integers(w.batch))
+    kvh = int(rng.integers(w.kv_heads))
+    u = oracle.OracleUnit.for_workload(w)
+    u.prefill(K[b, kvh, :T0], V[b, kvh, :T0])
+    for i in range(S):
+        u.append(K[b, kvh, T0 + i], V[b, kvh, T0 + i])
+    got = cache.export_unit(b, kvh)
+    ref = u.stores()
+    stores_equal = all(np.array_equal(got[k], ref[k]) for k in ref)
+    hs = slice(kvh * w.group_q, (kvh + 1) * w.group_q)
+    o_ref = u.attention(q_last[b, hs], w.softmax_scale)
+    o = out_last.float().cpu().numpy()[b, hs].astype(np.float64)
+    err = oracle.max_rel_err(o, o_ref)
+    ok = bool(stores_equal and err <= 2e-3)
+    if not ok:
+        raise RuntimeError(f"self-check failed on unit (b={b}, kvh={kvh}): stores equal {stores_equal}, "
+                           f"attention error {err:.3e}")
+    return {"unit": [b, kvh], "stores_bit_exact": stores_equal, "attention_max_rel_err": err, "ok": ok}
 
 
-def kernel_revision():
-    """Hash of the decode kernel's sources: DRAM counters are valid only for the kernel they were taken on."""
+KERNEL_SOURCES = {
+    "decode": ("kvq_decode_mma.cu", "kvq_decode_kernel.cuh", "kvq_decode.cu", "kvq_merge.cuh", "kvq_ptx.cuh",
+               "kvq_internal.h"),
+    "prefill": ("kvq_quant.cu", "kvq_quantizer.cuh", "kvq_ptx.cuh", "kvq_internal.h"),
+}
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+def kernel_revision(kind):
+    """Hash of a kernel's sources: DRAM counters are valid only for the kernel they were taken on."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_asymmetric_kv_kvq_gb300", "csrc")
-    for f in DECODE_SOURCES:
+    for f in KERNEL_SOURCES[kind]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def decode_traffic(w):
-    """DRAM read+write bytes per decode launch from the committed ncu summary, or None.
+def kernel_traffic(kind, w):
+    """DRAM read+write bytes per call from the committed ncu summary, or None.
 
-    The summary holds `key: value` lines; its figure counts only when it was taken
-    on this workload and on the current decode kernel sources."""
+    The summary holds blocks of `key: value` lines separated by blank lines; a block counts only when
+    it was taken on this kernel kind, this workload and the current sources of that kernel."""
     if not os.path.exists(TRAFFIC_SUMMARY):
         return None
-    kv = {}
+    blocks, cur = [], {}
     for line in open(TRAFFIC_SUMMARY):
+        if not line.strip():
+            if cur:
+                blocks.append(cur)
+            cur = {}
+            continue
         if ":" in line and not line.startswith((" ", "#")):
             k, v = line.split(":", 1)
-            kv[k.strip()] = v.strip()
-    if kv.get("workload") != w.name or kv.get("kernel_rev") != kernel_revision():
-        return None
-    try:
-        return float(kv["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+            cur[k.strip()] = v.strip()
+    if cur:
+        blocks.append(cur)
+    rev = kernel_revision(kind)
+    for kv in blocks:
+        if kv.get("kind") == kind and kv.get("workload") == w.name and kv.get("kernel_rev") == rev:
+            try:
+                return float(kv["dram_bytes_per_call"])
+            except (KeyError, ValueError):
+                return None
+    return None
 
 
 COPY_STREAMS = 4  # host->device copy streams for the prefill inputs (several copy engines)
@@ -469,7 +649,7 @@ def run_e2e(args, w, dist, caches, stream):
     hk, hv = pin(K[:, :, :T0]), pin(V[:, :, :T0])
     hkn = pin(K[:, :, T0:T0 + S].transpose(2, 0, 1, 3))
     hvn = pin(V[:, :, T0:T0 + S].transpose(2, 0, 1, 3))
-    hq = pin(np.stack([synth.queries(w, i) for i in range(S)]))
+    hq = pin(np.stack(all_queries(w)))
     hout = torch.empty((L, S) + tuple(hq.shape[1:]), dtype=torch.float16).pin_memory()
     # Copies run on streams of their own and overlap the compute; every byte is still copied inside
     # the timed region, and the compute stream waits for each copy it uses.  Every layer has its own
@@ -544,8 +724,10 @@ def run_e2e(args, w, dist, caches, stream):
     dist.barrier()
     ms = dist.max(e0.elapsed_time(e1) / args.e2e_steps)
     total = dist.sum(step_tokens(w, L))
+    link = (h2d // args.e2e_steps) / (ms * 1e-3) / 1e9
     return {"value": total / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d // args.e2e_steps, "d2h_bytes_per_step": d2h // args.e2e_steps}
+            "h2d_bytes_per_step": h2d // args.e2e_steps, "d2h_bytes_per_step": d2h // args.e2e_steps,
+            "h2d_gbs": link}
 
 
 # ------------------------------------------------------------------ reference arm: the CPU oracle
@@ -553,20 +735,26 @@ def run_e2e(args, w, dist, caches, stream):
 def run_reference(args, dist):
     w = workload_of(args)
     L = args.layers
-    # each step: a bounded sample of the workload through the oracle
-    per = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        cpu_baseline(w, per)
-    t0 = time.perf_counter()
-    vals = []
-    for _ in range(args.steps):
-        vals.append(cpu_baseline(w, per))
-    el = time.perf_counter() - t0
+    Q = all_queries(w)
+    # each step: every host core runs the oracle over its own units for a bounded time
+    per = max(0.2, args.cpu_seconds / max(1, args.steps + args.warmup))
+    pool = OraclePool()
+    try:
+        for i in range(args.warmup):
+            pool.run(w, Q, per, offset=i)
+        t0 = time.perf_counter()
+        vals = [pool.run(w, Q, per, offset=args.warmup + i) for i in range(args.steps)]
+        el = time.perf_counter() - t0
+    finally:
+        pool.close()
     value = statistics.mean(v["value"] for v in vals)
+    units = sum(v["units"] for v in vals)
     return {
         "impl": "reference", "value": value, "ms_per_step": el / args.steps * 1e3,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": vals[-1]["sample"] + f"; {args.steps} steps of ~{per:.1f} s"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.cores, "kind": "oracle",
+                         "host_cores": host_cores(),
+                         "sample": f"{units} (sequence, kv head) units over {args.steps} steps, each step "
+                                   f"~{per:.1f} s of oracle time on {pool.cores} single-threaded oracle processes"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0, "config": workload_config(w, L, False, 1),
     }
@@ -586,15 +774,26 @@ def main(argv=None):
         print(json.dumps(line))
         dist.close()
         return 0
-    res = run_ours(args, dist)
-    line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "u2 codes, f16 tensor-core mma (f32 accumulate), f16 out",
-            "data": "synthetic (seeded): keys N(0,1) with 4 outlier channels per head ~ sign*N(40,5), values N(0,1)",
-            "config": res["config"], "e2e": res["e2e"], "roofline": res["roofline"],
-            "decode_only": res["decode_only"], "gpu_launches": res["gpu_launches"], "clocks": res["clocks"]}
+    # the oracle processes start before the first GPU call (spawned, so nothing of CUDA is inherited)
+    pool = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(workload_of(args), args.cpu_seconds)
+        pool = OraclePool()
+    try:
+        res = run_ours(args, dist)
+        w = workload_of(args)
+        line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": f"u{w.k_bits}/u{w.v_bits} codes, f16 tensor-core mma (f32 accumulate), f16 out",
+                "data": "synthetic (seeded): keys N(0,1) with outlier channels, values N(0,1), queries N(0,1)",
+                "config": res["config"], "e2e": res["e2e"], "roofline": res["roofline"],
+                "decode_only": res["decode_only"], "kernels": res["kernels"], "self_check": res["self_check"],
+                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"]}
+        if pool is not None:
+            line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, pool)
+    finally:
+        if pool is not None:
+            pool.close()
     if dist.rank == 0:
         print(json.dumps(line))
     dist.close()

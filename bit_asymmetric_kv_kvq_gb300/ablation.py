@@ -7,7 +7,7 @@ The comparison at the centre of "KV cache has a geometry problem, not a bit prob
 kernels (kvq_axis_quantize, kvq_axis_dequantize, kvq_axis_attention); torch only holds device
 memory, and the error norms are taken on the host.
 
-    python -m bit_asymmetric_kv_kvq_gb300.ablation        # table for a seeded outlier-key workload
+    python bench_ablation.py        # (repository root) table for a seeded outlier-key workload
 """
 from __future__ import annotations
 
@@ -112,37 +112,3 @@ def time_kernels(K, V, Q, bits: int, group: int, scale: float, reps: int = 20) -
     for r in res.values():
         r["GBps"] = r["bytes"] / r["s"] / 1e9
     return res
-
-
-def _main():
-    import argparse
-    import json
-
-    import torch
-
-    import synth
-
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", type=int, default=1)
-    ap.add_argument("--units", type=int, default=32)
-    ap.add_argument("--tokens", type=int, default=4096)
-    ap.add_argument("--group", type=int, default=32)
-    args = ap.parse_args()
-    w = synth.WORKLOADS[args.workload]
-    w = w.scaled(batch=1, kv_heads=args.units, q_heads=args.units * w.group_q, prefill_tokens=args.tokens,
-                 decode_steps=1)
-    dev = torch.device("cuda:0")
-    K = torch.from_numpy(np.ascontiguousarray(synth.keys(w)[0, :, :args.tokens])).to(dev)
-    V = torch.from_numpy(np.ascontiguousarray(synth.values(w)[0, :, :args.tokens])).to(dev)
-    Q = torch.from_numpy(np.ascontiguousarray(synth.queries(w, 0)[0].reshape(args.units, w.group_q, -1))).to(dev)
-    for bits in (2, 3, 4):
-        for (ka, va), e in axis_errors(K, V, Q, bits, args.group, w.softmax_scale).items():
-            print(json.dumps({"bits": bits, "group": args.group, "key_axis": ka, "value_axis": va,
-                              **{k: round(v, 6) for k, v in e.items()}}))
-    for name, r in time_kernels(K, V, Q, 2, args.group, w.softmax_scale).items():
-        print(json.dumps({"kernel": name, "us": round(r["s"] * 1e6, 2), "bytes": r["bytes"],
-                          "GBps": round(r["GBps"], 1)}))
-
-
-if __name__ == "__main__":
-    _main()

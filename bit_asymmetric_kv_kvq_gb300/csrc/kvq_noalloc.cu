@@ -23,9 +23,18 @@ namespace {
 constexpr size_t kScratchBytes = size_t(8) << 20;  // 8 MiB
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
+// Fixed head of the array: the error word (256-byte block), then up to kRopeTables RoPE turn tables
+// (D/2 = 64 entries each), written once per device and rope base; the counters and partials follow.
+constexpr size_t kErrBytes = 256;
+constexpr int kRopeTables = 8;
+constexpr size_t kRopeTableBytes = (kvq::kHeadDim / 2) * sizeof(unsigned long long);
+constexpr size_t kHeadBytes = kErrBytes + kRopeTables * kRopeTableBytes;
+
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
+float g_rope_base[kMaxDevices][kRopeTables];  // bases whose tables are in place
+int g_rope_used[kMaxDevices] = {};
 
 // Device address of the scratch array on `device` (which must be current).
 // The first call on a device looks the symbol up once and remembers it.
@@ -36,9 +45,40 @@ cudaError_t scratch_address(int device, void** out) {
     void* ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
     if (e != cudaSuccess) return e;
+    // a fresh array holds zeros; clear the error word anyway (synchronous, once per device)
+    const cudaError_t z = cudaMemset(ptr, 0, kErrBytes);
+    if (z != cudaSuccess) return z;
     g_scratch_addr[device] = ptr;
   }
   *out = g_scratch_addr[device];
+  return cudaSuccess;
+}
+
+// The RoPE turn table of `base` inside the scratch array of `device`: written by a synchronous copy
+// the first time a base is used on the device, found again by later calls (which then copy nothing).
+// More than kRopeTables distinct bases on one device are refused: *full is set and nothing is copied.
+cudaError_t rope_table_address(int device, unsigned char* base_addr, float rope_base, unsigned long long** out,
+                               bool* full) {
+  *full = false;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  for (int i = 0; i < g_rope_used[device]; ++i)
+    if (g_rope_base[device][i] == rope_base) {
+      *out = reinterpret_cast<unsigned long long*>(base_addr + kErrBytes + i * kRopeTableBytes);
+      return cudaSuccess;
+    }
+  if (g_rope_used[device] >= kRopeTables) {
+    *full = true;
+    return cudaSuccess;
+  }
+  const int i = g_rope_used[device];
+  unsigned long long table[kvq::kHeadDim / 2];
+  kvq::rope_table(rope_base, kvq::kHeadDim, table);
+  unsigned long long* dst = reinterpret_cast<unsigned long long*>(base_addr + kErrBytes + i * kRopeTableBytes);
+  const cudaError_t e = cudaMemcpy(dst, table, sizeof(table), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return e;
+  g_rope_base[device][i] = rope_base;
+  g_rope_used[device] = i + 1;
+  *out = dst;
   return cudaSuccess;
 }
 
@@ -82,13 +122,12 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     return KVQ_ERR_UNSUPPORTED;
   }
 
-  // Scratch layout: the RoPE turn table, per-unit tickets and slot counts, then (m, l) and acc[D]
-  // per query head and partial slot.  The grid is the resident CTA count, lowered until the
-  // slots it needs (warps * (ceil(grid / units) + 2) per query head) fit; a size that does not
-  // fit even one CTA is refused.
+  // Scratch layout after the fixed head (error word, RoPE tables): the per-unit slot counters, then
+  // (m, l) and acc[D] per query head and partial slot.  The grid is the resident CTA count, lowered
+  // until the slots it needs (warps * (ceil(grid / units) + 2) per query head) fit; a size that does
+  // not fit even one CTA is refused.
   const int64_t wpu = n_pages + (n_tokens - tq > 0 ? 1 : 0);
-  const size_t rope_bytes = 256 * 8;  // room for the RoPE turn table (D/2 entries)
-  const size_t counter_bytes = rope_bytes + ((size_t)n_units * 2 * sizeof(int) + 255) / 256 * 256;
+  const size_t counter_bytes = kHeadBytes + ((size_t)n_units * sizeof(int) + 255) / 256 * 256;
   auto slots_for = [&](int64_t g) { return (int64_t)warps * ((g + n_units - 1) / n_units + 2); };
   auto ml_bytes_for = [&](int64_t sl) { return ((size_t)heads * sl * 2 * sizeof(float) + 255) / 256 * 256; };
   auto bytes_for = [&](int64_t g) {
@@ -102,20 +141,23 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   const int64_t slots = slots_for(grid);
 
   unsigned char* base = static_cast<unsigned char*>(scratch);
-  unsigned long long* rope_turns = reinterpret_cast<unsigned long long*>(base);
-  int* counters = reinterpret_cast<int*>(base + rope_bytes);
+  int* err_word = reinterpret_cast<int*>(base);
+  unsigned long long* rope_turns = nullptr;
+  if (cfg->rope) {
+    bool full = false;
+    const cudaError_t e = rope_table_address(device, base, cfg->rope_base, &rope_turns, &full);
+    if (full) return KVQ_ERR_CAPACITY;  // a ninth distinct rope base on this device
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return KVQ_ERR_CUDA;
+    }
+  }
+  int* counters = reinterpret_cast<int*>(base + kHeadBytes);
   float* part_ml = reinterpret_cast<float*>(base + counter_bytes);
   float* part_acc = reinterpret_cast<float*>(base + counter_bytes + ml_bytes_for(slots));
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  // the counters must start at zero; a call that stopped early may have left them set
-  if (cudaMemsetAsync(counters, 0, (size_t)n_units * 2 * sizeof(int), s) != cudaSuccess) return KVQ_ERR_CUDA;
-  if (cfg->rope) {
-    // pageable source: the copy has taken the table by the time the call returns
-    unsigned long long table[kvq::kHeadDim / 2];
-    kvq::rope_table(cfg->rope_base, D, table);
-    if (cudaMemcpyAsync(rope_turns, table, sizeof(table), cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-  }
+  // the slot counters must start at zero; a call that stopped early may have left them set
+  if (cudaMemsetAsync(counters, 0, (size_t)n_units * sizeof(int), s) != cudaSuccess) return KVQ_ERR_CUDA;
 
   kvq::DecodeParams dp{};
   dp.q = static_cast<const uint16_t*>(q_f16);
@@ -144,9 +186,25 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   dp.part_acc = part_acc;
   dp.nslot = counters;
   dp.out = static_cast<uint16_t*>(out_f16);
-  dp.err = nullptr;
+  dp.err = err_word;  // a device-side wait that runs out is recorded here (kvq_noalloc_sync_status)
   bool supported = false;
   if (kvq::launch_decode(dp, cfg->k_bits, cfg->v_bits, hg, cfg->rope != 0, (int)grid, s, &supported) != cudaSuccess)
     return supported ? KVQ_ERR_CUDA : KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
+}
+
+extern "C" kvq_status kvq_noalloc_sync_status(void* cuda_stream) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return KVQ_ERR_CUDA;
+  void* scratch = nullptr;
+  if (scratch_address(device, &scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  int err = 0;
+  if (cudaMemcpy(&err, scratch, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (err == 0) return KVQ_OK;
+  if (cudaMemset(scratch, 0, sizeof(int)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_ERR_CUDA;
 }

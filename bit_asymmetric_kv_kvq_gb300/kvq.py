@@ -75,6 +75,7 @@ SIGNATURES = {
     "kvq_set_codebooks": (ctypes.c_int, [_P, _P, _P]),
     "kvq_decode_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(kvq_config), _P, ctypes.c_int64, _P, _P,
                                                     ctypes.c_int64, _P, _P, _P]),
+    "kvq_noalloc_sync_status": (ctypes.c_int, [_P]),
     "kvq_get_state": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
                                      ctypes.POINTER(ctypes.c_int32)]),
     "kvq_unit_sizes": (ctypes.c_int, [_P, ctypes.POINTER(kvq_unit_view)]),
@@ -194,6 +195,11 @@ def kvq_decode_attention_noalloc(cfg: kvq_config, pages, pages_per_unit: int, wi
     _check(lib().kvq_decode_attention_noalloc(ctypes.byref(cfg), _ptr(pages), pages_per_unit, _ptr(window_k),
                                               _ptr(window_v), n_tokens, _ptr(q), _ptr(out), _stream(stream)),
            "kvq_decode_attention_noalloc")
+
+
+def kvq_noalloc_sync_status(stream=None) -> int:
+    """Status of kvq_decode_attention_noalloc on the current device (clears a recorded error)."""
+    return int(lib().kvq_noalloc_sync_status(_stream(stream)))
 
 
 def kvq_reset(handle) -> None:

@@ -140,13 +140,22 @@ kvq_status kvq_append(kvq_cache* cache, const void* k_f16, const void* v_f16, vo
  * rope = 1) followed by the fp16 window.  Computed as split-K flash decoding
  * in fp32 (token ranges in parallel, online softmax, log-sum-exp merge), then
  * rounded to fp16.  KVQ_ERR_STATE on an empty cache.
+ *
+ * Outputs are not bitwise reproducible from launch to launch: the warps of a
+ * launch take token ranges as they become free, and the partials are merged
+ * in the order they finish, so fp32 sums are taken in a different order each
+ * time and an fp16 output may differ by an ulp between two launches over the
+ * same cache (about 0.5 % of the outputs of a full-size launch do).  Every
+ * launch stays within the error bound against exact attention over the
+ * dequantized cache.
  */
 kvq_status kvq_decode_attention(kvq_cache* cache, const void* q_f16, void* out_f16, void* cuda_stream);
 
 /*
  * One decode step of a layer in one call: kvq_append(k, v) followed by
- * kvq_decode_attention(q, out), with identical results (the same cache state
- * and bit-identical outputs).  The append's flush, when the window is full,
+ * kvq_decode_attention(q, out): the same cache state bit for bit, and the
+ * same attention up to the launch-to-launch rounding differences described
+ * for kvq_decode_attention.  The append's flush, when the window is full,
  * is its own launch; the new token is read by the attention launch straight
  * from k and v and stored into its window slot by that launch, so a step costs
  * one launch (two on a flush) instead of two (three).  Buffers as for
@@ -221,17 +230,40 @@ kvq_status kvq_reset(kvq_cache* cache);
  * partials do not fit the 8 MiB array: B*Hq*(D+2)*4 bytes per partial slot,
  * 3*W slots per query head for a one-CTA launch (W = warps of one decode CTA:
  * 16 on the tensor-core kernel, 12 there with four query heads per kv head; 8
- * to 16 on the CUDA-core kernel), plus two counters per unit.  Larger sizes run
- * on fewer CTAs than the GPU holds, as many as the array allows.  The device is the current one.  The first call on a device looks up
- * the array's address once (a runtime symbol lookup), so make that first call
- * before any stream capture.  Every call shares the one array: it clears the
- * counters it needs at the start of each call, but calls whose work overlaps
- * on the GPU (different streams, or several host threads) race on it.
- * Nothing is allocated and no allocator is called.
+ * to 16 on the CUDA-core kernel), plus one counter per unit, after a fixed
+ * head of 4.3 KB.  Larger sizes run on fewer CTAs than the GPU holds, as many
+ * as the array allows.  KVQ_ERR_CAPACITY also refuses a ninth distinct
+ * rope_base on one device (the array keeps the turn tables of eight).
+ *
+ * The device is the current one.  The first call on a device looks up the
+ * array's address (a runtime symbol lookup) and clears its error word, and
+ * the first call with rope = 1 and a given rope_base on a device writes that
+ * base's turn table into the array with a synchronous copy; make those first
+ * calls before any stream capture.  Later calls issue only a memset of the
+ * counters and the two kernel launches.  The address is remembered for the
+ * life of the process: after cudaDeviceReset (or anything else that destroys
+ * the device's primary context) the remembered address is stale, so do not
+ * call this function on that device again in the same process.
+ *
+ * Every call shares the one array: it clears the counters it needs at the
+ * start of each call, but calls whose work overlaps on the GPU (different
+ * streams, or several host threads) race on it.  A device-side wait that runs
+ * out (see kvq_sync_status) is recorded in the array's error word; the call
+ * has then returned KVQ_OK with an unusable output, and
+ * kvq_noalloc_sync_status reports it.  Nothing is allocated and no allocator
+ * is called.
  */
 kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const void* pages, int64_t pages_per_unit,
                                         const void* window_k, const void* window_v, int64_t n_tokens,
                                         const void* q_f16, void* out_f16, void* cuda_stream);
+
+/*
+ * Device-side status of kvq_decode_attention_noalloc on the current device: waits for
+ * cuda_stream, then reads the scratch array's error word.  KVQ_OK if no call since the last
+ * check recorded an error; otherwise KVQ_ERR_CUDA, and the word is cleared.  Also KVQ_ERR_CUDA
+ * when the stream reports an error.  (The method pages have no counterpart.)
+ */
+kvq_status kvq_noalloc_sync_status(void* cuda_stream);
 
 /*
  * Page layout of a configuration, for callers that build or size the packed
@@ -297,7 +329,12 @@ typedef struct {
 /* Fill the *_bytes fields of `sizes` for the current state (pointers untouched). */
 kvq_status kvq_unit_sizes(const kvq_cache* cache, kvq_unit_view* sizes);
 
-/* Copy unit (b, kvh) to the host in the canonical layout; waits for `stream`. */
+/*
+ * Copy unit (b, kvh) to the host in the canonical layout; waits for `stream` (synchronous).  This
+ * is the cache export in per-unit form: a caller exports the whole cache by calling it for every
+ * (b, kvh), with host buffers sized by kvq_unit_sizes.  Pages stored in fragment order are converted
+ * back to the canonical bitstreams above, so the export is the same for every page layout.
+ */
 kvq_status kvq_export_unit(kvq_cache* cache, int32_t b, int32_t kvh, kvq_unit_view* dst, void* cuda_stream);
 
 /*

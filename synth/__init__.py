@@ -76,6 +76,10 @@ def normal(base: int, i: int) -> float:
 
 
 def _threads() -> int:
+    """Generator threads: KVQ_SYNTH_THREADS when set (a process pinned to one core sets 1), else the cores."""
+    env = os.environ.get("KVQ_SYNTH_THREADS")
+    if env:
+        return max(1, min(64, int(env)))
     return max(1, min(64, os.cpu_count() or 1))
 
 
