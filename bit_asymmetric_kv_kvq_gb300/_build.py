@@ -18,6 +18,10 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "libkvq.so")
+# the debug build: kernels check their buffer bounds, every cache buffer is followed by a canary
+DEBUG_LIB = os.path.join(LIBDIR, "libkvq_debug.so")
+DEBUG_OBJDIR = os.path.join(LIBDIR, "obj_debug")
+DEBUG_FLAGS = ("-DKVQ_DEBUG_CHECKS",)
 
 SOURCES = ["kvq_api.cpp", "kvq_quant.cu", "kvq_decode.cu", "kvq_decode_lut.cu", "kvq_decode_mma.cu", "kvq_noalloc.cu",
            "kvq_ablation.cu"]
@@ -84,5 +88,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), lib=None, 
     return target
 
 
+def build_debug(force: bool = False) -> str:
+    """Build the debug variant (libkvq_debug.so) if it is missing or older than its sources."""
+    if not force and os.path.exists(DEBUG_LIB) and all(os.path.getmtime(f) <= os.path.getmtime(DEBUG_LIB)
+                                                        for f in _deps()):
+        return DEBUG_LIB
+    return build(force=True, extra_flags=DEBUG_FLAGS, lib=DEBUG_LIB, objdir=DEBUG_OBJDIR)
+
+
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--debug" in sys.argv:
+        print(build_debug(force="--force" in sys.argv))
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -17,6 +17,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -24,8 +25,32 @@
 #include "kvq.h"
 #include "kvq_internal.h"
 
+namespace {
+
+// Device memory of a cache: the caller's allocator (kvq_set_device_allocator) or cudaMalloc.
+struct DeviceAllocator {
+  kvq_alloc_fn alloc = nullptr;
+  kvq_free_fn free = nullptr;
+  void* user = nullptr;
+};
+std::mutex g_alloc_mutex;
+DeviceAllocator g_alloc;
+
+#ifdef KVQ_DEBUG_CHECKS
+// Debug builds put a canary of this many bytes after every device buffer of a cache and check it
+// in kvq_debug_check (a stand-in for a memory checker).
+constexpr size_t kCanaryBytes = 256;
+constexpr unsigned char kCanaryByte = 0xA5;
+#endif
+
+}  // namespace
+
 struct kvq_cache {
   kvq_config cfg;
+  DeviceAllocator alloc;
+#ifdef KVQ_DEBUG_CHECKS
+  std::vector<std::pair<unsigned char*, size_t>> canaries;  // (buffer, bytes in use): a canary follows each
+#endif
   int device = 0;
   int sm_count = 0;
   kvq::PageLayout lay{};
@@ -53,6 +78,8 @@ struct kvq_cache {
   bool prefilled = false;
   bool broken = false;
   int64_t launches = 0;
+  unsigned long long test_wait_ns = 0;  // test hooks (kvq_test_inject)
+  int32_t test_withhold = 0;
 };
 
 namespace {
@@ -78,15 +105,60 @@ kvq_status fail_cuda(kvq_cache* c) {
 
 int64_t quantized_tokens(int64_t T, int R) { return T <= 0 ? 0 : (int64_t)R * ((T - 1) / R); }
 
+// One device buffer of the cache, through its allocator (debug builds add a canary after it).
+cudaError_t dev_alloc(kvq_cache* c, void** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes < 16) bytes = 16;
+#ifdef KVQ_DEBUG_CHECKS
+  const size_t total = bytes + kCanaryBytes;
+#else
+  const size_t total = bytes;
+#endif
+  if (c->alloc.alloc) {
+    void* q = c->alloc.alloc(total, c->device, c->alloc.user);
+    if (!q) return cudaErrorMemoryAllocation;
+    if (reinterpret_cast<uintptr_t>(q) & 255u) {
+      c->alloc.free(q, c->device, c->alloc.user);
+      return cudaErrorInvalidValue;
+    }
+    *p = q;
+  } else {
+    const cudaError_t e = cudaMalloc(p, total);
+    if (e != cudaSuccess) {
+      *p = nullptr;
+      return e;
+    }
+  }
+#ifdef KVQ_DEBUG_CHECKS
+  const cudaError_t e = cudaMemset(static_cast<unsigned char*>(*p) + bytes, kCanaryByte, kCanaryBytes);
+  if (e != cudaSuccess) return e;
+  c->canaries.push_back({static_cast<unsigned char*>(*p), bytes});
+#endif
+  return cudaSuccess;
+}
+
+void dev_free(kvq_cache* c, void* p) {
+  if (!p) return;
+#ifdef KVQ_DEBUG_CHECKS
+  for (size_t i = 0; i < c->canaries.size(); ++i)
+    if (c->canaries[i].first == p) {
+      c->canaries.erase(c->canaries.begin() + (long)i);
+      break;
+    }
+#endif
+  if (c->alloc.free) c->alloc.free(p, c->device, c->alloc.user);
+  else cudaFree(p);
+}
+
 void free_all(kvq_cache* c) {
-  cudaFree(c->pages);
-  cudaFree(c->wk);
-  cudaFree(c->wv);
-  cudaFree(c->part_ml);
-  cudaFree(c->part_acc);
-  cudaFree(c->counters);
-  cudaFree(c->err);
-  cudaFree(c->rope_turns);
+  dev_free(c, c->pages);
+  dev_free(c, c->wk);
+  dev_free(c, c->wv);
+  dev_free(c, c->part_ml);
+  dev_free(c, c->part_acc);
+  dev_free(c, c->counters);
+  dev_free(c, c->err);
+  dev_free(c, c->rope_turns);
   c->pages = nullptr;
   c->wk = c->wv = nullptr;
   c->part_ml = c->part_acc = nullptr;
@@ -148,17 +220,17 @@ cudaError_t ensure_slots(kvq_cache* c, int64_t slots) {
   if (slots <= c->max_slots) return cudaSuccess;
   const int64_t heads = (int64_t)c->cfg.batch * c->cfg.num_q_heads;
   float *ml = nullptr, *acc = nullptr;
-  cudaError_t e = cudaMalloc((void**)&ml, (size_t)(heads * slots * 2 * sizeof(float)));
-  if (e == cudaSuccess) e = cudaMalloc((void**)&acc, (size_t)(heads * slots * c->cfg.head_dim * sizeof(float)));
+  cudaError_t e = dev_alloc(c, (void**)&ml, (size_t)(heads * slots * 2 * sizeof(float)));
+  if (e == cudaSuccess) e = dev_alloc(c, (void**)&acc, (size_t)(heads * slots * c->cfg.head_dim * sizeof(float)));
   if (e != cudaSuccess) {
-    cudaFree(ml);
-    cudaFree(acc);
+    dev_free(c, ml);
+    dev_free(c, acc);
     return e;
   }
   // the buffers may still be read by work in flight on any stream
   cudaDeviceSynchronize();
-  cudaFree(c->part_ml);
-  cudaFree(c->part_acc);
+  dev_free(c, c->part_ml);
+  dev_free(c, c->part_acc);
   c->part_ml = ml;
   c->part_acc = acc;
   c->max_slots = (int32_t)slots;
@@ -228,6 +300,8 @@ cudaError_t flush_window(kvq_cache* c, cudaStream_t s) {
   qp.nsp = c->cfg.k_sparse;
   qp.lay = c->lay;
   qp.err = c->err;
+  qp.src_elems = c->n_units * rows_per_unit(c) * D;
+  qp.pages_bytes = c->n_units * c->unit_page_stride;
   set_codebook(c, &qp);
   const cudaError_t e = kvq::launch_quantize(qp, c->cfg.k_bits, c->cfg.v_bits, 1, s);
   if (e == cudaSuccess) {
@@ -301,6 +375,9 @@ kvq_status launch_decode_for(kvq_cache* c, const void* q, void* out, const void*
   dp.nslot = c->counters;
   dp.out = static_cast<uint16_t*>(out);
   dp.err = c->err;
+  dp.wait_ns = c->test_wait_ns;
+  dp.test_withhold = c->test_withhold;
+  dp.pages_bytes = c->n_units * c->unit_page_stride;
   if (c->cfg.codebook) {
     dp.lut = 1;
     std::memcpy(dp.k_lev, c->k_lev, sizeof(dp.k_lev));
@@ -396,9 +473,13 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
   c->max_slots = (int32_t)slots_for_grid(c, c->resident);
 
   const int64_t heads = (int64_t)cfg->batch * cfg->num_q_heads;
+  {
+    std::lock_guard<std::mutex> lock(g_alloc_mutex);
+    c->alloc = g_alloc;
+  }
   cudaError_t e = cudaSuccess;
   auto alloc = [&](void** p, size_t bytes) {
-    if (e == cudaSuccess) e = cudaMalloc(p, bytes < 16 ? 16 : bytes);
+    if (e == cudaSuccess) e = dev_alloc(c, p, bytes);
   };
   alloc((void**)&c->pages, (size_t)(c->n_units * c->unit_page_stride));
   alloc((void**)&c->wk, (size_t)(c->n_units * rows_per_unit(c) * D * 2));
@@ -416,14 +497,46 @@ kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out) {
     e = cudaMemcpy(c->rope_turns, turns.data(), turns.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice);
   }
   if (e != cudaSuccess) {
-    const bool oom = e == cudaErrorMemoryAllocation;
+    const kvq_status st = e == cudaErrorMemoryAllocation ? KVQ_ERR_OOM
+                          : e == cudaErrorInvalidValue  ? KVQ_ERR_INVALID_ARG
+                                                        : KVQ_ERR_CUDA;
     cudaGetLastError();
     free_all(c);
     delete c;
-    return oom ? KVQ_ERR_OOM : KVQ_ERR_CUDA;
+    return st;
   }
   *out = c;
   return KVQ_OK;
+}
+
+kvq_status kvq_set_device_allocator(kvq_alloc_fn alloc, kvq_free_fn free_fn, void* user) {
+  if ((alloc == nullptr) != (free_fn == nullptr)) return KVQ_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_alloc_mutex);
+  g_alloc.alloc = alloc;
+  g_alloc.free = free_fn;
+  g_alloc.user = alloc ? user : nullptr;
+  return KVQ_OK;
+}
+
+kvq_status kvq_debug_check(kvq_cache* c) {
+  if (!c) return KVQ_ERR_INVALID_ARG;
+#ifdef KVQ_DEBUG_CHECKS
+  DeviceGuard g(c->device);
+  if (!g.ok || cudaDeviceSynchronize() != cudaSuccess) return fail_cuda(c);
+  int err = 0;
+  if (cudaMemcpy(&err, c->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return fail_cuda(c);
+  if (err != 0) return fail_cuda(c);
+  std::vector<unsigned char> buf(kCanaryBytes);
+  for (const auto& cn : c->canaries) {
+    if (cudaMemcpy(buf.data(), cn.first + cn.second, kCanaryBytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return fail_cuda(c);
+    for (unsigned char b : buf)
+      if (b != kCanaryByte) return fail_cuda(c);
+  }
+  return KVQ_OK;
+#else
+  return KVQ_ERR_UNSUPPORTED;
+#endif
 }
 
 kvq_status kvq_destroy(kvq_cache* c) {
@@ -545,6 +658,8 @@ kvq_status kvq_prefill_quantize(kvq_cache* c, const void* k, const void* v, int6
     qp.nsp = c->cfg.k_sparse;
     qp.lay = c->lay;
     qp.err = c->err;
+    qp.src_elems = c->n_units * n_tokens * D;
+    qp.pages_bytes = c->n_units * c->unit_page_stride;
     set_codebook(c, &qp);
     if (kvq::launch_quantize(qp, c->cfg.k_bits, c->cfg.v_bits, (int)np, s) != cudaSuccess) return fail_cuda(c);
     c->launches++;
@@ -640,6 +755,13 @@ kvq_status kvq_decode_step(kvq_cache* c, const void* k, const void* v, const voi
   c->T += 1;
   c->prefilled = true;
   return launch_decode_for(c, q, out, k, v, s);
+}
+
+kvq_status kvq_test_inject(kvq_cache* c, int32_t withhold_page, int64_t wait_limit_ns) {
+  if (!c || withhold_page < -1 || wait_limit_ns < 0) return KVQ_ERR_INVALID_ARG;
+  c->test_withhold = withhold_page + 1;
+  c->test_wait_ns = (unsigned long long)wait_limit_ns;
+  return KVQ_OK;
 }
 
 kvq_status kvq_sync_status(kvq_cache* c, void* stream) {

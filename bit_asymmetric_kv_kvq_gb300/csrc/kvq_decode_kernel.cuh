@@ -262,10 +262,21 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
   const int n_pg = (int)(pages_before(w_end) - P_begin);
 
   // page k of the slice into stage k % n_stages (one thread)
+  const unsigned long long wlim = p.wait_ns ? p.wait_ns : kWaitLimitNs;  // page and stage waits
   auto issue_page = [&](int k) {
+    if (k + 1 == p.test_withhold) return;  // test hook: this page is never copied
     // 32-bit division: a cache never holds 2^32 pages
     const uint32_t P = (uint32_t)(P_begin + k), np = (uint32_t)p.n_pages;
     const uint32_t u = P / np, loc = P - u * np;
+#ifdef KVQ_DEBUG_CHECKS
+    {
+      const int64_t off = (int64_t)u * p.unit_page_stride + (int64_t)loc * page_bytes;
+      if (off < 0 || off + page_bytes > p.pages_bytes) {
+        report_error(p.err, kDevBounds);  // not copied: the waits for it run out and end the launch
+        return;
+      }
+    }
+#endif
     const int st = k & (n_stages - 1);
     mbar_arrive_expect_tx(&full_bar[st], (uint32_t)page_bytes);
     bulk_g2s(stage_mem + (size_t)st * page_bytes, p.pages + (int64_t)u * p.unit_page_stride + (int64_t)loc * page_bytes,
@@ -282,11 +293,11 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
     if (*(volatile int*)&stage_page[st] != k) {
       const unsigned long long t0 = global_ns();
       while (*(volatile int*)&stage_page[st] != k) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > wlim) return false;
         __nanosleep(128);
       }
     }
-    return mbar_wait(&full_bar[st], (k >> log2S) & 1);
+    return mbar_wait(&full_bar[st], (k >> log2S) & 1, wlim);
   };
 
   if (tid == 0) {
@@ -705,7 +716,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
         mbar_arrive(&empty_bar[stg]);
         if (atomicAdd(&stage_cnt[stg], 1) % SPP == SPP - 1 && kpg + n_stages < n_pg &&
             !*(volatile int*)&abort_flag) {
-          if (mbar_wait(&empty_bar[stg], (kpg >> log2S) & 1)) {
+          if (mbar_wait(&empty_bar[stg], (kpg >> log2S) & 1, wlim)) {
             issue_page(kpg + n_stages);
           } else {
             report_error(p.err, kDevWaitTimeout);

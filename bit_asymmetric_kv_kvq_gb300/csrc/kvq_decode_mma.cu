@@ -16,8 +16,13 @@
 // (see frag_key_pair / frag_value_pair for where each lane's codes sit).  The
 // position scale 2^(B*p) is folded into the B operand for keys (the B row of
 // that k-slot) and into the output scale for values (one position per M-tile).
-// B values are split into a high and a low fp16 part (two of the eight N
-// columns per head), which keeps them to about 22 significant bits.
+// Key B values are split into a high and a low fp16 part (two of the eight N
+// columns per head), which keeps them to about 22 significant bits: a score
+// error moves a softmax weight by the same relative amount.  Value B values
+// p_t * s_t are single fp16 numbers (one column per (group, head)): their
+// rounding (2^-12 relative per product) moves the output far less than the
+// 2e-3 the outputs are held to, and one column per head halves the value
+// operands to build.
 //
 // Scheduling is that of the CUDA-core kernel: one CTA per SM streams a
 // contiguous slice of the (window, pages) work list through a ring of page
@@ -35,11 +40,11 @@ namespace kvq {
 
 namespace {
 
-// Warps of the one CTA per SM: 16 at 128 registers, except with four query heads per kv head,
-// which hold more per lane (B fragments, softmax state per head) and spilled at 128: they take
-// 12 warps at up to 168 registers.
+// Warps of the one CTA per SM: 16 at up to 128 registers.  (Four query heads per kv head once held
+// value operands split into high and low parts and a scale per head, spilled at 128 registers and
+// ran 12 warps; with single fp16 value operands and one key scale they fit.)
 template <int HG>
-__host__ __device__ constexpr int mma_warps() { return HG == 4 ? 12 : 16; }
+__host__ __device__ constexpr int mma_warps() { return 16; }
 constexpr int kMmaMaxStages = 16;
 constexpr unsigned kAll = 0xffffffffu;
 constexpr float kLazy = 8.0f;  // the running maximum moves only when a score passes it by 8 (log2 units)
@@ -82,9 +87,10 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
 template <int BK, int BV, int HG, bool STD>
 __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(const DecodeParams p) {
   constexpr int D = kHeadDim, W = mma_warps<HG>();
-  constexpr int NCOL = 2 * HG;   // B columns per value group: (head, high/low)
+  constexpr int NCOL = HG;       // value B columns per value group: one per head
   constexpr int GPB = 8 / NCOL;  // value groups per B fragment
   constexpr int NBM = (D / 32 + GPB - 1) / GPB;  // B fragments per value tile at most (G = 32)
+  constexpr int KCOL = 2 * HG;   // key B columns: (head, high/low)
   constexpr int KPW = 8 / BK;    // key k-chunks per fragment word
   using PK = Pairs<BK>;
   using PV = Pairs<BV>;
@@ -111,7 +117,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
   // fragments (static arrays stay small: static shared memory is limited to 48 KB)
   extern __shared__ __align__(128) uint8_t stage_mem[];
   float(*qw_s)[HG][D] = reinterpret_cast<float(*)[HG][D]>(stage_mem + ((size_t)page_bytes << p.log2_stages));
-  uint32_t(*bk_s)[NCOL][4][16] = reinterpret_cast<uint32_t(*)[NCOL][4][16]>(qw_s + W);
+  uint32_t(*bk_s)[KCOL][4][16] = reinterpret_cast<uint32_t(*)[KCOL][4][16]>(qw_s + W);
   __shared__ __align__(8) uint64_t full_bar[kMmaMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMmaMaxStages];
   __shared__ int stage_cnt[kMmaMaxStages];
@@ -128,9 +134,20 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
   };
   const int64_t P_begin = pages_before(w_begin);
   const int n_pg = (int)(pages_before(w_end) - P_begin);
+  const unsigned long long wlim = p.wait_ns ? p.wait_ns : kWaitLimitNs;  // page and stage waits
   auto issue_page = [&](int k) {
+    if (k + 1 == p.test_withhold) return;  // test hook: this page is never copied
     const uint32_t P = (uint32_t)(P_begin + k), np = (uint32_t)p.n_pages;
     const uint32_t u = P / np, loc = P - u * np;
+#ifdef KVQ_DEBUG_CHECKS
+    {
+      const int64_t off = (int64_t)u * p.unit_page_stride + (int64_t)loc * page_bytes;
+      if (off < 0 || off + page_bytes > p.pages_bytes) {
+        report_error(p.err, kDevBounds);  // not copied: the waits for it run out and end the launch
+        return;
+      }
+    }
+#endif
     const int st = k & (n_stages - 1);
     mbar_arrive_expect_tx(&full_bar[st], (uint32_t)page_bytes);
     bulk_g2s(stage_mem + (size_t)st * page_bytes, p.pages + (int64_t)u * p.unit_page_stride + (int64_t)loc * page_bytes,
@@ -147,11 +164,11 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     if (*(volatile int*)&stage_page[st] != k) {
       const unsigned long long t0 = global_ns();
       while (*(volatile int*)&stage_page[st] != k) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > wlim) return false;
         __nanosleep(128);
       }
     }
-    return mbar_wait(&full_bar[st], (k >> log2S) & 1);
+    return mbar_wait(&full_bar[st], (k >> log2S) & 1, wlim);
   };
 
   if (tid < 64) (&zero_frag[0][0])[tid] = 0u;
@@ -174,11 +191,11 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     for (int k = 0; k < n_pg && k < n_stages; ++k) issue_page(k);
 
   float (*qs)[D] = qw_s[warp];
-  const int hcol = (g8 % NCOL) / 2;  // head of this lane's B column g8
-  const int hl = g8 & 1;             // high (0) or low (1) part in that column
-  const int gl = g8 / NCOL;          // value group of that column within a B fragment
-  const int hmine = t4 % HG;         // head of this lane's D columns 2*t4, 2*t4 + 1
-  const int gmine = t4 / HG;         // value group of those columns within a B fragment
+  const int hcol = g8 % HG;          // head of this lane's value B column g8
+  const int gl = g8 / HG;            // value group of that column within a B fragment
+  const int hmine = t4 % HG;         // head of this lane's scores (lanes t4 < HG) and running maximum
+  // the lane's value D columns n = 2*t4 + e are (group n / HG within the fragment, head n % HG)
+  const int hd0 = (2 * t4) % HG, hd1 = (2 * t4 + 1) % HG;
 
   // ---- per-warp state for the current unit
   float dv[8][4];            // value accumulators, one m16n8 tile per 16 channels
@@ -198,6 +215,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     es = -30;
   };
 
+  int eq = 0;  // exponent of the current unit's largest |q| (over its heads)
   auto load_q = [&](int64_t unit) {
     constexpr int PERL = HG * D / 32;
     const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
@@ -213,6 +231,12 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
       v[i + 2] = c.x;
       v[i + 3] = c.y;
     }
+    float mq = 0.0f;
+#pragma unroll
+    for (int i = 0; i < PERL; ++i) mq = fmaxf(mq, fabsf(v[i]));
+    // |q| >= 0 orders like its bit pattern: one integer reduction finds the unit's largest
+    const uint32_t mqb = __reduce_max_sync(kAll, __float_as_uint(mq));
+    eq = mqb != 0u ? (int)((mqb >> 23) & 0xFF) - 127 : 0;
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < PERL; ++i) (&qs[0][0])[lane * PERL + i] = v[i];
@@ -239,29 +263,36 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     }
     const int slot = slot_of(unit);
     if (slot < p.max_slots) {
-      // zero-point sums of this lane's (group, head): owned by the lanes of column 2*t4
-      float zs[NBM];
+      // zero-point sums of the (group, head) of this lane's D columns n = 2*t4 + e: owned by the
+      // lanes of B column n (lane 4n)
+      float zs[2][NBM];
 #pragma unroll
-      for (int i = 0; i < NBM; ++i) zs[i] = __shfl_sync(kAll, zacc[i], 4 * (2 * t4));
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int i = 0; i < NBM; ++i) zs[e][i] = __shfl_sync(kAll, zacc[i], 4 * (2 * t4 + e));
       const float osc = pow2f(24 - (6 - es));
 #pragma unroll
       for (int mc = 0; mc < 8; ++mc) {
         const int grp = (16 * mc) >> log2G;
-        if (grp % GPB != gmine) continue;
         const float s = osc * pow2f(-PV::pos(mc % PV::PER));
-        float z = zs[0];
 #pragma unroll
-        for (int i = 1; i < NBM; ++i)
-          if (grp / GPB == i) z = zs[i];
-        float* dst = p.part_acc + ((bh0 + hmine) * p.max_slots + slot) * D + 16 * mc + g8;
-        dst[0] = fmaf(dv[mc][0] + dv[mc][1], s, z);
-        dst[8] = fmaf(dv[mc][2] + dv[mc][3], s, z);
+        for (int e = 0; e < 2; ++e) {
+          const int n = 2 * t4 + e;
+          if (n / HG != grp % GPB) continue;  // this column holds another group's products
+          float z = zs[e][0];
+#pragma unroll
+          for (int i = 1; i < NBM; ++i)
+            if (grp / GPB == i) z = zs[e][i];
+          float* dst = p.part_acc + ((bh0 + n % HG) * p.max_slots + slot) * D + 16 * mc + g8;
+          dst[0] = fmaf(dv[mc][e], s, z);
+          dst[8] = fmaf(dv[mc][2 + e], s, z);
+        }
       }
-      // (m, l) of head h: m from lane h, l from the owners of column 2h (lane 8h)
+      // (m, l) of head h: m from lane h, l from the owners of B column h (lane 4h)
 #pragma unroll
       for (int h = 0; h < HG; ++h) {
         const float mh = __shfl_sync(kAll, mrun, h);
-        const float lh = __shfl_sync(kAll, lacc, 8 * h);
+        const float lh = __shfl_sync(kAll, lacc, 4 * h);
         if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + ((bh0 + h) * p.max_slots + slot) * 2) = make_float2(mh, lh);
       }
     } else if (lane == 0) {
@@ -410,8 +441,11 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     const int stt = stt0 + qq;
     const int gk = (32 * stt) >> log2G;  // key group
 
-    // -- key B fragments: q'_h[c] 2^(sig_h - pos) split high/low, four channels per lane
-    float zk[HG], sigk[HG];
+    // -- key B fragments: q'_h[c] 2^(sig - pos) split high/low, four channels per lane.  One
+    //    exponent serves every head: |q_h[c] s_c| < 2^(eq+1) 2^(es+1) with eq the unit's largest |q|
+    //    and es the group's largest step, so sig = 13 - eq - es keeps every |B| below 2^15.
+    float zl;   // Z = sum_c q_h[c] z_c of head (lane >> 3) (HG = 4), (lane >> 4) (HG = 2) or the head
+    float sgk;  // score = D * 2^(24 - sig)
     {
       const uint4 mz = *reinterpret_cast<const uint4*>(km + gk * D + 4 * lane);
       const uint32_t mzw[4] = {mz.x, mz.y, mz.z, mz.w};
@@ -425,42 +459,55 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
       // channel c = 4*lane + i = 16*kk + 8*hh + 2*tt + e
       const int kk = lane >> 2, hh = (lane >> 1) & 1;
       const int pk = PK::pos(2 * (kk % KPW) + hh);
+      // steps are >= 0: the largest orders like its bit pattern
+      const float smx = fmaxf(fmaxf(sc4[0], sc4[1]), fmaxf(sc4[2], sc4[3]));
+      const uint32_t smxb = __reduce_max_sync(kAll, __float_as_uint(smx));
+      const int esk = smxb != 0u ? (int)((smxb >> 23) & 0xFF) - 127 : 0;
+      const int sig = min(max(13 - eq - esk, -90), 90);
+      sgk = pow2f(24 - sig);
+      const float sscale = pow2f(sig - pk);
+      float ss[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ss[i] = sc4[i] * sscale;
+      float zp[HG];
 #pragma unroll
       for (int h = 0; h < HG; ++h) {
         const float4 q4 = *reinterpret_cast<const float4*>(&qs[h][4 * lane]);
-        const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-        float qp[4], z = 0.0f, mx = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          qp[i] = qv[i] * sc4[i];
-          z = fmaf(qv[i], zc[i], z);
-          mx = fmaxf(mx, fabsf(qp[i]));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(kAll, z, off);
-        // mx >= 0: its bit pattern orders like its value, so one integer reduction finds the maximum
-        const uint32_t mxb = __reduce_max_sync(kAll, __float_as_uint(mx));
-        zk[h] = z;
-        // largest |B| below 2^15: scale by 2^(14 - floor(log2 max))
-        const int emax = mxb != 0u ? (int)((mxb >> 23) & 0xFF) - 127 : 0;
-        const int sig = min(max(14 - emax, -90), 90);
-        sigk[h] = pow2f(24 - sig);  // score = D * 2^(24 - sig)
-        const float sc = pow2f(sig - pk);
+        zp[h] = fmaf(q4.x, zc[0], fmaf(q4.y, zc[1], fmaf(q4.z, zc[2], q4.w * zc[3])));
         const int tt0 = 2 * (lane & 1);
         uint32_t hi01, lo01, hi23, lo23;
-        split2(qp[0] * sc, qp[1] * sc, hi01, lo01);
-        split2(qp[2] * sc, qp[3] * sc, hi23, lo23);
+        split2(q4.x * ss[0], q4.y * ss[1], hi01, lo01);
+        split2(q4.z * ss[2], q4.w * ss[3], hi23, lo23);
         bk_s[warp][2 * h][tt0][2 * kk + hh] = hi01;
         bk_s[warp][2 * h][tt0 + 1][2 * kk + hh] = hi23;
         bk_s[warp][2 * h + 1][tt0][2 * kk + hh] = lo01;
         bk_s[warp][2 * h + 1][tt0 + 1][2 * kk + hh] = lo23;
+      }
+      // Z of every head summed over the lanes, transposed as it goes: each exchange hands the
+      // partner the heads it keeps, so the warp ends with head (lane >> (5 - log2 HG)) on each lane
+      if constexpr (HG == 4) {
+        const bool b4 = lane & 16, b3 = lane & 8;
+        const float k0 = (b4 ? zp[2] : zp[0]) + __shfl_xor_sync(kAll, b4 ? zp[0] : zp[2], 16);
+        const float k1 = (b4 ? zp[3] : zp[1]) + __shfl_xor_sync(kAll, b4 ? zp[1] : zp[3], 16);
+        zl = (b3 ? k1 : k0) + __shfl_xor_sync(kAll, b3 ? k0 : k1, 8);
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1) zl += __shfl_xor_sync(kAll, zl, off);
+      } else if constexpr (HG == 2) {
+        const bool b4 = lane & 16;
+        zl = (b4 ? zp[1] : zp[0]) + __shfl_xor_sync(kAll, b4 ? zp[0] : zp[1], 16);
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) zl += __shfl_xor_sync(kAll, zl, off);
+      } else {
+        zl = zp[0];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) zl += __shfl_xor_sync(kAll, zl, off);
       }
     }
     __syncwarp();
     uint32_t bf[16];
     {
       // lanes of the unused B columns read a block of zeros: one path for every lane
-      const uint4* src = reinterpret_cast<const uint4*>(g8 < NCOL ? &bk_s[warp][g8][t4][0] : &zero_frag[t4][0]);
+      const uint4* src = reinterpret_cast<const uint4*>(g8 < KCOL ? &bk_s[warp][g8][t4][0] : &zero_frag[t4][0]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 v = src[i];
@@ -518,20 +565,14 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
         for (int e = 0; e < 4; ++e) dsum[mt][e] = da[mt][0][e] + da[mt][1][e];
     }
     float sc[2][2];
+    // every lane computes (no branch); lanes past the heads take head 0 and are masked below
+    const int hq = t4 < HG ? t4 : 0;
+    const float zz = HG == 1 ? zl : __shfl_sync(kAll, zl, (32 / HG) * hq);
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
       const float* d = dsum[mt];
       float s0 = -INFINITY, s1 = -INFINITY;
       {
-        // every lane computes (no branch); lanes past the heads take head 0 and are masked below
-        const int hq = t4 < HG ? t4 : 0;
-        float sgk = sigk[0], zz = zk[0];
-#pragma unroll
-        for (int h = 1; h < HG; ++h)
-          if (hq == h) {
-            sgk = sigk[h];
-            zz = zk[h];
-          }
         s0 = fmaf(d[0] + d[1], sgk, zz);
         s1 = fmaf(d[2] + d[3], sgk, zz);
         if (nsp > 0) {
@@ -570,10 +611,16 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
         mx = __shfl_sync(kAll, mx, (lane & ~3) | hmine);  // the maximum of this lane's head
         const float mnew = fmaxf(mx, mrun);
         const float f = mrun == -INFINITY ? 0.0f : exp2f(mrun - mnew);
+        // the lane's D columns belong to heads hd0, hd1 (f of head h is on the lanes t4 = h)
+        const float f0 = HG == 1 ? f : __shfl_sync(kAll, f, (lane & ~3) | hd0);
+        const float f1 = HG == 1 ? f : __shfl_sync(kAll, f, (lane & ~3) | hd1);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) dv[i][j] *= f;
+        for (int i = 0; i < 8; ++i) {
+          dv[i][0] *= f0;
+          dv[i][1] *= f1;
+          dv[i][2] *= f0;
+          dv[i][3] *= f1;
+        }
         // lacc and zacc belong to head hcol
         const float fc = __shfl_sync(kAll, f, hcol);
         lacc *= fc;
@@ -634,15 +681,11 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
       uint32_t bv[NBM][2];
 #pragma unroll
       for (int bi = 0; bi < NBM; ++bi) {
-        uint32_t h0, l0, h1, l1;
-        split2(pb0 * vs[kc][bi][0], pb1 * vs[kc][bi][1], h0, l0);
-        split2(pb2 * vs[kc][bi][2], pb3 * vs[kc][bi][3], h1, l1);
-        bv[bi][0] = hl ? l0 : h0;
-        bv[bi][1] = hl ? l1 : h1;
-        // (every lane accumulates; only the lanes of the high columns are read in the epilogue)
+        bv[bi][0] = h2bits(__floats2half2_rn(pb0 * vs[kc][bi][0], pb1 * vs[kc][bi][1]));
+        bv[bi][1] = h2bits(__floats2half2_rn(pb2 * vs[kc][bi][2], pb3 * vs[kc][bi][3]));
         zacc[bi] = fmaf(p0, vz[kc][bi][0], fmaf(p1, vz[kc][bi][1], fmaf(p2, vz[kc][bi][2], fmaf(p3, vz[kc][bi][3], zacc[bi]))));
       }
-      lacc += (p0 + p1) + (p2 + p3);  // read from the lanes of head h's high column (lane 8h)
+      lacc += (p0 + p1) + (p2 + p3);  // read from the lanes of B column h (lane 4h)
 
       uint32_t wd[2 * BV];
       const uint4* wsrc = reinterpret_cast<const uint4*>(pgm + off_vc) + ((int64_t)tile * 32 + lane) * (2 * BV / 4);
@@ -683,7 +726,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     if (lane == 0) {
       for (int qq = 0; qq < GR; ++qq) mbar_arrive(&empty_bar[stg]);
       if (atomicAdd(&stage_cnt[stg], GR) % SPP == SPP - GR && kpg + n_stages < n_pg && !*(volatile int*)&abort_flag) {
-        if (mbar_wait(&empty_bar[stg], (kpg >> log2S) & 1)) {
+        if (mbar_wait(&empty_bar[stg], (kpg >> log2S) & 1, wlim)) {
           issue_page(kpg + n_stages);
         } else {
           report_error(p.err, kDevWaitTimeout);

@@ -80,6 +80,7 @@ enum DeviceError : int {
   kDevOk = 0,
   kDevWaitTimeout = 1,    // an mbarrier wait gave up
   kDevBadArgument = 2,    // a kernel saw parameters it cannot handle
+  kDevBounds = 3,         // debug builds: an access fell outside its buffer (and was skipped)
 };
 
 struct QuantizeParams {
@@ -93,6 +94,8 @@ struct QuantizeParams {
   int32_t n_units, Hkv, D, G, R, nsp;
   PageLayout lay;
   int* err;
+  int64_t src_elems;         // extent of k_src and v_src (elements) and of the pages (bytes):
+  int64_t pages_bytes;       //   the bounds checks of debug builds
   int32_t lut;               // 1: codes are codebook indices chosen by the thresholds below
   float k_thr[16];           // decision thresholds between consecutive key / value levels
   float v_thr[16];
@@ -141,6 +144,11 @@ struct DecodeParams {
   int32_t lut;              // 1: codebook cache (the CUDA-core kernel with level lookups)
   float k_lev[16];          // codebook caches: the level (in steps) of each key / value code
   float v_lev[16];
+  // test hooks (zero in normal use): a limit for the page and stage waits in place of the default
+  // kWaitLimitNs, and k + 1 to leave page k of every CTA's slice uncopied (its waits then run out)
+  unsigned long long wait_ns;
+  int32_t test_withhold;
+  int64_t pages_bytes;      // extent of the pages (the bounds checks of debug builds)
 };
 
 // Launchers (return cudaGetLastError() after the launch).

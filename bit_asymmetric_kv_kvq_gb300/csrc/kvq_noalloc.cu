@@ -186,6 +186,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   dp.part_acc = part_acc;
   dp.nslot = counters;
   dp.out = static_cast<uint16_t*>(out_f16);
+  dp.pages_bytes = n_units * dp.unit_page_stride;
   dp.err = err_word;  // a device-side wait that runs out is recorded here (kvq_noalloc_sync_status)
   bool supported = false;
   if (kvq::launch_decode(dp, cfg->k_bits, cfg->v_bits, hg, cfg->rope != 0, (int)grid, s, &supported) != cudaSuccess)

@@ -26,10 +26,14 @@
 // true division gives, at the cost of one multiply for all but ~1e-4 of the
 // elements.
 //
-// Data movement: the two fp16 input tiles (R x D each) arrive by bulk copy
-// into shared memory, each thread computes and packs whole 32-bit code words
+// Two kernels.  The general one (any R, G, sparse entries, code order,
+// codebooks): the two fp16 input tiles (R x D each) arrive by bulk copy into
+// shared memory, each thread computes and packs whole 32-bit code words
 // straight from the tile, the page is assembled in shared memory and leaves
-// by one bulk copy, so all global traffic is 16-byte granular and contiguous.
+// by one bulk copy.  The common page shape (R = 128, G = 32, 2- or 4-bit codes
+// in fragment order) has a kernel of its own, quantize_std_kernel, which
+// takes 2-bit codes by comparing fp16 inputs with exact per-group decision
+// thresholds (kvq_quantizer.cuh) instead of dividing.
 #include <cuda_fp16.h>
 
 #include "kvq_internal.h"
@@ -97,39 +101,31 @@ __device__ __forceinline__ void pack_chunk(const uint16_t* x, const Params& grp,
   for (int k = 0; k < BITS; ++k) out[k] = w[k];
 }
 
-// Threads of one page CTA: the common-shape variant runs 512 (it needs about 35 registers, and
-// its fragment packing gives keys and values to separate halves), the general one 256.
-template <bool STD>
-__host__ __device__ constexpr int quant_threads() { return STD ? 2 * kQuantThreads : kQuantThreads; }
-
-template <int BK, int BV, bool STD>
-__global__ void __launch_bounds__(quant_threads<STD>(), STD ? 3 : 2) quantize_pages_kernel(const QuantizeParams p) {
-  constexpr int NT = quant_threads<STD>();
+// The general page kernel: any R, G, sparse entries, bitstream or fragment order, codebooks.  The
+// common page shape has its own kernel below (quantize_std_kernel).
+template <int BK, int BV>
+__global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const QuantizeParams p) {
+  constexpr int NT = kQuantThreads;
   const int page = blockIdx.x;
   const int unit = blockIdx.y;
-  // STD: the common page shape (StdPage) with compile-time sizes and offsets
-  using SP = StdPage<BK, BV>;
-  const int D = STD ? kHeadDim : p.D, R = STD ? 128 : p.R, G = STD ? 32 : p.G, nsp = STD ? 0 : p.nsp;
-  const bool frag = STD ? true : p.lay.frag != 0;
-  const int lay_bytes = STD ? SP::bytes : p.lay.bytes;
-  const int off_kc = STD ? SP::kc : p.lay.off_kc, off_km = STD ? SP::km : p.lay.off_km;
-  const int off_vc = STD ? SP::vc : p.lay.off_vc, off_vm = STD ? SP::vm : p.lay.off_vm;
+  const int D = p.D, R = p.R, G = p.G, nsp = p.nsp;
+  const bool frag = p.lay.frag != 0;
+  const int lay_bytes = p.lay.bytes;
+  const int off_kc = p.lay.off_kc, off_km = p.lay.off_km;
+  const int off_vc = p.lay.off_vc, off_vm = p.lay.off_vm;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   constexpr int LK = (1 << BK) - 1, LV = (1 << BV) - 1;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  // the common shape writes its page straight to global memory (16-byte stores, coalesced per warp),
-  // which leaves room for three CTAs per SM; the general kernel assembles it in shared memory
-  const QuantSmem sm = quant_smem(R, D, G, STD ? 0 : lay_bytes);
+  // the page is assembled in shared memory and leaves by one bulk copy
+  const QuantSmem sm = quant_smem(R, D, G, lay_bytes);
   uint16_t* kt = reinterpret_cast<uint16_t*>(smem + sm.kt);  // [R][D]
   uint16_t* vt = reinterpret_cast<uint16_t*>(smem + sm.vt);  // [R][D]
   GroupQ* kq = reinterpret_cast<GroupQ*>(smem + sm.kq);      // [R/G][D]
   GroupQ* vq = reinterpret_cast<GroupQ*>(smem + sm.vq);      // [R][D/G]
   uint8_t* sidx = smem + sm.sidx;                            // [R][kMaxSparse]
-  uint8_t* const dst_page =
-      p.pages + (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)lay_bytes;
-  uint8_t* pg = STD ? dst_page : smem + sm.pg;                // page image (or the page itself)
+  uint8_t* pg = smem + sm.pg;                                // page image
   __shared__ __align__(8) uint64_t bar;
   __shared__ float thr_s[2][16];  // codebook decision thresholds (keys, values)
 
@@ -137,6 +133,16 @@ __global__ void __launch_bounds__(quant_threads<STD>(), STD ? 3 : 2) quantize_pa
   const uint16_t* ksrc = p.k_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
   const uint16_t* vsrc = p.v_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
   uint8_t* dst = p.pages + (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)lay_bytes;
+#ifdef KVQ_DEBUG_CHECKS
+  {
+    const int64_t so = (int64_t)unit * p.src_unit_stride + tok0 * D;
+    const int64_t po = (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)lay_bytes;
+    if (so < 0 || so + (int64_t)R * D > p.src_elems || po < 0 || po + lay_bytes > p.pages_bytes) {
+      if (tid == 0) report_error(p.err, kDevBounds);
+      return;  // the whole CTA, before any barrier
+    }
+  }
+#endif
 
   if (tid == 0) {
     mbar_init(&bar, 1);
@@ -405,7 +411,7 @@ __global__ void __launch_bounds__(quant_threads<STD>(), STD ? 3 : 2) quantize_pa
                      vthr);
     }
   }
-  if constexpr (!STD) {
+  {
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
@@ -413,6 +419,298 @@ __global__ void __launch_bounds__(quant_threads<STD>(), STD ? 3 : 2) quantize_pa
       bulk_commit();
       bulk_wait_all();
     }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// The common page shape (R = 128, D = 128, G = 32, 2- or 4-bit codes in fragment order, no sparse
+// entries, uniform codes): one CTA of 512 threads per page, three CTAs per SM.  Warps 0-7 take the
+// keys and warps 8-15 the values, through three phases separated by two barriers:
+//   fill    keys: 16-byte cp.async copies into a token-major tile; values: 16-byte loads of 8
+//           tokens x 8 channels, transposed in registers into a channel-major tile of token pairs
+//           (every operand register of the value products pairs two tokens of one channel);
+//   ranges  keys: a thread per (32-token group, channel pair) walks its column; values: a thread
+//           per (token pair, 32-channel group) walks its row; both on fp16 pairs (fp16 minimum and
+//           maximum are exact), then the zero point, the step and -- for 2-bit codes -- the three
+//           fp16 decision thresholds of each group (kvq::qthr), or the group quantizer (4-bit);
+//   codes   a thread per (16-token tile, lane) builds that lane's fragment words: 2-bit codes by
+//           comparing fp16 pairs with the thresholds (three packed compares per two codes), 4-bit
+//           codes with the group quantizer; each thread stores its words with 16-byte stores.
+// Both tiles are XOR-swizzled in 16-byte chunks so that no phase has shared-memory bank
+// conflicts: key row t keeps chunk c at c ^ (t & 7); value row (channel) c keeps chunk q at
+// q ^ ((c ^ (c >> 3)) & 7).
+constexpr int kStdThreads = 512;
+
+__device__ __forceinline__ int kswz(int cp, int tok) { return (((cp >> 2) ^ (tok & 7)) << 2) | (cp & 3); }
+__device__ __forceinline__ int vswz(int tp, int ch) { return (((tp >> 2) ^ ((ch ^ (ch >> 3)) & 7)) << 2) | (tp & 3); }
+
+// Shared memory of the common-shape kernel, in 32-bit words.
+template <int BK, int BV>
+struct StdSmem {
+  static constexpr int ks = 0;                                            // [128 tok][64] key pairs
+  static constexpr int vt = ks + 128 * 64;                                // [128 ch][64] value token pairs
+  static constexpr int kt = vt + 128 * 64;                                // thresholds [4][3][64] | GroupQ [4][128]
+  static constexpr int vth = kt + (BK == 2 ? 4 * 3 * 64 : 4 * 128 * 2);  // thresholds [4][3][64] | GroupQ [128][4]
+  static constexpr int vms = vth + (BV == 2 ? 4 * 3 * 64 : 128 * 4 * 2);  // value zero point / step words [128][4]
+  static constexpr int words = vms + 128 * 4;
+  static constexpr size_t bytes = (size_t)words * 4;
+};
+
+__device__ __forceinline__ __half2 as_h2(uint32_t x) {
+  __half2 h;
+  memcpy(&h, &x, 4);
+  return h;
+}
+
+// 2-bit codes of an fp16 pair against each half's thresholds t0 <= t1 <= t2: codes at bits 0-1
+// and 16-17 (code = number of thresholds reached: bit 0 = odd count, bit 1 = at least two).
+__device__ __forceinline__ uint32_t code2_pair(uint32_t x, uint32_t t0, uint32_t t1, uint32_t t2) {
+  const __half2 xh = as_h2(x);
+  const uint32_t m0 = __hge2_mask(xh, as_h2(t0)), m1 = __hge2_mask(xh, as_h2(t1)), m2 = __hge2_mask(xh, as_h2(t2));
+  return ((m0 ^ m1 ^ m2) & 0x00010001u) | (m1 & 0x00020002u);
+}
+
+// 4-bit codes of an fp16 pair with each half's quantizer: codes at bits 0-3 and 16-19.
+__device__ __forceinline__ uint32_t code4_pair(uint32_t x, const GroupQ& q0, const GroupQ& q1) {
+  const float2 f = __half22float2(as_h2(x));
+  return quant_code(f.x, q0, 15) | (quant_code(f.y, q1, 15) << 16);
+}
+
+__device__ __forceinline__ uint32_t comp(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+
+template <int BK, int BV>
+__global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const QuantizeParams p) {
+  static_assert((BK == 2 || BK == 4) && (BV == 2 || BV == 4), "fragment-order pages hold 2- or 4-bit codes");
+  using SP = StdPage<BK, BV>;
+  using SM = StdSmem<BK, BV>;
+  constexpr int D = kHeadDim;
+  const int page = blockIdx.x, unit = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool keys = warp < 8;
+  const int wl = warp & 7, ht = tid & 255;
+  extern __shared__ __align__(128) uint32_t sw[];
+  uint32_t* const ks = sw + SM::ks;
+  uint32_t* const vt = sw + SM::vt;
+
+  const int64_t tok0 = p.src_tok0 + (int64_t)page * 128;
+  const uint16_t* ksrc = p.k_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
+  const uint16_t* vsrc = p.v_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
+  uint8_t* const dst = p.pages + (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)SP::bytes;
+#ifdef KVQ_DEBUG_CHECKS
+  {
+    const int64_t so = (int64_t)unit * p.src_unit_stride + tok0 * D;
+    const int64_t po = (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)SP::bytes;
+    if (so < 0 || so + 128 * D > p.src_elems || po < 0 || po + SP::bytes > p.pages_bytes) {
+      if (tid == 0) report_error(p.err, kDevBounds);
+      return;  // the whole CTA, before any barrier
+    }
+  }
+#endif
+
+  // ---- fill
+  if (keys) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = ht + 256 * i, row = q >> 4, c16 = q & 15;
+      cp_async16(ks + row * 64 + ((c16 ^ (row & 7)) << 2), ksrc + row * D + c16 * 8);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+  } else {
+    const int o = ht >> 4, c8 = ht & 15;  // token octet, channel octet
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      // the upper channel octets take the two token quads in the other order: the 16 lanes of a
+      // half-warp then store to 16 different 8-byte slots
+      const int half = hh ^ (c8 >> 3);
+      uint4 r[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        r[i] = __ldcs(reinterpret_cast<const uint4*>(vsrc + (8 * o + 4 * half + i) * D + 8 * c8));
+      const int tp = 4 * o + 2 * half;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t a0 = comp(r[0], w), a1 = comp(r[1], w), a2 = comp(r[2], w), a3 = comp(r[3], w);
+        const int ch0 = 8 * c8 + 2 * w, ch1 = ch0 + 1;
+        *reinterpret_cast<uint2*>(vt + ch0 * 64 + vswz(tp, ch0)) =
+            make_uint2(__byte_perm(a0, a1, 0x5410), __byte_perm(a2, a3, 0x5410));
+        *reinterpret_cast<uint2*>(vt + ch1 * 64 + vswz(tp, ch1)) =
+            make_uint2(__byte_perm(a0, a1, 0x7632), __byte_perm(a2, a3, 0x7632));
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- ranges, zero points and steps, thresholds
+  {
+    const int grp = wl >> 1, pos = 32 * (wl & 1) + lane;  // keys: (token group, channel pair); values: (channel group, token pair)
+    // the swizzled word of this thread's column in row i of its group is base[(i & 7) ^ ...]: eight
+    // per-thread offsets cover the 32 rows of the scan
+    __half2 mn, mx;
+    if (keys) {
+      // key row 32*grp + t keeps chunk (pos >> 2) at (pos >> 2) ^ (t & 7)
+      const uint32_t* col = ks + 32 * grp * 64;
+      int off[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) off[k] = (((pos >> 2) ^ k) << 2) | (pos & 3);
+      mn = mx = as_h2(col[off[0]]);
+#pragma unroll
+      for (int t = 1; t < 32; ++t) {
+        const __half2 v = as_h2(col[t * 64 + off[t & 7]]);
+        mn = __hmin2(mn, v);
+        mx = __hmax2(mx, v);
+      }
+    } else {
+      // value row (channel) 32*grp + c keeps chunk (pos >> 2) at (pos >> 2) ^ ((c & 7) ^ (c >> 3) ^ 4*(grp & 1))
+      const uint32_t* col = vt + 32 * grp * 64;
+      int off[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) off[k] = (((pos >> 2) ^ k ^ (4 * (grp & 1))) << 2) | (pos & 3);
+      mn = mx = as_h2(col[off[0]]);
+#pragma unroll
+      for (int c = 1; c < 32; ++c) {
+        const __half2 v = as_h2(col[c * 64 + off[(c & 7) ^ (c >> 3)]]);
+        mn = __hmin2(mn, v);
+        mx = __hmax2(mx, v);
+      }
+    }
+    const float2 fmn = __half22float2(mn), fmx = __half22float2(mx);
+    // the two groups of this thread: keys channels 2*pos, 2*pos + 1; values tokens 2*pos, 2*pos + 1
+    const int B = keys ? BK : BV;
+    uint32_t zs0, zs1;
+    if (B == 2) {
+      uint32_t ta[3], tb[3];
+      zs0 = qthr::thresholds2(fmn.x, fmx.x, ta);
+      zs1 = qthr::thresholds2(fmn.y, fmx.y, tb);
+      uint32_t* th = sw + (keys ? SM::kt : SM::vth) + grp * 3 * 64 + pos;
+#pragma unroll
+      for (int k = 0; k < 3; ++k) th[k * 64] = ta[k] | (tb[k] << 16);
+    } else {
+      const GroupQ q0 = group_params(fmn.x, fmx.x, 15), q1 = group_params(fmn.y, fmx.y, 15);
+      zs0 = q0.bits;
+      zs1 = q1.bits;
+      GroupQ* gq = reinterpret_cast<GroupQ*>(sw + (keys ? SM::kt : SM::vth));
+      if (keys) {
+        gq[grp * 128 + 2 * pos] = q0;
+        gq[grp * 128 + 2 * pos + 1] = q1;
+      } else {
+        gq[(2 * pos) * 4 + grp] = q0;
+        gq[(2 * pos + 1) * 4 + grp] = q1;
+      }
+    }
+    if (keys) {
+      *reinterpret_cast<uint2*>(dst + SP::km + (grp * 128 + 2 * pos) * 4) = make_uint2(zs0, zs1);
+    } else {
+      sw[SM::vms + (2 * pos) * 4 + grp] = zs0;
+      sw[SM::vms + (2 * pos + 1) * 4 + grp] = zs1;
+    }
+  }
+  __syncthreads();
+
+  // ---- codes in fragment order: thread = (16-token tile wl, lane).  Every load address is a
+  //      per-lane base plus a compile-time offset: the XOR swizzle only depends on the lane (g8)
+  //      and on loop constants, so the swizzled chunk offsets are taken once per lane.
+  const int g8 = lane >> 2, t4 = lane & 3;
+  if (keys) {
+    // key rows 16m + g8 + 8r (row & 7 = g8); the lane's channel pairs are cp = 16q + 4j + t4 (4-bit
+    // words: q = word index u) or 32u + 4j + t4 (2-bit words), chunk cp >> 2, swizzled by g8
+    const int m = wl, gk = m >> 1;
+    const uint32_t* kr = ks + (16 * m + g8) * 64 + t4;
+    int sj[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sj[j] = (j ^ g8) << 2;
+    uint32_t wd[2 * BK];
+#pragma unroll
+    for (int i = 0; i < 2 * BK; ++i) wd[i] = 0;
+    if constexpr (BK == 2) {
+      // word r*2 + u, pair j: channel pair 32u + 4j + t4 (chunk 8u + j)
+      const uint32_t* th = sw + SM::kt + gk * 3 * 64 + t4;
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t t0 = th[32 * u + 4 * j], t1 = th[64 + 32 * u + 4 * j], t2 = th[128 + 32 * u + 4 * j];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const __half2 x = as_h2(kr[r * 8 * 64 + 32 * u + sj[j]]);
+            const uint32_t m0 = __hge2_mask(x, as_h2(t0)), m1 = __hge2_mask(x, as_h2(t1)),
+                           m2 = __hge2_mask(x, as_h2(t2));
+            // code = thresholds reached: bit 0 = odd count, bit 1 = at least two
+            wd[r * 2 + u] |= ((m0 ^ m1 ^ m2) & (0x00010001u << (2 * j))) | (m1 & (0x00020002u << (2 * j)));
+          }
+        }
+    } else {
+      // word r*4 + u, pair j: channel pair 16u + 4j + t4 (chunk 4u + j)
+      const GroupQ* gq = reinterpret_cast<const GroupQ*>(sw + SM::kt) + gk * 128 + 2 * t4;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = 4 * u + j;  // chunk
+          const GroupQ q0 = gq[2 * (16 * u + 4 * j)], q1 = gq[2 * (16 * u + 4 * j) + 1];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const uint32_t x = kr[r * 8 * 64 + 4 * (c & 8) + sj[c & 7]];
+            wd[r * 4 + u] |= code4_pair(x, q0, q1) << (4 * j);
+          }
+        }
+    }
+    uint4* o = reinterpret_cast<uint4*>(dst + SP::kc) + (m * 32 + lane) * (2 * BK / 4);
+#pragma unroll
+    for (int i = 0; i < 2 * BK / 4; ++i) o[i] = make_uint4(wd[4 * i], wd[4 * i + 1], wd[4 * i + 2], wd[4 * i + 3]);
+  } else {
+    // value token pairs tp = 8m + 4(r >> 1) + t4 (chunk 2m ^ (r >> 1)), channels ch = 16mc + g8 + 8(r & 1)
+    // (ch & 7 = g8, ch >> 3 = 2mc + (r & 1)): the swizzled chunk is (2m ^ g8) ^ K with
+    // K = (r >> 1) ^ ((2mc + (r & 1)) & 7), so eight per-lane bases cover every load
+    const int m = wl;
+    const int A = (2 * m) ^ g8;
+    const uint32_t* vb[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) vb[k] = vt + g8 * 64 + (((A ^ k) << 2) | t4);
+    uint32_t wd[2 * BV];
+#pragma unroll
+    for (int i = 0; i < 2 * BV; ++i) wd[i] = 0;
+    if constexpr (BV == 2) {
+      // word r, pair j = M-tile mc; thresholds of (token pair, group mc >> 1)
+      const uint32_t* th = sw + SM::vth + 8 * m + t4;
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh)
+#pragma unroll
+        for (int gv = 0; gv < 4; ++gv) {
+          const uint32_t t0 = th[gv * 192 + 4 * rh], t1 = th[gv * 192 + 64 + 4 * rh], t2 = th[gv * 192 + 128 + 4 * rh];
+#pragma unroll
+          for (int rl = 0; rl < 2; ++rl)
+#pragma unroll
+            for (int jl = 0; jl < 2; ++jl) {
+              const int r = 2 * rh + rl, j = 2 * gv + jl;
+              const int K = rh ^ ((2 * j + rl) & 7);
+              const __half2 x = as_h2(vb[K][(16 * j + 8 * rl) * 64]);
+              const uint32_t m0 = __hge2_mask(x, as_h2(t0)), m1 = __hge2_mask(x, as_h2(t1)),
+                             m2 = __hge2_mask(x, as_h2(t2));
+              wd[r] |= ((m0 ^ m1 ^ m2) & (0x00010001u << (2 * j))) | (m1 & (0x00020002u << (2 * j)));
+            }
+        }
+    } else {
+      // word r*2 + u, pair j: M-tile mc = 4u + j
+      const GroupQ* gq = reinterpret_cast<const GroupQ*>(sw + SM::vth) + (2 * (8 * m + t4)) * 4;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int mc = 4 * u + j, gv = mc >> 1;
+            const int K = (r >> 1) ^ ((2 * mc + (r & 1)) & 7);
+            const uint32_t x = vb[K][(16 * mc + 8 * (r & 1)) * 64];
+            const int tb = 2 * 4 * (r >> 1);  // token offset 8(r >> 1), times 4 groups per token
+            wd[r * 2 + u] |= code4_pair(x, gq[tb * 4 + gv], gq[(tb + 1) * 4 + gv]) << (4 * j);
+          }
+    }
+    uint4* o = reinterpret_cast<uint4*>(dst + SP::vc) + (m * 32 + lane) * (2 * BV / 4);
+#pragma unroll
+    for (int i = 0; i < 2 * BV / 4; ++i) o[i] = make_uint4(wd[4 * i], wd[4 * i + 1], wd[4 * i + 2], wd[4 * i + 3]);
+    // the value zero points and steps (2 KB) leave in 16-byte stores
+    if (ht < 128) reinterpret_cast<uint4*>(dst + SP::vm)[ht] = reinterpret_cast<const uint4*>(sw + SM::vms)[ht];
   }
 }
 
@@ -436,12 +734,22 @@ cudaError_t launch_quantize_t(const QuantizeParams& p, int n_pages, cudaStream_t
   const bool std_shape = can_std && p.R == 128 && p.D == kHeadDim && p.G == 32 && p.nsp == 0 && p.lay.frag &&
                          !p.lut && p.lay.bytes == SP::bytes && p.lay.off_kc == SP::kc && p.lay.off_km == SP::km &&
                          p.lay.off_vc == SP::vc && p.lay.off_vm == SP::vm;
-  auto kern = std_shape ? quantize_pages_kernel<BK, BV, can_std> : quantize_pages_kernel<BK, BV, false>;
-  const size_t smem = std_shape ? quant_smem(p.R, p.D, p.G, 0).total : quantize_smem_bytes(p.R, p.D, p.G, p.lay);
+  dim3 grid((unsigned)n_pages, (unsigned)p.n_units);
+  if constexpr (can_std) {
+    if (std_shape) {
+      constexpr size_t smem = StdSmem<BK, BV>::bytes;
+      cudaError_t e = cudaFuncSetAttribute(quantize_std_kernel<BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+      if (e != cudaSuccess) return e;
+      quantize_std_kernel<BK, BV><<<grid, kStdThreads, smem, s>>>(p);
+      return cudaGetLastError();
+    }
+  }
+  auto kern = quantize_pages_kernel<BK, BV>;
+  const size_t smem = quantize_smem_bytes(p.R, p.D, p.G, p.lay);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)n_pages, (unsigned)p.n_units);
-  kern<<<grid, std_shape ? quant_threads<can_std>() : kQuantThreads, smem, s>>>(p);
+  kern<<<grid, kQuantThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 

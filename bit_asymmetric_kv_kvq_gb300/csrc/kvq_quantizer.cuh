@@ -79,3 +79,144 @@ __device__ __forceinline__ uint32_t code_of(float x, const GroupQ& g, int L, con
 
 }  // namespace
 }  // namespace kvq
+
+// ---------------------------------------------------------------------------------------------
+// Decision thresholds of the uniform quantizer, for comparing fp16 inputs directly.
+//
+// For a group with stored zero point z and step s > 0 (fp16 values widened to fp32), the code of an
+// fp16 value x is clamp(rint(q), 0, L) with q = fl(fl(x - z) / s), both roundings to nearest even.
+// It is non-decreasing in x, so for every k < L there is a smallest fp16 value t_k whose code is
+// at least k + 1, and code(x) = #{k : x >= t_k} for every x of the group.  t_k is found by testing
+// "code(x) >= k + 1" exactly, without a division:
+//
+//   with h = k + 1/2 and d = fl(x - z) >= 0, rint(q) >= k + 1 means q > h, or q == h when k + 1 is
+//   even (ties go to even).  h has at most five significant bits, so it is even as an fp32 value
+//   and the fp32 numbers next to it are h -/+ ulp(h) (h is not a power of two for k >= 1; for
+//   k = 0, h = 1/2 and only the number above it matters).  Rounding to nearest then gives
+//     k odd :  q >= h       <=>  d / s >= h - ulp(h)/2   (a tie rounds to h, which is even)
+//     k even:  q >= h + ulp <=>  d / s >  h + ulp(h)/2   (a tie rounds to h, not above it)
+//   With A = h*s and B = -/+ s*ulp(h)/2 (both exact in fp32: 5 + 11 significant bits, and a power
+//   of two times s), that is d - A >= B (k odd) or d - A > B (k even).  fl(d - A) decides it
+//   exactly: within a factor of two of A the subtraction is exact (Sterbenz), and outside it
+//   |d - A| >= A/2 is far larger than |B| <= A * 2^-24, so the rounded difference has the same
+//   order against B as the exact one.
+//
+// The candidate t_k is the fp16 rounding of z + A + B; the exact test at it and at its neighbour
+// confirms it (or its neighbour) almost always, and a bisection over the fp16 values between the
+// group's minimum (code 0) and maximum settles the rest.  A threshold no value of the group reaches
+// is +inf (0x7C00), which no finite input passes.
+namespace kvq {
+namespace qthr {
+
+__host__ __device__ __forceinline__ float sub_rn(float a, float b) {
+#ifdef __CUDA_ARCH__
+  return __fsub_rn(a, b);
+#else
+  volatile float r = a - b;
+  return r;
+#endif
+}
+__host__ __device__ __forceinline__ float add_rn(float a, float b) {
+#ifdef __CUDA_ARCH__
+  return __fadd_rn(a, b);
+#else
+  volatile float r = a + b;
+  return r;
+#endif
+}
+__host__ __device__ __forceinline__ float mul_rn(float a, float b) {
+#ifdef __CUDA_ARCH__
+  return __fmul_rn(a, b);
+#else
+  volatile float r = a * b;
+  return r;
+#endif
+}
+__host__ __device__ __forceinline__ float div_rn(float a, float b) {
+#ifdef __CUDA_ARCH__
+  return __fdiv_rn(a, b);
+#else
+  volatile float r = a / b;
+  return r;
+#endif
+}
+__host__ __device__ __forceinline__ float half_to_float(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+__host__ __device__ __forceinline__ uint16_t float_to_half(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+// fp16 bit patterns in value order (-0 and +0 both 0), and back
+__host__ __device__ __forceinline__ int ord(uint32_t b) { return (b & 0x8000u) ? -(int)(b & 0x7FFFu) : (int)b; }
+__host__ __device__ __forceinline__ uint32_t bits_of(int o) { return o >= 0 ? (uint32_t)o : (0x8000u | (uint32_t)(-o)); }
+
+// 2^e as an fp32 constant (-40 < e < 40)
+__host__ __device__ constexpr float pow2(int e) { return e == 0 ? 1.0f : e > 0 ? 2.0f * pow2(e - 1) : 0.5f * pow2(e + 1); }
+
+// h = k + 1/2 and the signed half-ulp factor of the test above (B = s * bfac)
+__host__ __device__ constexpr int half_exp(int k) { return k == 0 ? -1 : k < 2 ? 0 : k < 4 ? 1 : k < 8 ? 2 : 3; }
+__host__ __device__ constexpr float bfac(int k) { return ((k & 1) ? -1.0f : 1.0f) * pow2(half_exp(k) - 24); }
+
+// code(x) >= k + 1, exactly (z, A = (k+1/2)*s, B = s*bfac(k))
+template <int K>
+__host__ __device__ __forceinline__ bool above(float x, float z, float A, float B) {
+  const float e = sub_rn(sub_rn(x, z), A);
+  return (K & 1) ? e >= B : e > B;
+}
+
+// t_k of a group with zero point z, step s > 0, minimum and maximum in value order lo0 < hi0.  Only
+// the group's values are ever compared with it, so any value above the maximum serves when the
+// maximum does not reach code k + 1 (the candidate may then land past it, up to +inf).
+template <int K>
+__host__ __device__ __forceinline__ uint32_t threshold(float z, float s, int lo0, int hi0) {
+  const float A = mul_rn(s, (float)K + 0.5f), B = mul_rn(s, bfac(K));
+  // the candidate and the neighbour on the other side of the test (the minimum, lo0, always fails)
+  const int o = ord(float_to_half(add_rn(add_rn(z, A), B)));
+  const bool pc = o > lo0 && above<K>(half_to_float((uint16_t)bits_of(o)), z, A, B);
+  const int o2 = pc ? o - 1 : o + 1;
+  const bool p2 = o2 > lo0 && above<K>(half_to_float((uint16_t)bits_of(o2)), z, A, B);
+  if (pc != p2) return bits_of(pc ? o : o2);
+  int lo, hi;  // above() is false at lo and true at hi (or hi is past the maximum)
+  if (pc) {
+    lo = lo0;
+    hi = o2;
+  } else {
+    lo = o2;
+    hi = hi0;
+    if (lo >= hi || !above<K>(half_to_float((uint16_t)bits_of(hi0)), z, A, B)) return 0x7C00u;
+  }
+  while (hi - lo > 1) {  // at most 16 halvings of the fp16 value range
+    const int mid = (lo + hi) >> 1;
+    if (above<K>(half_to_float((uint16_t)bits_of(mid)), z, A, B)) hi = mid;
+    else lo = mid;
+  }
+  return bits_of(hi);
+}
+
+// Zero point and step of a group from its exact fp16 minimum and maximum (as in group_params):
+// returns the stored pair (zero point low, step high) and the widened values.
+template <int L>
+__host__ __device__ __forceinline__ uint32_t zero_step(float mn, float mx, float* z, float* s) {
+  mn = add_rn(mn, 0.0f);  // -0 -> +0
+  float range = sub_rn(mx, mn);
+  if (!(range > 0.0f)) range = 0.0f;
+  const uint16_t zb = float_to_half(mn), sb = float_to_half(div_rn(range, (float)L));
+  *z = half_to_float(zb);
+  *s = half_to_float(sb);
+  return (uint32_t)zb | ((uint32_t)sb << 16);
+}
+
+// The three thresholds of a 2-bit group (t[0] <= t[1] <= t[2]); all +inf for a zero step.
+__host__ __device__ __forceinline__ uint32_t thresholds2(float mn, float mx, uint32_t t[3]) {
+  float z, s;
+  const uint32_t zs = zero_step<3>(mn, mx, &z, &s);
+  if (!(s > 0.0f)) {
+    t[0] = t[1] = t[2] = 0x7C00u;
+    return zs;
+  }
+  const int lo0 = ord(float_to_half(mn)), hi0 = ord(float_to_half(mx));
+  t[0] = threshold<0>(z, s, lo0, hi0);
+  t[1] = threshold<1>(z, s, lo0, hi0);
+  t[2] = threshold<2>(z, s, lo0, hi0);
+  return zs;
+}
+
+}  // namespace qthr
+}  // namespace kvq

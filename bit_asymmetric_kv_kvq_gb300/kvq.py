@@ -20,7 +20,8 @@ import numpy as np
 
 from . import _build
 
-LIB_PATH = _build.LIB
+# KVQ_LIB selects another build of the library (the debug build of the tests)
+LIB_PATH = os.environ.get("KVQ_LIB") or _build.LIB
 
 KVQ_OK = 0
 KVQ_ERR_INVALID_ARG = -1
@@ -83,6 +84,9 @@ SIGNATURES = {
     "kvq_set_splits": (ctypes.c_int, [_P, ctypes.c_int32]),
     "kvq_get_splits": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "kvq_sync_status": (ctypes.c_int, [_P, _P]),
+    "kvq_test_inject": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64]),
+    "kvq_debug_check": (ctypes.c_int, [_P]),
+    "kvq_set_device_allocator": (ctypes.c_int, [_P, _P, _P]),
     "kvq_launch_count": (ctypes.c_int64, [_P]),
     "kvq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kvq_version": (ctypes.c_int32, []),
@@ -224,6 +228,29 @@ def kvq_get_splits(handle) -> int:
 
 def kvq_sync_status(handle, stream=None) -> int:
     return int(lib().kvq_sync_status(handle, _stream(stream)))
+
+
+def kvq_test_inject(handle, withhold_page: int, wait_limit_ns: int) -> None:
+    """Test hook: shorten the decode kernels' wait limit and leave one page uncopied (see include/kvq.h)."""
+    _check(lib().kvq_test_inject(handle, withhold_page, wait_limit_ns), "kvq_test_inject")
+
+
+def kvq_debug_check(handle) -> int:
+    """Debug builds: error word and buffer canaries of a cache (KVQ_OK when intact)."""
+    return int(lib().kvq_debug_check(handle))
+
+
+# C function types of kvq_set_device_allocator
+KVQ_ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p)
+KVQ_FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p)
+
+
+def kvq_set_device_allocator(alloc=None, free_fn=None, user=None) -> None:
+    """Device allocator of caches created from now on: KVQ_ALLOC_FN / KVQ_FREE_FN objects (keep them
+    alive while any cache made with them exists), or None and None for cudaMalloc / cudaFree."""
+    _check(lib().kvq_set_device_allocator(ctypes.cast(alloc, ctypes.c_void_p) if alloc else None,
+                                          ctypes.cast(free_fn, ctypes.c_void_p) if free_fn else None, user),
+           "kvq_set_device_allocator")
 
 
 def kvq_launch_count(handle) -> int:

@@ -47,6 +47,7 @@
 #ifndef KVQ_H
 #define KVQ_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -101,6 +102,21 @@ typedef struct kvq_cache kvq_cache; /* opaque */
  * KVQ_ERR_OOM, KVQ_ERR_CUDA.  On error *out is set to NULL.
  */
 kvq_status kvq_create(const kvq_config* cfg, int device, kvq_cache** out);
+
+/*
+ * Device memory of the caches created from now on (process-wide; each cache keeps the functions
+ * it was created with and frees through them).  alloc(bytes, device, user) returns device memory
+ * of `device` aligned to 256 bytes, or NULL when it has none; free_fn(ptr, device, user) gives it
+ * back.  For callers that manage GPU memory in a pool of their own.  Both NULL: cudaMalloc and
+ * cudaFree (the default).  A cache allocates only in kvq_create and kvq_set_splits; when an
+ * allocation fails, kvq_create frees what it had allocated and returns KVQ_ERR_OOM (a block that
+ * is not 256-byte aligned is handed back and counts as KVQ_ERR_INVALID_ARG).  Not thread-safe
+ * against a concurrent kvq_create.  KVQ_ERR_INVALID_ARG if exactly one of the two is NULL.
+ * (The method pages have no counterpart.)
+ */
+typedef void* (*kvq_alloc_fn)(size_t bytes, int device, void* user);
+typedef void (*kvq_free_fn)(void* ptr, int device, void* user);
+kvq_status kvq_set_device_allocator(kvq_alloc_fn alloc, kvq_free_fn free_fn, void* user);
 
 /* Free the cache and its device memory (synchronizes the device first).
    NULL is a no-op returning KVQ_OK. */
@@ -229,8 +245,8 @@ kvq_status kvq_reset(kvq_cache* cache);
  * KVQ_ERR_UNSUPPORTED, and KVQ_ERR_CAPACITY when even the smallest launch's
  * partials do not fit the 8 MiB array: B*Hq*(D+2)*4 bytes per partial slot,
  * 3*W slots per query head for a one-CTA launch (W = warps of one decode CTA:
- * 16 on the tensor-core kernel, 12 there with four query heads per kv head; 8
- * to 16 on the CUDA-core kernel), plus one counter per unit, after a fixed
+ * 16 on the tensor-core kernel, 8 to 16 on the CUDA-core kernel), plus one
+ * counter per unit, after a fixed
  * head of 4.3 KB.  Larger sizes run on fewer CTAs than the GPU holds, as many
  * as the array allows.  KVQ_ERR_CAPACITY also refuses a ninth distinct
  * rope_base on one device (the array keeps the turn tables of eight).
@@ -357,6 +373,29 @@ kvq_status kvq_get_splits(const kvq_cache* cache, int32_t* splits);
  * and records an error code instead of hanging.
  */
 kvq_status kvq_sync_status(kvq_cache* cache, void* cuda_stream);
+
+/*
+ * Test hook for the device-side time limits (not for production use).  Every wait of the decode
+ * kernels -- for a page copy to land, for a stage to be released -- gives up after a time limit
+ * (2 s by default), records an error in the cache's error word and lets the kernel finish without
+ * leaving copies in flight; kvq_sync_status then reports KVQ_ERR_CUDA.  This hook makes that path
+ * testable without a fault: for the decode launches that follow, wait_limit_ns > 0 replaces the
+ * default limit, and withhold_page = k >= 0 leaves page k of every CTA's slice of the work list
+ * uncopied, so the warps that reach it wait until the limit runs out.  (-1, 0) restores normal
+ * operation.  Outputs of affected launches are not meaningful.  KVQ_ERR_INVALID_ARG for
+ * withhold_page < -1 or wait_limit_ns < 0.  (The method pages have no counterpart.)
+ */
+kvq_status kvq_test_inject(kvq_cache* cache, int32_t withhold_page, int64_t wait_limit_ns);
+
+/*
+ * Debug builds only (the library compiled with KVQ_DEBUG_CHECKS, e.g. bit_asymmetric_kv_kvq_gb300/_build.py
+ * --debug): waits for the device, then checks the cache's error word -- where the kernels' bounds
+ * checks of debug builds and the time limits of every build record -- and the canary bytes that
+ * follow each of the cache's device buffers in debug builds.  KVQ_OK when all are intact,
+ * KVQ_ERR_CUDA otherwise; KVQ_ERR_UNSUPPORTED in a normal build.  A stand-in for a device memory
+ * checker.  (The method pages have no counterpart.)
+ */
+kvq_status kvq_debug_check(kvq_cache* cache);
 
 /* Kernel launches issued by this cache since creation (decode, append, flush...). */
 int64_t kvq_launch_count(const kvq_cache* cache);

@@ -115,8 +115,8 @@ def test_noalloc_matches_regular_decode_twice(case):
     elif case == "gqa-rope-sparse-3bit":
         w = synth.WORKLOADS[4].scaled(batch=1, kv_heads=2, q_heads=8, prefill_tokens=900, decode_steps=2)
     else:
-        # 72 units of four query heads (the 12-warp tensor-core kernel): on a 152-SM GPU the full
-        # resident grid needs 12 * (ceil(152/72) + 2) = 60 slots per head, 8.6 MB of partials, more
+        # 72 units of four query heads (the tensor-core kernel, 16 warps): on a 152-SM GPU the full
+        # resident grid needs 16 * (ceil(152/72) + 2) = 80 slots per head, 12 MB of partials, more
         # than the 8 MiB array holds, so the call lowers the grid until they fit
         w = synth.WORKLOADS[3].scaled(batch=9, kv_heads=8, q_heads=32, prefill_tokens=300, decode_steps=2)
     K = synth.keys(w)
