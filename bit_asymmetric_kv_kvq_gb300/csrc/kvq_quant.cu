@@ -462,14 +462,6 @@ __device__ __forceinline__ __half2 as_h2(uint32_t x) {
   return h;
 }
 
-// 2-bit codes of an fp16 pair against each half's thresholds t0 <= t1 <= t2: codes at bits 0-1
-// and 16-17 (code = number of thresholds reached: bit 0 = odd count, bit 1 = at least two).
-__device__ __forceinline__ uint32_t code2_pair(uint32_t x, uint32_t t0, uint32_t t1, uint32_t t2) {
-  const __half2 xh = as_h2(x);
-  const uint32_t m0 = __hge2_mask(xh, as_h2(t0)), m1 = __hge2_mask(xh, as_h2(t1)), m2 = __hge2_mask(xh, as_h2(t2));
-  return ((m0 ^ m1 ^ m2) & 0x00010001u) | (m1 & 0x00020002u);
-}
-
 // 4-bit codes of an fp16 pair with each half's quantizer: codes at bits 0-3 and 16-19.
 __device__ __forceinline__ uint32_t code4_pair(uint32_t x, const GroupQ& q0, const GroupQ& q1) {
   const float2 f = __half22float2(as_h2(x));
@@ -714,6 +706,250 @@ __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const Quan
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Pages whose codes are token-major bitstreams (3-bit codes, or keys rotated at decode; uniform
+// codes), R = 128, D = 128, G = 32 or 64, up to four sparse entries per key vector: one CTA of 512
+// threads per page, two CTAs per SM (64 registers), the tiles and swizzles of quantize_std_kernel.
+//   fill     as in quantize_std_kernel;
+//   phase 2  warps 0-3: the sparse entries of each key vector, a thread per token scanning its row
+//            in channel order (largest |x|, ties to the lower channel); each entry is written out
+//            and replaced in the tile by a NaN, which the fp16 minimum and maximum skip and which
+//            quantizes to code 0 -- exactly the exclusion the method asks for.  Warps 8-15: value
+//            ranges and quantizers, a thread per (token pair, channel group);
+//   phase 3  warps 0-7: key ranges and quantizers, a thread per (token group, channel pair);
+//            warps 8-15: value codes, a thread per (token pair, 32-channel chunk);
+//   phase 4  key codes, a thread per (token, 32-channel chunk).
+// Codes come from the group quantizer (quant_code) and are packed 32 at a time into B words.
+template <int BK, int BV>
+__global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const QuantizeParams p) {
+  constexpr int D = kHeadDim, R = 128;
+  constexpr int LK = (1 << BK) - 1, LV = (1 << BV) - 1;
+  constexpr int WK = D * BK / 32, WV = D * BV / 32;  // words of one token's bitstream
+  const int G = p.G, nsp = p.nsp;
+  const int ngv = D / G, ngk = R / G;  // value groups per token, key groups per page
+  const int page = blockIdx.x, unit = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ht = tid & 255;
+  extern __shared__ __align__(128) uint32_t sw[];
+  uint32_t* const ks = sw;                                            // [128 tok][64] key pairs
+  uint32_t* const vt = sw + 128 * 64;                                 // [128 ch][64] value token pairs
+  GroupQ* const kq = reinterpret_cast<GroupQ*>(sw + 2 * 128 * 64);    // [R/G][D]
+  GroupQ* const vq = kq + 4 * 128;                                    // [R][D/G]
+  const int64_t tok0 = p.src_tok0 + (int64_t)page * R;
+  const uint16_t* ksrc = p.k_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
+  const uint16_t* vsrc = p.v_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
+  uint8_t* const dst = p.pages + (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)p.lay.bytes;
+#ifdef KVQ_DEBUG_CHECKS
+  {
+    const int64_t so = (int64_t)unit * p.src_unit_stride + tok0 * D;
+    const int64_t po = (int64_t)unit * p.unit_page_stride + (p.page0 + page) * (int64_t)p.lay.bytes;
+    if (so < 0 || so + R * D > p.src_elems || po < 0 || po + p.lay.bytes > p.pages_bytes) {
+      if (tid == 0) report_error(p.err, kDevBounds);
+      return;  // the whole CTA, before any barrier
+    }
+  }
+#endif
+
+  // ---- fill (as in quantize_std_kernel)
+  if (warp < 8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = ht + 256 * i, row = q >> 4, c16 = q & 15;
+      cp_async16(ks + row * 64 + ((c16 ^ (row & 7)) << 2), ksrc + row * D + c16 * 8);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+  } else {
+    const int o = ht >> 4, c8 = ht & 15;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int half = hh ^ (c8 >> 3);
+      uint4 r[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        r[i] = __ldcs(reinterpret_cast<const uint4*>(vsrc + (8 * o + 4 * half + i) * D + 8 * c8));
+      const int tp = 4 * o + 2 * half;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t a0 = comp(r[0], w), a1 = comp(r[1], w), a2 = comp(r[2], w), a3 = comp(r[3], w);
+        const int ch0 = 8 * c8 + 2 * w, ch1 = ch0 + 1;
+        *reinterpret_cast<uint2*>(vt + ch0 * 64 + vswz(tp, ch0)) =
+            make_uint2(__byte_perm(a0, a1, 0x5410), __byte_perm(a2, a3, 0x5410));
+        *reinterpret_cast<uint2*>(vt + ch1 * 64 + vswz(tp, ch1)) =
+            make_uint2(__byte_perm(a0, a1, 0x7632), __byte_perm(a2, a3, 0x7632));
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 2: sparse key entries (warps 0-3); value ranges and quantizers (warps 8-15)
+  if (warp < 4) {
+    if (nsp > 0) {
+      const int t = tid;  // token
+      // the nsp largest |x| in channel order (|x| as fp16 bits orders like its value), kept
+      // sorted by value; a later channel displaces an entry only when strictly larger
+      int bv[kMaxSparse], bi[kMaxSparse];
+#pragma unroll
+      for (int k = 0; k < kMaxSparse; ++k) {
+        bv[k] = -1;
+        bi[k] = 0;
+      }
+      int cut = -1;  // bv[nsp - 1]
+      auto insert = [&](int v, int c) {
+        if (v <= cut) return;
+#pragma unroll
+        for (int k = kMaxSparse - 1; k >= 0; --k) {
+          if (k >= nsp) continue;
+          const bool above = k == 0 || v <= bv[k - 1];  // v lands at slot k
+          if (v > bv[k]) {
+            if (above) {
+              bv[k] = v;
+              bi[k] = c;
+            } else {
+              bv[k] = bv[k - 1];
+              bi[k] = bi[k - 1];
+            }
+          }
+        }
+        cut = bv[0];
+#pragma unroll
+        for (int k = 1; k < kMaxSparse; ++k)
+          if (k < nsp) cut = bv[k];
+      };
+      const uint32_t* row = ks + t * 64;
+#pragma unroll 2
+      for (int ch = 0; ch < 16; ++ch) {  // 16-byte chunks of 8 channels
+        const uint4 v = *reinterpret_cast<const uint4*>(row + ((ch ^ (t & 7)) << 2));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t a = w4[e] & 0x7FFF7FFFu;
+          const int lo = (int)(a & 0xFFFFu), hi = (int)(a >> 16);
+          if (max(lo, hi) > cut) {
+            insert(lo, 8 * ch + 2 * e);
+            insert(hi, 8 * ch + 2 * e + 1);
+          }
+        }
+      }
+      // ascending channel order, then out: the channel, the exact fp16 value; the tile entry
+      // becomes a NaN
+      for (int i = 1; i < nsp; ++i) {
+        const int c = bi[i];
+        int j = i - 1;
+        while (j >= 0 && bi[j] > c) {
+          bi[j + 1] = bi[j];
+          --j;
+        }
+        bi[j + 1] = c;
+      }
+      uint8_t* si = dst + p.lay.off_si + t * nsp;
+      uint16_t* sv = reinterpret_cast<uint16_t*>(dst + p.lay.off_sv) + t * nsp;
+      uint16_t* rowh = reinterpret_cast<uint16_t*>(ks + t * 64);
+      for (int k = 0; k < nsp; ++k) {
+        const int c = bi[k];
+        const int hw = 2 * ((((c >> 3) ^ (t & 7)) << 2) | ((c >> 1) & 3)) + (c & 1);  // half index in the row
+        si[k] = (uint8_t)c;
+        sv[k] = rowh[hw];
+        rowh[hw] = 0x7E00u;  // NaN
+      }
+    }
+  } else if (warp >= 8) {
+    for (int it = ht; it < 64 * ngv; it += 256) {
+      const int g = it >> 6, tp = it & 63;  // tokens 2*tp, 2*tp + 1; channels G*g ..
+      const int c0 = G * g;
+      __half2 mn = as_h2(vt[c0 * 64 + vswz(tp, c0)]), mx = mn;
+      for (int c = 1; c < G; ++c) {
+        const __half2 v = as_h2(vt[(c0 + c) * 64 + vswz(tp, c0 + c)]);
+        mn = __hmin2(mn, v);
+        mx = __hmax2(mx, v);
+      }
+      const float2 fmn = __half22float2(mn), fmx = __half22float2(mx);
+      const GroupQ q0 = group_params(fmn.x, fmx.x, LV), q1 = group_params(fmn.y, fmx.y, LV);
+      vq[(2 * tp) * ngv + g] = q0;
+      vq[(2 * tp + 1) * ngv + g] = q1;
+      uint32_t* vm = reinterpret_cast<uint32_t*>(dst + p.lay.off_vm);
+      vm[(2 * tp) * ngv + g] = q0.bits;
+      vm[(2 * tp + 1) * ngv + g] = q1.bits;
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 3: key ranges and quantizers (warps 0-7); value codes (warps 8-15)
+  if (warp < 8) {
+    for (int it = tid; it < ngk * 64; it += 256) {
+      const int gk = it >> 6, cp = it & 63;  // token group, channel pair
+      const int r0 = G * gk;
+      // NaN (a sparse entry) never wins a minimum or maximum against a number
+      __half2 mn = as_h2(ks[r0 * 64 + kswz(cp, r0)]), mx = mn;
+      for (int t = 1; t < G; ++t) {
+        const __half2 v = as_h2(ks[(r0 + t) * 64 + kswz(cp, r0 + t)]);
+        mn = __hmin2(mn, v);
+        mx = __hmax2(mx, v);
+      }
+      float2 fmn = __half22float2(mn), fmx = __half22float2(mx);
+      if (fmn.x != fmn.x) fmn.x = fmx.x = 0.0f;  // every entry sparse: range 0
+      if (fmn.y != fmn.y) fmn.y = fmx.y = 0.0f;
+      const GroupQ q0 = group_params(fmn.x, fmx.x, LK), q1 = group_params(fmn.y, fmx.y, LK);
+      kq[gk * 128 + 2 * cp] = q0;
+      kq[gk * 128 + 2 * cp + 1] = q1;
+      *reinterpret_cast<uint2*>(dst + p.lay.off_km + (gk * 128 + 2 * cp) * 4) = make_uint2(q0.bits, q1.bits);
+    }
+  } else {
+    const int q = ht >> 6, tp = ht & 63;  // 32-channel chunk, token pair
+    const int g = (32 * q) / G;
+    const GroupQ qa = vq[(2 * tp) * ngv + g], qb = vq[(2 * tp + 1) * ngv + g];
+    uint32_t wa[BV], wb[BV];
+#pragma unroll
+    for (int i = 0; i < BV; ++i) wa[i] = wb[i] = 0;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int ch = 32 * q + c;
+      const float2 f = __half22float2(as_h2(vt[ch * 64 + vswz(tp, ch)]));
+      const uint32_t ca = quant_code(f.x, qa, LV), cb = quant_code(f.y, qb, LV);
+      const int b = BV * c;
+      wa[b >> 5] |= ca << (b & 31);
+      wb[b >> 5] |= cb << (b & 31);
+      if ((b & 31) + BV > 32) {
+        wa[(b >> 5) + 1] |= ca >> (32 - (b & 31));
+        wb[(b >> 5) + 1] |= cb >> (32 - (b & 31));
+      }
+    }
+    uint32_t* vc = reinterpret_cast<uint32_t*>(dst + p.lay.off_vc);
+#pragma unroll
+    for (int i = 0; i < BV; ++i) {
+      vc[(2 * tp) * WV + q * BV + i] = wa[i];
+      vc[(2 * tp + 1) * WV + q * BV + i] = wb[i];
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 4: key codes, thread = (token, 32-channel chunk)
+  {
+    const int q = warp >> 2, t = ((warp & 3) << 5) | lane;
+    const GroupQ* gq = kq + (t / G) * 128 + 32 * q;
+    uint32_t w[BK];
+#pragma unroll
+    for (int i = 0; i < BK; ++i) w[i] = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = *reinterpret_cast<const uint4*>(ks + t * 64 + (((4 * q + i) ^ (t & 7)) << 2));
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = 8 * i + e;
+        const uint16_t xb = (uint16_t)((e & 1) ? (w4[e >> 1] >> 16) : (w4[e >> 1] & 0xFFFFu));
+        const uint32_t code = quant_code(h2f(xb), gq[c], LK);  // a NaN (sparse entry) gives 0
+        const int b = BK * c;
+        w[b >> 5] |= code << (b & 31);
+        if ((b & 31) + BK > 32) w[(b >> 5) + 1] |= code >> (32 - (b & 31));
+      }
+    }
+    uint32_t* kc = reinterpret_cast<uint32_t*>(dst + p.lay.off_kc);
+#pragma unroll
+    for (int i = 0; i < BK; ++i) kc[t * WK + q * BK + i] = w[i];
+  }
+}
+
 __global__ void copy_tokens_kernel(const CopyTokensParams p) {
   const int unit = blockIdx.x;
   const int64_t n16 = (int64_t)p.n_tok * p.D / 8;  // 16-byte vectors per tensor
@@ -744,6 +980,15 @@ cudaError_t launch_quantize_t(const QuantizeParams& p, int n_pages, cudaStream_t
       quantize_std_kernel<BK, BV><<<grid, kStdThreads, smem, s>>>(p);
       return cudaGetLastError();
     }
+  }
+  if (!p.lay.frag && !p.lut && p.R == 128 && p.D == kHeadDim && (p.G == 32 || p.G == 64) && p.nsp <= kMaxSparse) {
+    constexpr size_t smem = StdSmem<2, 2>::bytes;  // the same two tiles; quantizers in place of thresholds
+    static_assert((2 * 128 * 64 + 4 * 128 * 2 + 128 * 4 * 2) * 4 <= smem, "bitstream page kernel smem");
+    cudaError_t e = cudaFuncSetAttribute(quantize_bits_kernel<BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    quantize_bits_kernel<BK, BV><<<grid, kStdThreads, smem, s>>>(p);
+    return cudaGetLastError();
   }
   auto kern = quantize_pages_kernel<BK, BV>;
   const size_t smem = quantize_smem_bytes(p.R, p.D, p.G, p.lay);

@@ -72,7 +72,7 @@ def test_decode_wait_runs_out_and_is_reported(case):
     cache, K, V = _filled_cache(w)
     assert cache.sync_status() == 0
     q = _dev(synth.queries(w, 0))
-    kvq.kvq.kvq_test_inject(cache.handle, 1, 1_000_000)  # page 1 of every slice never arrives; 1 ms limit
+    kvq.kvq.kvq_test_inject(cache.handle, 0, 1_000_000)  # page 0 of every slice never arrives; 1 ms limit
     t0 = time.perf_counter()
     cache.decode_attention(q)
     st = cache.sync_status()
