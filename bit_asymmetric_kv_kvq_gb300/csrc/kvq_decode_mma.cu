@@ -567,14 +567,16 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     float sc[2][2];
     // every lane computes (no branch); lanes past the heads take head 0 and are masked below
     const int hq = t4 < HG ? t4 : 0;
-    const float zz = HG == 1 ? zl : __shfl_sync(kAll, zl, (32 / HG) * hq);
+    // scores in log2 units: the softmax scale folded into the product's scale and into Z
+    const float zz = (HG == 1 ? zl : __shfl_sync(kAll, zl, (32 / HG) * hq)) * p.qk_scale_log2;
+    const float sgl = sgk * p.qk_scale_log2;
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
       const float* d = dsum[mt];
       float s0 = -INFINITY, s1 = -INFINITY;
       {
-        s0 = fmaf(d[0] + d[1], sgk, zz);
-        s1 = fmaf(d[2] + d[3], sgk, zz);
+        s0 = fmaf(d[0] + d[1], sgl, zz);
+        s1 = fmaf(d[2] + d[3], sgl, zz);
         if (nsp > 0) {
           // sparse entries: the dense code there is 0 (value z); add q_c (x_c - z_c)
           const uint8_t* si = pgm + p.lay.off_si;
@@ -589,12 +591,12 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
               const float z = __half2float(__ushort_as_half((uint16_t)(km[gk * D + c] & 0xFFFFu)));
               add = fmaf(qs[hq][c], xv - z, add);
             }
-            if (rh == 0) s0 += add;
-            else s1 += add;
+            if (rh == 0) s0 = fmaf(add, p.qk_scale_log2, s0);
+            else s1 = fmaf(add, p.qk_scale_log2, s1);
           }
         }
-        s0 = t4 < HG ? s0 * p.qk_scale_log2 : -INFINITY;
-        s1 = t4 < HG ? s1 * p.qk_scale_log2 : -INFINITY;
+        s0 = t4 < HG ? s0 : -INFINITY;
+        s1 = t4 < HG ? s1 : -INFINITY;
       }
       sc[mt][0] = s0;
       sc[mt][1] = s1;
@@ -677,12 +679,15 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
       const int la = 4 * (2 * t4) + hcol, lb = 4 * (2 * t4 + 1) + hcol;
       const float p0 = __shfl_sync(kAll, sc[kc][0], la), p1 = __shfl_sync(kAll, sc[kc][0], lb);
       const float p2 = __shfl_sync(kAll, sc[kc][1], la), p3 = __shfl_sync(kAll, sc[kc][1], lb);
-      const float pb0 = p0 * bscale, pb1 = p1 * bscale, pb2 = p2 * bscale, pb3 = p3 * bscale;
+      const float2 p01 = make_float2(p0, p1), p23 = make_float2(p2, p3);
+      const float2 pb01 = __fmul2_rn(p01, make_float2(bscale, bscale)), pb23 = __fmul2_rn(p23, make_float2(bscale, bscale));
       uint32_t bv[NBM][2];
 #pragma unroll
       for (int bi = 0; bi < NBM; ++bi) {
-        bv[bi][0] = h2bits(__floats2half2_rn(pb0 * vs[kc][bi][0], pb1 * vs[kc][bi][1]));
-        bv[bi][1] = h2bits(__floats2half2_rn(pb2 * vs[kc][bi][2], pb3 * vs[kc][bi][3]));
+        const float2 b01 = __fmul2_rn(pb01, make_float2(vs[kc][bi][0], vs[kc][bi][1]));
+        const float2 b23 = __fmul2_rn(pb23, make_float2(vs[kc][bi][2], vs[kc][bi][3]));
+        bv[bi][0] = h2bits(__floats2half2_rn(b01.x, b01.y));
+        bv[bi][1] = h2bits(__floats2half2_rn(b23.x, b23.y));
         zacc[bi] = fmaf(p0, vz[kc][bi][0], fmaf(p1, vz[kc][bi][1], fmaf(p2, vz[kc][bi][2], fmaf(p3, vz[kc][bi][3], zacc[bi]))));
       }
       lacc += (p0 + p1) + (p2 + p3);  // read from the lanes of B column h (lane 4h)

@@ -711,15 +711,68 @@ __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const Quan
 // codes), R = 128, D = 128, G = 32 or 64, up to four sparse entries per key vector: one CTA of 512
 // threads per page, two CTAs per SM (64 registers), the tiles and swizzles of quantize_std_kernel.
 //   fill     as in quantize_std_kernel;
-//   phase 2  warps 0-3: the sparse entries of each key vector, a thread per token scanning its row
-//            in channel order (largest |x|, ties to the lower channel); each entry is written out
-//            and replaced in the tile by a NaN, which the fp16 minimum and maximum skip and which
-//            quantizes to code 0 -- exactly the exclusion the method asks for.  Warps 8-15: value
-//            ranges and quantizers, a thread per (token pair, channel group);
-//   phase 3  warps 0-7: key ranges and quantizers, a thread per (token group, channel pair);
-//            warps 8-15: value codes, a thread per (token pair, 32-channel chunk);
-//   phase 4  key codes, a thread per (token, 32-channel chunk).
-// Codes come from the group quantizer (quant_code) and are packed 32 at a time into B words.
+//   sparse   a thread per (token, 32-channel quarter) finds the quarter's largest |x| in channel
+//            order, the four lanes of a token merge their lists by shuffles (larger |x| first,
+//            ties to the lower channel); each entry is written out and replaced in the tile by a
+//            NaN, which the fp16 minimum and maximum skip and which quantizes to code 0 --
+//            exactly the exclusion the method asks for;
+//   ranges   warps 0-7: key ranges and quantizers, a thread per (token group, channel pair);
+//            warps 8-15: value ranges and quantizers, a thread per (token pair, channel group);
+//   codes    every thread: the key codes of one (token, 32-channel chunk) and the value codes of
+//            one (token, 32-channel chunk), each packed 32 at a time into B words.
+// A code comes from the group's reciprocal; elements whose product lies within 2^-14 of a
+// half-integer (where it could round differently from the IEEE quotient) are collected in a mask
+// and taken again with the IEEE quotient after the loop, behind one vote per chunk.
+struct __align__(8) QuantF {  // a group quantizer in the form the code loop uses
+  float inv, z;
+};
+// shared memory of quantize_bits_kernel: the two tiles, the key and value quantizers (QuantF) and
+// their stored (zero point, step) words
+constexpr size_t kBitsSmemBytes = (size_t)(2 * 128 * 64 + 4 * 128 * 2 + 128 * 4 * 2 + 4 * 128 + 128 * 4) * 4;
+
+// Codes of 32 channels of one token (x: fp16 values, e-th of chunk at (w4[e/2] >> 16*(e&1))) into
+// BITS words; q(c) gives channel c's quantizer and bits(c) its stored (zero point, step).
+// xval(c) is called with compile-time c in the main loop; xdyn(c) and qbits(c) only in the rare
+// pass over near-tie elements, with a run-time c (so they read shared memory, not register arrays).
+template <int BITS, class QF, class QB, class XF, class XD>
+__device__ __forceinline__ void code_chunk(const XF& xval, const XD& xdyn, const QF& qf, const QB& qbits,
+                                           uint32_t (&w)[BITS]) {
+  constexpr int L = (1 << BITS) - 1;
+#pragma unroll
+  for (int i = 0; i < BITS; ++i) w[i] = 0;
+  uint32_t near = 0;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const QuantF q = qf(c);
+    const float d = __fsub_rn(xval(c), q.z);  // a NaN (sparse entry) stays NaN and gives code 0
+    const float r = __fmul_rn(d, q.inv);
+    const float rq = rintf(r);
+    near |= (fabsf(__fsub_rn(r, rq)) >= 0.5f - 0x1.0p-14f ? 1u : 0u) << c;
+    const uint32_t code = (uint32_t)fminf(fmaxf(rq, 0.0f), (float)L);
+    const int b = BITS * c;
+    w[b >> 5] |= code << (b & 31);
+    if ((b & 31) + BITS > 32) w[(b >> 5) + 1] |= code >> (32 - (b & 31));
+  }
+  if (__any_sync(0xffffffffu, near != 0)) {
+    while (near) {
+      const int c = __ffs(near) - 1;
+      near &= near - 1;
+      const uint32_t zs = qbits(c);
+      const float sf = h2f((uint16_t)(zs >> 16));
+      const float rq = rintf(__fdiv_rn(__fsub_rn(xdyn(c), h2f((uint16_t)(zs & 0xFFFFu))), sf));  // s > 0 here
+      const uint32_t code = (uint32_t)fminf(fmaxf(rq, 0.0f), (float)L);
+      const int b = BITS * c;
+      const uint64_t m = (uint64_t)L << (b & 31);
+      const uint64_t v = (uint64_t)code << (b & 31);
+#pragma unroll
+      for (int i = 0; i < BITS; ++i) {  // word b >> 5 and, for a code that straddles, the next one
+        if (i == (b >> 5)) w[i] = (w[i] & ~(uint32_t)m) | (uint32_t)v;
+        if (i == (b >> 5) + 1) w[i] = (w[i] & ~(uint32_t)(m >> 32)) | (uint32_t)(v >> 32);
+      }
+    }
+  }
+}
+
 template <int BK, int BV>
 __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const QuantizeParams p) {
   constexpr int D = kHeadDim, R = 128;
@@ -731,10 +784,12 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ht = tid & 255;
   extern __shared__ __align__(128) uint32_t sw[];
-  uint32_t* const ks = sw;                                            // [128 tok][64] key pairs
-  uint32_t* const vt = sw + 128 * 64;                                 // [128 ch][64] value token pairs
-  GroupQ* const kq = reinterpret_cast<GroupQ*>(sw + 2 * 128 * 64);    // [R/G][D]
-  GroupQ* const vq = kq + 4 * 128;                                    // [R][D/G]
+  uint32_t* const ks = sw;                                           // [128 tok][64] key pairs
+  uint32_t* const vt = sw + 128 * 64;                                // [128 ch][64] value token pairs
+  QuantF* const kqf = reinterpret_cast<QuantF*>(sw + 2 * 128 * 64);  // [R/G][D]
+  QuantF* const vqf = kqf + 4 * 128;                                 // [R][D/G]
+  uint32_t* const kzs = reinterpret_cast<uint32_t*>(vqf + 128 * 4);  // [R/G][D] stored (zero point, step)
+  uint32_t* const vzs = kzs + 4 * 128;                               // [R][D/G]
   const int64_t tok0 = p.src_tok0 + (int64_t)page * R;
   const uint16_t* ksrc = p.k_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
   const uint16_t* vsrc = p.v_src + (int64_t)unit * p.src_unit_stride + tok0 * D;
@@ -782,91 +837,169 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
   }
   __syncthreads();
 
-  // ---- phase 2: sparse key entries (warps 0-3); value ranges and quantizers (warps 8-15)
-  if (warp < 4) {
-    if (nsp > 0) {
-      const int t = tid;  // token
-      // the nsp largest |x| in channel order (|x| as fp16 bits orders like its value), kept
-      // sorted by value; a later channel displaces an entry only when strictly larger
-      int bv[kMaxSparse], bi[kMaxSparse];
+  // ---- sparse key entries: thread = (token t, quarter qt of 32 channels); lanes 4t' .. 4t'+3 of a
+  //      warp hold one token's four quarters.  |x| as fp16 bits orders like its value; entry (v, c)
+  //      outranks (v', c') when v > v', or v == v' and c < c' (ties to the lower channel).
+  if (nsp > 0) {
+    const int t = tid >> 2, qt = tid & 3;
+    const uint32_t* row = ks + t * 64;
+    int bc[kMaxSparse];  // the chosen channels (unused slots hold a channel past the end)
+    if (nsp <= 2) {
+      // two slots, branch-free: within the quarter channels come in increasing order, so a later
+      // channel enters only when strictly larger
+      int v0 = -1, c0 = 1 << 20, v1 = -1, c1 = 1 << 20;
 #pragma unroll
-      for (int k = 0; k < kMaxSparse; ++k) {
-        bv[k] = -1;
-        bi[k] = 0;
-      }
-      int cut = -1;  // bv[nsp - 1]
-      auto insert = [&](int v, int c) {
-        if (v <= cut) return;
-#pragma unroll
-        for (int k = kMaxSparse - 1; k >= 0; --k) {
-          if (k >= nsp) continue;
-          const bool above = k == 0 || v <= bv[k - 1];  // v lands at slot k
-          if (v > bv[k]) {
-            if (above) {
-              bv[k] = v;
-              bi[k] = c;
-            } else {
-              bv[k] = bv[k - 1];
-              bi[k] = bi[k - 1];
-            }
-          }
-        }
-        cut = bv[0];
-#pragma unroll
-        for (int k = 1; k < kMaxSparse; ++k)
-          if (k < nsp) cut = bv[k];
-      };
-      const uint32_t* row = ks + t * 64;
-#pragma unroll 2
-      for (int ch = 0; ch < 16; ++ch) {  // 16-byte chunks of 8 channels
+      for (int i = 0; i < 4; ++i) {
+        const int ch = 4 * qt + i;  // 16-byte chunk: channels 8ch .. 8ch+7
         const uint4 v = *reinterpret_cast<const uint4*>(row + ((ch ^ (t & 7)) << 2));
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t a = w4[e] & 0x7FFF7FFFu;
-          const int lo = (int)(a & 0xFFFFu), hi = (int)(a >> 16);
-          if (max(lo, hi) > cut) {
-            insert(lo, 8 * ch + 2 * e);
-            insert(hi, 8 * ch + 2 * e + 1);
+        for (int e = 0; e < 8; ++e) {
+          const int x = (int)((w4[e >> 1] >> (16 * (e & 1))) & 0x7FFFu), c = 8 * ch + e;
+          const bool g0 = x > v0, g1 = x > v1;
+          v1 = g0 ? v0 : (g1 ? x : v1);
+          c1 = g0 ? c0 : (g1 ? c : c1);
+          v0 = g0 ? x : v0;
+          c0 = g0 ? c : c0;
+        }
+      }
+      // merge the four quarters' pairs (the partner's channels lie in another quarter)
+#pragma unroll
+      for (int off = 1; off < 4; off <<= 1) {
+        const int w0 = __shfl_xor_sync(0xffffffffu, v0, off), d0 = __shfl_xor_sync(0xffffffffu, c0, off);
+        const int w1 = __shfl_xor_sync(0xffffffffu, v1, off), d1 = __shfl_xor_sync(0xffffffffu, c1, off);
+        const bool a = v0 > w0 || (v0 == w0 && c0 < d0);  // own head first
+        // the runner-up: the loser of the heads against the winner's second
+        const int lv = a ? w0 : v0, lc = a ? d0 : c0, sv2 = a ? v1 : w1, sc2 = a ? c1 : d1;
+        const bool b = lv > sv2 || (lv == sv2 && lc < sc2);
+        const int nv0 = a ? v0 : w0, nc0 = a ? c0 : d0;
+        v1 = b ? lv : sv2;
+        c1 = b ? lc : sc2;
+        v0 = nv0;
+        c0 = nc0;
+      }
+      bc[0] = min(c0, c1);
+      bc[1] = nsp == 2 ? max(c0, c1) : (1 << 20);
+      bc[0] = nsp == 2 ? bc[0] : c0;
+#pragma unroll
+      for (int k = 2; k < kMaxSparse; ++k) bc[k] = 1 << 20;
+    } else {
+      int bv[kMaxSparse];
+#pragma unroll
+      for (int k = 0; k < kMaxSparse; ++k) {
+        bv[k] = -1;
+        bc[k] = 1 << 20;
+      }
+      auto outranks = [](int v, int c, int v2, int c2) { return v > v2 || (v == v2 && c < c2); };
+      auto insert = [&](int v, int c) {
+#pragma unroll
+        for (int k = kMaxSparse - 1; k >= 0; --k) {
+          if (k >= nsp || !outranks(v, c, bv[k], bc[k])) continue;
+          if (k == 0 || !outranks(v, c, bv[k - 1], bc[k - 1])) {
+            bv[k] = v;
+            bc[k] = c;
+          } else {
+            bv[k] = bv[k - 1];
+            bc[k] = bc[k - 1];
           }
         }
+      };
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int ch = 4 * qt + i;
+        const uint4 v = *reinterpret_cast<const uint4*>(row + ((ch ^ (t & 7)) << 2));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) insert((int)((w4[e >> 1] >> (16 * (e & 1))) & 0x7FFFu), 8 * ch + e);
       }
-      // ascending channel order, then out: the channel, the exact fp16 value; the tile entry
-      // becomes a NaN
-      for (int i = 1; i < nsp; ++i) {
-        const int c = bi[i];
-        int j = i - 1;
-        while (j >= 0 && bi[j] > c) {
-          bi[j + 1] = bi[j];
-          --j;
+#pragma unroll
+      for (int off = 1; off < 4; off <<= 1) {
+        int ov[kMaxSparse], oc[kMaxSparse];
+#pragma unroll
+        for (int k = 0; k < kMaxSparse; ++k) {
+          ov[k] = __shfl_xor_sync(0xffffffffu, bv[k], off);
+          oc[k] = __shfl_xor_sync(0xffffffffu, bc[k], off);
         }
-        bi[j + 1] = c;
+#pragma unroll
+        for (int k = 0; k < kMaxSparse; ++k)
+          if (k < nsp) insert(ov[k], oc[k]);
       }
-      uint8_t* si = dst + p.lay.off_si + t * nsp;
-      uint16_t* sv = reinterpret_cast<uint16_t*>(dst + p.lay.off_sv) + t * nsp;
-      uint16_t* rowh = reinterpret_cast<uint16_t*>(ks + t * 64);
-      for (int k = 0; k < nsp; ++k) {
-        const int c = bi[k];
-        const int hw = 2 * ((((c >> 3) ^ (t & 7)) << 2) | ((c >> 1) & 3)) + (c & 1);  // half index in the row
-        si[k] = (uint8_t)c;
-        sv[k] = rowh[hw];
-        rowh[hw] = 0x7E00u;  // NaN
-      }
+      // ascending channel order (a sorting network; unused slots stay last)
+      auto order = [&](int i, int j) {
+        const int lo = min(bc[i], bc[j]), hi = max(bc[i], bc[j]);
+        bc[i] = lo;
+        bc[j] = hi;
+      };
+      order(0, 1);
+      order(2, 3);
+      order(0, 2);
+      order(1, 3);
+      order(1, 2);
     }
-  } else if (warp >= 8) {
+    // each lane writes and masks the entries of its own quarter
+    uint16_t* rowh = reinterpret_cast<uint16_t*>(ks + t * 64);
+#pragma unroll
+    for (int k = 0; k < kMaxSparse; ++k) {
+      const int c = bc[k];
+      if (k >= nsp || (c >> 5) != qt) continue;
+      const int hw = 2 * ((((c >> 3) ^ (t & 7)) << 2) | ((c >> 1) & 3)) + (c & 1);  // half index in the row
+      dst[p.lay.off_si + t * nsp + k] = (uint8_t)c;
+      reinterpret_cast<uint16_t*>(dst + p.lay.off_sv)[t * nsp + k] = rowh[hw];
+      rowh[hw] = 0x7E00u;  // NaN
+    }
+    __syncthreads();
+  }
+
+  // ---- ranges and quantizers: keys (warps 0-7), values (warps 8-15)
+  if (warp < 8) {
+    for (int it = tid; it < ngk * 64; it += 256) {
+      const int gk = it >> 6, cp = it & 63;  // token group, channel pair
+      const uint32_t* col = ks + G * gk * 64;
+      int off[8];  // row 8*b + k keeps chunk cp >> 2 at (cp >> 2) ^ k
+#pragma unroll
+      for (int k = 0; k < 8; ++k) off[k] = (((cp >> 2) ^ k) << 2) | (cp & 3);
+      // NaN (a sparse entry) never wins a minimum or maximum against a number: start from NaN
+      __half2 mn = as_h2(0x7E007E00u), mx = mn;
+      for (int tb = 0; tb < G; tb += 8) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const __half2 v = as_h2(col[(tb + k) * 64 + off[k]]);
+          mn = __hmin2(mn, v);
+          mx = __hmax2(mx, v);
+        }
+      }
+      float2 fmn = __half22float2(mn), fmx = __half22float2(mx);
+      if (fmn.x != fmn.x) fmn.x = fmx.x = 0.0f;  // every entry sparse: range 0
+      if (fmn.y != fmn.y) fmn.y = fmx.y = 0.0f;
+      const GroupQ q0 = group_params(fmn.x, fmx.x, LK), q1 = group_params(fmn.y, fmx.y, LK);
+      kqf[gk * 128 + 2 * cp] = QuantF{q0.inv, q0.zf()};
+      kqf[gk * 128 + 2 * cp + 1] = QuantF{q1.inv, q1.zf()};
+      kzs[gk * 128 + 2 * cp] = q0.bits;
+      kzs[gk * 128 + 2 * cp + 1] = q1.bits;
+      *reinterpret_cast<uint2*>(dst + p.lay.off_km + (gk * 128 + 2 * cp) * 4) = make_uint2(q0.bits, q1.bits);
+    }
+  } else {
     for (int it = ht; it < 64 * ngv; it += 256) {
-      const int g = it >> 6, tp = it & 63;  // tokens 2*tp, 2*tp + 1; channels G*g ..
+      const int g = it >> 6, tp = it & 63;  // channel group, tokens 2*tp, 2*tp + 1
       const int c0 = G * g;
-      __half2 mn = as_h2(vt[c0 * 64 + vswz(tp, c0)]), mx = mn;
-      for (int c = 1; c < G; ++c) {
-        const __half2 v = as_h2(vt[(c0 + c) * 64 + vswz(tp, c0 + c)]);
-        mn = __hmin2(mn, v);
-        mx = __hmax2(mx, v);
+      __half2 mn = as_h2(0x7E007E00u), mx = mn;  // values hold no NaN: the first row replaces these
+      for (int cb = 0; cb < G; cb += 8) {
+        // rows c0 + cb + k keep chunk tp >> 2 at (tp >> 2) ^ k ^ (((c0 + cb) >> 3) & 7)
+        const int u = (tp >> 2) ^ (((c0 + cb) >> 3) & 7);
+        const uint32_t* rows = vt + (c0 + cb) * 64 + (tp & 3);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const __half2 v = as_h2(rows[k * 64 + ((u ^ k) << 2)]);
+          mn = __hmin2(mn, v);
+          mx = __hmax2(mx, v);
+        }
       }
       const float2 fmn = __half22float2(mn), fmx = __half22float2(mx);
       const GroupQ q0 = group_params(fmn.x, fmx.x, LV), q1 = group_params(fmn.y, fmx.y, LV);
-      vq[(2 * tp) * ngv + g] = q0;
-      vq[(2 * tp + 1) * ngv + g] = q1;
+      vqf[(2 * tp) * ngv + g] = QuantF{q0.inv, q0.zf()};
+      vqf[(2 * tp + 1) * ngv + g] = QuantF{q1.inv, q1.zf()};
+      vzs[(2 * tp) * ngv + g] = q0.bits;
+      vzs[(2 * tp + 1) * ngv + g] = q1.bits;
       uint32_t* vm = reinterpret_cast<uint32_t*>(dst + p.lay.off_vm);
       vm[(2 * tp) * ngv + g] = q0.bits;
       vm[(2 * tp + 1) * ngv + g] = q1.bits;
@@ -874,79 +1007,59 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
   }
   __syncthreads();
 
-  // ---- phase 3: key ranges and quantizers (warps 0-7); value codes (warps 8-15)
-  if (warp < 8) {
-    for (int it = tid; it < ngk * 64; it += 256) {
-      const int gk = it >> 6, cp = it & 63;  // token group, channel pair
-      const int r0 = G * gk;
-      // NaN (a sparse entry) never wins a minimum or maximum against a number
-      __half2 mn = as_h2(ks[r0 * 64 + kswz(cp, r0)]), mx = mn;
-      for (int t = 1; t < G; ++t) {
-        const __half2 v = as_h2(ks[(r0 + t) * 64 + kswz(cp, r0 + t)]);
-        mn = __hmin2(mn, v);
-        mx = __hmax2(mx, v);
-      }
-      float2 fmn = __half22float2(mn), fmx = __half22float2(mx);
-      if (fmn.x != fmn.x) fmn.x = fmx.x = 0.0f;  // every entry sparse: range 0
-      if (fmn.y != fmn.y) fmn.y = fmx.y = 0.0f;
-      const GroupQ q0 = group_params(fmn.x, fmx.x, LK), q1 = group_params(fmn.y, fmx.y, LK);
-      kq[gk * 128 + 2 * cp] = q0;
-      kq[gk * 128 + 2 * cp + 1] = q1;
-      *reinterpret_cast<uint2*>(dst + p.lay.off_km + (gk * 128 + 2 * cp) * 4) = make_uint2(q0.bits, q1.bits);
-    }
-  } else {
-    const int q = ht >> 6, tp = ht & 63;  // 32-channel chunk, token pair
-    const int g = (32 * q) / G;
-    const GroupQ qa = vq[(2 * tp) * ngv + g], qb = vq[(2 * tp + 1) * ngv + g];
-    uint32_t wa[BV], wb[BV];
-#pragma unroll
-    for (int i = 0; i < BV; ++i) wa[i] = wb[i] = 0;
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int ch = 32 * q + c;
-      const float2 f = __half22float2(as_h2(vt[ch * 64 + vswz(tp, ch)]));
-      const uint32_t ca = quant_code(f.x, qa, LV), cb = quant_code(f.y, qb, LV);
-      const int b = BV * c;
-      wa[b >> 5] |= ca << (b & 31);
-      wb[b >> 5] |= cb << (b & 31);
-      if ((b & 31) + BV > 32) {
-        wa[(b >> 5) + 1] |= ca >> (32 - (b & 31));
-        wb[(b >> 5) + 1] |= cb >> (32 - (b & 31));
-      }
-    }
-    uint32_t* vc = reinterpret_cast<uint32_t*>(dst + p.lay.off_vc);
-#pragma unroll
-    for (int i = 0; i < BV; ++i) {
-      vc[(2 * tp) * WV + q * BV + i] = wa[i];
-      vc[(2 * tp + 1) * WV + q * BV + i] = wb[i];
-    }
-  }
-  __syncthreads();
-
-  // ---- phase 4: key codes, thread = (token, 32-channel chunk)
+  // ---- codes: every thread one key chunk and one value chunk
   {
+    // keys: (token t, chunk q); the quarter-warps read rows t .. t+7, whose swizzles differ
     const int q = warp >> 2, t = ((warp & 3) << 5) | lane;
-    const GroupQ* gq = kq + (t / G) * 128 + 32 * q;
-    uint32_t w[BK];
-#pragma unroll
-    for (int i = 0; i < BK; ++i) w[i] = 0;
+    const int gk = t / G;
+    uint32_t xw[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint4 v = *reinterpret_cast<const uint4*>(ks + t * 64 + (((4 * q + i) ^ (t & 7)) << 2));
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int c = 8 * i + e;
-        const uint16_t xb = (uint16_t)((e & 1) ? (w4[e >> 1] >> 16) : (w4[e >> 1] & 0xFFFFu));
-        const uint32_t code = quant_code(h2f(xb), gq[c], LK);  // a NaN (sparse entry) gives 0
-        const int b = BK * c;
-        w[b >> 5] |= code << (b & 31);
-        if ((b & 31) + BK > 32) w[(b >> 5) + 1] |= code >> (32 - (b & 31));
-      }
+      xw[4 * i] = v.x;
+      xw[4 * i + 1] = v.y;
+      xw[4 * i + 2] = v.z;
+      xw[4 * i + 3] = v.w;
     }
+    const QuantF* qf = kqf + gk * 128 + 32 * q;
+    const uint32_t* qb = kzs + gk * 128 + 32 * q;
+    uint32_t w[BK];
+    const uint16_t* rowh = reinterpret_cast<const uint16_t*>(ks + t * 64);
+    code_chunk<BK>([&](int c) { return h2f((uint16_t)((c & 1) ? (xw[c >> 1] >> 16) : (xw[c >> 1] & 0xFFFFu))); },
+                   [&](int c) {
+                     const int ch = 32 * q + c;
+                     return h2f(rowh[2 * ((((ch >> 3) ^ (t & 7)) << 2) | ((ch >> 1) & 3)) + (ch & 1)]);
+                   },
+                   [&](int c) { return qf[c]; }, [&](int c) { return qb[c]; }, w);
     uint32_t* kc = reinterpret_cast<uint32_t*>(dst + p.lay.off_kc);
 #pragma unroll
     for (int i = 0; i < BK; ++i) kc[t * WK + q * BK + i] = w[i];
+  }
+  {
+    // values: (token 2tp + hf, chunk q); the two lanes of a token pair read the same words
+    const int q = warp >> 2, hf = lane & 1, tp = ((warp & 3) << 4) | (lane >> 1);
+    const int tok = 2 * tp + hf, g = (32 * q) / G;
+    const QuantF qv = vqf[tok * ngv + g];
+    const uint32_t qvb = vzs[tok * ngv + g];
+    const int c0 = 32 * q;
+    int off[8];  // row c0 + c keeps chunk tp >> 2 at (tp >> 2) ^ ((c ^ (c >> 3)) & 7) ^ ((c0 >> 3) & 7)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) off[k] = (((tp >> 2) ^ k ^ ((c0 >> 3) & 7)) << 2) | (tp & 3);
+    const uint32_t* col = vt + c0 * 64;
+    uint32_t w[BV];
+    code_chunk<BV>(
+        [&](int c) {
+          const uint32_t x = col[c * 64 + off[(c ^ (c >> 3)) & 7]];
+          return h2f((uint16_t)(hf ? (x >> 16) : (x & 0xFFFFu)));
+        },
+        [&](int c) {
+          const uint32_t x = vt[(c0 + c) * 64 + vswz(tp, c0 + c)];
+          return h2f((uint16_t)(hf ? (x >> 16) : (x & 0xFFFFu)));
+        },
+        [&](int) { return qv; }, [&](int) { return qvb; }, w);
+    uint32_t* vc = reinterpret_cast<uint32_t*>(dst + p.lay.off_vc);
+#pragma unroll
+    for (int i = 0; i < BV; ++i) vc[tok * WV + q * BV + i] = w[i];
   }
 }
 
@@ -982,8 +1095,7 @@ cudaError_t launch_quantize_t(const QuantizeParams& p, int n_pages, cudaStream_t
     }
   }
   if (!p.lay.frag && !p.lut && p.R == 128 && p.D == kHeadDim && (p.G == 32 || p.G == 64) && p.nsp <= kMaxSparse) {
-    constexpr size_t smem = StdSmem<2, 2>::bytes;  // the same two tiles; quantizers in place of thresholds
-    static_assert((2 * 128 * 64 + 4 * 128 * 2 + 128 * 4 * 2) * 4 <= smem, "bitstream page kernel smem");
+    constexpr size_t smem = kBitsSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(quantize_bits_kernel<BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
