@@ -142,6 +142,8 @@ __host__ __device__ __forceinline__ float div_rn(float a, float b) {
 }
 __host__ __device__ __forceinline__ float half_to_float(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 __host__ __device__ __forceinline__ uint16_t float_to_half(float f) { return __half_as_ushort(__float2half_rn(f)); }
+__host__ __device__ __forceinline__ uint16_t half_rd(float f) { return __half_as_ushort(__float2half_rd(f)); }
+__host__ __device__ __forceinline__ uint16_t half_ru(float f) { return __half_as_ushort(__float2half_ru(f)); }
 
 // fp16 bit patterns in value order (-0 and +0 both 0), and back
 __host__ __device__ __forceinline__ int ord(uint32_t b) { return (b & 0x8000u) ? -(int)(b & 0x7FFFu) : (int)b; }
@@ -164,11 +166,28 @@ __host__ __device__ __forceinline__ bool above(float x, float z, float A, float 
 // t_k of a group with zero point z, step s > 0, minimum and maximum in value order lo0 < hi0.  Only
 // the group's values are ever compared with it, so any value above the maximum serves when the
 // maximum does not reach code k + 1 (the candidate may then land past it, up to +inf).
+//
+// Fast path: the test switches at a real X* with |X* - (z + A + B)| <= 1.5 ulp(A + B) (where
+// fl(x - z) crosses A + B), and y = fl(fl(z + A) + B) is within 2^-24 (|z + A| + |y|) of
+// z + A + B, so |y - X*| < 2^-21 (|z| + |A| + |y|) = eps/2.  Let a be the smallest and b the
+// largest fp16 value in [y - eps, y + eps] (the ends rounded in fp32 stay well inside the margin).
+// No fp16 value there (a > b): X* lies strictly between b and a, the next value up from b, and a
+// is t_k.  Exactly one, a == b: every value below a fails, every value above passes, and one test
+// at a decides between a and the next value up.  Two or more (an fp16 spacing below eps: values
+// far smaller than the group's range, rare) go to the exact search below.
 template <int K>
 __host__ __device__ __forceinline__ uint32_t threshold(float z, float s, int lo0, int hi0) {
   const float A = mul_rn(s, (float)K + 0.5f), B = mul_rn(s, bfac(K));
+  const float y = add_rn(add_rn(z, A), B);
+  {
+    const float eps = mul_rn(add_rn(add_rn(fabsf(z), A), fabsf(y)), 0x1.0p-20f);
+    const uint16_t a = half_ru(sub_rn(y, eps)), b = half_rd(add_rn(y, eps));
+    const float fa = half_to_float(a), fb = half_to_float(b);
+    if (fa > fb) return a;
+    if (fa == fb) return above<K>(fa, z, A, B) ? a : bits_of(ord(a) + 1);
+  }
   // the candidate and the neighbour on the other side of the test (the minimum, lo0, always fails)
-  const int o = ord(float_to_half(add_rn(add_rn(z, A), B)));
+  const int o = ord(float_to_half(y));
   const bool pc = o > lo0 && above<K>(half_to_float((uint16_t)bits_of(o)), z, A, B);
   const int o2 = pc ? o - 1 : o + 1;
   const bool p2 = o2 > lo0 && above<K>(half_to_float((uint16_t)bits_of(o2)), z, A, B);
