@@ -61,7 +61,7 @@ DEFAULT_WORKLOAD = 3
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description="Decode-attention throughput of the quantized KV cache (one JSON line).")
     ap.add_argument("--gpus", type=int, default=1, help="GPUs (one process each under torchrun; replicas)")
-    ap.add_argument("--steps", type=int, default=100, help="timed steps")
+    ap.add_argument("--steps", type=int, default=300, help="timed steps")
     ap.add_argument("--warmup", type=int, default=3, help="untimed warm-up steps (at least 3)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
                     help="the CUDA library, or the CPU oracle on a bounded sample")
@@ -529,11 +529,11 @@ def run_ours(args, dist):
         "decode_attention": {
             "bound": "hbm", "achieved": dec_gbs, "peak": peak, "unit": "GB/s", "frac": dec_gbs / peak,
             "traffic": kernel_traffic("decode", w), "bytes_per_call": dec_b, **dec, "tokens_attended": T_dec,
-            "kernel": "decode attention call: decode kernel + merge_kernel (programmatic dependent launch)"},
+            "kernel": f"decode attention call: {decode_kernel_name(w)} + merge_kernel (programmatic dependent launch)"},
         "prefill": {
             "bound": "hbm", "achieved": pre_gbs, "peak": peak, "unit": "GB/s", "frac": pre_gbs / peak,
             "traffic": kernel_traffic("prefill", w), "bytes_per_call": pre_b, **pre,
-            "kernel": "prefill call: quantize_pages_kernel + copy_tokens_kernel (window tail)"},
+            "kernel": f"prefill call: {prefill_kernel_name(w)} + copy_tokens_kernel (window tail)"},
     }
     # the dominant kernel: the larger share of the step
     share_pre = L * pre["median_us"]
@@ -546,6 +546,12 @@ def run_ours(args, dist):
 
     # ---------------- end to end through the C ABI from pinned host memory
     e2e = run_e2e(args, w, dist, caches, stream) if args.e2e_steps > 0 else None
+    if e2e and e2e["link_peak_gbs"]:
+        # the step cannot end before its inputs have crossed the link nor before its compute has run
+        link_ms = e2e["h2d_bytes_per_step"] / (e2e["link_peak_gbs"] * 1e9) * 1e3
+        e2e["floor_ms_per_step"] = max(link_ms, ms_step)
+        e2e["floor_bound"] = "link" if link_ms > ms_step else "compute"
+        e2e["frac_of_floor"] = e2e["floor_ms_per_step"] / e2e["ms_per_step"]
 
     tokens = step_tokens(w, L)
     total_tokens = dist.sum(tokens)
@@ -588,20 +594,45 @@ def check_against_oracle(w, cache, out_last, K, V, q_last):
     return {"unit": [b, kvh], "stores_bit_exact": stores_equal, "attention_max_rel_err": err, "ok": ok}
 
 
+# sources of each kernel family: a change to any of them invalidates that family's DRAM counters
 KERNEL_SOURCES = {
-    "decode": ("kvq_decode_mma.cu", "kvq_decode_kernel.cuh", "kvq_decode.cu", "kvq_merge.cuh", "kvq_ptx.cuh",
-               "kvq_internal.h"),
+    "decode_mma": ("kvq_decode_mma.cu", "kvq_decode.cu", "kvq_merge.cuh", "kvq_ptx.cuh", "kvq_internal.h"),
+    "decode_cuda_core": ("kvq_decode_kernel.cuh", "kvq_decode.cu", "kvq_merge.cuh", "kvq_ptx.cuh", "kvq_internal.h"),
     "prefill": ("kvq_quant.cu", "kvq_quantizer.cuh", "kvq_ptx.cuh", "kvq_internal.h"),
 }
+
+
+def decode_kernel_name(w):
+    return "decode_mma_kernel" if kernel_family("decode", w) == "decode_mma" else "decode_kernel"
+
+
+def prefill_kernel_name(w):
+    """The page kernel the library picks for this layout (fragment order: 2/4-bit codes, keys after RoPE)."""
+    frag = not w.rope and w.k_bits in (2, 4) and w.v_bits in (2, 4)
+    if frag and w.residual == 128 and w.head_dim == 128 and w.group == 32 and not w.k_sparse and not w.k_levels:
+        return "quantize_std_kernel"
+    if not frag and not w.k_levels and w.residual == 128 and w.head_dim == 128 and w.group in (32, 64) and w.k_sparse <= 4:
+        return "quantize_bits_kernel"
+    return "quantize_pages_kernel"
+
+
+def kernel_family(kind, w):
+    """The kernel that serves a call of this workload (the launch-time choice of the library)."""
+    if kind == "prefill":
+        return "prefill"
+    mma = not w.rope and not w.k_levels and w.k_bits in (2, 4) and w.v_bits in (2, 4)
+    return "decode_mma" if mma else "decode_cuda_core"
+
+
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
-def kernel_revision(kind):
-    """Hash of a kernel's sources: DRAM counters are valid only for the kernel they were taken on."""
+def kernel_revision(family):
+    """Hash of a kernel family's sources: DRAM counters are valid only for the kernel they were taken on."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_asymmetric_kv_kvq_gb300", "csrc")
-    for f in KERNEL_SOURCES[kind]:
+    for f in KERNEL_SOURCES[family]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -625,7 +656,7 @@ def kernel_traffic(kind, w):
             cur[k.strip()] = v.strip()
     if cur:
         blocks.append(cur)
-    rev = kernel_revision(kind)
+    rev = kernel_revision(kernel_family(kind, w))
     for kv in blocks:
         if kv.get("kind") == kind and kv.get("workload") == w.name and kv.get("kernel_rev") == rev:
             try:
@@ -708,6 +739,16 @@ def run_e2e(args, w, dist, caches, stream):
         hout.copy_(dout, non_blocking=True)
         d2h += hout.nbytes
 
+    # the link's own rate: one plain pinned host->device copy of a prompt buffer, best of three
+    link_peak = 0.0
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            dk[0].copy_(hk, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        link_peak = max(link_peak, hk.nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
     with torch.cuda.stream(stream):
         step()
         torch.cuda.synchronize(dev)
@@ -727,7 +768,7 @@ def run_e2e(args, w, dist, caches, stream):
     link = (h2d // args.e2e_steps) / (ms * 1e-3) / 1e9
     return {"value": total / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d // args.e2e_steps, "d2h_bytes_per_step": d2h // args.e2e_steps,
-            "h2d_gbs": link}
+            "h2d_gbs": link, "link_peak_gbs": link_peak, "link_frac": link / link_peak if link_peak else None}
 
 
 # ------------------------------------------------------------------ reference arm: the CPU oracle
