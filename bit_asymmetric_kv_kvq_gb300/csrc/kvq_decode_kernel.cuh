@@ -108,6 +108,9 @@ struct Shape {
   static constexpr bool FAST_K = HG == 1 && !ROPE && (BK == 2 || BK == 4);
   static constexpr bool FAST_V = HG == 1 && (BV == 2 || BV == 4);
   static constexpr int KBITS_FAST = (BK == 2 || BK == 4) ? BK : 2;
+  // keys rotated at decode with four query heads per kv head: the page sub-tiles on packed fp32
+  // pairs with masked codes (rope_subtile in decode_kernel)
+  static constexpr bool FAST_ROPE = ROPE && HG == 4;
   // warps of the one CTA per SM: as many as the register budget of the path allows (keys
   // rotated at decode need about 255 registers: at 168, one head per kv head spilled 1.4 KB)
   static constexpr int WARPS = ROPE ? 8 : (HG == 4 ? 8 : 16);
@@ -194,7 +197,9 @@ __device__ __forceinline__ void rope_cs(unsigned long long F, uint32_t t, float&
 template <int HG, int CPL>
 struct LaneState {
   float m[HG], l[HG], zsum[HG], acc[HG][CPL];
+  float lp;  // rope_subtile: this lane's share of l for head (lane % KAPPA) % 4, merged in the epilogue
   __device__ __forceinline__ void reset() {
+    lp = 0.0f;
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
       m[h] = -INFINITY;
@@ -221,6 +226,11 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
   constexpr int D = S::D, CPL = S::CPL, KAPPA = S::KAPPA, TAU = S::TAU, TPL = S::TPL, W = S::WARPS;
   // the mask-based fast paths need codes that stand for themselves
   constexpr bool FAST_K = S::FAST_K && !LUT, FAST_V = S::FAST_V && !LUT;
+  constexpr bool FAST_ROPE = S::FAST_ROPE && !LUT;
+  // rope_subtile's value units: the accumulator of channel i of a lane's chunk holds
+  // value * 2^(BV*(i%4) - kCodeExp) (codes masked in place at bit BV*(i%4) of a four-code run)
+  auto rope_v_scale_out = [](int i) { return __uint_as_float((uint32_t)(127 + kCodeExp - BV * (i & 3)) << 23); };
+  auto rope_v_scale_back = [](int i) { return __uint_as_float((uint32_t)(127 - kCodeExp + BV * (i & 3)) << 23); };
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = blockIdx.x, grid = gridDim.x;
@@ -355,6 +365,24 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
     k_unscale[j] = FAST_K ? MaskCodes<S::KBITS_FAST>::scale_in((lane + 32 * j) % MaskCodes<S::KBITS_FAST>::PER_WORD)
                              : 1.0f;
   float (*qs)[D] = qw_s[warp];
+  // rope_subtile lane constants: where the lane's key channels (kc_lo .. +3 and the same in the
+  // second half of the head) and value channels (vc_lo .. +7) sit in a token's bitstream record,
+  // and the turn of its four frequencies over TAU tokens
+  const int rk_wl = (kc_lo * BK) >> 5, rk_sl = (kc_lo * BK) & 31;
+  const int rk_wh = ((kc_lo + D / 2) * BK) >> 5, rk_sh = ((kc_lo + D / 2) * BK) & 31;
+  const int rv_w = (vc_lo * BV) >> 5, rv_s = (vc_lo * BV) & 31;
+  float2 rstep_c[2], rstep_s[2], rstep_ns[2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    if constexpr (FAST_ROPE) {
+      const float2 a = rope_step[kc_lo + 2 * m], b = rope_step[kc_lo + 2 * m + 1];
+      rstep_c[m] = make_float2(a.x, b.x);
+      rstep_s[m] = make_float2(a.y, b.y);
+      rstep_ns[m] = make_float2(-a.y, -b.y);
+    } else {
+      rstep_c[m] = rstep_s[m] = rstep_ns[m] = make_float2(0.0f, 0.0f);
+    }
+  }
 
   LaneState<HG, CPL> st;
   st.reset();
@@ -379,6 +407,9 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
         st.zsum[h] *= f;
 #pragma unroll
         for (int i = 0; i < CPL; ++i) st.acc[h][i] *= f;
+        if constexpr (FAST_ROPE) {
+          if (((lane % KAPPA) & 3) == h) st.lp *= f;
+        }
         st.m[h] = mnew;
       }
       const bool live = st.m[h] != -INFINITY;
@@ -404,6 +435,15 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
   auto epilogue = [&](int64_t unit) {
     constexpr int NOUT = CPL / TAU;  // channels per head a lane holds after the reduction
     static_assert(NOUT == 4, "the partial of a lane is one float4 per head");
+    if constexpr (FAST_ROPE) {
+      // page weights: lane kap of a slot summed head kap % 4; gather them into every lane's l
+      float lq = st.lp;
+      lq += __shfl_xor_sync(kFull, lq, 4);
+      lq += __shfl_xor_sync(kFull, lq, 8);
+#pragma unroll
+      for (int h = 0; h < HG; ++h) st.l[h] += __shfl_sync(kFull, lq, tau * KAPPA + h);
+      st.lp = 0.0f;
+    }
     // l and the value zero-point sums over the warp's token slots (lanes of one slot hold copies)
 #pragma unroll
     for (int h = 0; h < HG; ++h)
@@ -434,6 +474,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       for (int i = 0; i < NOUT; ++i) {
         float a = st.acc[h][i];
         if constexpr (FAST_V) a *= MaskCodes<FAST_V ? BV : 2>::scale_out((vc_lo + NOUT * tau + i) % (32 / BV));
+        if constexpr (FAST_ROPE) a *= rope_v_scale_out(i);  // channel 4*tau + i of the chunk: position i
         st.acc[h][i] = a + st.zsum[h];
       }
     const int64_t b = unit / p.Hkv, kvh = unit - b * p.Hkv;
@@ -451,6 +492,230 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       }
     } else if (lane == 0) {
       report_error(p.err, kDevBadArgument);  // slots are sized for the grid: not reached
+    }
+  };
+
+  // ---------------- keys stored before RoPE, four query heads per kv head: one 32-token page
+  // sub-tile on packed fp32 pairs.  Lane (tau, kap) covers tokens tau + TAU*j (j < 16) on key
+  // channels kc_lo + i and kc_lo + D/2 + i (i < 4: four frequencies) and value channels vc_lo + i
+  // (i < 8).
+  //  * Keys: the lane's two 4-code runs of a token are funnel-shifted out of the record; code i,
+  //    masked in place, is the fp32 subnormal code * 2^(BK*i) * 2^-149, so one FMA against
+  //    s * 2^(85 - BK*i) and z * 2^-64 gives the dequantized key times 2^-64, exactly as rounded as
+  //    z + s*code.  The pairs (c, c + D/2) are rotated by the token's angle, turned on from the
+  //    lane's first token by angle addition, and dotted with the four heads' query rows.
+  //  * Sparse entries: the dense code there is 0 (value z), so each adds (x - z) times the rotated
+  //    query at its channel, computed once per entry by the lane of its token.
+  //  * Scores of four tokens x four heads are reduce-scattered over the slot's 16 lanes (15
+  //    exchanges instead of 64 butterflies), so lane kap ends with token 4b + kap/4, head kap%4 of
+  //    block b and the softmax runs once per score, not once per lane.
+  //  * Values: the lane's eight codes are two masked 4-code runs against p*s*2^(149 - kCodeExp)
+  //    (accumulator units as rope_v_scale_out undoes), four heads per code in packed FMAs.
+  auto rope_subtile = [&](const uint8_t* pgm, int stt, int64_t page_tok0) {
+    if constexpr (FAST_ROPE) {
+      static_assert(HG == 4 && S::HALF == 4 && CPL == 8 && KAPPA == 16 && TAU == 2 && TPL == 16, "one layout");
+      const uint32_t* kc = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_kc);
+      const uint32_t* km = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_km);
+      const uint32_t* vcw = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vc);
+      const uint32_t* vm = reinterpret_cast<const uint32_t*>(pgm + p.lay.off_vm);
+      constexpr uint32_t KMASK = (1u << BK) - 1u, VMASK = (1u << BV) - 1u;
+      constexpr int KW = D * BK / 32, VW = D * BV / 32;  // words of a token's key / value record
+      const int g = (stt * 32) >> p.log2G;                 // key group (G >= 32)
+      const int hl = kap & 3;                              // head of this lane's scores
+      // query rows of the lane's key channels, as pairs of neighbouring channels
+      float2 ql[HG][2], qh[HG][2];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        const float4 a = *reinterpret_cast<const float4*>(&qs[h][kc_lo]);
+        const float4 b = *reinterpret_cast<const float4*>(&qs[h][kc_lo + D / 2]);
+        ql[h][0] = make_float2(a.x, a.y);
+        ql[h][1] = make_float2(a.z, a.w);
+        qh[h][0] = make_float2(b.x, b.y);
+        qh[h][1] = make_float2(b.z, b.w);
+      }
+      // the group's zero points and steps in the masked codes' units (see above)
+      float2 zl2[2], sl2[2], zh2[2], sh2[2];
+      {
+        const uint4 a = *reinterpret_cast<const uint4*>(km + g * D + kc_lo);
+        const uint4 b = *reinterpret_cast<const uint4*>(km + g * D + kc_lo + D / 2);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+        float zl[4], sl[4], zh[4], sh[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float pos = __uint_as_float((uint32_t)(127 + 85 - BK * i) << 23);
+          const float2 za = __half22float2(*reinterpret_cast<const __half2*>(&aw[i]));
+          const float2 zb = __half22float2(*reinterpret_cast<const __half2*>(&bw[i]));
+          zl[i] = za.x * 0x1.0p-64f;
+          sl[i] = za.y * pos;
+          zh[i] = zb.x * 0x1.0p-64f;
+          sh[i] = zb.y * pos;
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          zl2[m] = make_float2(zl[2 * m], zl[2 * m + 1]);
+          sl2[m] = make_float2(sl[2 * m], sl[2 * m + 1]);
+          zh2[m] = make_float2(zh[2 * m], zh[2 * m + 1]);
+          sh2[m] = make_float2(sh[2 * m], sh[2 * m + 1]);
+        }
+      }
+      // cos/sin of the lane's four frequencies at its first token (exact from the turn count)
+      float2 rc[2], rs[2];
+      {
+        float c[4], sn[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rope_cs(p.rope_turns[kc_lo + i], (uint32_t)(page_tok0 + stt * 32 + tau), c[i], sn[i]);
+        rc[0] = make_float2(c[0], c[1]);
+        rc[1] = make_float2(c[2], c[3]);
+        rs[0] = make_float2(sn[0], sn[1]);
+        rs[1] = make_float2(sn[2], sn[3]);
+      }
+      // sparse entries of token `lane` of the sub-tile: their score corrections per head
+      float dlt[HG];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) dlt[h] = 0.0f;
+      const int nsp = p.nsp;
+      if (nsp > 0) {
+        const int tt = stt * 32 + lane;
+        const uint8_t* si = pgm + p.lay.off_si;
+        const uint16_t* sv = reinterpret_cast<const uint16_t*>(pgm + p.lay.off_sv);
+        for (int k = 0; k < nsp; ++k) {
+          const int c = si[tt * nsp + k];
+          const float dx = h2f(sv[tt * nsp + k]) - h2f((uint16_t)(km[g * D + c] & 0xFFFFu));
+          float cs, sn;
+          rope_cs(p.rope_turns[c & (D / 2 - 1)], (uint32_t)(page_tok0 + tt), cs, sn);
+          const float sg = c < D / 2 ? sn : -sn;  // the rotated query at c: q_c cos +- q_(c^D/2) sin
+#pragma unroll
+          for (int h = 0; h < HG; ++h) dlt[h] = fmaf(dx, fmaf(qs[h][c], cs, qs[h][c ^ (D / 2)] * sg), dlt[h]);
+        }
+      }
+      // ---- scores, four tokens at a time
+      float r[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        float v[16];  // entry 4*jj + h: token 4b + jj, head h (this lane's channels only)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * b + jj;
+          const uint32_t* rec = kc + (stt * 32 + tau + TAU * j) * KW;
+          const uint32_t xl = __funnelshift_r(rec[rk_wl], rec[rk_wl + 1], rk_sl);
+          const uint32_t xh = __funnelshift_r(rec[rk_wh], rec[rk_wh + 1], rk_sh);
+          float2 acc[HG];
+#pragma unroll
+          for (int h = 0; h < HG; ++h) acc[h] = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const float2 fl = make_float2(__uint_as_float(xl & (KMASK << (BK * 2 * m))),
+                                          __uint_as_float(xl & (KMASK << (BK * (2 * m + 1)))));
+            const float2 fh = make_float2(__uint_as_float(xh & (KMASK << (BK * 2 * m))),
+                                          __uint_as_float(xh & (KMASK << (BK * (2 * m + 1)))));
+            const float2 kl = __ffma2_rn(fl, sl2[m], zl2[m]);
+            const float2 kh = __ffma2_rn(fh, sh2[m], zh2[m]);
+            const float2 nsn = make_float2(-rs[m].x, -rs[m].y);
+            const float2 rl = __ffma2_rn(kh, nsn, __fmul2_rn(kl, rc[m]));   // kl cos - kh sin
+            const float2 rh = __ffma2_rn(kl, rs[m], __fmul2_rn(kh, rc[m]));  // kh cos + kl sin
+#pragma unroll
+            for (int h = 0; h < HG; ++h) acc[h] = __ffma2_rn(qh[h][m], rh, __ffma2_rn(ql[h][m], rl, acc[h]));
+          }
+#pragma unroll
+          for (int h = 0; h < HG; ++h) v[4 * jj + h] = acc[h].x + acc[h].y;
+          if (j + 1 < TPL) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              const float2 c = rc[m], sn = rs[m];
+              rc[m] = __ffma2_rn(c, rstep_c[m], __fmul2_rn(sn, rstep_ns[m]));  // cos(a + d)
+              rs[m] = __ffma2_rn(sn, rstep_c[m], __fmul2_rn(c, rstep_s[m]));   // sin(a + d)
+            }
+          }
+        }
+        // reduce-scatter over the slot's lanes (kap bits 3..0): lane kap keeps entry kap
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) {
+          const bool up = (kap & off) != 0;
+#pragma unroll
+          for (int i = 0; i < off; ++i) {
+            const float send = up ? v[i] : v[i + off];
+            const float keep = up ? v[i + off] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, off);
+          }
+        }
+        r[b] = v[0];
+      }
+      // final scores (log2 units) of token 4b + kap/4 of the slot, head hl
+      const float sgl = 0x1.0p64f * p.qk_scale_log2;
+      float sb[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        float d = 0.0f;
+        if (nsp > 0) {
+          const int src = tau + TAU * (4 * b + (kap >> 2));  // the lane that holds that token's corrections
+          const float d0 = __shfl_sync(kFull, dlt[0], src), d1 = __shfl_sync(kFull, dlt[1], src);
+          const float d2 = __shfl_sync(kFull, dlt[2], src), d3 = __shfl_sync(kFull, dlt[3], src);
+          d = hl == 0 ? d0 : hl == 1 ? d1 : hl == 2 ? d2 : d3;
+        }
+        sb[b] = fmaf(r[b], sgl, d * p.qk_scale_log2);
+      }
+      // ---- online softmax: the lane's four scores all belong to head hl
+      auto mof = [&](int h) { return h == 0 ? st.m[0] : h == 1 ? st.m[1] : h == 2 ? st.m[2] : st.m[3]; };
+      float ml = mof(hl);
+      const float tmax = fmaxf(fmaxf(sb[0], sb[1]), fmaxf(sb[2], sb[3]));
+      const bool over = tmax > ml + kLazyRescale || (ml == -INFINITY && tmax != -INFINITY);
+      if (__any_sync(kFull, over)) {
+        float mx = tmax;  // the largest of head hl over the sub-tile: lanes kap % 4 == hl of both slots
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          const float mnew = fmaxf(__shfl_sync(kFull, mx, h), st.m[h]);  // lane h holds head h
+          const float f = st.m[h] == -INFINITY ? 0.0f : exp2f(st.m[h] - mnew);
+          st.l[h] *= f;
+          st.zsum[h] *= f;
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) st.acc[h][i] *= f;
+          if (hl == h) st.lp *= f;
+          st.m[h] = mnew;
+        }
+        ml = mof(hl);
+      }
+      float pb[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        pb[b] = exp2f(sb[b] - ml);
+        st.lp += pb[b];
+      }
+      // ---- values
+      const float kScIn = __uint_as_float((uint32_t)(127 + 149 - kCodeExp) << 23);
+#pragma unroll
+      for (int j = 0; j < TPL; ++j) {
+        const int tt = stt * 32 + tau + TAU * j;
+        float ph[HG];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) ph[h] = __shfl_sync(kFull, pb[j >> 2], tau * KAPPA + 4 * (j & 3) + h);
+        const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(vm + tt * ng + gv));
+        const float sv = zs.y * kScIn;
+        const uint32_t* rec = vcw + tt * VW;
+        const uint32_t x = __funnelshift_r(rec[rv_w], rec[rv_w + 1], rv_s);
+        const uint32_t x2 = x >> (4 * BV);
+        float2 f2[4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          f2[m] = make_float2(__uint_as_float(x & (VMASK << (BV * 2 * m))), __uint_as_float(x & (VMASK << (BV * (2 * m + 1)))));
+          f2[2 + m] = make_float2(__uint_as_float(x2 & (VMASK << (BV * 2 * m))),
+                                  __uint_as_float(x2 & (VMASK << (BV * (2 * m + 1)))));
+        }
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          const float ps = ph[h] * sv;
+          const float2 ps2 = make_float2(ps, ps);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float2 a = __ffma2_rn(f2[m], ps2, make_float2(st.acc[h][2 * m], st.acc[h][2 * m + 1]));
+            st.acc[h][2 * m] = a.x;
+            st.acc[h][2 * m + 1] = a.y;
+          }
+          st.zsum[h] = fmaf(ph[h], zs.x, st.zsum[h]);
+        }
+      }
     }
   };
 
@@ -490,6 +755,9 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       const uint16_t* sv = reinterpret_cast<const uint16_t*>(pgm + p.lay.off_sv);
       const int64_t page_tok0 = p.n_s + (loc - hw) * (int64_t)p.R;
 
+      if constexpr (FAST_ROPE) {
+        rope_subtile(pgm, stt, page_tok0);
+      } else {
       const int g = (stt * 32) >> p.log2G;  // key group of this sub-tile (G >= 32)
       float sc[TPL][HG];
 
@@ -709,6 +977,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
           }
         }
       }
+      }  // !FAST_ROPE
       __syncwarp();
       if (lane == 0) {
         // release this sub-tile of the stage; the warp releasing its last sub-tile refills the
@@ -807,8 +1076,9 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
 #pragma unroll
             for (int i = 0; i < CPL; ++i) {
               // in the units of the fast value path (exact powers of two), undone by the fold
-              const float sb = FAST_V ? MaskCodes<FAST_V ? BV : 2>::scale_back((vc_lo + i) % (32 / (FAST_V ? BV : 2)))
-                                         : 1.0f;
+              const float sb = FAST_ROPE ? rope_v_scale_back(i)
+                               : FAST_V ? MaskCodes<FAST_V ? BV : 2>::scale_back((vc_lo + i) % (32 / (FAST_V ? BV : 2)))
+                                        : 1.0f;
               st.acc[h][i] = fmaf(pw * sb, xv[i], st.acc[h][i]);
             }
           }
