@@ -57,6 +57,7 @@ constexpr float kLazyRescale = 8.0f;
 
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
+
 // Exact small-integer to float: 2^23 + code has code in the low mantissa bits.
 __device__ __forceinline__ float code_to_float(uint32_t code) {
   return __uint_as_float(0x4B000000u | code) - 8388608.0f;
@@ -96,7 +97,7 @@ struct MaskCodes {
   }
 };
 
-template <int BK, int BV, int HG, bool ROPE>
+template <int BK, int BV, int HG, bool ROPE, bool LUT = false>
 struct Shape {
   static constexpr int D = kHeadDim;
   static constexpr int CPL = 32 / HG;    // channels per lane
@@ -110,10 +111,14 @@ struct Shape {
   static constexpr int KBITS_FAST = (BK == 2 || BK == 4) ? BK : 2;
   // keys rotated at decode with four query heads per kv head: the page sub-tiles on packed fp32
   // pairs with masked codes (rope_subtile in decode_kernel)
-  static constexpr bool FAST_ROPE = ROPE && HG == 4;
+  static constexpr bool FAST_ROPE = ROPE && HG == 4 && !LUT;
   // warps of the one CTA per SM: as many as the register budget of the path allows (keys
   // rotated at decode need about 255 registers: at 168, one head per kv head spilled 1.4 KB)
-  static constexpr int WARPS = ROPE ? 8 : (HG == 4 ? 8 : 16);
+  // (rope_subtile keeps each lane's value accumulators in shared memory between sub-tiles, which
+  // brings it to 128 registers)
+  static constexpr int WARPS = FAST_ROPE ? 16 : ROPE ? 8 : (HG == 4 ? 8 : 16);
+  // dynamic shared memory beside the page stages: rope_subtile's accumulators, 4 KB per warp
+  static constexpr int ACC_SMEM = FAST_ROPE ? WARPS * 32 * HG * CPL * 4 : 0;
 };
 
 // Extract N codes of BITS bits starting at bit `bit0` of a token record held
@@ -221,8 +226,8 @@ struct LaneState {
 // LUT: codes index caller-supplied codebooks (non-uniform levels in step units) instead of
 // standing for themselves; the mask-based fast paths, which rely on linear codes, are off.
 template <int BK, int BV, int HG, bool ROPE, bool LUT>
-__global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode_kernel(const DecodeParams p) {
-  using S = Shape<BK, BV, HG, ROPE>;
+__global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE, LUT>::WARPS * 32, 1) decode_kernel(const DecodeParams p) {
+  using S = Shape<BK, BV, HG, ROPE, LUT>;
   constexpr int D = S::D, CPL = S::CPL, KAPPA = S::KAPPA, TAU = S::TAU, TPL = S::TPL, W = S::WARPS;
   // the mask-based fast paths need codes that stand for themselves
   constexpr bool FAST_K = S::FAST_K && !LUT, FAST_V = S::FAST_V && !LUT;
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
   __shared__ int stage_issued[kMaxStages];  // copies issued into each stage so far
   __shared__ int stage_page[kMaxStages];    // page of the slice a stage holds or is being filled with
   __shared__ __align__(16) float qw_s[W][HG][D];  // each warp's query rows (fp32) for its unit
-  __shared__ __align__(16) float qp_s[W][HG][D];  // each warp's q' for its key group
+  __shared__ __align__(16) float qp_s[ROPE ? 1 : W][HG][D];  // each warp's q' for its key group
   __shared__ int next_sub;
   __shared__ int abort_flag;
   // rope: the turn of frequency i over TAU tokens (cos, sin), the step between a lane's tokens
@@ -385,7 +390,31 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
   }
 
   LaneState<HG, CPL> st;
+  // rope_subtile: st.acc lives in this warp's shared-memory slot between sub-tiles (float4 i of
+  // lane l at [i][l]: conflict-free), and in registers only where values are accumulated
+  float4* acc_s = reinterpret_cast<float4*>(stage_mem + ((size_t)page_bytes << log2S)) + warp * (HG * CPL / 4) * 32;
+  auto acc_store = [&]() {
+    if constexpr (FAST_ROPE) {
+#pragma unroll
+      for (int i = 0; i < HG * CPL / 4; ++i)
+        acc_s[i * 32 + lane] = make_float4(st.acc[i / (CPL / 4)][4 * (i % (CPL / 4))], st.acc[i / (CPL / 4)][4 * (i % (CPL / 4)) + 1],
+                                           st.acc[i / (CPL / 4)][4 * (i % (CPL / 4)) + 2], st.acc[i / (CPL / 4)][4 * (i % (CPL / 4)) + 3]);
+    }
+  };
+  auto acc_load = [&]() {
+    if constexpr (FAST_ROPE) {
+#pragma unroll
+      for (int i = 0; i < HG * CPL / 4; ++i) {
+        const float4 v = acc_s[i * 32 + lane];
+        st.acc[i / (CPL / 4)][4 * (i % (CPL / 4))] = v.x;
+        st.acc[i / (CPL / 4)][4 * (i % (CPL / 4)) + 1] = v.y;
+        st.acc[i / (CPL / 4)][4 * (i % (CPL / 4)) + 2] = v.z;
+        st.acc[i / (CPL / 4)][4 * (i % (CPL / 4)) + 3] = v.w;
+      }
+    }
+  };
   st.reset();
+  acc_store();
 
   // Online-softmax update of one sub-tile: sc[j][h] are final scores (log2 units) of the
   // lane's tokens (-inf for masked ones); returns the weights in sc.
@@ -435,6 +464,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
   auto epilogue = [&](int64_t unit) {
     constexpr int NOUT = CPL / TAU;  // channels per head a lane holds after the reduction
     static_assert(NOUT == 4, "the partial of a lane is one float4 per head");
+    acc_load();
     if constexpr (FAST_ROPE) {
       // page weights: lane kap of a slot summed head kap % 4; gather them into every lane's l
       float lq = st.lp;
@@ -588,9 +618,9 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
           for (int h = 0; h < HG; ++h) dlt[h] = fmaf(dx, fmaf(qs[h][c], cs, qs[h][c ^ (D / 2)] * sg), dlt[h]);
         }
       }
-      // ---- scores, four tokens at a time
-      float r[4];
-#pragma unroll
+      // ---- scores, four tokens at a time (one block in registers at a time)
+      float r0 = 0.0f, r1 = 0.0f, r2 = 0.0f, r3 = 0.0f;
+#pragma unroll 1
       for (int b = 0; b < 4; ++b) {
         float v[16];  // entry 4*jj + h: token 4b + jj, head h (this lane's channels only)
 #pragma unroll
@@ -618,7 +648,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
           }
 #pragma unroll
           for (int h = 0; h < HG; ++h) v[4 * jj + h] = acc[h].x + acc[h].y;
-          if (j + 1 < TPL) {
+          {  // (the turn past the last token is not used)
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
               const float2 c = rc[m], sn = rs[m];
@@ -638,8 +668,12 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
             v[i] = keep + __shfl_xor_sync(kFull, send, off);
           }
         }
-        r[b] = v[0];
+        r0 = b == 0 ? v[0] : r0;
+        r1 = b == 1 ? v[0] : r1;
+        r2 = b == 2 ? v[0] : r2;
+        r3 = b == 3 ? v[0] : r3;
       }
+      const float r[4] = {r0, r1, r2, r3};
       // final scores (log2 units) of token 4b + kap/4 of the slot, head hl
       const float sgl = 0x1.0p64f * p.qk_scale_log2;
       float sb[4];
@@ -659,6 +693,9 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       float ml = mof(hl);
       const float tmax = fmaxf(fmaxf(sb[0], sb[1]), fmaxf(sb[2], sb[3]));
       const bool over = tmax > ml + kLazyRescale || (ml == -INFINITY && tmax != -INFINITY);
+      float fac[HG];  // rescale of the accumulators (applied when they are loaded for the values)
+#pragma unroll
+      for (int h = 0; h < HG; ++h) fac[h] = 1.0f;
       if (__any_sync(kFull, over)) {
         float mx = tmax;  // the largest of head hl over the sub-tile: lanes kap % 4 == hl of both slots
         mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
@@ -670,8 +707,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
           const float f = st.m[h] == -INFINITY ? 0.0f : exp2f(st.m[h] - mnew);
           st.l[h] *= f;
           st.zsum[h] *= f;
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) st.acc[h][i] *= f;
+          fac[h] = f;
           if (hl == h) st.lp *= f;
           st.m[h] = mnew;
         }
@@ -684,13 +720,22 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
         st.lp += pb[b];
       }
       // ---- values
-      const float kScIn = __uint_as_float((uint32_t)(127 + 149 - kCodeExp) << 23);
+      acc_load();
 #pragma unroll
-      for (int j = 0; j < TPL; ++j) {
+      for (int h = 0; h < HG; ++h)
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) st.acc[h][i] *= fac[h];
+      const float kScIn = __uint_as_float((uint32_t)(127 + 149 - kCodeExp) << 23);
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+      const float pbb = b == 0 ? pb[0] : b == 1 ? pb[1] : b == 2 ? pb[2] : pb[3];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = 4 * b + jj;
         const int tt = stt * 32 + tau + TAU * j;
         float ph[HG];
 #pragma unroll
-        for (int h = 0; h < HG; ++h) ph[h] = __shfl_sync(kFull, pb[j >> 2], tau * KAPPA + 4 * (j & 3) + h);
+        for (int h = 0; h < HG; ++h) ph[h] = __shfl_sync(kFull, pbb, tau * KAPPA + 4 * jj + h);
         const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(vm + tt * ng + gv));
         const float sv = zs.y * kScIn;
         const uint32_t* rec = vcw + tt * VW;
@@ -716,6 +761,8 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
           st.zsum[h] = fmaf(ph[h], zs.x, st.zsum[h]);
         }
       }
+      }
+      acc_store();
     }
   };
 
@@ -733,6 +780,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
       cur = x / wpu;
       ustart = cur * wpu;
       st.reset();
+      acc_store();
       load_q(cur);
     }
     const int loc = (int)(x - ustart);
@@ -1010,6 +1058,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
         reinterpret_cast<uint4*>(dst)[lane & 15] = __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15));
       }
       if (32 * f < p.n_w) {
+        acc_load();
         float sc[TPL][HG];
 #pragma unroll
         for (int j = 0; j < TPL; ++j) {
@@ -1083,6 +1132,7 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE>::WARPS * 32, 1) decode
             }
           }
         }
+        acc_store();
       }
     }
   }
@@ -1111,7 +1161,7 @@ int log2_stages_t(int page_bytes) {
     static_smem = (int)a.sharedSizeBytes;
   }
   if (static_smem > 48 * 1024) return -1;  // more static shared memory than a kernel may declare
-  const int avail = optin - static_smem;
+  const int avail = optin - static_smem - Shape<BK, BV, HG, ROPE, LUT>::ACC_SMEM;
   int l = 4;  // kMaxStages = 16
   while (l >= 0 && ((int64_t)page_bytes << l) > avail) --l;
   return l;
@@ -1123,23 +1173,23 @@ cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t s) {
   if (l < 0) return cudaErrorInvalidValue;
   DecodeParams q = p;
   q.log2_stages = l;
-  const size_t smem = (size_t)p.lay.bytes << l;
+  const size_t smem = ((size_t)p.lay.bytes << l) + Shape<BK, BV, HG, ROPE, LUT>::ACC_SMEM;
   auto kern = decode_kernel<BK, BV, HG, ROPE, LUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, (unsigned)grid, Shape<BK, BV, HG, ROPE>::WARPS * 32, smem, s, q);
+  return launch_pdl(kern, (unsigned)grid, Shape<BK, BV, HG, ROPE, LUT>::WARPS * 32, smem, s, q);
 }
 
 template <int BK, int BV, int HG, bool ROPE, bool LUT>
 int resident_t(int page_bytes, int* warps) {
-  *warps = Shape<BK, BV, HG, ROPE>::WARPS;
+  *warps = Shape<BK, BV, HG, ROPE, LUT>::WARPS;
   const int l = log2_stages_t<BK, BV, HG, ROPE, LUT>(page_bytes);
   if (l < 0) return 0;
-  const size_t smem = (size_t)page_bytes << l;
+  const size_t smem = ((size_t)page_bytes << l) + Shape<BK, BV, HG, ROPE, LUT>::ACC_SMEM;
   auto kern = decode_kernel<BK, BV, HG, ROPE, LUT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape<BK, BV, HG, ROPE>::WARPS * 32, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape<BK, BV, HG, ROPE, LUT>::WARPS * 32, smem) !=
       cudaSuccess)
     return 0;
   return n;
