@@ -542,7 +542,9 @@ def run_ours(args, dist):
     roof = dict(kernels[dom])
     roof["name"] = dom
     roof["peak_source"] = peak_source
-    roof["step_share"] = (share_pre if dom == "prefill" else share_dec) / (ms_step * 1e3)
+    # its share of the step's device time, from the per-call medians (calls timed one by one carry
+    # their own launch gaps, so the two shares are taken relative to each other, not to ms_per_step)
+    roof["step_share"] = (share_pre if dom == "prefill" else share_dec) / (share_pre + share_dec)
 
     # ---------------- end to end through the C ABI from pinned host memory
     e2e = run_e2e(args, w, dist, caches, stream) if args.e2e_steps > 0 else None
