@@ -140,6 +140,23 @@ __host__ __device__ __forceinline__ float div_rn(float a, float b) {
   return r;
 #endif
 }
+__host__ __device__ __forceinline__ float fma_rn(float a, float b, float c) {
+#ifdef __CUDA_ARCH__
+  return __fmaf_rn(a, b, c);
+#else
+  return fmaf(a, b, c);
+#endif
+}
+// a / L correctly rounded for a >= 0 (L = 3, 7, 15): the product with the rounded reciprocal,
+// corrected once with the exact remainder a - q*L.  Every step scales exactly with a power of two
+// of a, so one binade of significands and the range of subnormal quotients cover every a; both
+// are checked exhaustively against the IEEE division on the host (tests/host/threshold_check.cu).
+template <int L>
+__host__ __device__ __forceinline__ float div_const(float a) {
+  constexpr float inv = 1.0f / (float)L;
+  const float q = mul_rn(a, inv);
+  return fma_rn(fma_rn(-q, (float)L, a), inv, q);
+}
 __host__ __device__ __forceinline__ float half_to_float(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 __host__ __device__ __forceinline__ uint16_t float_to_half(float f) { return __half_as_ushort(__float2half_rn(f)); }
 __host__ __device__ __forceinline__ uint16_t half_rd(float f) { return __half_as_ushort(__float2half_rd(f)); }
@@ -163,9 +180,8 @@ __host__ __device__ __forceinline__ bool above(float x, float z, float A, float 
   return (K & 1) ? e >= B : e > B;
 }
 
-// t_k of a group with zero point z, step s > 0, minimum and maximum in value order lo0 < hi0.  Only
-// the group's values are ever compared with it, so any value above the maximum serves when the
-// maximum does not reach code k + 1 (the candidate may then land past it, up to +inf).
+// t_k of a group with zero point z and step s > 0 (+inf when no finite fp16 value reaches code
+// k + 1).
 //
 // Fast path: the test switches at a real X* with |X* - (z + A + B)| <= 1.5 ulp(A + B) (where
 // fl(x - z) crosses A + B), and y = fl(fl(z + A) + B) is within 2^-24 (|z + A| + |y|) of
@@ -174,34 +190,20 @@ __host__ __device__ __forceinline__ bool above(float x, float z, float A, float 
 // No fp16 value there (a > b): X* lies strictly between b and a, the next value up from b, and a
 // is t_k.  Exactly one, a == b: every value below a fails, every value above passes, and one test
 // at a decides between a and the next value up.  Two or more (an fp16 spacing below eps: values
-// far smaller than the group's range, rare) go to the exact search below.
+// far smaller than the group's range, rare): X* is still inside the window, so the value below a
+// fails and the value above b passes, and a bisection over the window's values finds t_k (a few
+// halvings: the window holds about eps / spacing values).
 template <int K>
-__host__ __device__ __forceinline__ uint32_t threshold(float z, float s, int lo0, int hi0) {
+__host__ __device__ __forceinline__ uint32_t threshold(float z, float s) {
   const float A = mul_rn(s, (float)K + 0.5f), B = mul_rn(s, bfac(K));
   const float y = add_rn(add_rn(z, A), B);
-  {
-    const float eps = mul_rn(add_rn(add_rn(fabsf(z), A), fabsf(y)), 0x1.0p-20f);
-    const uint16_t a = half_ru(sub_rn(y, eps)), b = half_rd(add_rn(y, eps));
-    const float fa = half_to_float(a), fb = half_to_float(b);
-    if (fa > fb) return a;
-    if (fa == fb) return above<K>(fa, z, A, B) ? a : bits_of(ord(a) + 1);
-  }
-  // the candidate and the neighbour on the other side of the test (the minimum, lo0, always fails)
-  const int o = ord(float_to_half(y));
-  const bool pc = o > lo0 && above<K>(half_to_float((uint16_t)bits_of(o)), z, A, B);
-  const int o2 = pc ? o - 1 : o + 1;
-  const bool p2 = o2 > lo0 && above<K>(half_to_float((uint16_t)bits_of(o2)), z, A, B);
-  if (pc != p2) return bits_of(pc ? o : o2);
-  int lo, hi;  // above() is false at lo and true at hi (or hi is past the maximum)
-  if (pc) {
-    lo = lo0;
-    hi = o2;
-  } else {
-    lo = o2;
-    hi = hi0;
-    if (lo >= hi || !above<K>(half_to_float((uint16_t)bits_of(hi0)), z, A, B)) return 0x7C00u;
-  }
-  while (hi - lo > 1) {  // at most 16 halvings of the fp16 value range
+  const float eps = mul_rn(add_rn(add_rn(fabsf(z), A), fabsf(y)), 0x1.0p-20f);
+  const uint16_t a = half_ru(sub_rn(y, eps)), b = half_rd(add_rn(y, eps));
+  const float fa = half_to_float(a), fb = half_to_float(b);
+  if (fa > fb) return a;
+  if (fa == fb) return above<K>(fa, z, A, B) ? a : bits_of(ord(a) + 1);
+  int lo = ord(a) - 1, hi = ord(b) + 1;  // above() is false at lo and true at hi
+  while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (above<K>(half_to_float((uint16_t)bits_of(mid)), z, A, B)) hi = mid;
     else lo = mid;
@@ -216,7 +218,7 @@ __host__ __device__ __forceinline__ uint32_t zero_step(float mn, float mx, float
   mn = add_rn(mn, 0.0f);  // -0 -> +0
   float range = sub_rn(mx, mn);
   if (!(range > 0.0f)) range = 0.0f;
-  const uint16_t zb = float_to_half(mn), sb = float_to_half(div_rn(range, (float)L));
+  const uint16_t zb = float_to_half(mn), sb = float_to_half(div_const<L>(range));
   *z = half_to_float(zb);
   *s = half_to_float(sb);
   return (uint32_t)zb | ((uint32_t)sb << 16);
@@ -230,10 +232,9 @@ __host__ __device__ __forceinline__ uint32_t thresholds2(float mn, float mx, uin
     t[0] = t[1] = t[2] = 0x7C00u;
     return zs;
   }
-  const int lo0 = ord(float_to_half(mn)), hi0 = ord(float_to_half(mx));
-  t[0] = threshold<0>(z, s, lo0, hi0);
-  t[1] = threshold<1>(z, s, lo0, hi0);
-  t[2] = threshold<2>(z, s, lo0, hi0);
+  t[0] = threshold<0>(z, s);
+  t[1] = threshold<1>(z, s);
+  t[2] = threshold<2>(z, s);
   return zs;
 }
 

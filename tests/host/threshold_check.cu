@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 
 #include "kvq_quantizer.cuh"
 
@@ -39,8 +40,32 @@ static uint32_t exact_code(float x, float z, float s) {
 
 static bool ge16(uint16_t a, uint16_t b) { return half_to_float(a) >= half_to_float(b); }
 
+// div_const<L> against the IEEE division for every significand of one binade and for every
+// a < 2^-121 (the quotient q turns subnormal below a = L * 2^-126 < 2^-122); while q is normal the
+// computation scales exactly with a power of two of a (the remainder a - q*L is a multiple of
+// ulp(q), exact even when subnormal, and the last FMA rounds once), so this covers every finite
+// a >= 0.  Returns the values checked.
+template <int L>
+static long long check_div_const() {
+  long long n = 0;
+  auto one = [&](uint32_t bits) {
+    float a;
+    std::memcpy(&a, &bits, 4);
+    volatile float want = a / (float)L;
+    const float got = div_const<L>(a);
+    if (std::memcmp(&got, (const void*)&want, 4) != 0) {
+      std::printf("div_const<%d> mismatch: a %a got %a want %a\n", L, a, got, (float)want);
+      std::exit(1);
+    }
+    ++n;
+  };
+  for (uint32_t m = 0; m < (1u << 23); ++m) one(0x3F800000u | m);        // [1, 2)
+  for (uint32_t b = 0; b < (6u << 23); ++b) one(b);                      // 0 .. 2^-121 (subnormals included)
+  return n;
+}
+
 int main() {
-  long long checked = 0;
+  long long checked = check_div_const<3>() + check_div_const<7>() + check_div_const<15>();
   for (int g = 0; g < 4000; ++g) {
     // a group of 32 fp16 values from one of several distributions
     const int kind = g % 8;

@@ -5,7 +5,9 @@ kvq_quantizer.cuh, host-compiled) and checks, for 4000 groups of 32 fp16 values 
 distributions (standard normal, an outlier channel, subnormal and tiny ranges, magnitudes up to
 the fp16 maximum, all-negative groups, powers of two of both signs), that every fp16 value between
 a group's minimum and maximum gets the same code from the thresholds as from
-clamp(rint(fl(fl(x - z) / s)), 0, 3) in plain fp32 -- about 10^8 values.
+clamp(rint(fl(fl(x - z) / s)), 0, 3) in plain fp32 -- about 10^8 values; and that the division of
+a group's range by L = 3, 7, 15 (a rounded reciprocal product with one exact-remainder correction)
+equals the IEEE division for every significand of a binade and every subnormal quotient.
 """
 import os
 import shutil
