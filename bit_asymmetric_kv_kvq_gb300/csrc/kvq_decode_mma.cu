@@ -315,7 +315,9 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     // the slot early, so the atomic's round trip overlaps the row loads
     int slot = 0;
     if (lane == 0) slot = atomicAdd(p.nslot + unit, 1);
-    // rows come from DRAM: keep eight 16-byte loads in flight per lane
+    // rows come from DRAM: with one query head the whole 256-byte key row of a lane is in flight at
+    // once (one round trip), and sixteen value rows; more heads keep half of that (registers)
+    constexpr int NK = HG == 1 ? 16 : 8, NV = HG == 1 ? 16 : 8;
     float s[HG];
 #pragma unroll
     for (int h = 0; h < HG; ++h) s[h] = 0.0f;
@@ -323,12 +325,12 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
       const uint4* row =
           reinterpret_cast<const uint4*>(tok == newest ? p.k_new + unit * D : wk + (int64_t)tok * D);
 #pragma unroll
-      for (int v0 = 0; v0 < D / 8; v0 += 8) {
-        uint4 w[8];
+      for (int v0 = 0; v0 < D / 8; v0 += NK) {
+        uint4 w[NK];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) w[v] = __ldg(row + v0 + v);
+        for (int v = 0; v < NK; ++v) w[v] = __ldg(row + v0 + v);
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
+        for (int v = 0; v < NK; ++v) {
           const uint32_t ws[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -355,17 +357,17 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
 #pragma unroll
       for (int i = 0; i < 4; ++i) a[h][i] = 0.0f;
     }
-    // values: lane l owns channels 4l .. 4l+3 of every row; eight rows' loads in flight
-    for (int j0 = 0; j0 < nt; j0 += 8) {
-      uint2 w[8];
+    // values: lane l owns channels 4l .. 4l+3 of every row; NV rows' loads in flight
+    for (int j0 = 0; j0 < nt; j0 += NV) {
+      uint2 w[NV];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < NV; ++i) {
         const int r = 32 * stt + j0 + i;
         const uint16_t* vrow = r == newest ? p.v_new + unit * D : wv + (int64_t)r * D;
         w[i] = j0 + i < nt ? __ldg(reinterpret_cast<const uint2*>(vrow + 4 * lane)) : make_uint2(0u, 0u);
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < NV; ++i) {
         const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&w[i].x));
         const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&w[i].y));
 #pragma unroll
