@@ -315,6 +315,12 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     // the slot early, so the atomic's round trip overlaps the row loads
     int slot = 0;
     if (lane == 0) slot = atomicAdd(p.nslot + unit, 1);
+    // the value row of this lane's token heads for L2 while the key rows are read
+    if (live) {
+      const uint16_t* vr = tok == newest ? p.v_new + unit * D : wv + (int64_t)tok * D;
+      prefetch_l2(vr);
+      prefetch_l2(vr + 64);
+    }
     // rows come from DRAM: with one query head the whole 256-byte key row of a lane is in flight at
     // once (one round trip), and sixteen value rows; more heads keep half of that (registers)
     constexpr int NK = HG == 1 ? 16 : 8, NV = HG == 1 ? 16 : 8;

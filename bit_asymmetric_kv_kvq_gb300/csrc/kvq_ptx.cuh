@@ -148,4 +148,7 @@ cudaError_t launch_pdl(void (*kern)(Args...), unsigned grid, unsigned block, siz
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Ask L2 for the 128-byte line holding p (no register result; the address must be valid).
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 }  // namespace kvq
