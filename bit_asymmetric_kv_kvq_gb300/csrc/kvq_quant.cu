@@ -845,9 +845,10 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
     const uint32_t* row = ks + t * 64;
     int bc[kMaxSparse];  // the chosen channels (unused slots hold a channel past the end)
     if (nsp <= 2) {
-      // two slots, branch-free: within the quarter channels come in increasing order, so a later
-      // channel enters only when strictly larger
-      int v0 = -1, c0 = 1 << 20, v1 = -1, c1 = 1 << 20;
+      // two slots, branch-free: each entry as the key (|x| bits << 7) | (127 - channel), so that a
+      // larger key is a larger |x|, or the same |x| at a lower channel, and no two keys are equal;
+      // the two largest keys take three integer min/max per entry
+      int k0 = -1, k1 = -1;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int ch = 4 * qt + i;  // 16-byte chunk: channels 8ch .. 8ch+7
@@ -855,29 +856,21 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int x = (int)((w4[e >> 1] >> (16 * (e & 1))) & 0x7FFFu), c = 8 * ch + e;
-          const bool g0 = x > v0, g1 = x > v1;
-          v1 = g0 ? v0 : (g1 ? x : v1);
-          c1 = g0 ? c0 : (g1 ? c : c1);
-          v0 = g0 ? x : v0;
-          c0 = g0 ? c : c0;
+          const uint32_t w = w4[e >> 1];
+          const int k = (int)((e & 1) ? (((w >> 9) & (0x7FFFu << 7)) | (uint32_t)(127 - (8 * ch + e)))
+                                      : (((w & 0x7FFFu) << 7) | (uint32_t)(127 - (8 * ch + e))));
+          k1 = max(k1, min(k0, k));
+          k0 = max(k0, k);
         }
       }
-      // merge the four quarters' pairs (the partner's channels lie in another quarter)
+      // merge the four quarters' pairs
 #pragma unroll
       for (int off = 1; off < 4; off <<= 1) {
-        const int w0 = __shfl_xor_sync(0xffffffffu, v0, off), d0 = __shfl_xor_sync(0xffffffffu, c0, off);
-        const int w1 = __shfl_xor_sync(0xffffffffu, v1, off), d1 = __shfl_xor_sync(0xffffffffu, c1, off);
-        const bool a = v0 > w0 || (v0 == w0 && c0 < d0);  // own head first
-        // the runner-up: the loser of the heads against the winner's second
-        const int lv = a ? w0 : v0, lc = a ? d0 : c0, sv2 = a ? v1 : w1, sc2 = a ? c1 : d1;
-        const bool b = lv > sv2 || (lv == sv2 && lc < sc2);
-        const int nv0 = a ? v0 : w0, nc0 = a ? c0 : d0;
-        v1 = b ? lv : sv2;
-        c1 = b ? lc : sc2;
-        v0 = nv0;
-        c0 = nc0;
+        const int o0 = __shfl_xor_sync(0xffffffffu, k0, off), o1 = __shfl_xor_sync(0xffffffffu, k1, off);
+        k1 = max(min(k0, o0), max(k1, o1));
+        k0 = max(k0, o0);
       }
+      const int c0 = 127 - (k0 & 127), c1 = 127 - (k1 & 127);
       bc[0] = min(c0, c1);
       bc[1] = nsp == 2 ? max(c0, c1) : (1 << 20);
       bc[0] = nsp == 2 ? bc[0] : c0;
