@@ -724,7 +724,7 @@ __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const Quan
 // half-integer (where it could round differently from the IEEE quotient) are collected in a mask
 // and taken again with the IEEE quotient after the loop, behind one vote per chunk.
 struct __align__(8) QuantF {  // a group quantizer in the form the code loop uses
-  float inv, z;
+  float inv, nz;  // 1/s and -z
 };
 // shared memory of quantize_bits_kernel: the two tiles, the key and value quantizers (QuantF) and
 // their stored (zero point, step) words
@@ -738,20 +738,31 @@ template <int BITS, class QF, class QB, class XF, class XD>
 __device__ __forceinline__ void code_chunk(const XF& xval, const XD& xdyn, const QF& qf, const QB& qbits,
                                            uint32_t (&w)[BITS]) {
   constexpr int L = (1 << BITS) - 1;
+  constexpr float M = 0x1.8p23f;  // r + M has rint(r) in its low mantissa bits (0 <= r < 2^22)
 #pragma unroll
   for (int i = 0; i < BITS; ++i) w[i] = 0;
   uint32_t near = 0;
+  // two codes at a time on packed fp32 pairs: d = max(x - z, 0) (a sparse entry, NaN, gives 0 and
+  // code 0; every other x is at least the group minimum z), r = d / s as d * (1/s), t = r + M,
+  // code = min(rint(r), L) from t's bits; near when |r - rint(r)| >= 1/2 - 2^-14 (exact difference)
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    const QuantF q = qf(c);
-    const float d = __fsub_rn(xval(c), q.z);  // a NaN (sparse entry) stays NaN and gives code 0
-    const float r = __fmul_rn(d, q.inv);
-    const float rq = rintf(r);
-    near |= (fabsf(__fsub_rn(r, rq)) >= 0.5f - 0x1.0p-14f ? 1u : 0u) << c;
-    const uint32_t code = (uint32_t)fminf(fmaxf(rq, 0.0f), (float)L);
-    const int b = BITS * c;
-    w[b >> 5] |= code << (b & 31);
-    if ((b & 31) + BITS > 32) w[(b >> 5) + 1] |= code >> (32 - (b & 31));
+  for (int c = 0; c < 32; c += 2) {
+    const QuantF q0 = qf(c), q1 = qf(c + 1);
+    float2 d = __fadd2_rn(make_float2(xval(c), xval(c + 1)), make_float2(q0.nz, q1.nz));
+    d = make_float2(fmaxf(d.x, 0.0f), fmaxf(d.y, 0.0f));
+    const float2 r = __fmul2_rn(d, make_float2(q0.inv, q1.inv));
+    const float2 t = __fadd2_rn(r, make_float2(M, M));
+    const float2 e = __ffma2_rn(__fadd2_rn(t, make_float2(-M, -M)), make_float2(-1.0f, -1.0f), r);
+    near |= (fabsf(e.x) >= 0.5f - 0x1.0p-14f ? 1u << c : 0u) | (fabsf(e.y) >= 0.5f - 0x1.0p-14f ? 2u << c : 0u);
+    const uint32_t code0 = min(__float_as_uint(t.x) - __float_as_uint(M), (uint32_t)L);
+    const uint32_t code1 = min(__float_as_uint(t.y) - __float_as_uint(M), (uint32_t)L);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t code = k ? code1 : code0;
+      const int b = BITS * (c + k);
+      w[b >> 5] |= code << (b & 31);
+      if ((b & 31) + BITS > 32) w[(b >> 5) + 1] |= code >> (32 - (b & 31));
+    }
   }
   if (__any_sync(0xffffffffu, near != 0)) {
     while (near) {
@@ -965,8 +976,8 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
       if (fmn.x != fmn.x) fmn.x = fmx.x = 0.0f;  // every entry sparse: range 0
       if (fmn.y != fmn.y) fmn.y = fmx.y = 0.0f;
       const GroupQ q0 = group_params(fmn.x, fmx.x, LK), q1 = group_params(fmn.y, fmx.y, LK);
-      kqf[gk * 128 + 2 * cp] = QuantF{q0.inv, q0.zf()};
-      kqf[gk * 128 + 2 * cp + 1] = QuantF{q1.inv, q1.zf()};
+      kqf[gk * 128 + 2 * cp] = QuantF{q0.inv, -q0.zf()};
+      kqf[gk * 128 + 2 * cp + 1] = QuantF{q1.inv, -q1.zf()};
       kzs[gk * 128 + 2 * cp] = q0.bits;
       kzs[gk * 128 + 2 * cp + 1] = q1.bits;
       *reinterpret_cast<uint2*>(dst + p.lay.off_km + (gk * 128 + 2 * cp) * 4) = make_uint2(q0.bits, q1.bits);
@@ -989,8 +1000,8 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
       }
       const float2 fmn = __half22float2(mn), fmx = __half22float2(mx);
       const GroupQ q0 = group_params(fmn.x, fmx.x, LV), q1 = group_params(fmn.y, fmx.y, LV);
-      vqf[(2 * tp) * ngv + g] = QuantF{q0.inv, q0.zf()};
-      vqf[(2 * tp + 1) * ngv + g] = QuantF{q1.inv, q1.zf()};
+      vqf[(2 * tp) * ngv + g] = QuantF{q0.inv, -q0.zf()};
+      vqf[(2 * tp + 1) * ngv + g] = QuantF{q1.inv, -q1.zf()};
       vzs[(2 * tp) * ngv + g] = q0.bits;
       vzs[(2 * tp + 1) * ngv + g] = q1.bits;
       uint32_t* vm = reinterpret_cast<uint32_t*>(dst + p.lay.off_vm);
