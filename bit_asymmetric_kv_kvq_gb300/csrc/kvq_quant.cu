@@ -462,6 +462,25 @@ __device__ __forceinline__ __half2 as_h2(uint32_t x) {
   return h;
 }
 
+// 4-bit codes of an fp16 pair of group values (x >= the group's minimum) with each half's quantizer,
+// codes at bits 0-3 and 16-19, on packed fp32 pairs: r = (x - z) * (1/s), t = r + 1.5*2^23 holds
+// rint(r) in its low mantissa bits, the clamp is one integer minimum.  Where r lies within 2^-14 of a
+// half-integer (where it could round differently from the IEEE quotient) the pair's bit 0 / 1 of
+// `near` is set and the caller takes that code again with code4_exact.
+__device__ __forceinline__ uint32_t code4_pair_fast(uint32_t x, const GroupQ& q0, const GroupQ& q1, uint32_t& near) {
+  constexpr float M = 0x1.8p23f;
+  const float2 d = __fadd2_rn(__half22float2(as_h2(x)), make_float2(-q0.zf(), -q1.zf()));
+  const float2 r = __fmul2_rn(d, make_float2(q0.inv, q1.inv));
+  const float2 t = __fadd2_rn(r, make_float2(M, M));
+  const float2 e = __ffma2_rn(__fadd2_rn(t, make_float2(-M, -M)), make_float2(-1.0f, -1.0f), r);
+  near = (fabsf(e.x) >= 0.5f - 0x1.0p-14f ? 1u : 0u) | (fabsf(e.y) >= 0.5f - 0x1.0p-14f ? 2u : 0u);
+  return min(__float_as_uint(t.x) - __float_as_uint(M), 15u) | (min(__float_as_uint(t.y) - __float_as_uint(M), 15u) << 16);
+}
+__device__ __forceinline__ uint32_t code4_exact(float x, const GroupQ& g) {
+  const float q = rintf(__fdiv_rn(__fsub_rn(x, g.zf()), g.sf()));  // s > 0: a zero step is never near
+  return (uint32_t)fminf(fmaxf(q, 0.0f), 15.0f);
+}
+
 // 4-bit codes of an fp16 pair with each half's quantizer: codes at bits 0-3 and 16-19.
 __device__ __forceinline__ uint32_t code4_pair(uint32_t x, const GroupQ& q0, const GroupQ& q1) {
   const float2 f = __half22float2(as_h2(x));
@@ -634,6 +653,7 @@ __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const Quan
     } else {
       // word r*4 + u, pair j: channel pair 16u + 4j + t4 (chunk 4u + j)
       const GroupQ* gq = reinterpret_cast<const GroupQ*>(sw + SM::kt) + gk * 128 + 2 * t4;
+      uint32_t nm0 = 0, nm1 = 0;  // near-tie elements: bit 4c + 2r + e of element e of pair (chunk c, row r)
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -643,9 +663,28 @@ __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const Quan
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const uint32_t x = kr[r * 8 * 64 + 4 * (c & 8) + sj[c & 7]];
-            wd[r * 4 + u] |= code4_pair(x, q0, q1) << (4 * j);
+            uint32_t nb;
+            wd[r * 4 + u] |= code4_pair_fast(x, q0, q1, nb) << (4 * j);
+            const int b = 4 * c + 2 * r;
+            if (b < 32) nm0 |= nb << b;
+            else nm1 |= nb << (b - 32);
           }
         }
+      // the rare near-tie elements again with the IEEE quotient, behind one vote
+      if (__any_sync(0xffffffffu, (nm0 | nm1) != 0)) {
+        uint64_t nm = ((uint64_t)nm1 << 32) | nm0;
+        while (nm) {
+          const int b = __ffsll((long long)nm) - 1;
+          nm &= nm - 1;
+          const int e = b & 1, r = (b >> 1) & 1, c = b >> 2, u = c >> 2, j = c & 3;
+          const uint32_t x = kr[r * 8 * 64 + 4 * (c & 8) + (((c & 7) ^ g8) << 2)];
+          const uint32_t code = code4_exact(h2f((uint16_t)(e ? (x >> 16) : (x & 0xFFFFu))), gq[2 * (16 * u + 4 * j) + e]);
+          const int sh = 4 * j + 16 * e;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i == r * 4 + u) wd[i] = (wd[i] & ~(0xFu << sh)) | (code << sh);
+        }
+      }
     }
     uint4* o = reinterpret_cast<uint4*>(dst + SP::kc) + (m * 32 + lane) * (2 * BK / 4);
 #pragma unroll
