@@ -75,13 +75,18 @@ struct Pairs {
 
 __device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
 
-// (a, b) split into fp16 high parts and the fp16 rounding of what they leave: a = hi + lo to about
-// 22 significant bits.  Two values per conversion.
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
-  const float2 f = __half22float2(h);
-  hi = h2bits(h);
-  lo = h2bits(__floats2half2_rn(a - f.x, b - f.y));
+// x = q * s for a pair of channels, split into fp16 high parts and the fp16 rounding of what they
+// leave, for |x| < 2^(15 - pk).  With M = 1.5 * 2^(27 - pk), fl(x + M) lies in [2^(27-pk), 2^(28-pk))
+// whose fp32 spacing is 2^(4 - pk), so fl(x + M) - M is x rounded to that grid (exact subtraction):
+// a multiple of 2^(4-pk) below 2^(15-pk) in magnitude, at most 11 significant bits, exact in fp16.
+// What it leaves (|r| <= 2^(3-pk), exact in fp32) is rounded to fp16 once: hi + lo = x within
+// 2^-23 of the bound.  Two values per instruction, no conversion back from fp16.
+__device__ __forceinline__ void split_qs(float2 q, float2 s, float2 M, uint32_t& hi, uint32_t& lo) {
+  const float2 t = __ffma2_rn(q, s, M);
+  const float2 h = __fadd2_rn(t, make_float2(-M.x, -M.y));
+  const float2 r = __ffma2_rn(q, s, make_float2(-h.x, -h.y));
+  hi = h2bits(__float22half2_rn(h));
+  lo = h2bits(__float22half2_rn(r));
 }
 
 template <int BK, int BV, int HG, bool STD>
@@ -108,7 +113,10 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
   const int off_vc = STD ? SP::vc : p.lay.off_vc, off_vm = STD ? SP::vm : p.lay.off_vm;
   const int log2G = STD ? 5 : p.log2G;
   const int nsp = STD ? 0 : p.nsp;
-  const int log2S = p.log2_stages, n_stages = 1 << log2S;
+  // the page ring: page k of the slice goes to stage k mod n_stages on lap k / n_stages
+  const int n_stages = p.n_stages;
+  const uint32_t smagic = p.stage_magic;
+  auto lap_of = [&](int k) { return (int)__umulhi((uint32_t)k, smagic); };
   const int SPP = STD ? 4 : p.R / 32;
   const int n_sub = (int)(w_end - w_begin) * SPP;
   const int ng = D >> log2G;               // value groups per token
@@ -116,7 +124,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
   // dynamic shared memory: the page stages, then each warp's query rows (fp32) and key B
   // fragments (static arrays stay small: static shared memory is limited to 48 KB)
   extern __shared__ __align__(128) uint8_t stage_mem[];
-  float(*qw_s)[HG][D] = reinterpret_cast<float(*)[HG][D]>(stage_mem + ((size_t)page_bytes << p.log2_stages));
+  float(*qw_s)[HG][D] = reinterpret_cast<float(*)[HG][D]>(stage_mem + (size_t)page_bytes * n_stages);
   uint32_t(*bk_s)[KCOL][4][16] = reinterpret_cast<uint32_t(*)[KCOL][4][16]>(qw_s + W);
   __shared__ __align__(8) uint64_t full_bar[kMmaMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMmaMaxStages];
@@ -148,11 +156,11 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
       }
     }
 #endif
-    const int st = k & (n_stages - 1);
+    const int lap = lap_of(k), st = k - lap * n_stages;
     mbar_arrive_expect_tx(&full_bar[st], (uint32_t)page_bytes);
     bulk_g2s(stage_mem + (size_t)st * page_bytes, p.pages + (int64_t)u * p.unit_page_stride + (int64_t)loc * page_bytes,
              (uint32_t)page_bytes, &full_bar[st]);
-    stage_issued[st] = (k >> log2S) + 1;
+    stage_issued[st] = lap + 1;
     stage_page[st] = k;
   };
   // A warp may have taken a sub-tile of page k while a stage still serves page k - n_stages
@@ -160,7 +168,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
   // parity wait cannot tell phases 2*n_stages pages apart.  So wait until the stage is assigned
   // page k, then for its copy.  Bounded like every wait here.
   auto wait_page = [&](int k) -> bool {
-    const int st = k & (n_stages - 1);
+    const int lap = lap_of(k), st = k - lap * n_stages;
     if (*(volatile int*)&stage_page[st] != k) {
       const unsigned long long t0 = global_ns();
       while (*(volatile int*)&stage_page[st] != k) {
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
         __nanosleep(128);
       }
     }
-    return mbar_wait(&full_bar[st], (k >> log2S) & 1, wlim);
+    return mbar_wait(&full_bar[st], lap & 1, wlim);
   };
 
   if (tid < 64) (&zero_frag[0][0])[tid] = 0u;
@@ -436,7 +444,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     // ---------------- sub-tiles of a page: tokens 32*stt .. 32*stt+31 for stt = stt0 .. stt0+GR-1
     touched = true;
     const int kpg = (int)(cur * p.n_pages + (loc - hw) - P_begin);
-    const int stg = kpg & (n_stages - 1);
+    const int kpg_lap = lap_of(kpg), stg = kpg - kpg_lap * n_stages;
     if (!wait_page(kpg)) {
       report_error(p.err, kDevWaitTimeout);
       atomicExch(&abort_flag, 1);
@@ -456,36 +464,37 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     float sgk;  // score = D * 2^(24 - sig)
     {
       const uint4 mz = *reinterpret_cast<const uint4*>(km + gk * D + 4 * lane);
-      const uint32_t mzw[4] = {mz.x, mz.y, mz.z, mz.w};
-      float zc[4], sc4[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(&mzw[i]));
-        zc[i] = zs.x;
-        sc4[i] = zs.y;
-      }
+      // (z, s) of channels 4*lane + i
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&mz.x));
+      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&mz.y));
+      const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&mz.z));
+      const float2 f3 = __half22float2(*reinterpret_cast<const __half2*>(&mz.w));
       // channel c = 4*lane + i = 16*kk + 8*hh + 2*tt + e
       const int kk = lane >> 2, hh = (lane >> 1) & 1;
       const int pk = PK::pos(2 * (kk % KPW) + hh);
       // steps are >= 0: the largest orders like its bit pattern
-      const float smx = fmaxf(fmaxf(sc4[0], sc4[1]), fmaxf(sc4[2], sc4[3]));
+      const float smx = fmaxf(fmaxf(f0.y, f1.y), fmaxf(f2.y, f3.y));
       const uint32_t smxb = __reduce_max_sync(kAll, __float_as_uint(smx));
       const int esk = smxb != 0u ? (int)((smxb >> 23) & 0xFF) - 127 : 0;
       const int sig = min(max(13 - eq - esk, -90), 90);
       sgk = pow2f(24 - sig);
       const float sscale = pow2f(sig - pk);
-      float ss[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ss[i] = sc4[i] * sscale;
+      const float2 ss01 = __fmul2_rn(make_float2(f0.y, f1.y), make_float2(sscale, sscale));
+      const float2 ss23 = __fmul2_rn(make_float2(f2.y, f3.y), make_float2(sscale, sscale));
+      const float2 z01 = make_float2(f0.x, f1.x), z23 = make_float2(f2.x, f3.x);
+      const float mg = pow2f(27 - pk) * 1.5f;
+      const float2 M = make_float2(mg, mg);
       float zp[HG];
+      const int tt0 = 2 * (lane & 1);
 #pragma unroll
       for (int h = 0; h < HG; ++h) {
         const float4 q4 = *reinterpret_cast<const float4*>(&qs[h][4 * lane]);
-        zp[h] = fmaf(q4.x, zc[0], fmaf(q4.y, zc[1], fmaf(q4.z, zc[2], q4.w * zc[3])));
-        const int tt0 = 2 * (lane & 1);
+        const float2 q01 = make_float2(q4.x, q4.y), q23 = make_float2(q4.z, q4.w);
+        const float2 zq = __ffma2_rn(q23, z23, __fmul2_rn(q01, z01));
+        zp[h] = zq.x + zq.y;
         uint32_t hi01, lo01, hi23, lo23;
-        split2(q4.x * ss[0], q4.y * ss[1], hi01, lo01);
-        split2(q4.z * ss[2], q4.w * ss[3], hi23, lo23);
+        split_qs(q01, ss01, M, hi01, lo01);
+        split_qs(q23, ss23, M, hi23, lo23);
         bk_s[warp][2 * h][tt0][2 * kk + hh] = hi01;
         bk_s[warp][2 * h][tt0 + 1][2 * kk + hh] = hi23;
         bk_s[warp][2 * h + 1][tt0][2 * kk + hh] = lo01;
@@ -696,7 +705,20 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
         const float2 b23 = __fmul2_rn(pb23, make_float2(vs[kc][bi][2], vs[kc][bi][3]));
         bv[bi][0] = h2bits(__floats2half2_rn(b01.x, b01.y));
         bv[bi][1] = h2bits(__floats2half2_rn(b23.x, b23.y));
-        zacc[bi] = fmaf(p0, vz[kc][bi][0], fmaf(p1, vz[kc][bi][1], fmaf(p2, vz[kc][bi][2], fmaf(p3, vz[kc][bi][3], zacc[bi]))));
+      }
+      if constexpr (NBM == 2) {
+        // both fragments' zero-point sums at once: (zacc[0], zacc[1]) += p_i (z of either group)
+        float2 za = make_float2(zacc[0], zacc[1]);
+        za = __ffma2_rn(make_float2(p3, p3), make_float2(vz[kc][0][3], vz[kc][1][3]), za);
+        za = __ffma2_rn(make_float2(p2, p2), make_float2(vz[kc][0][2], vz[kc][1][2]), za);
+        za = __ffma2_rn(make_float2(p1, p1), make_float2(vz[kc][0][1], vz[kc][1][1]), za);
+        za = __ffma2_rn(make_float2(p0, p0), make_float2(vz[kc][0][0], vz[kc][1][0]), za);
+        zacc[0] = za.x;
+        zacc[1] = za.y;
+      } else {
+#pragma unroll
+        for (int bi = 0; bi < NBM; ++bi)
+          zacc[bi] = fmaf(p0, vz[kc][bi][0], fmaf(p1, vz[kc][bi][1], fmaf(p2, vz[kc][bi][2], fmaf(p3, vz[kc][bi][3], zacc[bi]))));
       }
       lacc += (p0 + p1) + (p2 + p3);  // read from the lanes of B column h (lane 4h)
 
@@ -739,7 +761,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     if (lane == 0) {
       for (int qq = 0; qq < GR; ++qq) mbar_arrive(&empty_bar[stg]);
       if (atomicAdd(&stage_cnt[stg], GR) % SPP == SPP - GR && kpg + n_stages < n_pg && !*(volatile int*)&abort_flag) {
-        if (mbar_wait(&empty_bar[stg], (kpg >> log2S) & 1, wlim)) {
+        if (mbar_wait(&empty_bar[stg], kpg_lap & 1, wlim)) {
           issue_page(kpg + n_stages);
         } else {
           report_error(p.err, kDevWaitTimeout);
@@ -762,11 +784,11 @@ constexpr size_t warp_bufs_bytes() {
   return (size_t)mma_warps<HG>() * (HG * kHeadDim * sizeof(float) + 2 * HG * 4 * 16 * sizeof(uint32_t));
 }
 
-// Page stages of one CTA: the largest power of two up to kMmaMaxStages whose pages fit the
-// opt-in shared memory beside the static arrays and the per-warp buffers; -1 when none fits
-// (or the static arrays exceed the 48 KB a kernel may declare).
+// Page stages of one CTA: as many as fit (up to kMmaMaxStages) in the opt-in shared memory beside
+// the static arrays and the per-warp buffers; -1 when none fits (or the static arrays exceed the
+// 48 KB a kernel may declare).
 template <int BK, int BV, int HG>
-int log2_stages_mma(int page_bytes) {
+int stages_mma(int page_bytes) {
   auto kern = decode_mma_kernel<BK, BV, HG, false>;  // both variants declare the same static arrays
   static int static_smem = -1, optin = -1;
   if (static_smem < 0) {
@@ -779,18 +801,18 @@ int log2_stages_mma(int page_bytes) {
   }
   if (static_smem > 48 * 1024) return -1;
   const int64_t avail = (int64_t)optin - static_smem - (int64_t)warp_bufs_bytes<HG>();
-  int l = 4;  // kMmaMaxStages = 16
-  while (l >= 0 && ((int64_t)page_bytes << l) > avail) --l;
-  return l;
+  const int64_t n = avail / page_bytes;
+  return n < 1 ? -1 : (int)(n < kMmaMaxStages ? n : kMmaMaxStages);
 }
 
 template <int BK, int BV, int HG>
 cudaError_t launch_mma_t(const DecodeParams& p, int grid, cudaStream_t s) {
-  const int l = log2_stages_mma<BK, BV, HG>(p.lay.bytes);
-  if (l < 0) return cudaErrorInvalidValue;
+  const int n = stages_mma<BK, BV, HG>(p.lay.bytes);
+  if (n < 0) return cudaErrorInvalidValue;
   DecodeParams q = p;
-  q.log2_stages = l;
-  const size_t smem = ((size_t)p.lay.bytes << l) + warp_bufs_bytes<HG>();
+  q.n_stages = n;
+  q.stage_magic = (uint32_t)((0x100000000ull + (uint64_t)n - 1) / (uint64_t)n);  // ceil(2^32 / n)
+  const size_t smem = (size_t)p.lay.bytes * n + warp_bufs_bytes<HG>();
   const bool std_shape = p.R == 128 && p.G == 32 && p.nsp == 0 && p.lay.bytes == StdPage<BK, BV>::bytes &&
                          p.lay.off_km == StdPage<BK, BV>::km && p.lay.off_vc == StdPage<BK, BV>::vc &&
                          p.lay.off_vm == StdPage<BK, BV>::vm && p.lay.off_kc == 0;
@@ -802,17 +824,18 @@ cudaError_t launch_mma_t(const DecodeParams& p, int grid, cudaStream_t s) {
 
 template <int BK, int BV, int HG>
 int resident_mma_t(int page_bytes) {
-  const int l = log2_stages_mma<BK, BV, HG>(page_bytes);
-  if (l < 0) return 0;
-  const size_t smem = ((size_t)page_bytes << l) + warp_bufs_bytes<HG>();
+  const int n = stages_mma<BK, BV, HG>(page_bytes);
+  if (n < 0) return 0;
+  const size_t smem = (size_t)page_bytes * n + warp_bufs_bytes<HG>();
   auto kern = decode_mma_kernel<BK, BV, HG, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
   if (cudaFuncSetAttribute(decode_mma_kernel<BK, BV, HG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return 0;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, mma_warps<HG>() * 32, smem) != cudaSuccess) return 0;
-  return n;
+  int n_ctas = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n_ctas, kern, mma_warps<HG>() * 32, smem) != cudaSuccess)
+    return 0;
+  return n_ctas;
 }
 
 }  // namespace

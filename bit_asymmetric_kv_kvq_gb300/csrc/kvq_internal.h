@@ -129,7 +129,9 @@ struct DecodeParams {
   int32_t n_s;              // sink tokens; positions: sink 0..n_s, pages n_s.., window n_s + Tq..
   int32_t n_w;              // fp16 rows n_s + n_r: the sink rows, then the window rows
   int32_t max_slots;        // partial slots per query head
-  int32_t log2_stages;      // page stages per CTA (set by the launcher)
+  int32_t log2_stages;      // page stages per CTA (set by the launcher; CUDA-core kernels)
+  int32_t n_stages;         // page stages per CTA of the tensor-core kernel (any count up to 16)
+  uint32_t stage_magic;     //   and ceil(2^32 / n_stages): k / n_stages = umulhi(k, stage_magic)
   int32_t Hkv, Hq, D, G, R, nsp;
   int32_t log2G;            // G = 1 << log2G
   PageLayout lay;
