@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
   constexpr int NCOL = HG;       // value B columns per value group: one per head
   constexpr int GPB = 8 / NCOL;  // value groups per B fragment
   constexpr int NBM = (D / 32 + GPB - 1) / GPB;  // B fragments per value tile at most (G = 32)
+  // value group g sits in B fragment g % NBM, column block g / NBM: the groups a lane feeds are
+  // consecutive (one 8-byte load per token when NBM = 2)
   constexpr int KCOL = 2 * HG;   // key B columns: (head, high/low)
   constexpr int KPW = 8 / BK;    // key k-chunks per fragment word
   using PK = Pairs<BK>;
@@ -286,11 +288,11 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int n = 2 * t4 + e;
-          if (n / HG != grp % GPB) continue;  // this column holds another group's products
+          if (n / HG != grp / NBM) continue;  // this column holds another group's products
           float z = zs[e][0];
 #pragma unroll
           for (int i = 1; i < NBM; ++i)
-            if (grp / GPB == i) z = zs[e][i];
+            if (grp % NBM == i) z = zs[e][i];
           float* dst = p.part_acc + ((bh0 + n % HG) * p.max_slots + slot) * D + 16 * mc + g8;
           dst[0] = fmaf(dv[mc][e], s, z);
           dst[8] = fmaf(dv[mc][2 + e], s, z);
@@ -411,7 +413,10 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     }
   };
 
-  int64_t cur = -1, ustart = 0;
+  int64_t cur = -1;
+  // for the current unit, relative to the slice's item index sx: the first item past the unit,
+  // the unit's item of index 0 and the slice page of its first page (32-bit: a slice is small)
+  int uend = 0, lofs = 0, kofs = 0;
   bool touched = false;  // the warp has state (page sub-tiles) for the current unit
   // sub-tiles taken at a time: two (of one page) when a page has an even number of them, which
   // halves the scheduling, page-wait and release work per sub-tile
@@ -423,16 +428,19 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     if (s >= n_sub || *(volatile int*)&abort_flag) break;
     const int sx = SPP == 4 ? s >> 2 : SPP == 2 ? s >> 1 : SPP == 1 ? s : s / 3;
     const int stt0 = s - sx * SPP;
-    const int64_t x = w_begin + sx;
-    if (cur < 0 || x >= ustart + wpu) {
+    if (cur < 0 || sx >= uend) {
       if (cur >= 0 && touched) epilogue(cur);
+      const int64_t x = w_begin + sx;
       cur = x / wpu;
-      ustart = cur * wpu;
+      const int64_t ustart = cur * wpu;
+      uend = (int)(ustart + wpu - w_begin);
+      lofs = (int)(w_begin - ustart);
+      kofs = (int)(cur * p.n_pages - hw - P_begin) + lofs;
       touched = false;
       reset();
       load_q(cur);
     }
-    const int loc = (int)(x - ustart);
+    const int loc = sx + lofs;
     if (loc < hw) {
       for (int qq = 0; qq < GR; ++qq) {
         const int f = loc * SPP + stt0 + qq;  // sub-tile of the unit's fp16 rows
@@ -443,7 +451,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
 
     // ---------------- sub-tiles of a page: tokens 32*stt .. 32*stt+31 for stt = stt0 .. stt0+GR-1
     touched = true;
-    const int kpg = (int)(cur * p.n_pages + (loc - hw) - P_begin);
+    const int kpg = sx + kofs;  // = cur * n_pages + (loc - hw) - P_begin
     const int kpg_lap = lap_of(kpg), stg = kpg - kpg_lap * n_stages;
     if (!wait_page(kpg)) {
       report_error(p.err, kDevWaitTimeout);
@@ -661,17 +669,33 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
 #pragma unroll
       for (int kc = 0; kc < 2; ++kc) {
         const int tb = 16 * (2 * stt + kc) + 2 * t4;
-#pragma unroll
-        for (int bi = 0; bi < NBM; ++bi) {
-          const int grp = bi * GPB + gl;
+        if constexpr (STD && NBM == 2) {
+          // groups 2*gl and 2*gl + 1 of a token: adjacent words
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int tok = tb + (i & 1) + 8 * (i >> 1);
-            float2 zsv = make_float2(0.0f, 0.0f);
-            if (grp < ng) zsv = __half22float2(*reinterpret_cast<const __half2*>(vm + tok * ng + grp));
-            vz[kc][bi][i] = zsv.x;
-            vs[kc][bi][i] = zsv.y;
-            smax = fmaxf(smax, zsv.y);
+            const uint2 w = *reinterpret_cast<const uint2*>(vm + tok * 4 + 2 * gl);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+            vz[kc][0][i] = a.x;
+            vs[kc][0][i] = a.y;
+            vz[kc][1][i] = b.x;
+            vs[kc][1][i] = b.y;
+            smax = fmaxf(smax, fmaxf(a.y, b.y));
+          }
+        } else {
+#pragma unroll
+          for (int bi = 0; bi < NBM; ++bi) {
+            const int grp = gl * NBM + bi;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int tok = tb + (i & 1) + 8 * (i >> 1);
+              float2 zsv = make_float2(0.0f, 0.0f);
+              if (grp < ng) zsv = __half22float2(*reinterpret_cast<const __half2*>(vm + tok * ng + grp));
+              vz[kc][bi][i] = zsv.x;
+              vs[kc][bi][i] = zsv.y;
+              smax = fmaxf(smax, zsv.y);
+            }
           }
         }
       }
@@ -741,7 +765,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
         constexpr int WPR = BV / 2;  // words per register slot
         uint32_t b0 = bv[0][0], b1 = bv[0][1];
         if constexpr (NBM > 1) {
-          const int bi = ((16 * mc) >> log2G) / GPB;
+          const int bi = ((16 * mc) >> log2G) % NBM;
 #pragma unroll
           for (int i = 1; i < NBM; ++i)
             if (bi == i) {
