@@ -48,6 +48,9 @@ __host__ __device__ constexpr int mma_warps() { return 16; }
 constexpr int kMmaMaxStages = 16;
 constexpr unsigned kAll = 0xffffffffu;
 constexpr float kLazy = 8.0f;  // the running maximum moves only when a score passes it by 8 (log2 units)
+// Running maximum before the first score: finite, below every score, so the first sub-tile raises it
+// by the plain lazy test and the rescale factor 2^(kNoMax - m) of the (empty) sums is 0.
+constexpr float kNoMax = -1.0e30f;
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
@@ -58,6 +61,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }  // |e| <= 126
+
+// 2^x by the hardware approximation, results below 2^-126 flushed to zero: softmax weights that
+// small (relative to a running maximum at most 2^8 below the largest) change no sum.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Code pairs of one fragment word (B-bit codes): pair j read in place for j < DIR, from the
 // word shifted down by SHIFT bits otherwise; pos(j) is the exponent of its position scale.
@@ -209,7 +220,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
 
   // ---- per-warp state for the current unit
   float dv[8][4];            // value accumulators, one m16n8 tile per 16 channels
-  float mrun;                // running maximum of head hmine (log2 units)
+  float mrun;                // running maximum of head hmine (log2 units), kNoMax before the first score
   float lacc, zacc[NBM];     // sum of p (column owners) and p*z per B fragment
   int es;                    // exponent bound of the value scales seen (B values carry 2^(6-es));
                              // starts below every fp16 scale (>= 2^-24)
@@ -218,7 +229,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) dv[i][j] = 0.0f;
-    mrun = -INFINITY;
+    mrun = kNoMax;
     lacc = 0.0f;
 #pragma unroll
     for (int i = 0; i < NBM; ++i) zacc[i] = 0.0f;
@@ -366,7 +377,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
       m[h] = sc;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m[h] = fmaxf(m[h], __shfl_xor_sync(kAll, m[h], off));
-      pw[h] = live ? exp2f(sc - m[h]) : 0.0f;
+      pw[h] = live ? ex2_ftz(sc - m[h]) : 0.0f;
       l[h] = pw[h];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) l[h] += __shfl_xor_sync(kAll, l[h], off);
@@ -484,7 +495,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
       const float smx = fmaxf(fmaxf(f0.y, f1.y), fmaxf(f2.y, f3.y));
       const uint32_t smxb = __reduce_max_sync(kAll, __float_as_uint(smx));
       const int esk = smxb != 0u ? (int)((smxb >> 23) & 0xFF) - 127 : 0;
-      const int sig = min(max(13 - eq - esk, -90), 90);
+      const int sig = 13 - eq - esk;  // fp16 exponents: within [-17, 61]
       sgk = pow2f(24 - sig);
       const float sscale = pow2f(sig - pk);
       const float2 ss01 = __fmul2_rn(make_float2(f0.y, f1.y), make_float2(sscale, sscale));
@@ -579,7 +590,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
 #pragma unroll
           for (int jj = 0; jj < KPW; ++jj) {
             const int kk = u * KPW + jj;
-            mma16816(da[mt][kk & 1], PK::get(X, Xs, 2 * jj), PK::get(Y, Ys, 2 * jj), PK::get(X, Xs, 2 * jj + 1),
+            mma16816(da[mt][0], PK::get(X, Xs, 2 * jj), PK::get(Y, Ys, 2 * jj), PK::get(X, Xs, 2 * jj + 1),
                      PK::get(Y, Ys, 2 * jj + 1), bf[2 * kk], bf[2 * kk + 1]);
           }
         }
@@ -587,7 +598,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) dsum[mt][e] = da[mt][0][e] + da[mt][1][e];
+        for (int e = 0; e < 4; ++e) dsum[mt][e] = da[mt][0][e];
     }
     float sc[2][2];
     // every lane computes (no branch); lanes past the heads take head 0 and are masked below
@@ -630,14 +641,14 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     // -- online softmax (lazy maximum), per head over lanes t4 = head
     {
       const float tmax = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-      const bool over = tmax > mrun + kLazy || (mrun == -INFINITY && tmax != -INFINITY);
+      const bool over = tmax > mrun + kLazy;  // masked lanes hold -inf
       if (__any_sync(kAll, over)) {
         float mx = tmax;
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, off));
         mx = __shfl_sync(kAll, mx, (lane & ~3) | hmine);  // the maximum of this lane's head
         const float mnew = fmaxf(mx, mrun);
-        const float f = mrun == -INFINITY ? 0.0f : exp2f(mrun - mnew);
+        const float f = ex2_ftz(mrun - mnew);  // 0 on the first sub-tile
         // the lane's D columns belong to heads hd0, hd1 (f of head h is on the lanes t4 = h)
         const float f0 = HG == 1 ? f : __shfl_sync(kAll, f, (lane & ~3) | hd0);
         const float f1 = HG == 1 ? f : __shfl_sync(kAll, f, (lane & ~3) | hd1);
@@ -658,7 +669,7 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int rh = 0; rh < 2; ++rh) sc[mt][rh] = t4 < HG ? exp2f(sc[mt][rh] - mrun) : 0.0f;
+        for (int rh = 0; rh < 2; ++rh) sc[mt][rh] = t4 < HG ? ex2_ftz(sc[mt][rh] - mrun) : 0.0f;
     }
 
     // -- values: scales and zero points of the lane's column groups for the 8 tokens it feeds
