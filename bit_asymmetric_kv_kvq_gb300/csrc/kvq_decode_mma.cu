@@ -556,8 +556,9 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
     __syncwarp();  // bk_s is free for the next sub-tile
 
     // -- scores of the two 16-token tiles: lane (g8, t4 < HG) gets head t4 of tokens g8, g8 + 8.
-    //    The tiles' products are interleaved, two accumulator chains each (k-chunks kk % 2), so four
-    //    independent chains keep the mma latency off the path.
+    //    The two tiles' products are interleaved: two accumulator chains of eight products each
+    //    (splitting each chain in two and adding the halves measured slower: the adds cost more
+    //    than the latency they hide behind the other warps).
     float dsum[2][4];
     {
       uint32_t wd[2][2 * BK];
@@ -574,13 +575,10 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
           wd[mt][4 * i + 3] = v.w;
         }
       }
-      float da[2][2][4];
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) da[mt][c][e] = 0.0f;
+        for (int e = 0; e < 4; ++e) dsum[mt][e] = 0.0f;
 #pragma unroll
       for (int u = 0; u < BK; ++u) {
 #pragma unroll
@@ -590,15 +588,11 @@ __global__ void __launch_bounds__(mma_warps<HG>() * 32, 1) decode_mma_kernel(con
 #pragma unroll
           for (int jj = 0; jj < KPW; ++jj) {
             const int kk = u * KPW + jj;
-            mma16816(da[mt][0], PK::get(X, Xs, 2 * jj), PK::get(Y, Ys, 2 * jj), PK::get(X, Xs, 2 * jj + 1),
+            mma16816(dsum[mt], PK::get(X, Xs, 2 * jj), PK::get(Y, Ys, 2 * jj), PK::get(X, Xs, 2 * jj + 1),
                      PK::get(Y, Ys, 2 * jj + 1), bf[2 * kk], bf[2 * kk + 1]);
           }
         }
       }
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dsum[mt][e] = da[mt][0][e];
     }
     float sc[2][2];
     // every lane computes (no branch); lanes past the heads take head 0 and are masked below
