@@ -500,6 +500,9 @@ def run_ours(args, dist):
     def per_call(n, call):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         with torch.cuda.stream(stream):
+            # the GPU spins first (about 60 us per call to come) so that the host has enqueued every
+            # call before the first runs: the events then bracket device time, not the host's launches
+            torch.cuda._sleep(int(120_000 * n))
             for j in range(n):
                 evs[j][0].record(stream)
                 call(j)
