@@ -489,6 +489,12 @@ __device__ __forceinline__ uint32_t code4_pair(uint32_t x, const GroupQ& q0, con
 
 __device__ __forceinline__ uint32_t comp(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
 
+// A barrier over one half of the 512 threads (warps 0-7 or warps 8-15).
+__device__ __forceinline__ void half_barrier(bool first_half) {
+  if (first_half) asm volatile("bar.sync 1, 256;" ::: "memory");
+  else asm volatile("bar.sync 2, 256;" ::: "memory");
+}
+
 template <int BK, int BV>
 __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const QuantizeParams p) {
   static_assert((BK == 2 || BK == 4) && (BV == 2 || BV == 4), "fragment-order pages hold 2- or 4-bit codes");
@@ -550,7 +556,10 @@ __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const Quan
       }
     }
   }
-  __syncthreads();
+  // keys (warps 0-7) and values (warps 8-15) share nothing until the end: each half waits only for
+  // itself, so one half computes while the other still waits for its data (barriers 1 and 2, as
+  // immediates: a barrier index in a register would reserve all sixteen and cost occupancy)
+  half_barrier(keys);
 
   // ---- ranges, zero points and steps, thresholds
   {
@@ -616,7 +625,7 @@ __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const Quan
       sw[SM::vms + (2 * pos + 1) * 4 + grp] = zs1;
     }
   }
-  __syncthreads();
+  half_barrier(keys);
 
   // ---- codes in fragment order: thread = (16-token tile wl, lane).  Every load address is a
   //      per-lane base plus a compile-time offset: the XOR swizzle only depends on the lane (g8)
