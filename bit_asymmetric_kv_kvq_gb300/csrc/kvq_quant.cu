@@ -759,15 +759,17 @@ __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const Quan
 // codes), R = 128, D = 128, G = 32 or 64, up to four sparse entries per key vector: one CTA of 512
 // threads per page, two CTAs per SM (64 registers), the tiles and swizzles of quantize_std_kernel.
 //   fill     as in quantize_std_kernel;
-//   sparse   a thread per (token, 32-channel quarter) finds the quarter's largest |x| in channel
-//            order, the four lanes of a token merge their lists by shuffles (larger |x| first,
-//            ties to the lower channel); each entry is written out and replaced in the tile by a
+//   sparse   warps 0-7: a thread per (token, 64-channel half) finds the half's largest |x| in
+//            channel order, the two lanes of a token merge their lists by a shuffle (larger |x|
+//            first, ties to the lower channel); each entry is written out and replaced in the tile by a
 //            NaN, which the fp16 minimum and maximum skip and which quantizes to code 0 --
 //            exactly the exclusion the method asks for;
 //   ranges   warps 0-7: key ranges and quantizers, a thread per (token group, channel pair);
 //            warps 8-15: value ranges and quantizers, a thread per (token pair, channel group);
-//   codes    every thread: the key codes of one (token, 32-channel chunk) and the value codes of
-//            one (token, 32-channel chunk), each packed 32 at a time into B words.
+//   codes    warps 0-7 the key codes, warps 8-15 the value codes: two (token, 32-channel chunk)
+//            per thread, each packed 32 at a time into B words.
+// The key half (warps 0-7) and the value half (warps 8-15) share nothing, so each waits at barriers
+// of its own and computes while the other still waits for its data.
 // A code comes from the group's reciprocal; elements whose product lies within 2^-14 of a
 // half-integer (where it could round differently from the IEEE quotient) are collected in a mask
 // and taken again with the IEEE quotient after the loop, behind one vote per chunk.
@@ -894,13 +896,13 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
       }
     }
   }
-  __syncthreads();
+  half_barrier(warp < 8);
 
-  // ---- sparse key entries: thread = (token t, quarter qt of 32 channels); lanes 4t' .. 4t'+3 of a
-  //      warp hold one token's four quarters.  |x| as fp16 bits orders like its value; entry (v, c)
+  // ---- sparse key entries (warps 0-7): thread = (token t, half qt of 64 channels); lanes 2t', 2t'+1
+  //      of a warp hold one token's two halves.  |x| as fp16 bits orders like its value; entry (v, c)
   //      outranks (v', c') when v > v', or v == v' and c < c' (ties to the lower channel).
-  if (nsp > 0) {
-    const int t = tid >> 2, qt = tid & 3;
+  if (nsp > 0 && warp < 8) {
+    const int t = tid >> 1, qt = tid & 1;
     const uint32_t* row = ks + t * 64;
     int bc[kMaxSparse];  // the chosen channels (unused slots hold a channel past the end)
     if (nsp <= 2) {
@@ -909,8 +911,8 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
       // the two largest keys take three integer min/max per entry
       int k0 = -1, k1 = -1;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int ch = 4 * qt + i;  // 16-byte chunk: channels 8ch .. 8ch+7
+      for (int i = 0; i < 8; ++i) {
+        const int ch = 8 * qt + i;  // 16-byte chunk: channels 8ch .. 8ch+7
         const uint4 v = *reinterpret_cast<const uint4*>(row + ((ch ^ (t & 7)) << 2));
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -922,9 +924,9 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
           k0 = max(k0, k);
         }
       }
-      // merge the four quarters' pairs
+      // merge the two halves' pairs
 #pragma unroll
-      for (int off = 1; off < 4; off <<= 1) {
+      for (int off = 1; off < 2; off <<= 1) {
         const int o0 = __shfl_xor_sync(0xffffffffu, k0, off), o1 = __shfl_xor_sync(0xffffffffu, k1, off);
         k1 = max(min(k0, o0), max(k1, o1));
         k0 = max(k0, o0);
@@ -957,15 +959,15 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
         }
       };
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int ch = 4 * qt + i;
+      for (int i = 0; i < 8; ++i) {
+        const int ch = 8 * qt + i;
         const uint4 v = *reinterpret_cast<const uint4*>(row + ((ch ^ (t & 7)) << 2));
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 8; ++e) insert((int)((w4[e >> 1] >> (16 * (e & 1))) & 0x7FFFu), 8 * ch + e);
       }
 #pragma unroll
-      for (int off = 1; off < 4; off <<= 1) {
+      for (int off = 1; off < 2; off <<= 1) {
         int ov[kMaxSparse], oc[kMaxSparse];
 #pragma unroll
         for (int k = 0; k < kMaxSparse; ++k) {
@@ -988,18 +990,18 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
       order(1, 3);
       order(1, 2);
     }
-    // each lane writes and masks the entries of its own quarter
+    // each lane writes and masks the entries of its own half
     uint16_t* rowh = reinterpret_cast<uint16_t*>(ks + t * 64);
 #pragma unroll
     for (int k = 0; k < kMaxSparse; ++k) {
       const int c = bc[k];
-      if (k >= nsp || (c >> 5) != qt) continue;
+      if (k >= nsp || (c >> 6) != qt) continue;
       const int hw = 2 * ((((c >> 3) ^ (t & 7)) << 2) | ((c >> 1) & 3)) + (c & 1);  // half index in the row
       dst[p.lay.off_si + t * nsp + k] = (uint8_t)c;
       reinterpret_cast<uint16_t*>(dst + p.lay.off_sv)[t * nsp + k] = rowh[hw];
       rowh[hw] = 0x7E00u;  // NaN
     }
-    __syncthreads();
+    half_barrier(true);  // the key half only
   }
 
   // ---- ranges and quantizers: keys (warps 0-7), values (warps 8-15)
@@ -1057,61 +1059,70 @@ __global__ void __launch_bounds__(kStdThreads, 2) quantize_bits_kernel(const Qua
       vm[(2 * tp + 1) * ngv + g] = q1.bits;
     }
   }
-  __syncthreads();
+  half_barrier(warp < 8);
 
-  // ---- codes: every thread one key chunk and one value chunk
-  {
+  // ---- codes: the key half codes the keys and the value half the values, two 32-channel chunks a
+  //      thread, so each half goes on as soon as its own ranges are done
+  if (warp < 8) {
     // keys: (token t, chunk q); the quarter-warps read rows t .. t+7, whose swizzles differ
-    const int q = warp >> 2, t = ((warp & 3) << 5) | lane;
+    const int t = ((warp & 3) << 5) | lane;
     const int gk = t / G;
-    uint32_t xw[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = *reinterpret_cast<const uint4*>(ks + t * 64 + (((4 * q + i) ^ (t & 7)) << 2));
-      xw[4 * i] = v.x;
-      xw[4 * i + 1] = v.y;
-      xw[4 * i + 2] = v.z;
-      xw[4 * i + 3] = v.w;
-    }
-    const QuantF* qf = kqf + gk * 128 + 32 * q;
-    const uint32_t* qb = kzs + gk * 128 + 32 * q;
-    uint32_t w[BK];
     const uint16_t* rowh = reinterpret_cast<const uint16_t*>(ks + t * 64);
-    code_chunk<BK>([&](int c) { return h2f((uint16_t)((c & 1) ? (xw[c >> 1] >> 16) : (xw[c >> 1] & 0xFFFFu))); },
-                   [&](int c) {
-                     const int ch = 32 * q + c;
-                     return h2f(rowh[2 * ((((ch >> 3) ^ (t & 7)) << 2) | ((ch >> 1) & 3)) + (ch & 1)]);
-                   },
-                   [&](int c) { return qf[c]; }, [&](int c) { return qb[c]; }, w);
     uint32_t* kc = reinterpret_cast<uint32_t*>(dst + p.lay.off_kc);
+#pragma unroll 1
+    for (int qq = 0; qq < 2; ++qq) {
+      const int q = (warp >> 2) + 2 * qq;
+      uint32_t xw[16];
 #pragma unroll
-    for (int i = 0; i < BK; ++i) kc[t * WK + q * BK + i] = w[i];
-  }
-  {
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(ks + t * 64 + (((4 * q + i) ^ (t & 7)) << 2));
+        xw[4 * i] = v.x;
+        xw[4 * i + 1] = v.y;
+        xw[4 * i + 2] = v.z;
+        xw[4 * i + 3] = v.w;
+      }
+      const QuantF* qf = kqf + gk * 128 + 32 * q;
+      const uint32_t* qb = kzs + gk * 128 + 32 * q;
+      uint32_t w[BK];
+      code_chunk<BK>([&](int c) { return h2f((uint16_t)((c & 1) ? (xw[c >> 1] >> 16) : (xw[c >> 1] & 0xFFFFu))); },
+                     [&](int c) {
+                       const int ch = 32 * q + c;
+                       return h2f(rowh[2 * ((((ch >> 3) ^ (t & 7)) << 2) | ((ch >> 1) & 3)) + (ch & 1)]);
+                     },
+                     [&](int c) { return qf[c]; }, [&](int c) { return qb[c]; }, w);
+#pragma unroll
+      for (int i = 0; i < BK; ++i) kc[t * WK + q * BK + i] = w[i];
+    }
+  } else {
     // values: (token 2tp + hf, chunk q); the two lanes of a token pair read the same words
-    const int q = warp >> 2, hf = lane & 1, tp = ((warp & 3) << 4) | (lane >> 1);
-    const int tok = 2 * tp + hf, g = (32 * q) / G;
-    const QuantF qv = vqf[tok * ngv + g];
-    const uint32_t qvb = vzs[tok * ngv + g];
-    const int c0 = 32 * q;
-    int off[8];  // row c0 + c keeps chunk tp >> 2 at (tp >> 2) ^ ((c ^ (c >> 3)) & 7) ^ ((c0 >> 3) & 7)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) off[k] = (((tp >> 2) ^ k ^ ((c0 >> 3) & 7)) << 2) | (tp & 3);
-    const uint32_t* col = vt + c0 * 64;
-    uint32_t w[BV];
-    code_chunk<BV>(
-        [&](int c) {
-          const uint32_t x = col[c * 64 + off[(c ^ (c >> 3)) & 7]];
-          return h2f((uint16_t)(hf ? (x >> 16) : (x & 0xFFFFu)));
-        },
-        [&](int c) {
-          const uint32_t x = vt[(c0 + c) * 64 + vswz(tp, c0 + c)];
-          return h2f((uint16_t)(hf ? (x >> 16) : (x & 0xFFFFu)));
-        },
-        [&](int) { return qv; }, [&](int) { return qvb; }, w);
+    const int hf = lane & 1, tp = ((warp & 3) << 4) | (lane >> 1);
+    const int tok = 2 * tp + hf;
     uint32_t* vc = reinterpret_cast<uint32_t*>(dst + p.lay.off_vc);
+#pragma unroll 1
+    for (int qq = 0; qq < 2; ++qq) {
+      const int q = ((warp - 8) >> 2) + 2 * qq;
+      const int g = (32 * q) / G;
+      const QuantF qv = vqf[tok * ngv + g];
+      const uint32_t qvb = vzs[tok * ngv + g];
+      const int c0 = 32 * q;
+      int off[8];  // row c0 + c keeps chunk tp >> 2 at (tp >> 2) ^ ((c ^ (c >> 3)) & 7) ^ ((c0 >> 3) & 7)
 #pragma unroll
-    for (int i = 0; i < BV; ++i) vc[tok * WV + q * BV + i] = w[i];
+      for (int k = 0; k < 8; ++k) off[k] = (((tp >> 2) ^ k ^ ((c0 >> 3) & 7)) << 2) | (tp & 3);
+      const uint32_t* col = vt + c0 * 64;
+      uint32_t w[BV];
+      code_chunk<BV>(
+          [&](int c) {
+            const uint32_t x = col[c * 64 + off[(c ^ (c >> 3)) & 7]];
+            return h2f((uint16_t)(hf ? (x >> 16) : (x & 0xFFFFu)));
+          },
+          [&](int c) {
+            const uint32_t x = vt[(c0 + c) * 64 + vswz(tp, c0 + c)];
+            return h2f((uint16_t)(hf ? (x >> 16) : (x & 0xFFFFu)));
+          },
+          [&](int) { return qv; }, [&](int) { return qvb; }, w);
+#pragma unroll
+      for (int i = 0; i < BV; ++i) vc[tok * WV + q * BV + i] = w[i];
+    }
   }
 }
 
