@@ -434,7 +434,8 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_pages_kernel(const 
 //           maximum are exact), then the zero point, the step and -- for 2-bit codes -- the three
 //           fp16 decision thresholds of each group (kvq::qthr), or the group quantizer (4-bit);
 //   codes   a thread per (16-token tile, lane) builds that lane's fragment words: 2-bit codes by
-//           comparing fp16 pairs with the thresholds (three packed compares per two codes), 4-bit
+//           comparing fp16 pairs with the thresholds (two packed compares and a select per two
+//           codes: bit 1 from t1, bit 0 from t2 or t0 as bit 1 says), 4-bit
 //           codes with the group quantizer; each thread stores its words with 16-byte stores.
 // Both tiles are XOR-swizzled in 16-byte chunks so that no phase has shared-memory bank
 // conflicts: key row t keeps chunk c at c ^ (t & 7); value row (channel) c keeps chunk q at
@@ -653,10 +654,11 @@ __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const Quan
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const __half2 x = as_h2(kr[r * 8 * 64 + 32 * u + sj[j]]);
-            const uint32_t m0 = __hge2_mask(x, as_h2(t0)), m1 = __hge2_mask(x, as_h2(t1)),
-                           m2 = __hge2_mask(x, as_h2(t2));
-            // code = thresholds reached: bit 0 = odd count, bit 1 = at least two
-            wd[r * 2 + u] |= ((m0 ^ m1 ^ m2) & (0x00010001u << (2 * j))) | (m1 & (0x00020002u << (2 * j)));
+            // code = thresholds reached (t0 <= t1 <= t2): bit 1 = x >= t1; bit 0 = x >= t2 where
+            // x >= t1, else x >= t0 -- two packed compares and a select per two codes
+            const uint32_t m1 = __hge2_mask(x, as_h2(t1));
+            const uint32_t m0 = __hge2_mask(x, as_h2((m1 & t2) | (~m1 & t0)));
+            wd[r * 2 + u] |= (m0 & (0x00010001u << (2 * j))) | (m1 & (0x00020002u << (2 * j)));
           }
         }
     } else {
@@ -725,9 +727,9 @@ __global__ void __launch_bounds__(kStdThreads, 3) quantize_std_kernel(const Quan
               const int r = 2 * rh + rl, j = 2 * gv + jl;
               const int K = rh ^ ((2 * j + rl) & 7);
               const __half2 x = as_h2(vb[K][(16 * j + 8 * rl) * 64]);
-              const uint32_t m0 = __hge2_mask(x, as_h2(t0)), m1 = __hge2_mask(x, as_h2(t1)),
-                             m2 = __hge2_mask(x, as_h2(t2));
-              wd[r] |= ((m0 ^ m1 ^ m2) & (0x00010001u << (2 * j))) | (m1 & (0x00020002u << (2 * j)));
+              const uint32_t m1 = __hge2_mask(x, as_h2(t1));
+              const uint32_t m0 = __hge2_mask(x, as_h2((m1 & t2) | (~m1 & t0)));
+              wd[r] |= (m0 & (0x00010001u << (2 * j))) | (m1 & (0x00020002u << (2 * j)));
             }
         }
     } else {
