@@ -136,6 +136,17 @@ def test_split_counts_agree(splits):
     run_case(w, 1, splits=splits)
 
 
+@pytest.mark.parametrize("bits,q_heads", [((2, 2), 4), ((4, 2), 4), ((4, 4), 1)],
+                         ids=["k2v2-4heads-13-stages", "k4v2-4heads-10-stages", "k4v4-1head-10-stages"])
+def test_page_ring_wraps_many_times(bits, q_heads):
+    """One CTA streams the 100 pages of one unit through its page ring: the ring's stage counts that
+    are not powers of two (13 stages of 12 KB pages beside four query heads' buffers, 10 of 16 KB or
+    20 KB pages) wrap around seven to ten times within one launch."""
+    w = synth.WORKLOADS[3].scaled(batch=1, kv_heads=1, q_heads=q_heads, prefill_tokens=100 * 128 + 3,
+                                  decode_steps=1, k_bits=bits[0], v_bits=bits[1])
+    run_case(w, 1, splits=1)
+
+
 def test_capacity_and_state_errors():
     kvq = _kvq()
     w = synth.WORKLOADS[0].scaled(batch=1, kv_heads=1, q_heads=1, prefill_tokens=5, decode_steps=1)  # capacity 6
