@@ -725,17 +725,23 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE, LUT>::WARPS * 32, 1) d
       for (int h = 0; h < HG; ++h)
 #pragma unroll
         for (int i = 0; i < CPL; ++i) st.acc[h][i] *= fac[h];
+      // while the accumulators are in registers their shared-memory slot holds the sub-tile's
+      // weights, [slot tau][token j][head h]: one 16-byte load gives a token's four heads
+      __syncwarp();
+      float* const p_s = reinterpret_cast<float*>(acc_s);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) p_s[tau * 64 + 16 * b + kap] = pb[b];  // token 4b + kap/4, head kap%4
+      __syncwarp();
+      float2 z01 = make_float2(st.zsum[0], st.zsum[1]), z23 = make_float2(st.zsum[2], st.zsum[3]);
       const float kScIn = __uint_as_float((uint32_t)(127 + 149 - kCodeExp) << 23);
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
-      const float pbb = b == 0 ? pb[0] : b == 1 ? pb[1] : b == 2 ? pb[2] : pb[3];
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const int j = 4 * b + jj;
         const int tt = stt * 32 + tau + TAU * j;
-        float ph[HG];
-#pragma unroll
-        for (int h = 0; h < HG; ++h) ph[h] = __shfl_sync(kFull, pbb, tau * KAPPA + 4 * jj + h);
+        const float4 pq = *reinterpret_cast<const float4*>(p_s + (tau * 16 + j) * 4);
+        const float2 p01 = make_float2(pq.x, pq.y), p23 = make_float2(pq.z, pq.w);
         const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(vm + tt * ng + gv));
         const float sv = zs.y * kScIn;
         const uint32_t* rec = vcw + tt * VW;
@@ -748,20 +754,27 @@ __global__ void __launch_bounds__(Shape<BK, BV, HG, ROPE, LUT>::WARPS * 32, 1) d
           f2[2 + m] = make_float2(__uint_as_float(x2 & (VMASK << (BV * 2 * m))),
                                   __uint_as_float(x2 & (VMASK << (BV * (2 * m + 1)))));
         }
+        const float2 ps01 = __fmul2_rn(p01, make_float2(sv, sv)), ps23 = __fmul2_rn(p23, make_float2(sv, sv));
+        const float psh[HG] = {ps01.x, ps01.y, ps23.x, ps23.y};
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
-          const float ps = ph[h] * sv;
-          const float2 ps2 = make_float2(ps, ps);
+          const float2 ps2 = make_float2(psh[h], psh[h]);
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             const float2 a = __ffma2_rn(f2[m], ps2, make_float2(st.acc[h][2 * m], st.acc[h][2 * m + 1]));
             st.acc[h][2 * m] = a.x;
             st.acc[h][2 * m + 1] = a.y;
           }
-          st.zsum[h] = fmaf(ph[h], zs.x, st.zsum[h]);
         }
+        z01 = __ffma2_rn(p01, make_float2(zs.x, zs.x), z01);
+        z23 = __ffma2_rn(p23, make_float2(zs.x, zs.x), z23);
       }
       }
+      st.zsum[0] = z01.x;
+      st.zsum[1] = z01.y;
+      st.zsum[2] = z23.x;
+      st.zsum[3] = z23.y;
+      __syncwarp();  // every lane is done with the weights before the accumulators go back
       acc_store();
     }
   };
