@@ -814,8 +814,10 @@ constexpr size_t warp_bufs_bytes() {
 }
 
 // Page stages of one CTA: as many as fit (up to kMmaMaxStages) in the opt-in shared memory beside
-// the static arrays and the per-warp buffers; -1 when none fits (or the static arrays exceed the
-// 48 KB a kernel may declare).
+// the static arrays and the per-warp buffers; -1 when fewer than two fit (or the static arrays
+// exceed the 48 KB a kernel may declare).  Two at least: the ring's lap is a multiply-high by
+// ceil(2^32 / n), which fits in 32 bits only for n >= 2 (pages of R <= 128 tokens leave room for
+// seven or more).
 template <int BK, int BV, int HG>
 int stages_mma(int page_bytes) {
   auto kern = decode_mma_kernel<BK, BV, HG, false>;  // both variants declare the same static arrays
@@ -831,7 +833,7 @@ int stages_mma(int page_bytes) {
   if (static_smem > 48 * 1024) return -1;
   const int64_t avail = (int64_t)optin - static_smem - (int64_t)warp_bufs_bytes<HG>();
   const int64_t n = avail / page_bytes;
-  return n < 1 ? -1 : (int)(n < kMmaMaxStages ? n : kMmaMaxStages);
+  return n < 2 ? -1 : (int)(n < kMmaMaxStages ? n : kMmaMaxStages);
 }
 
 template <int BK, int BV, int HG>
